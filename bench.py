@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of one full-size MoE decode layer on GB300 (one JSON line).
+
+Headline: microseconds per layer for the full-size layer at B = 1 (d=7168,
+f=1536, 896 MXFP4 experts, top-16, bf16 shared expert, residual + RMSNorm
+tail), event-timed on the device with L2 flushed between steps, plus the
+achieved HBM bandwidth against the bytes the layer must touch.  B = 8 and
+B = 64 are reported in the same line under "batches".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 statement of the layer)
+on the host cores instead: that is this project's reference arm.
+Multi-GPU (torchrun, one rank per GPU): independent replicas, no collective on
+the data path; the reported time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per MoE decode layer at B=1/8/64; achieved HBM TB/s vs GB300 peak"
+DTYPE = "mxfp4(e2m1,e8m0) x f16 -> f32 routed; bf16 x bf16 -> f32 router/shared"
+DATA = "synthetic: seeded Philox4x32-10 normal draws (no trained weights, no dataset)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="full_b1")
+    p.add_argument("--no-batches", action="store_true", help="skip the B=8 / B=64 extras")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (identity at world size 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def bytes_touched(cfg, n_distinct, B):
+    """Algorithmic HBM bytes of one layer: touched experts + router + shared
+    expert + gamma + activations (x read, residual read+write, out write)."""
+    return (n_distinct * cfg.expert_bytes() + cfg.n_experts * cfg.d * 2 + 4 * cfg.n_experts
+            + 3 * cfg.d * cfg.f_shared * 2 + 2 * cfg.d + 8 * B * cfg.d)
+
+
+def fc1_bytes(cfg, n_distinct, B):
+    """Algorithmic bytes of one routed FC1 launch: gate+up nibbles and scales of
+    the touched experts, x, and h written."""
+    per_expert = 2 * cfg.f * cfg.d // 2 + 2 * cfg.f * cfg.d // 32
+    return n_distinct * per_expert + 2 * B * cfg.d + 4 * B * cfg.top_k * cfg.f
+
+
+def traffic_from_profile(kernel_file):
+    """dram bytes per launch recorded by the ncu summary of the routed FC1
+    kernel, or None when missing or taken on a different kernel source."""
+    summ = os.path.join(ROOT, "profiles", "routed_fc1_full_b1.md")
+    try:
+        text = open(summ).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch_full_b1:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+def time_layer(layer, cfg, x, res0, steps, warmup, flush, timing=True):
+    """Event-timed forwards (median us) with L2 flushed between steps.
+    Returns (per-step us list, per-step phase lists)."""
+    import torch
+    res = res0.clone()
+    out = torch.empty_like(x)
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        res.copy_(res0)
+        flush.zero_()
+        layer.forward(x, res, out)
+    torch.cuda.synchronize()
+    layer.set_timing(timing)
+    times, phases = [], []
+    for i in range(steps):
+        res.copy_(res0)
+        flush.fill_(i & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        layer.forward(x, res, out)
+        b.record(st)
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1000.0)
+        if timing:
+            phases.append(layer.get_timing())
+    layer.set_timing(False)
+    return times, phases
+
+
+def time_e2e(layer, cfg, x, res0, steps, warmup, flush):
+    """The same layer through the host-buffer entry point: H2D of x and the
+    residual, forward, D2H of residual and out, stream sync, per step."""
+    import torch
+    xh = x.cpu().pin_memory()
+    r0 = res0.cpu()
+    rh = torch.empty_like(r0).pin_memory()
+    oh = torch.empty_like(r0).pin_memory()
+    for _ in range(warmup):
+        rh.copy_(r0)
+        flush.zero_()
+        torch.cuda.synchronize()
+        layer.forward_host(xh, rh, oh)
+    times = []
+    for i in range(steps):
+        rh.copy_(r0)
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        layer.forward_host(xh, rh, oh)
+        times.append((time.perf_counter() - t0) * 1e6)
+    nbytes = x.numel() * 2
+    return times, 2 * nbytes, 2 * nbytes
+
+
+def cpu_oracle_sample(cfg_name, repeats=1):
+    """Time the CPU oracle on one full layer (layer compute only; drawing and
+    MXFP4 packing of the weights are excluded)."""
+    import gen
+    import oracle
+    from gen.configs import CONFIGS
+    cfg = CONFIGS[cfg_name]
+    inp = oracle.LayerInputs(cfg)
+    for e in set(oracle.route(inp)[1].ravel().tolist()):
+        inp.expert_packed(int(e))
+    ts = []
+    for _ in range(repeats):
+        tm = {}
+        oracle.forward(inp, timings=tm)
+        ts.append(tm["compute_s"] * 1e6)
+    return ts, gen.host_threads()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from gen.configs import CONFIGS
+    cfg = CONFIGS[args.config]
+    # warm-up: draws and packing happen here (excluded from the timed steps)
+    warm_ts, cores = cpu_oracle_sample(args.config, repeats=max(1, min(args.warmup, 1)))
+    t0 = time.perf_counter()
+    ts, _ = cpu_oracle_sample(args.config, repeats=args.steps)
+    wall = time.perf_counter() - t0
+    v = statistics.median(ts)
+    sample = (f"{args.config}: one full layer per step (router over {cfg.n_experts} experts, "
+              f"{cfg.top_k} MXFP4 experts, shared expert, tail) in fp64; weight draws and "
+              "packing excluded")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": DATA,
+            "config": {"workload": args.config, "B": cfg.B, "d": cfg.d, "f": cfg.f,
+                       "n_experts": cfg.n_experts, "top_k": cfg.top_k, "f_shared": cfg.f_shared},
+            "cpu_baseline": {"value": v, "unit": "us", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from gen.configs import CONFIGS
+    from moe_decode_step_gb300 import synthetic
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    cfg = CONFIGS[args.config]
+    peak, peak_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    layer = synthetic.make_layer(cfg)
+    x, res0 = synthetic.make_activations(cfg)
+    idx, _ = layer.router_topk(x)
+    n_distinct = int(torch.unique(idx).numel())
+    torch.cuda.synchronize()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        times, phases = time_layer(layer, cfg, x, res0, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+
+    us = reduce_max(statistics.median(times), world, dev)
+    btouch = bytes_touched(cfg, n_distinct, cfg.B)
+    fc1_us = statistics.median(p[1] for p in phases)
+    fc1_b = fc1_bytes(cfg, n_distinct, cfg.B)
+    kernel_src = os.path.join(ROOT, "moe_decode_step_gb300", "csrc", "routed.cuh")
+    traffic = traffic_from_profile(kernel_src)
+    if traffic is not None:
+        traffic = traffic * n_distinct / 16.0
+    phase_names = ["router_topk", "routed_fc1", "routed_fc2", "shared_side_stream", "tail",
+                   "layer"]
+    phase_med = {n: statistics.median(p[i] for p in phases) for i, n in enumerate(phase_names)}
+
+    e2e_times, h2d, d2h = time_e2e(layer, cfg, x, res0, max(5, args.steps // 2),
+                                   max(3, args.warmup), flush)
+    e2e_us = reduce_max(statistics.median(e2e_times), world, dev)
+    launches = layer.launches_per_forward(cfg.B) * args.steps
+    layer.close()
+    del layer
+
+    batches = {}
+    if not args.no_batches and args.config == "full_b1":
+        for name in ("full_b8", "full_b64"):
+            c2 = CONFIGS[name]
+            L2 = synthetic.make_layer(c2)
+            x2, r2 = synthetic.make_activations(c2)
+            i2, _ = L2.router_topk(x2)
+            nd2 = int(torch.unique(i2).numel())
+            st2 = max(5, min(args.steps, 20))
+            t2, p2 = time_layer(L2, c2, x2, r2, st2, max(3, args.warmup), flush)
+            v2 = reduce_max(statistics.median(t2), world, dev)
+            b2 = bytes_touched(c2, nd2, c2.B)
+            batches[str(c2.B)] = {
+                "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
+                "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,
+                "phases_us": {n: statistics.median(p[i] for p in p2)
+                              for i, n in enumerate(phase_names)}}
+            L2.close()
+            del L2
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        ts, cores = cpu_oracle_sample(args.config, repeats=1)
+        cpu = {"value": statistics.median(ts), "unit": "us", "cores": cores, "kind": "oracle",
+               "sample": f"{args.config}: one full layer (router, {cfg.top_k} MXFP4 experts, "
+                         "shared expert, tail) in fp64; weight draws and packing excluded"}
+
+    agg_tbs = reduce_sum(btouch / us / 1e6, world, dev)
+    line = {
+        "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": DATA,
+        "config": {"workload": f"{args.config}: one MoE decode layer, B={cfg.B}, d={cfg.d}, "
+                               f"f={cfg.f}, E={cfg.n_experts}, top-{cfg.top_k}, MXFP4 experts, "
+                               f"bf16 shared expert f={cfg.f_shared}, residual+RMSNorm tail",
+                   "B": cfg.B, "l2": "flushed between timed steps (write of 2x L2 size)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm": {"bytes_touched": btouch, "n_distinct_experts": n_distinct,
+                "tbs": btouch / us / 1e6, "frac_of_peak": btouch / us / 1e3 / peak,
+                "frac_of_nominal_8tbs": btouch / us / 1e6 / 8.0, "aggregate_tbs": agg_tbs,
+                "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "routed_fc1_kernel", "bound": "hbm",
+                     "achieved": fc1_b / fc1_us / 1e3, "peak": peak, "unit": "GB/s",
+                     "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,
+                     "algorithmic_bytes": fc1_b, "launch_us": fc1_us, "peak_kind": peak_kind},
+        "phases_us": phase_med,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "batches": batches,
+        "wall_s": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * moe_decode.h — C ABI of a single-GPU (GB300, sm_103a) mixture-of-experts
+ * decode layer for 1..64 rows.
+ *
+ * The layer (one call of moe_decode_forward) is, for every row b of x:
+ *   router      logits = x_b . W_r^T; s = sigmoid(logits); the top_k experts
+ *               by s + bias (ties to the lower index); combine weights
+ *               w = routed_scale * s_sel / sum(s_sel)
+ *   routed      for each selected expert e: h = silu(W_gate,e x_b) * (W_up,e x_b),
+ *               y_e = W_down,e h; y_routed = sum_j w_j y_{e_j}
+ *               (expert weights are MXFP4: E2M1 nibbles, one E8M0 scale per
+ *               32 contiguous K elements)
+ *   shared      y_shared = W_sd (silu(W_sg x_b) * (W_su x_b)), bf16 weights
+ *   tail        z = residual_b + y_routed + y_shared; residual_b <- bf16(z);
+ *               out_b = bf16(z / sqrt(mean(z^2) + eps) * gamma)
+ *
+ * Sources: "Kimi K3 on GB300: 13 kernels a layer, and what 842 and 423 tokens
+ * a second measure" — section "What one decode step of Kimi K3 does" (16 of
+ * 896 experts per token, 17,547,264-byte MXFP4 experts), section "Why batch 1
+ * on a rack is not only a bandwidth problem" (packed FP4 expert weights),
+ * section "What the fused path changes" (router/MoE front, shared expert on a
+ * side stream, one persistent routed-expert kernel for FC1 and FC2, a tail that
+ * folds the down-projection reduction and the next norm together, L2 prefetch
+ * of upcoming weights on a third stream).  The pages give the structure only;
+ * the formulas above are the plainest reading of that structure.  Element and
+ * scale encodings: OCP Microscaling Formats (MX) Specification v1.0.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are CUDA device pointers on the device that was
+ *    current at moe_layer_create; "host" pointers are ordinary host memory.
+ *    The caller owns every buffer it passes; the library borrows weight
+ *    pointers for the handle's lifetime and never frees them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Forward calls are asynchronous on that stream, allocate nothing and never
+ *    synchronise the host, so they may be captured into a CUDA graph.
+ *  - Every call returns a moe_status (0 = MOE_OK).  Nothing aborts or throws
+ *    across the ABI.  A handle must not be used from two streams at once.
+ *  - bf16 tensors are row-major uint16 bit patterns (torch.bfloat16 layout).
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size or dims */
+  MOE_ERR_UNSUPPORTED = 2,   /* B outside [1, max_batch], device is not sm_103, misaligned
+                                pointer: the caller should use another implementation */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed (the error is kept for
+                                moe_last_cuda_error) */
+  MOE_ERR_ALLOC = 4,         /* workspace allocation failed at create time */
+  MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait expired (see moe_layer_status) */
+} moe_status;
+
+typedef struct moe_layer* moe_layer_t;
+
+/* Layer dimensions.  d % 256 == 0 and d <= 8192; f % 256 == 0 and f <= 4096;
+ * f_shared % 256 == 0 and f_shared <= 4096; 1 <= top_k <= 32; top_k <= n_experts
+ * <= 1024; 1 <= max_batch <= 64.  mxfp4_layout must be 0 (canonical). */
+typedef struct {
+  int32_t d;              /* hidden size */
+  int32_t f;              /* routed-expert intermediate size */
+  int32_t n_experts;      /* E */
+  int32_t top_k;          /* k */
+  int32_t f_shared;       /* shared-expert intermediate size */
+  int32_t max_batch;      /* largest B forward will be called with */
+  float routed_scale;     /* combine weights sum to this (2.5 for the Kimi-style router) */
+  float rms_eps;          /* RMSNorm epsilon (1e-6) */
+  int32_t mxfp4_layout;   /* 0: canonical layout, see mxfp4_pack */
+} moe_dims_t;
+
+/* Device pointers to the layer's weights (borrowed, never freed).
+ * Expert e's FC1 rows 0..f-1 are the gate projection and rows f..2f-1 the up
+ * projection; row i of the gate pairs with row i of the up projection. */
+typedef struct {
+  const void* router_w;        /* device bf16 [E][d] */
+  const float* router_bias;    /* device fp32 [E], used for selection only */
+  const uint8_t* w_gu_q;       /* device [E][2f][d/2]  E2M1 nibbles, canonical layout */
+  const uint8_t* w_gu_s;       /* device [E][2f][d/32] E8M0 scale bytes */
+  const uint8_t* w_d_q;        /* device [E][d][f/2] */
+  const uint8_t* w_d_s;        /* device [E][d][f/32] */
+  const void* shared_gu;       /* device bf16 [2 f_shared][d] (gate rows, then up rows) */
+  const void* shared_d;        /* device bf16 [d][f_shared] */
+  const void* rms_gamma;       /* device bf16 [d] */
+} moe_weights_t;
+
+/* Validate dims, device (must be sm_103) and pointer alignment (16 bytes),
+ * allocate the workspace (routing tables, intermediates, two events and one
+ * side stream) on the current device and return a handle in *out.
+ * Errors: INVALID_ARG (null or bad dims), UNSUPPORTED (device/alignment),
+ * ALLOC (workspace), CUDA. */
+int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_layer_t* out);
+
+/* Free the workspace (synchronises the device first).  NULL is accepted. */
+int moe_layer_destroy(moe_layer_t layer);
+
+/* Router only: x device bf16 [B][d] -> idx device int32 [B][k] (descending by
+ * score + bias, ties to the lower index) and w device fp32 [B][k] (combine
+ * weights).  Same kernel as the first step of moe_decode_forward.
+ * Errors: INVALID_ARG, UNSUPPORTED (B), CUDA. */
+int moe_router_topk(moe_layer_t layer, void* stream, const void* x, int B, int32_t* idx, float* w);
+
+/* The whole layer.  x device bf16 [B][d] (read only); residual device bf16
+ * [B][d], read and overwritten with bf16(z); out device bf16 [B][d].  x, out
+ * and residual must not overlap.  Asynchronous, allocation-free. */
+int moe_decode_forward(moe_layer_t layer, void* stream, const void* x, int B, void* residual,
+                       void* out);
+
+/* The same layer with HOST buffers: copies x and residual host -> device on
+ * `stream`, runs moe_decode_forward on the handle's own device staging
+ * buffers, copies residual and out back, and synchronises `stream` before
+ * returning.  x_host, residual_host, out_host: host bf16 [B][d] (pinned memory
+ * gives asynchronous copies; pageable memory works but copies synchronously). */
+int moe_decode_forward_host(moe_layer_t layer, void* stream, const void* x_host, int B,
+                            void* residual_host, void* out_host);
+
+/* moe_decode_forward that also exports intermediates (any may be NULL):
+ * y_routed device fp32 [B][d], y_shared device fp32 [B][d],
+ * h device fp32 [B][k][f] (h[b][j] belongs to expert idx[b][j]). */
+int moe_decode_forward_debug(moe_layer_t layer, void* stream, const void* x, int B, void* residual,
+                             void* out, float* y_routed, float* y_shared, float* h);
+
+/* Dequantise one expert matrix on the GPU with the kernels' own decode path:
+ * which = 0 -> FC1 [2f][d], which = 1 -> FC2 [d][f]; out device fp32. */
+int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, float* out);
+
+/* Chain layers: while this layer's routed experts run, an L2-prefetch kernel on
+ * a third stream touches `next`'s router and shared-expert weights.  next may be
+ * NULL to switch it off.  Both handles must live on the same device. */
+int moe_set_prefetch_next(moe_layer_t layer, moe_layer_t next);
+
+/* Synchronise the layer's streams and report the device status word
+ * (0 = ok, else a moe_status such as MOE_ERR_TIMEOUT); clears it. */
+int moe_layer_status(moe_layer_t layer, int* device_status);
+
+/* Per-phase timing of forward calls (CUDA events on the launching streams).
+ * enable != 0 records events around each phase from the next forward on.
+ * moe_get_timing synchronises and writes up to n floats (microseconds) for
+ * the last forward: [0] router+top-k, [1] routed FC1, [2] routed FC2,
+ * [3] shared expert (side stream), [4] tail, [5] whole layer. */
+int moe_set_timing(moe_layer_t layer, int enable);
+int moe_get_timing(moe_layer_t layer, float* us, int n);
+
+/* Number of kernel launches one forward makes for batch B (excluding the
+ * optional prefetch kernel, which adds one when enabled). */
+int moe_launches_per_forward(moe_layer_t layer, int B);
+
+/* ---- MXFP4 packing (OCP MX v1.0: E2M1 elements, E8M0 scale per 32 K) ---- */
+/* Canonical layout 0: row-major; byte j of a row holds elements 2j (low
+ * nibble) and 2j+1 (high nibble); scale byte b of a row covers elements
+ * 32b..32b+31.  Scale exponent = floor(log2(amax)) - 2 clamped to [-127, 127]
+ * (all-zero block: -127); element code = nearest E2M1 value to w / 2^exp,
+ * ties to the even code, magnitudes past 6 saturate to 6, sign bit = sign of w. */
+
+/* Bytes of nibbles for rows x k (k % 32 == 0); *scale_bytes gets the scale
+ * bytes when non-NULL.  Returns 0 on bad arguments. */
+size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes);
+
+/* Host packer: w host fp32 [rows][k] -> q host [rows][k/2], s host [rows][k/32]. */
+int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, int layout);
+
+/* Device packer, asynchronous on stream: w device fp32 -> q, s device. */
+int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
+                      uint8_t* s, int layout);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* The last CUDA error code a call saw (cudaError_t as int), 0 if none. */
+int moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,193 @@
+"""GB300-native (sm_103a) MoE decode layer: router + biased top-k, MXFP4 routed
+SwiGLU experts with weighted combine, bf16 shared expert, residual + RMSNorm.
+
+The compute path is the CUDA library `libmoe_decode.so` behind the C ABI in
+include/moe_decode.h; this package only marshals arguments (PyTorch tensors
+supply device memory and streams).
+"""
+import ctypes
+
+import torch
+
+from ._binding import (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA,
+                       MOE_ERR_ALLOC, MOE_ERR_TIMEOUT, MoEDims, MoEError, MoEWeights, check, lib,
+                       status_string)
+
+__all__ = ["MoELayer", "MoEDims", "MoEWeights", "MoEError", "mxfp4_pack", "mxfp4_pack_device",
+           "mxfp4_packed_bytes", "status_string", "lib", "MOE_OK", "MOE_ERR_INVALID_ARG",
+           "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_ALLOC", "MOE_ERR_TIMEOUT"]
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _expect(t, dtype, shape, name, device=True):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: want {dtype} {tuple(shape)} contiguous, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+class MoELayer:
+    """One MoE decode layer bound to borrowed device weight tensors.
+
+    weights: dict with router_w bf16 [E,d], router_bias f32 [E], w_gu_q u8
+    [E,2f,d/2], w_gu_s u8 [E,2f,d/32], w_d_q u8 [E,d,f/2], w_d_s u8 [E,d,f/32],
+    shared_gu bf16 [2fs,d], shared_d bf16 [d,fs], rms_gamma bf16 [d].
+    """
+
+    def __init__(self, d, f, n_experts, top_k, f_shared, max_batch, weights,
+                 routed_scale=2.5, rms_eps=1e-6):
+        self.dims = MoEDims(d, f, n_experts, top_k, f_shared, max_batch, routed_scale, rms_eps, 0)
+        E, fs = n_experts, f_shared
+        spec = {
+            "router_w": (torch.bfloat16, (E, d)), "router_bias": (torch.float32, (E,)),
+            "w_gu_q": (torch.uint8, (E, 2 * f, d // 2)), "w_gu_s": (torch.uint8, (E, 2 * f, d // 32)),
+            "w_d_q": (torch.uint8, (E, d, f // 2)), "w_d_s": (torch.uint8, (E, d, f // 32)),
+            "shared_gu": (torch.bfloat16, (2 * fs, d)), "shared_d": (torch.bfloat16, (d, fs)),
+            "rms_gamma": (torch.bfloat16, (d,)),
+        }
+        for name, (dt, shape) in spec.items():
+            _expect(weights[name], dt, shape, name)
+        self._weights = dict(weights)   # keep the borrowed tensors alive
+        w = MoEWeights(*[weights[n].data_ptr() for n in spec])
+        h = ctypes.c_void_p()
+        check(lib().moe_layer_create(ctypes.byref(self.dims), ctypes.byref(w), ctypes.byref(h)),
+              "moe_layer_create")
+        self._h = h
+        self.device = weights["router_w"].device
+        self._next = None
+
+    # -- lifetime ---------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().moe_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    # -- calls --------------------------------------------------------------
+    def router_topk(self, x, idx=None, w=None, stream=None):
+        B = x.shape[0]
+        k = self.dims.top_k
+        _expect(x, torch.bfloat16, (B, self.dims.d), "x")
+        if idx is None:
+            idx = torch.empty((B, k), dtype=torch.int32, device=x.device)
+        if w is None:
+            w = torch.empty((B, k), dtype=torch.float32, device=x.device)
+        check(lib().moe_router_topk(self._h, _stream(stream), _ptr(x), B, _ptr(idx), _ptr(w)),
+              "moe_router_topk")
+        return idx, w
+
+    def forward(self, x, residual, out=None, stream=None):
+        B = x.shape[0]
+        _expect(x, torch.bfloat16, (B, self.dims.d), "x")
+        _expect(residual, torch.bfloat16, (B, self.dims.d), "residual")
+        if out is None:
+            out = torch.empty_like(x)
+        check(lib().moe_decode_forward(self._h, _stream(stream), _ptr(x), B, _ptr(residual),
+                                       _ptr(out)), "moe_decode_forward")
+        return out
+
+    def forward_host(self, x, residual, out, stream=None):
+        """Host (CPU) bf16 tensors; residual and out are written in place."""
+        B = x.shape[0]
+        for t, n in ((x, "x"), (residual, "residual"), (out, "out")):
+            _expect(t, torch.bfloat16, (B, self.dims.d), n, device=False)
+            if t.is_cuda:
+                raise ValueError(f"{n} must be a host tensor")
+        check(lib().moe_decode_forward_host(self._h, _stream(stream), _ptr(x), B, _ptr(residual),
+                                            _ptr(out)), "moe_decode_forward_host")
+        return out
+
+    def forward_debug(self, x, residual, out=None, stream=None):
+        B = x.shape[0]
+        d, k, f = self.dims.d, self.dims.top_k, self.dims.f
+        if out is None:
+            out = torch.empty_like(x)
+        y_r = torch.empty((B, d), dtype=torch.float32, device=x.device)
+        y_s = torch.empty((B, d), dtype=torch.float32, device=x.device)
+        h = torch.empty((B, k, f), dtype=torch.float32, device=x.device)
+        check(lib().moe_decode_forward_debug(self._h, _stream(stream), _ptr(x), B, _ptr(residual),
+                                             _ptr(out), _ptr(y_r), _ptr(y_s), _ptr(h)),
+              "moe_decode_forward_debug")
+        return out, y_r, y_s, h
+
+    def debug_dequant(self, expert, which, stream=None):
+        d, f = self.dims.d, self.dims.f
+        shape = (2 * f, d) if which == 0 else (d, f)
+        out = torch.empty(shape, dtype=torch.float32, device=self.device)
+        check(lib().moe_debug_dequant(self._h, _stream(stream), int(expert), int(which), _ptr(out)),
+              "moe_debug_dequant")
+        return out
+
+    def set_prefetch_next(self, other):
+        self._next = other
+        check(lib().moe_set_prefetch_next(self._h, other._h if other is not None else None),
+              "moe_set_prefetch_next")
+
+    def status(self):
+        v = ctypes.c_int()
+        check(lib().moe_layer_status(self._h, ctypes.byref(v)), "moe_layer_status")
+        return v.value
+
+    def set_timing(self, enable):
+        check(lib().moe_set_timing(self._h, int(bool(enable))), "moe_set_timing")
+
+    def get_timing(self):
+        """[router, routed FC1, routed FC2, shared (side stream), tail, layer] in us."""
+        arr = (ctypes.c_float * 6)()
+        check(lib().moe_get_timing(self._h, arr, 6), "moe_get_timing")
+        return list(arr)
+
+    def launches_per_forward(self, B):
+        return lib().moe_launches_per_forward(self._h, int(B))
+
+
+def mxfp4_packed_bytes(rows, k, layout=0):
+    sb = ctypes.c_size_t()
+    qb = lib().mxfp4_packed_bytes(int(rows), int(k), int(layout), ctypes.byref(sb))
+    return qb, sb.value
+
+
+def mxfp4_pack(w):
+    """Host packer: w CPU float32 [rows, k] -> (q uint8 [rows, k/2], s uint8 [rows, k/32])."""
+    if w.is_cuda or w.dtype != torch.float32 or w.dim() != 2:
+        raise ValueError("mxfp4_pack wants a CPU float32 matrix")
+    w = w.contiguous()
+    rows, k = w.shape
+    q = torch.empty((rows, k // 2), dtype=torch.uint8)
+    s = torch.empty((rows, k // 32), dtype=torch.uint8)
+    check(lib().mxfp4_pack(_ptr(w), rows, k, _ptr(q), _ptr(s), 0), "mxfp4_pack")
+    return q, s
+
+
+def mxfp4_pack_device(w, q=None, s=None, stream=None):
+    """Device packer: w CUDA float32 [rows, k] -> q, s on the same device."""
+    if not w.is_cuda or w.dtype != torch.float32 or w.dim() != 2:
+        raise ValueError("mxfp4_pack_device wants a CUDA float32 matrix")
+    w = w.contiguous()
+    rows, k = w.shape
+    if q is None:
+        q = torch.empty((rows, k // 2), dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty((rows, k // 32), dtype=torch.uint8, device=w.device)
+    check(lib().mxfp4_pack_device(_stream(stream), _ptr(w), rows, k, _ptr(q), _ptr(s), 0),
+          "mxfp4_pack_device")
+    return q, s

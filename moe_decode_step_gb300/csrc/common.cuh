@@ -1,0 +1,155 @@
+// Device helpers shared by the MoE decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------
+// Loads.  Weights are streamed once per forward: no L1 allocation.  Routing
+// tables and activations written by an earlier kernel are read with plain
+// coherent loads (ld.global.cg / default), never the non-coherent path.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream_u128(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u64(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u8(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP4 decode.  cvt.rn.f16x2.e2m1x2 turns one byte (two E2M1 codes) into an
+// f16x2; every E2M1 value is exact in f16.  E8M0 byte -> 2^(s-127) as fp32
+// (byte 0 is the subnormal 2^-127).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// c + a.lo*b.lo + a.hi*b.hi with f16 inputs, exact products, fp32 accumulate.
+__device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float c) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+
+// Same with bf16 inputs.
+__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float c) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// fp32 -> bf16 bits, round to nearest even (inputs here are finite).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// Two fp32 -> f16x2 (lo = a, hi = b), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// 2^e for integer e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Exponent shift that keeps |v| <= amax below 2^15 after scaling by 2^-shift,
+// so f16 (max 65504) never overflows: 0 for amax < 2^15.
+__device__ __forceinline__ int f16_shift_for_amax(float amax) {
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // floor(log2) for normals
+  return e >= 15 ? e - 14 : 0;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Butterfly reduce-scatter of V = 2^m per-lane partials over the warp.  On
+// return, lane l holds the full warp sum of value index
+//   vidx(l) = l >> (5 - m)            (the top m bits of the lane id)
+// and every lane in a group of 2^(5-m) consecutive lanes holds the same value.
+// Costs V - 1 + (5 - m) shuffles instead of 5 V.
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
+  int width = V;
+  int bit = 16;
+#pragma unroll
+  for (int step = 0; (1 << step) < V; ++step) {
+    const int half = width >> 1;
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+      if (i < half) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+      }
+    }
+    width = half;
+    bit >>= 1;
+  }
+  float r = v[0];
+#pragma unroll
+  for (int b = 1; b <= 16; b <<= 1) {
+    if (b <= bit) r += __shfl_xor_sync(0xffffffffu, r, b);
+  }
+  return r;
+}
+
+}  // namespace moe

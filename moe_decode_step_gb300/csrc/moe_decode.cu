@@ -1,0 +1,599 @@
+// C ABI of the MoE decode layer (see include/moe_decode.h for the contract).
+//
+// One forward = six kernels on two streams:
+//   main stream : router_topk -> routed_fc1 -> routed_fc2 -> [join] -> tail
+//   side stream : shared_fc1 -> shared_fc2                 (forked at entry)
+//   third stream: l2_prefetch of the next layer's dense weights (optional)
+// No allocation, no host synchronisation: capturable into a CUDA graph.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "moe_decode.h"
+#include "common.cuh"
+#include "mxfp4.cuh"
+#include "router.cuh"
+#include "routed.cuh"
+#include "shared.cuh"
+#include "tail.cuh"
+
+using namespace moe;
+
+namespace {
+
+std::atomic<int> g_last_cuda_error{0};
+
+inline int cuda_fail(cudaError_t e) {
+  g_last_cuda_error.store((int)e);
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call)                       \
+  do {                                       \
+    cudaError_t e_ = (call);                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+enum { kTimeRouterStart, kTimeRouterEnd, kTimeFc1End, kTimeFc2End, kTimeTailEnd, kTimeSharedStart,
+       kTimeSharedEnd, kNumTimeEvents };
+
+struct Workspace {
+  float* logits;
+  unsigned* done;
+  int* x_shift;
+  int32_t* topk_idx;
+  float* topk_w;
+  int* n_active;
+  int* active_expert;
+  int* active_off;
+  int* pair_list;
+  unsigned* h_amax;
+  int* work;
+  float* h;
+  float* y_pair;
+  float* hs;
+  float* y_s;
+  float* z;
+  float* psum;
+  unsigned* ticket;
+  int* status;
+  uint16_t* x_stage;
+  uint16_t* res_stage;
+  uint16_t* out_stage;
+};
+
+}  // namespace
+
+struct moe_layer {
+  moe_dims_t dims;
+  moe_weights_t w;
+  int device = 0;
+  int n_sm = 0;
+  void* ws_base = nullptr;
+  Workspace ws{};
+  cudaStream_t side = nullptr, pref = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_pref = nullptr;
+  cudaEvent_t ev_time[kNumTimeEvents] = {};
+  bool timing = false, timed_once = false;
+  moe_layer* next = nullptr;
+  // launch shapes
+  int tail_slices = 0;
+  int fc1_threads = 0, fc2_threads = 0, sh1_threads = 0, sh2_threads = 0;
+  int fc1_grid[3] = {}, fc2_grid[2] = {}, sh1_grid[3] = {}, sh2_grid[3] = {};  // by RMAX 1/2/4
+  size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
+};
+
+namespace {
+
+template <typename T>
+T* carve(char*& p, size_t count) {
+  T* r = reinterpret_cast<T*>(p);
+  p += (count * sizeof(T) + 255) & ~size_t(255);
+  return r;
+}
+
+size_t workspace_bytes(const moe_dims_t& d, int tail_slices, Workspace* ws, char* base) {
+  char* p = base;
+  const size_t B = d.max_batch, E = d.n_experts, k = d.top_k, P = B * k;
+  Workspace w;
+  w.logits = carve<float>(p, B * E);
+  w.done = carve<unsigned>(p, 1);
+  w.x_shift = carve<int>(p, B);
+  w.topk_idx = carve<int32_t>(p, P);
+  w.topk_w = carve<float>(p, P);
+  w.n_active = carve<int>(p, 1);
+  w.active_expert = carve<int>(p, E);
+  w.active_off = carve<int>(p, E + 1);
+  w.pair_list = carve<int>(p, P);
+  w.h_amax = carve<unsigned>(p, P);
+  w.work = carve<int>(p, 4);
+  w.h = carve<float>(p, P * d.f);
+  w.y_pair = carve<float>(p, P * d.d);
+  w.hs = carve<float>(p, B * d.f_shared);
+  w.y_s = carve<float>(p, B * d.d);
+  w.z = carve<float>(p, B * d.d);
+  w.psum = carve<float>(p, B * tail_slices);
+  w.ticket = carve<unsigned>(p, B);
+  w.status = carve<int>(p, 1);
+  w.x_stage = carve<uint16_t>(p, B * d.d);
+  w.res_stage = carve<uint16_t>(p, B * d.d);
+  w.out_stage = carve<uint16_t>(p, B * d.d);
+  if (ws) *ws = w;
+  return (size_t)(p - base);
+}
+
+int validate_dims(const moe_dims_t& d) {
+  if (d.d <= 0 || d.d % 256 != 0 || d.d > 8192) return MOE_ERR_INVALID_ARG;
+  if (d.f <= 0 || d.f % 256 != 0 || d.f > 4096) return MOE_ERR_INVALID_ARG;
+  if (d.f_shared <= 0 || d.f_shared % 256 != 0 || d.f_shared > 4096) return MOE_ERR_INVALID_ARG;
+  if (d.top_k < 1 || d.top_k > 32) return MOE_ERR_INVALID_ARG;
+  if (d.n_experts < d.top_k || d.n_experts > 1024) return MOE_ERR_INVALID_ARG;
+  if (d.max_batch < 1 || d.max_batch > 64) return MOE_ERR_INVALID_ARG;
+  if (!(d.routed_scale > 0.f) || !(d.rms_eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (d.mxfp4_layout != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// KW warps split K (ceil(K / elements per warp)); up to 8 warps per CTA.
+int shape_threads(int K, int per_warp) {
+  const int KW = (K + per_warp - 1) / per_warp;
+  return 32 * KW * std::max(1, 8 / KW);
+}
+
+template <typename K>
+int grid_for(K kernel, int threads, int n_sm) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  return occ * n_sm;
+}
+
+int rmax_fc1(int B) { return B == 1 ? 1 : (B <= 8 ? 2 : 4); }
+int rmax_fc2(int B) { return B == 1 ? 1 : 2; }
+int rmax_shared(int B) { return B == 1 ? 1 : (B <= 3 ? 2 : 4); }
+
+RouterArgs router_args(moe_layer* L, const void* x, int B, int32_t* idx, float* w) {
+  RouterArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.wr = static_cast<const uint16_t*>(L->w.router_w);
+  a.bias = L->w.router_bias;
+  a.B = B;
+  a.d = L->dims.d;
+  a.E = L->dims.n_experts;
+  a.k = L->dims.top_k;
+  a.routed_scale = L->dims.routed_scale;
+  a.logits = L->ws.logits;
+  a.done = L->ws.done;
+  a.x_shift = L->ws.x_shift;
+  a.topk_idx = idx;
+  a.topk_w = w;
+  a.n_active = L->ws.n_active;
+  a.active_expert = L->ws.active_expert;
+  a.active_off = L->ws.active_off;
+  a.pair_list = L->ws.pair_list;
+  a.h_amax = L->ws.h_amax;
+  a.work = L->ws.work;
+  return a;
+}
+
+int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* idx, float* w) {
+  const RouterArgs a = router_args(L, x, B, idx, w);
+  const int grid = (L->dims.n_experts + kRouterExpertsPerCta - 1) / kRouterExpertsPerCta;
+  const int threads = kRouterWarps * 32;
+  if (B == 1) router_topk_kernel<1><<<grid, threads, 0, st>>>(a);
+  else if (B == 2) router_topk_kernel<2><<<grid, threads, 0, st>>>(a);
+  else if (B <= 4) router_topk_kernel<4><<<grid, threads, 0, st>>>(a);
+  else router_topk_kernel<8><<<grid, threads, 0, st>>>(a);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+RoutedArgs routed_args(moe_layer* L, const void* x, bool fc1) {
+  RoutedArgs a;
+  const moe_dims_t& d = L->dims;
+  a.q = fc1 ? L->w.w_gu_q : L->w.w_d_q;
+  a.s = fc1 ? L->w.w_gu_s : L->w.w_d_s;
+  a.q_stride = fc1 ? L->q_gu_stride : L->q_d_stride;
+  a.s_stride = fc1 ? L->s_gu_stride : L->s_d_stride;
+  a.K = fc1 ? d.d : d.f;
+  a.N = fc1 ? d.f : d.d;
+  a.k = d.top_k;
+  a.x = static_cast<const uint16_t*>(x);
+  a.x_shift = L->ws.x_shift;
+  a.h = L->ws.h;
+  a.h_amax = L->ws.h_amax;
+  a.out = fc1 ? L->ws.h : L->ws.y_pair;
+  a.out_amax = L->ws.h_amax;
+  a.n_active = L->ws.n_active;
+  a.active_expert = L->ws.active_expert;
+  a.active_off = L->ws.active_off;
+  a.pair_list = L->ws.pair_list;
+  a.work = L->ws.work + (fc1 ? 0 : 1);
+  return a;
+}
+
+int launch_routed(moe_layer* L, cudaStream_t st, const void* x, int B) {
+  const RoutedArgs a1 = routed_args(L, x, true);
+  switch (rmax_fc1(B)) {
+    case 1: routed_fc1_kernel<1><<<L->fc1_grid[0], L->fc1_threads, 0, st>>>(a1); break;
+    case 2: routed_fc1_kernel<2><<<L->fc1_grid[1], L->fc1_threads, 0, st>>>(a1); break;
+    default: routed_fc1_kernel<4><<<L->fc1_grid[2], L->fc1_threads, 0, st>>>(a1); break;
+  }
+  MOE_CUDA(cudaGetLastError());
+  if (L->timing) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeFc1End], st));
+  const RoutedArgs a2 = routed_args(L, x, false);
+  if (rmax_fc2(B) == 1) routed_fc2_kernel<1><<<L->fc2_grid[0], L->fc2_threads, 0, st>>>(a2);
+  else routed_fc2_kernel<2><<<L->fc2_grid[1], L->fc2_threads, 0, st>>>(a2);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_shared(moe_layer* L, cudaStream_t st, const void* x, int B) {
+  const moe_dims_t& d = L->dims;
+  SharedArgs a1;
+  a1.w = static_cast<const uint16_t*>(L->w.shared_gu);
+  a1.K = d.d;
+  a1.N = d.f_shared;
+  a1.B = B;
+  a1.x = static_cast<const uint16_t*>(x);
+  a1.hs = nullptr;
+  a1.out = L->ws.hs;
+  SharedArgs a2;
+  a2.w = static_cast<const uint16_t*>(L->w.shared_d);
+  a2.K = d.f_shared;
+  a2.N = d.d;
+  a2.B = B;
+  a2.x = nullptr;
+  a2.hs = L->ws.hs;
+  a2.out = L->ws.y_s;
+  switch (rmax_shared(B)) {
+    case 1:
+      shared_fc1_kernel<1><<<L->sh1_grid[0], L->sh1_threads, 0, st>>>(a1);
+      MOE_CUDA(cudaGetLastError());
+      shared_fc2_kernel<1><<<L->sh2_grid[0], L->sh2_threads, 0, st>>>(a2);
+      break;
+    case 2:
+      shared_fc1_kernel<2><<<L->sh1_grid[1], L->sh1_threads, 0, st>>>(a1);
+      MOE_CUDA(cudaGetLastError());
+      shared_fc2_kernel<2><<<L->sh2_grid[1], L->sh2_threads, 0, st>>>(a2);
+      break;
+    default:
+      shared_fc1_kernel<4><<<L->sh1_grid[2], L->sh1_threads, 0, st>>>(a1);
+      MOE_CUDA(cudaGetLastError());
+      shared_fc2_kernel<4><<<L->sh2_grid[2], L->sh2_threads, 0, st>>>(a2);
+      break;
+  }
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg) {
+  TailArgs a;
+  a.y_pair = L->ws.y_pair;
+  a.topk_w = L->ws.topk_w;
+  a.y_s = L->ws.y_s;
+  a.gamma = static_cast<const uint16_t*>(L->w.rms_gamma);
+  a.residual = static_cast<uint16_t*>(residual);
+  a.out = static_cast<uint16_t*>(out);
+  a.z = L->ws.z;
+  a.psum = L->ws.psum;
+  a.ticket = L->ws.ticket;
+  a.y_r_dbg = y_r_dbg;
+  a.B = B;
+  a.d = L->dims.d;
+  a.k = L->dims.top_k;
+  a.eps = L->dims.rms_eps;
+  tail_kernel<<<dim3(L->tail_slices, B), kTailThreads, 0, st>>>(a);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_prefetch(moe_layer* L) {
+  moe_layer* n = L->next;
+  if (!n) return MOE_OK;
+  PrefetchArgs a;
+  a.n = 3;
+  a.ptr[0] = static_cast<const char*>(n->w.router_w);
+  a.bytes[0] = (size_t)n->dims.n_experts * n->dims.d * 2;
+  a.ptr[1] = static_cast<const char*>(n->w.shared_gu);
+  a.bytes[1] = (size_t)2 * n->dims.f_shared * n->dims.d * 2;
+  a.ptr[2] = static_cast<const char*>(n->w.shared_d);
+  a.bytes[2] = (size_t)n->dims.d * n->dims.f_shared * 2;
+  MOE_CUDA(cudaStreamWaitEvent(L->pref, L->ev_fork, 0));
+  l2_prefetch_kernel<<<L->n_sm, 256, 0, L->pref>>>(a);
+  MOE_CUDA(cudaGetLastError());
+  MOE_CUDA(cudaEventRecord(L->ev_pref, L->pref));
+  return MOE_OK;
+}
+
+int check_forward_args(moe_layer* L, const void* x, int B) {
+  if (!L || !x) return MOE_ERR_INVALID_ARG;
+  if (B < 1 || B > L->dims.max_batch) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* residual, void* out,
+                 float* y_r_dbg, float* y_s_dbg, float* h_dbg) {
+  int rc = check_forward_args(L, x, B);
+  if (rc) return rc;
+  if (!residual || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(residual) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+  const bool tm = L->timing;
+  MOE_CUDA(cudaEventRecord(L->ev_fork, st));
+  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeRouterStart], st));
+  if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
+  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeRouterEnd], st));
+  // side stream: shared expert, overlapping router + routed experts
+  MOE_CUDA(cudaStreamWaitEvent(L->side, L->ev_fork, 0));
+  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeSharedStart], L->side));
+  if ((rc = launch_shared(L, L->side, x, B))) return rc;
+  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeSharedEnd], L->side));
+  MOE_CUDA(cudaEventRecord(L->ev_join, L->side));
+  if ((rc = launch_prefetch(L))) return rc;
+  if ((rc = launch_routed(L, st, x, B))) return rc;
+  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeFc2End], st));
+  MOE_CUDA(cudaStreamWaitEvent(st, L->ev_join, 0));
+  if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
+  if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg))) return rc;
+  if (tm) {
+    MOE_CUDA(cudaEventRecord(L->ev_time[kTimeTailEnd], st));
+    L->timed_once = true;
+  }
+  const size_t P = (size_t)B * L->dims.top_k;
+  if (y_s_dbg)
+    MOE_CUDA(cudaMemcpyAsync(y_s_dbg, L->ws.y_s, (size_t)B * L->dims.d * 4,
+                             cudaMemcpyDeviceToDevice, st));
+  if (h_dbg)
+    MOE_CUDA(cudaMemcpyAsync(h_dbg, L->ws.h, P * L->dims.f * 4, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported (use another implementation)";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_ALLOC: return "allocation failed";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_layer_t* out) {
+  if (!dims || !weights || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_dims(*dims);
+  if (rc) return rc;
+  const moe_weights_t& w = *weights;
+  const void* ptrs[] = {w.router_w, w.router_bias, w.w_gu_q, w.w_gu_s, w.w_d_q,
+                        w.w_d_s,    w.shared_gu,   w.shared_d, w.rms_gamma};
+  for (const void* p : ptrs) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_UNSUPPORTED;
+  }
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  MOE_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
+
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_ALLOC;
+  L->dims = *dims;
+  L->w = w;
+  L->device = dev;
+  L->n_sm = prop.multiProcessorCount;
+  L->tail_slices = (dims->d + kTailThreads - 1) / kTailThreads;
+  const size_t f = dims->f, dd = dims->d;
+  L->q_gu_stride = 2 * f * dd / 2;
+  L->s_gu_stride = 2 * f * dd / 32;
+  L->q_d_stride = dd * f / 2;
+  L->s_d_stride = dd * f / 32;
+  const size_t bytes = workspace_bytes(*dims, L->tail_slices, nullptr, nullptr);
+  if (cudaMalloc(&L->ws_base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete L;
+    return MOE_ERR_ALLOC;
+  }
+  workspace_bytes(*dims, L->tail_slices, &L->ws, static_cast<char*>(L->ws_base));
+  auto fail = [&](cudaError_t e) {
+    moe_layer_destroy(L);
+    return cuda_fail(e);
+  };
+  cudaError_t e;
+  if ((e = cudaMemset(L->ws_base, 0, bytes)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamCreateWithFlags(&L->side, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamCreateWithFlags(&L->pref, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
+  if ((e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+  if ((e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+  if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+  for (int i = 0; i < kNumTimeEvents; ++i)
+    if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
+  L->fc1_threads = shape_threads(dims->d, 1024);
+  L->fc2_threads = shape_threads(dims->f, 512);
+  L->sh1_threads = shape_threads(dims->d, 1024);
+  L->sh2_threads = shape_threads(dims->f_shared, 512);
+  L->fc1_grid[0] = grid_for(routed_fc1_kernel<1>, L->fc1_threads, L->n_sm);
+  L->fc1_grid[1] = grid_for(routed_fc1_kernel<2>, L->fc1_threads, L->n_sm);
+  L->fc1_grid[2] = grid_for(routed_fc1_kernel<4>, L->fc1_threads, L->n_sm);
+  L->fc2_grid[0] = grid_for(routed_fc2_kernel<1>, L->fc2_threads, L->n_sm);
+  L->fc2_grid[1] = grid_for(routed_fc2_kernel<2>, L->fc2_threads, L->n_sm);
+  {
+    const int rows1 = (L->sh1_threads / 32 / ((dims->d + 1023) / 1024)) * kSh1RPW;
+    const int items1 = (dims->f_shared + rows1 - 1) / rows1;
+    const int rows2 = (L->sh2_threads / 32 / ((dims->f_shared + 511) / 512)) * kSh2RPW;
+    const int items2 = (dims->d + rows2 - 1) / rows2;
+    L->sh1_grid[0] = std::min(items1, grid_for(shared_fc1_kernel<1>, L->sh1_threads, L->n_sm));
+    L->sh1_grid[1] = std::min(items1, grid_for(shared_fc1_kernel<2>, L->sh1_threads, L->n_sm));
+    L->sh1_grid[2] = std::min(items1, grid_for(shared_fc1_kernel<4>, L->sh1_threads, L->n_sm));
+    L->sh2_grid[0] = std::min(items2, grid_for(shared_fc2_kernel<1>, L->sh2_threads, L->n_sm));
+    L->sh2_grid[1] = std::min(items2, grid_for(shared_fc2_kernel<2>, L->sh2_threads, L->n_sm));
+    L->sh2_grid[2] = std::min(items2, grid_for(shared_fc2_kernel<4>, L->sh2_threads, L->n_sm));
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+int moe_layer_destroy(moe_layer_t L) {
+  if (!L) return MOE_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(L->device);
+  cudaDeviceSynchronize();
+  if (L->side) cudaStreamDestroy(L->side);
+  if (L->pref) cudaStreamDestroy(L->pref);
+  if (L->ev_fork) cudaEventDestroy(L->ev_fork);
+  if (L->ev_join) cudaEventDestroy(L->ev_join);
+  if (L->ev_pref) cudaEventDestroy(L->ev_pref);
+  for (int i = 0; i < kNumTimeEvents; ++i)
+    if (L->ev_time[i]) cudaEventDestroy(L->ev_time[i]);
+  if (L->ws_base) cudaFree(L->ws_base);
+  cudaSetDevice(prev);
+  delete L;
+  return MOE_OK;
+}
+
+int moe_router_topk(moe_layer_t L, void* stream, const void* x, int B, int32_t* idx, float* w) {
+  int rc = check_forward_args(L, x, B);
+  if (rc) return rc;
+  if (!idx || !w) return MOE_ERR_INVALID_ARG;
+  return launch_router(L, static_cast<cudaStream_t>(stream), x, B, idx, w);
+}
+
+int moe_decode_forward(moe_layer_t L, void* stream, const void* x, int B, void* residual,
+                       void* out) {
+  return forward_impl(L, static_cast<cudaStream_t>(stream), x, B, residual, out, nullptr, nullptr,
+                      nullptr);
+}
+
+int moe_decode_forward_debug(moe_layer_t L, void* stream, const void* x, int B, void* residual,
+                             void* out, float* y_routed, float* y_shared, float* h) {
+  return forward_impl(L, static_cast<cudaStream_t>(stream), x, B, residual, out, y_routed,
+                      y_shared, h);
+}
+
+int moe_decode_forward_host(moe_layer_t L, void* stream, const void* x_host, int B,
+                            void* residual_host, void* out_host) {
+  if (!L || !x_host || !residual_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (B < 1 || B > L->dims.max_batch) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)B * L->dims.d * 2;
+  MOE_CUDA(cudaMemcpyAsync(L->ws.x_stage, x_host, bytes, cudaMemcpyHostToDevice, st));
+  MOE_CUDA(cudaMemcpyAsync(L->ws.res_stage, residual_host, bytes, cudaMemcpyHostToDevice, st));
+  int rc = moe_decode_forward(L, stream, L->ws.x_stage, B, L->ws.res_stage, L->ws.out_stage);
+  if (rc) return rc;
+  MOE_CUDA(cudaMemcpyAsync(residual_host, L->ws.res_stage, bytes, cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaMemcpyAsync(out_host, L->ws.out_stage, bytes, cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float* out) {
+  if (!L || !out || expert < 0 || expert >= L->dims.n_experts || (which != 0 && which != 1))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t rows = which == 0 ? 2LL * L->dims.f : L->dims.d;
+  const int64_t k = which == 0 ? L->dims.d : L->dims.f;
+  const uint8_t* q = (which == 0 ? L->w.w_gu_q : L->w.w_d_q) +
+                     (size_t)expert * (which == 0 ? L->q_gu_stride : L->q_d_stride);
+  const uint8_t* s = (which == 0 ? L->w.w_gu_s : L->w.w_d_s) +
+                     (size_t)expert * (which == 0 ? L->s_gu_stride : L->s_d_stride);
+  const int64_t blocks = std::min<int64_t>((rows * (k / 32) + 255) / 256, 4096);
+  mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(q, s, rows,
+                                                                                       k, out);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int moe_set_prefetch_next(moe_layer_t L, moe_layer_t next) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (next && next->device != L->device) return MOE_ERR_INVALID_ARG;
+  L->next = next;
+  return MOE_OK;
+}
+
+int moe_layer_status(moe_layer_t L, int* device_status) {
+  if (!L || !device_status) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(cudaStreamSynchronize(L->side));
+  MOE_CUDA(cudaStreamSynchronize(L->pref));
+  MOE_CUDA(cudaDeviceSynchronize());
+  int v = 0;
+  MOE_CUDA(cudaMemcpy(&v, L->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(L->ws.status, 0, sizeof(int)));
+  *device_status = v;
+  return MOE_OK;
+}
+
+int moe_set_timing(moe_layer_t L, int enable) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  L->timing = enable != 0;
+  L->timed_once = false;
+  return MOE_OK;
+}
+
+int moe_get_timing(moe_layer_t L, float* us, int n) {
+  if (!L || !us || n < 0) return MOE_ERR_INVALID_ARG;
+  if (!L->timed_once) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(cudaEventSynchronize(L->ev_time[kTimeTailEnd]));
+  MOE_CUDA(cudaEventSynchronize(L->ev_time[kTimeSharedEnd]));
+  float t[6];
+  MOE_CUDA(cudaEventElapsedTime(&t[0], L->ev_time[kTimeRouterStart], L->ev_time[kTimeRouterEnd]));
+  MOE_CUDA(cudaEventElapsedTime(&t[1], L->ev_time[kTimeRouterEnd], L->ev_time[kTimeFc1End]));
+  MOE_CUDA(cudaEventElapsedTime(&t[2], L->ev_time[kTimeFc1End], L->ev_time[kTimeFc2End]));
+  MOE_CUDA(cudaEventElapsedTime(&t[3], L->ev_time[kTimeSharedStart], L->ev_time[kTimeSharedEnd]));
+  MOE_CUDA(cudaEventElapsedTime(&t[4], L->ev_time[kTimeFc2End], L->ev_time[kTimeTailEnd]));
+  MOE_CUDA(cudaEventElapsedTime(&t[5], L->ev_time[kTimeRouterStart], L->ev_time[kTimeTailEnd]));
+  for (int i = 0; i < n && i < 6; ++i) us[i] = t[i] * 1000.f;
+  return MOE_OK;
+}
+
+int moe_launches_per_forward(moe_layer_t L, int B) {
+  if (!L || B < 1 || B > L->dims.max_batch) return -1;
+  return 6;   // router, shared FC1, shared FC2, routed FC1, routed FC2, tail
+}
+
+size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {
+  if (rows < 0 || k <= 0 || k % 32 != 0 || layout != 0) return 0;
+  if (scale_bytes) *scale_bytes = (size_t)(rows * (k / 32));
+  return (size_t)(rows * (k / 2));
+}
+
+int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, int layout) {
+  if (!w || !q || !s || rows < 0 || k <= 0 || k % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (layout != 0) return MOE_ERR_UNSUPPORTED;
+  const int64_t nb = k / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b)
+      s[r * nb + b] = mx_pack_block(w + r * k + b * 32, q + r * (k / 2) + b * 16);
+  return MOE_OK;
+}
+
+int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
+                      uint8_t* s, int layout) {
+  if (!w || !q || !s || rows < 0 || k <= 0 || k % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (layout != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(q)) return MOE_ERR_UNSUPPORTED;
+  const int64_t total = rows * (k / 32);
+  if (total == 0) return MOE_OK;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
+  mxfp4_pack_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(w, rows, k, q,
+                                                                                     s);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+}  // extern "C"

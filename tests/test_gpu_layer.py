@@ -1,0 +1,162 @@
+"""GPU parity of the whole layer against the CPU oracle on the tiny layer
+(d=1024, f=256, 64 experts, top-4) at several batch sizes, plus determinism,
+CUDA-graph capture, the host-buffer entry point and error codes."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_decode_step_gb300 as M
+from gen.configs import CONFIGS
+from moe_decode_step_gb300 import synthetic
+
+from _parity import assert_close, bf16_ulp_distance
+
+pytestmark = pytest.mark.gpu
+
+TINY = CONFIGS["tiny_b1"]
+BATCHES = [1, 3, 8, 17, 64]
+
+
+def tiny_cfg(B):
+    return dataclasses.replace(TINY, name=f"tiny_b{B}", B=B)
+
+
+@pytest.fixture(scope="module")
+def tiny_layer():
+    layer = synthetic.make_layer(TINY, max_batch=64)
+    yield layer
+    layer.close()
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_against_oracle(ref, idx, w, out, res_out, y_r, y_s, h, rows):
+    k = idx.shape[1]
+    for b in rows:
+        assert sorted(idx[b].tolist()) == sorted(ref["idx"][b].tolist()), b
+        order = {int(e): j for j, e in enumerate(ref["idx"][b])}
+        for j in range(k):
+            jr = order[int(idx[b, j])]
+            assert abs(w[b, j] - ref["w"][b, jr]) <= 1e-6
+            if h is not None:
+                assert_close(h[b, j], ref["h"][b, jr], 1e-3, 1e-4, what=f"h[{b},{j}]")
+    r = list(rows)
+    assert_close(y_s[r], ref["y_s"][r], 1e-4, 1e-5, what="y_shared")
+    assert_close(y_r[r], ref["y_r"][r], 2e-3, 5e-4, what="y_routed")
+    m_out = assert_close(out[r], ref["out"][r], what="out")
+    m_res = assert_close(res_out[r], ref["z"][r], what="residual")
+    assert bf16_ulp_distance(out[r], ref["out_bf16"][r]).max() <= 1
+    assert bf16_ulp_distance(res_out[r], ref["residual_bf16"][r]).max() <= 1
+    return m_out, m_res
+
+
+@pytest.mark.parametrize("B", BATCHES)
+def test_tiny_layer_matches_oracle(tiny_layer, B):
+    cfg = tiny_cfg(B)
+    inp = oracle.clean_inputs(cfg)
+    ref = oracle.forward(inp)
+    x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
+    assert np.array_equal(_np(x), inp.x) and np.array_equal(_np(res), inp.residual)
+    idx, w = tiny_layer.router_topk(x)
+    out, y_r, y_s, h = tiny_layer.forward_debug(x, res)
+    torch.cuda.synchronize()
+    assert tiny_layer.status() == 0
+    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), _np(out),
+                         _np(res), _np(y_r), _np(y_s), _np(h), range(B))
+
+
+def test_router_weights_sum_to_routed_scale(tiny_layer):
+    cfg = tiny_cfg(64)
+    x, _ = synthetic.make_activations(cfg)
+    _, w = tiny_layer.router_topk(x)
+    np.testing.assert_allclose(w.sum(dim=1).cpu().numpy(), 2.5, rtol=2e-6)
+    assert bool((w > 0).all())
+
+
+def test_forward_is_deterministic(tiny_layer):
+    cfg = tiny_cfg(17)
+    x, res = synthetic.make_activations(cfg)
+    outs = []
+    for _ in range(3):
+        r = res.clone()
+        o = tiny_layer.forward(x, r)
+        outs.append((o.clone(), r.clone()))
+    torch.cuda.synchronize()
+    for o, r in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(r.view(torch.int16), outs[0][1].view(torch.int16))
+
+
+def test_cuda_graph_replay_equals_eager(tiny_layer):
+    cfg = tiny_cfg(8)
+    x, res = synthetic.make_activations(cfg)
+    r_e = res.clone()
+    o_e = tiny_layer.forward(x, r_e)
+    r_g = res.clone()
+    o_g = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tiny_layer.forward(x, r_g.clone(), o_g)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tiny_layer.forward(x, r_g, o_g)
+    for _ in range(2):
+        r_g.copy_(res)
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g.view(torch.int16), o_e.view(torch.int16))
+    assert torch.equal(r_g.view(torch.int16), r_e.view(torch.int16))
+
+
+def test_host_buffer_entry_matches_device_entry(tiny_layer):
+    cfg = tiny_cfg(5)
+    x, res = synthetic.make_activations(cfg)
+    r_d = res.clone()
+    o_d = tiny_layer.forward(x, r_d)
+    xh = x.cpu().pin_memory()
+    rh = res.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    tiny_layer.forward_host(xh, rh, oh)
+    assert torch.equal(oh.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(rh.view(torch.int16), r_d.cpu().view(torch.int16))
+
+
+def test_batch_outside_range_is_unsupported(tiny_layer):
+    x = torch.zeros((65, 1024), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(M.MoEError) as e:
+        tiny_layer.forward(x, x.clone())
+    assert e.value.code == M.MOE_ERR_UNSUPPORTED
+    x0 = torch.zeros((0, 1024), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(M.MoEError) as e:
+        tiny_layer.router_topk(x0)
+    assert e.value.code == M.MOE_ERR_UNSUPPORTED
+    with pytest.raises(M.MoEError) as e:   # misaligned activation pointer
+        xb = torch.zeros(1024 * 2 + 1, dtype=torch.bfloat16, device="cuda")[1:1025].view(1, 1024)
+        tiny_layer.router_topk(xb)
+    assert e.value.code == M.MOE_ERR_UNSUPPORTED
+    assert tiny_layer.status() == 0
+
+
+def test_zero_down_weights_leave_rmsnorm_of_residual_plus_shared():
+    w = synthetic.make_weights(TINY)
+    w["w_d_s"].zero_()
+    w["w_d_q"].zero_()
+    layer = synthetic.make_layer(TINY, max_batch=4, weights=w)
+    cfg = tiny_cfg(4)
+    inp = oracle.clean_inputs(cfg)
+    ref = oracle.forward(inp)
+    x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
+    out, y_r, y_s, _ = layer.forward_debug(x, res)
+    torch.cuda.synchronize()
+    assert float(y_r.abs().max()) == 0.0
+    z = inp.residual + ref["y_s"]
+    want = z / np.sqrt((z ** 2).mean(axis=1, keepdims=True) + TINY.rms_eps) * inp.gamma
+    assert_close(_np(out), want, what="out with zero experts")
+    layer.close()
