@@ -190,33 +190,76 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def time_layer(layer, cfg, x, res0, steps, warmup, flush, timing=True):
-    """Event-timed forwards (median us) with L2 flushed between steps.
-    Returns (per-step us list, per-step phase lists)."""
+class L2Flush:
+    """Evict L2 between timed steps: write a buffer of 2x L2, then read a second
+    one, so no dirty lines from the flush are written back inside the timed
+    region."""
+
+    def __init__(self, device):
+        import torch
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.w = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+        self.r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+        self.i = 0
+
+    def __call__(self):
+        import torch
+        self.i += 1
+        self.w.fill_(self.i & 0xFF)
+        torch.sum(self.r, out=self.sink)
+
+
+SLEEP_CYCLES = 1_000_000   # ~0.5 ms head start so the host enqueues a whole forward
+
+
+def time_layer(layer, x, res0, steps, warmup, flush, graph=True):
+    """Device time of one forward per step (CUDA events on the launching stream),
+    L2 flushed before every step.  graph=True replays a captured CUDA graph of
+    the forward (the production mode: no host launch gaps); graph=False runs the
+    eager forward behind a sleep kernel so that the host has enqueued all of it
+    before the GPU reaches it.  Returns (us per step, per-phase us per step)."""
     import torch
     res = res0.clone()
     out = torch.empty_like(x)
-    st = torch.cuda.current_stream()
+    cur = torch.cuda.current_stream()
+    layer.set_timing(True)
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            layer.forward(x, res, out)
+        cur.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer.forward(x, res, out)
+        run = g.replay
+    else:
+        def run():
+            layer.forward(x, res, out)
     for _ in range(warmup):
         res.copy_(res0)
-        flush.zero_()
-        layer.forward(x, res, out)
+        flush()
+        run()
     torch.cuda.synchronize()
-    layer.set_timing(timing)
     times, phases = [], []
-    for i in range(steps):
+    for _ in range(steps):
         res.copy_(res0)
-        flush.fill_(i & 0xFF)
+        flush()
+        if not graph:
+            torch.cuda._sleep(SLEEP_CYCLES)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(st)
-        layer.forward(x, res, out)
-        b.record(st)
+        a.record(cur)
+        run()
+        b.record(cur)
         b.synchronize()
         times.append(a.elapsed_time(b) * 1000.0)
-        if timing:
-            phases.append(layer.get_timing())
+        phases.append(layer.get_timing())
     layer.set_timing(False)
+    if graph:
+        del g
     return times, phases
 
 
@@ -230,13 +273,13 @@ def time_e2e(layer, cfg, x, res0, steps, warmup, flush):
     oh = torch.empty_like(r0).pin_memory()
     for _ in range(warmup):
         rh.copy_(r0)
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         layer.forward_host(xh, rh, oh)
     times = []
     for i in range(steps):
         rh.copy_(r0)
-        flush.fill_(i & 0xFF)
+        flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         layer.forward_host(xh, rh, oh)
@@ -301,8 +344,7 @@ def run_ours(args, rank, world, local):
     init_dist(world, "nccl")
     cfg = CONFIGS[args.config]
     peak, peak_kind = measured_peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     layer = synthetic.make_layer(cfg)
     x, res0 = synthetic.make_activations(cfg)
@@ -314,10 +356,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with ClockSampler(local) as clk:
-        times, phases = time_layer(layer, cfg, x, res0, args.steps, args.warmup, flush)
+        times, phases = time_layer(layer, x, res0, args.steps, args.warmup, flush, graph=True)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
+    eager_times, eager_phases = time_layer(layer, x, res0, max(5, args.steps // 2),
+                                           max(3, args.warmup), flush, graph=False)
 
     us = reduce_max(statistics.median(times), world, dev)
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
@@ -347,7 +391,7 @@ def run_ours(args, rank, world, local):
             i2, _ = L2.router_topk(x2)
             nd2 = int(torch.unique(i2).numel())
             st2 = max(5, min(args.steps, 20))
-            t2, p2 = time_layer(L2, c2, x2, r2, st2, max(3, args.warmup), flush)
+            t2, p2 = time_layer(L2, x2, r2, st2, max(3, args.warmup), flush, graph=True)
             v2 = reduce_max(statistics.median(t2), world, dev)
             b2 = bytes_touched(c2, nd2, c2.B)
             batches[str(c2.B)] = {
@@ -385,6 +429,10 @@ def run_ours(args, rank, world, local):
                      "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,
                      "algorithmic_bytes": fc1_b, "launch_us": fc1_us, "peak_kind": peak_kind},
         "phases_us": phase_med,
+        "timing_mode": "CUDA graph replay of the forward; per-phase events are graph nodes",
+        "eager_us": statistics.median(eager_times),
+        "eager_phases_us": {n: statistics.median(p[i] for p in eager_phases)
+                            for i, n in enumerate(phase_names)},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -122,9 +122,12 @@ int moe_decode_forward_host(moe_layer_t layer, void* stream, const void* x_host,
 
 /* moe_decode_forward that also exports intermediates (any may be NULL):
  * y_routed device fp32 [B][d], y_shared device fp32 [B][d],
- * h device fp32 [B][k][f] (h[b][j] belongs to expert idx[b][j]). */
+ * h device fp32 [B][k][f] (h[b][j] belongs to expert idx[b][j]),
+ * z device fp32 [B][d] (residual + y_routed + y_shared before bf16 rounding),
+ * out_f32 device fp32 [B][d] (the normalised output before bf16 rounding). */
 int moe_decode_forward_debug(moe_layer_t layer, void* stream, const void* x, int B, void* residual,
-                             void* out, float* y_routed, float* y_shared, float* h);
+                             void* out, float* y_routed, float* y_shared, float* h, float* z,
+                             float* out_f32);
 
 /* Dequantise one expert matrix on the GPU with the kernels' own decode path:
  * which = 0 -> FC1 [2f][d], which = 1 -> FC2 [d][f]; out device fp32. */

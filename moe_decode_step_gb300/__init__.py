@@ -124,10 +124,13 @@ class MoELayer:
         y_r = torch.empty((B, d), dtype=torch.float32, device=x.device)
         y_s = torch.empty((B, d), dtype=torch.float32, device=x.device)
         h = torch.empty((B, k, f), dtype=torch.float32, device=x.device)
+        z = torch.empty((B, d), dtype=torch.float32, device=x.device)
+        o32 = torch.empty((B, d), dtype=torch.float32, device=x.device)
         check(lib().moe_decode_forward_debug(self._h, _stream(stream), _ptr(x), B, _ptr(residual),
-                                             _ptr(out), _ptr(y_r), _ptr(y_s), _ptr(h)),
+                                             _ptr(out), _ptr(y_r), _ptr(y_s), _ptr(h), _ptr(z),
+                                             _ptr(o32)),
               "moe_decode_forward_debug")
-        return out, y_r, y_s, h
+        return dict(out=out, y_routed=y_r, y_shared=y_s, h=h, z=z, out_f32=o32)
 
     def debug_dequant(self, expert, which, stream=None):
         d, f = self.dims.d, self.dims.f

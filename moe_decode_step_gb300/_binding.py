@@ -51,7 +51,8 @@ _PROTOS = {
     "moe_router_topk": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P]),
     "moe_decode_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P]),
     "moe_decode_forward_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P]),
-    "moe_decode_forward_debug": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P]),
+    "moe_decode_forward_debug": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P,
+                                                _P, _P]),
     "moe_debug_dequant": (ctypes.c_int, [_P, _P, ctypes.c_int, ctypes.c_int, _P]),
     "moe_set_prefetch_next": (ctypes.c_int, [_P, _P]),
     "moe_layer_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),

@@ -159,6 +159,17 @@ int rmax_fc1(int B) { return B == 1 ? 1 : (B <= 8 ? 2 : 4); }
 int rmax_fc2(int B) { return B == 1 ? 1 : 2; }
 int rmax_shared(int B) { return B == 1 ? 1 : (B <= 3 ? 2 : 4); }
 
+// Timing events: inside a stream capture they must be external record nodes so
+// that every graph replay records them.
+cudaError_t record_time(moe_layer* L, int which, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(L->ev_time[which], st, cudaEventRecordExternal);
+  return cudaEventRecord(L->ev_time[which], st);
+}
+
 RouterArgs router_args(moe_layer* L, const void* x, int B, int32_t* idx, float* w) {
   RouterArgs a;
   a.x = static_cast<const uint16_t*>(x);
@@ -227,7 +238,7 @@ int launch_routed(moe_layer* L, cudaStream_t st, const void* x, int B) {
     default: routed_fc1_kernel<4><<<L->fc1_grid[2], L->fc1_threads, 0, st>>>(a1); break;
   }
   MOE_CUDA(cudaGetLastError());
-  if (L->timing) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeFc1End], st));
+  if (L->timing) MOE_CUDA(record_time(L, kTimeFc1End, st));
   const RoutedArgs a2 = routed_args(L, x, false);
   if (rmax_fc2(B) == 1) routed_fc2_kernel<1><<<L->fc2_grid[0], L->fc2_threads, 0, st>>>(a2);
   else routed_fc2_kernel<2><<<L->fc2_grid[1], L->fc2_threads, 0, st>>>(a2);
@@ -274,7 +285,8 @@ int launch_shared(moe_layer* L, cudaStream_t st, const void* x, int B) {
   return MOE_OK;
 }
 
-int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg) {
+int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg,
+                float* out_dbg) {
   TailArgs a;
   a.y_pair = L->ws.y_pair;
   a.topk_w = L->ws.topk_w;
@@ -286,6 +298,7 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.psum = L->ws.psum;
   a.ticket = L->ws.ticket;
   a.y_r_dbg = y_r_dbg;
+  a.out_dbg = out_dbg;
   a.B = B;
   a.d = L->dims.d;
   a.k = L->dims.top_k;
@@ -314,37 +327,39 @@ int launch_prefetch(moe_layer* L) {
 }
 
 int check_forward_args(moe_layer* L, const void* x, int B) {
-  if (!L || !x) return MOE_ERR_INVALID_ARG;
+  if (!L) return MOE_ERR_INVALID_ARG;
   if (B < 1 || B > L->dims.max_batch) return MOE_ERR_UNSUPPORTED;
+  if (!x) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
+
 int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* residual, void* out,
-                 float* y_r_dbg, float* y_s_dbg, float* h_dbg) {
+                 float* y_r_dbg, float* y_s_dbg, float* h_dbg, float* z_dbg, float* out_dbg) {
   int rc = check_forward_args(L, x, B);
   if (rc) return rc;
   if (!residual || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(residual) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   const bool tm = L->timing;
   MOE_CUDA(cudaEventRecord(L->ev_fork, st));
-  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeRouterStart], st));
+  if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
-  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeRouterEnd], st));
+  if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
   // side stream: shared expert, overlapping router + routed experts
   MOE_CUDA(cudaStreamWaitEvent(L->side, L->ev_fork, 0));
-  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeSharedStart], L->side));
+  if (tm) MOE_CUDA(record_time(L, kTimeSharedStart, L->side));
   if ((rc = launch_shared(L, L->side, x, B))) return rc;
-  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeSharedEnd], L->side));
+  if (tm) MOE_CUDA(record_time(L, kTimeSharedEnd, L->side));
   MOE_CUDA(cudaEventRecord(L->ev_join, L->side));
   if ((rc = launch_prefetch(L))) return rc;
   if ((rc = launch_routed(L, st, x, B))) return rc;
-  if (tm) MOE_CUDA(cudaEventRecord(L->ev_time[kTimeFc2End], st));
+  if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   MOE_CUDA(cudaStreamWaitEvent(st, L->ev_join, 0));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
-  if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg))) return rc;
+  if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, out_dbg))) return rc;
   if (tm) {
-    MOE_CUDA(cudaEventRecord(L->ev_time[kTimeTailEnd], st));
+    MOE_CUDA(record_time(L, kTimeTailEnd, st));
     L->timed_once = true;
   }
   const size_t P = (size_t)B * L->dims.top_k;
@@ -353,6 +368,9 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
                              cudaMemcpyDeviceToDevice, st));
   if (h_dbg)
     MOE_CUDA(cudaMemcpyAsync(h_dbg, L->ws.h, P * L->dims.f * 4, cudaMemcpyDeviceToDevice, st));
+  if (z_dbg)
+    MOE_CUDA(cudaMemcpyAsync(z_dbg, L->ws.z, (size_t)B * L->dims.d * 4, cudaMemcpyDeviceToDevice,
+                             st));
   return MOE_OK;
 }
 
@@ -478,13 +496,14 @@ int moe_router_topk(moe_layer_t L, void* stream, const void* x, int B, int32_t* 
 int moe_decode_forward(moe_layer_t L, void* stream, const void* x, int B, void* residual,
                        void* out) {
   return forward_impl(L, static_cast<cudaStream_t>(stream), x, B, residual, out, nullptr, nullptr,
-                      nullptr);
+                      nullptr, nullptr, nullptr);
 }
 
 int moe_decode_forward_debug(moe_layer_t L, void* stream, const void* x, int B, void* residual,
-                             void* out, float* y_routed, float* y_shared, float* h) {
+                             void* out, float* y_routed, float* y_shared, float* h, float* z,
+                             float* out_f32) {
   return forward_impl(L, static_cast<cudaStream_t>(stream), x, B, residual, out, y_routed,
-                      y_shared, h);
+                      y_shared, h, z, out_f32);
 }
 
 int moe_decode_forward_host(moe_layer_t L, void* stream, const void* x_host, int B,

@@ -25,6 +25,7 @@ struct TailArgs {
   float* psum;             // workspace [B][S]
   unsigned* ticket;        // workspace [B], 0 at rest
   float* y_r_dbg;          // optional export [B][d]
+  float* out_dbg;          // optional export of out before bf16 rounding [B][d]
   int B, d, k;
   float eps;
 };
@@ -75,7 +76,9 @@ tail_kernel(const TailArgs a) {
   const float inv = s_warp[0];
   for (int i = threadIdx.x; i < a.d; i += kTailThreads) {
     const size_t o = (size_t)b * a.d + i;
-    a.out[o] = f32_to_bf16_bits(__ldcg(a.z + o) * inv * bf16_bits_to_f32(a.gamma[i]));
+    const float v = __ldcg(a.z + o) * inv * bf16_bits_to_f32(a.gamma[i]);
+    a.out[o] = f32_to_bf16_bits(v);
+    if (a.out_dbg) a.out_dbg[o] = v;
   }
 }
 

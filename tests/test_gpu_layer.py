@@ -35,7 +35,18 @@ def _np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def check_against_oracle(ref, idx, w, out, res_out, y_r, y_s, h, rows):
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).float().numpy().astype(
+        np.float64)
+
+
+def check_against_oracle(ref, idx, w, dbg, res_out, rows):
+    """Parity of one forward (GPU outputs as float64 numpy) against the oracle.
+
+    The stated tolerance (max |err| <= 1e-2 RMS, mean rel <= 2e-3) applies to
+    the fp32 values before the bf16 output rounding; the bf16 outputs must be
+    exactly the round-to-nearest-even of those values and lie within half a
+    bf16 step plus the tolerance of the oracle's exact value."""
     k = idx.shape[1]
     for b in rows:
         assert sorted(idx[b].tolist()) == sorted(ref["idx"][b].tolist()), b
@@ -43,16 +54,29 @@ def check_against_oracle(ref, idx, w, out, res_out, y_r, y_s, h, rows):
         for j in range(k):
             jr = order[int(idx[b, j])]
             assert abs(w[b, j] - ref["w"][b, jr]) <= 1e-6
-            if h is not None:
-                assert_close(h[b, j], ref["h"][b, jr], 1e-3, 1e-4, what=f"h[{b},{j}]")
+            assert_close(dbg["h"][b, j], ref["h"][b, jr], 1e-3, 1e-4, what=f"h[{b},{j}]")
     r = list(rows)
-    assert_close(y_s[r], ref["y_s"][r], 1e-4, 1e-5, what="y_shared")
-    assert_close(y_r[r], ref["y_r"][r], 2e-3, 5e-4, what="y_routed")
-    m_out = assert_close(out[r], ref["out"][r], what="out")
-    m_res = assert_close(res_out[r], ref["z"][r], what="residual")
-    assert bf16_ulp_distance(out[r], ref["out_bf16"][r]).max() <= 1
-    assert bf16_ulp_distance(res_out[r], ref["residual_bf16"][r]).max() <= 1
-    return m_out, m_res
+    assert_close(dbg["y_shared"][r], ref["y_s"][r], 1e-4, 1e-5, what="y_shared")
+    assert_close(dbg["y_routed"][r], ref["y_r"][r], 2e-3, 5e-4, what="y_routed")
+    m_z = assert_close(dbg["z"][r], ref["z"][r], what="z (fp32, before rounding)")
+    m_o = assert_close(dbg["out_f32"][r], ref["out"][r], what="out (fp32, before rounding)")
+    assert_close(dbg["z"][r], ref["z"][r], 2e-3, 5e-4, what="z tight")
+    assert_close(dbg["out_f32"][r], ref["out"][r], 2e-3, 5e-4, what="out tight")
+    for got, f32, want in ((dbg["out"], dbg["out_f32"], ref["out"]),
+                           (res_out, dbg["z"], ref["z"])):
+        assert np.array_equal(got[r], _bf16(f32[r])), "bf16 output is not RNE of its fp32 value"
+        rms = np.sqrt((want[r] ** 2).mean())
+        half_step = np.exp2(np.floor(np.log2(np.maximum(np.abs(want[r]), 1e-30))) - 8)
+        assert np.all(np.abs(got[r] - want[r]) <= half_step + 1e-2 * rms)
+        assert np.abs(got[r] - want[r]).sum() / np.abs(want[r]).sum() <= 2e-3
+    print(f"parity rows={len(r)} z {m_z} out {m_o}")
+    return m_z, m_o
+
+
+def run_debug(layer, x, res):
+    d = layer.forward_debug(x, res)
+    torch.cuda.synchronize()
+    return {k: _np(v) for k, v in d.items()}
 
 
 @pytest.mark.parametrize("B", BATCHES)
@@ -63,11 +87,10 @@ def test_tiny_layer_matches_oracle(tiny_layer, B):
     x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
     assert np.array_equal(_np(x), inp.x) and np.array_equal(_np(res), inp.residual)
     idx, w = tiny_layer.router_topk(x)
-    out, y_r, y_s, h = tiny_layer.forward_debug(x, res)
-    torch.cuda.synchronize()
+    dbg = run_debug(tiny_layer, x, res)
     assert tiny_layer.status() == 0
-    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), _np(out),
-                         _np(res), _np(y_r), _np(y_s), _np(h), range(B))
+    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg,
+                         _np(res), range(B))
 
 
 def test_router_weights_sum_to_routed_scale(tiny_layer):
@@ -153,10 +176,9 @@ def test_zero_down_weights_leave_rmsnorm_of_residual_plus_shared():
     inp = oracle.clean_inputs(cfg)
     ref = oracle.forward(inp)
     x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
-    out, y_r, y_s, _ = layer.forward_debug(x, res)
-    torch.cuda.synchronize()
-    assert float(y_r.abs().max()) == 0.0
+    dbg = run_debug(layer, x, res)
+    assert float(np.abs(dbg["y_routed"]).max()) == 0.0
     z = inp.residual + ref["y_s"]
     want = z / np.sqrt((z ** 2).mean(axis=1, keepdims=True) + TINY.rms_eps) * inp.gamma
-    assert_close(_np(out), want, what="out with zero experts")
+    assert_close(dbg["out_f32"], want, 2e-3, 5e-4, what="out with zero experts")
     layer.close()
