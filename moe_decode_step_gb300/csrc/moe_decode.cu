@@ -1,25 +1,25 @@
 // C ABI of the MoE decode layer (see include/moe_decode.h for the contract).
 //
-// One forward = six kernels on two streams:
-//   main stream : router_topk -> routed_fc1 -> routed_fc2 -> [join] -> tail
-//   side stream : shared_fc1 -> shared_fc2                 (forked at entry)
-//   third stream: l2_prefetch of the next layer's dense weights (optional)
+// One forward, main stream (kernels chained with programmatic dependent launch):
+//   router GEMV (streamed bf16) -> top-k + routing tables -> routed FC1
+//   (streamed MXFP4, SwiGLU) -> routed FC2 (streamed MXFP4) -> [join] -> tail
+// side stream, forked at entry: shared FC1 -> shared FC2 (streamed bf16)
+// third stream (chained layers only): L2 prefetch of the next layer's router
+// and shared-expert weights.
 // No allocation, no host synchronisation: capturable into a CUDA graph.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <atomic>
-#include <cstdio>
 #include <cstring>
 #include <new>
 
 #include "moe_decode.h"
 #include "common.cuh"
 #include "mxfp4.cuh"
-#include "router.cuh"
-#include "routed.cuh"
-#include "shared.cuh"
+#include "stream.cuh"
 #include "tail.cuh"
+#include "topk.cuh"
 
 using namespace moe;
 
@@ -32,10 +32,10 @@ inline int cuda_fail(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
-#define MOE_CUDA(call)                       \
-  do {                                       \
-    cudaError_t e_ = (call);                 \
-    if (e_ != cudaSuccess) return cuda_fail(e_); \
+#define MOE_CUDA(call)                             \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_);   \
   } while (0)
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -54,19 +54,22 @@ struct Workspace {
   int* active_off;
   int* pair_list;
   unsigned* h_amax;
-  int* work;
   float* h;
   float* y_pair;
   float* hs;
   float* y_s;
-  float* z;
-  float* psum;
-  unsigned* ticket;
   int* status;
   uint16_t* x_stage;
   uint16_t* res_stage;
   uint16_t* out_stage;
 };
+
+// Launch shape of one streaming-GEMV step.
+struct StreamPlan {
+  int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0;
+};
+
+enum { kStepRouter, kStepFc1, kStepFc2, kStepSh1, kStepSh2, kNumSteps };
 
 }  // namespace
 
@@ -82,10 +85,7 @@ struct moe_layer {
   cudaEvent_t ev_time[kNumTimeEvents] = {};
   bool timing = false, timed_once = false;
   moe_layer* next = nullptr;
-  // launch shapes
-  int tail_slices = 0;
-  int fc1_threads = 0, fc2_threads = 0, sh1_threads = 0, sh2_threads = 0;
-  int fc1_grid[3] = {}, fc2_grid[2] = {}, sh1_grid[3] = {}, sh2_grid[3] = {};  // by RMAX 1/2/4
+  StreamPlan plan[kNumSteps][3];   // by RMAX slot (1, 2, 4)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
 };
 
@@ -98,7 +98,7 @@ T* carve(char*& p, size_t count) {
   return r;
 }
 
-size_t workspace_bytes(const moe_dims_t& d, int tail_slices, Workspace* ws, char* base) {
+size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   char* p = base;
   const size_t B = d.max_batch, E = d.n_experts, k = d.top_k, P = B * k;
   Workspace w;
@@ -112,14 +112,10 @@ size_t workspace_bytes(const moe_dims_t& d, int tail_slices, Workspace* ws, char
   w.active_off = carve<int>(p, E + 1);
   w.pair_list = carve<int>(p, P);
   w.h_amax = carve<unsigned>(p, P);
-  w.work = carve<int>(p, 4);
   w.h = carve<float>(p, P * d.f);
   w.y_pair = carve<float>(p, P * d.d);
   w.hs = carve<float>(p, B * d.f_shared);
   w.y_s = carve<float>(p, B * d.d);
-  w.z = carve<float>(p, B * d.d);
-  w.psum = carve<float>(p, B * tail_slices);
-  w.ticket = carve<unsigned>(p, B);
   w.status = carve<int>(p, 1);
   w.x_stage = carve<uint16_t>(p, B * d.d);
   w.res_stage = carve<uint16_t>(p, B * d.d);
@@ -140,24 +136,81 @@ int validate_dims(const moe_dims_t& d) {
   return MOE_OK;
 }
 
-// KW warps split K (ceil(K / elements per warp)); up to 8 warps per CTA.
-int shape_threads(int K, int per_warp) {
-  const int KW = (K + per_warp - 1) / per_warp;
-  return 32 * KW * std::max(1, 8 / KW);
-}
-
-template <typename K>
-int grid_for(K kernel, int threads, int n_sm) {
+// Size the stage ring for one instantiation and record its launch shape.
+template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
+int plan_stream(int K, int n_sm, int smem_budget, StreamPlan* p) {
+  using Sh = StreamShape<WF, ACTH>;
+  const int KW = (K + Sh::WARP_K - 1) / Sh::WARP_K;
+  const int G = GLU ? 2 : 1;
+  StreamPlan r;
+  r.threads = 32 * (KW + 1);
+  r.stage_bytes = (int)((G * stream_rows_bytes(WF, K, SP) + 127) / 128 * 128);
+  const int red_bytes = 2 * 64 * KW * 4;
+  r.NS = std::min(8, (smem_budget - red_bytes) / (r.stage_bytes + 16));
+  if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
+  r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
+  auto kern = stream_gemv_kernel<WF, GLU, ACTH, ROUTED, SP, RW, RMAX>;
+  MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess ||
-      occ < 1)
-    occ = 1;
-  return occ * n_sm;
+  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, r.threads, r.smem));
+  if (occ < 1) return MOE_ERR_UNSUPPORTED;
+  r.grid = occ * n_sm;
+  *p = r;
+  return MOE_OK;
 }
 
-int rmax_fc1(int B) { return B == 1 ? 1 : (B <= 8 ? 2 : 4); }
-int rmax_fc2(int B) { return B == 1 ? 1 : 2; }
-int rmax_shared(int B) { return B == 1 ? 1 : (B <= 3 ? 2 : 4); }
+// Kernel instantiations of the five streaming steps.
+#define MOE_ROUTER_KERNEL(R) stream_gemv_kernel<kWfBf16, false, false, false, 1, 2, R>
+#define MOE_FC1_KERNEL(R) stream_gemv_kernel<kWfMx, true, false, true, 4, 16, R>
+#define MOE_FC2_KERNEL(R) stream_gemv_kernel<kWfMx, false, true, true, 16, 32, R>
+#define MOE_SH1_KERNEL(R) stream_gemv_kernel<kWfBf16, true, false, false, 1, 4, R>
+#define MOE_SH2_KERNEL(R) stream_gemv_kernel<kWfBf16, false, true, false, 8, 16, R>
+
+constexpr int kBudgetOne = 220 * 1024;   // one CTA per SM
+constexpr int kBudgetTwo = 110 * 1024;   // two CTAs per SM
+
+int plan_all(moe_layer* L) {
+  const moe_dims_t& d = L->dims;
+  const int n = L->n_sm;
+  int rc;
+#define MOE_PLAN(step, slot, expr) \
+  if ((rc = (expr))) return rc;
+  MOE_PLAN(kStepRouter, 2, (plan_stream<kWfBf16, false, false, false, 1, 2, 4>(
+                               d.d, n, kBudgetTwo, &L->plan[kStepRouter][2])));
+  MOE_PLAN(kStepFc1, 0, (plan_stream<kWfMx, true, false, true, 4, 16, 1>(
+                            d.d, n, kBudgetOne, &L->plan[kStepFc1][0])));
+  MOE_PLAN(kStepFc1, 1, (plan_stream<kWfMx, true, false, true, 4, 16, 2>(
+                            d.d, n, kBudgetOne, &L->plan[kStepFc1][1])));
+  MOE_PLAN(kStepFc2, 0, (plan_stream<kWfMx, false, true, true, 16, 32, 1>(
+                            d.f, n, kBudgetTwo, &L->plan[kStepFc2][0])));
+  MOE_PLAN(kStepFc2, 1, (plan_stream<kWfMx, false, true, true, 16, 32, 2>(
+                            d.f, n, kBudgetTwo, &L->plan[kStepFc2][1])));
+  MOE_PLAN(kStepSh1, 2, (plan_stream<kWfBf16, true, false, false, 1, 4, 4>(
+                            d.d, n, kBudgetOne, &L->plan[kStepSh1][2])));
+  MOE_PLAN(kStepSh2, 2, (plan_stream<kWfBf16, false, true, false, 8, 16, 4>(
+                            d.f_shared, n, kBudgetTwo, &L->plan[kStepSh2][2])));
+#undef MOE_PLAN
+  return MOE_OK;
+}
+
+// Launch with programmatic stream serialization when `pdl` (the kernel may
+// start while its predecessor in the stream finishes; it waits with
+// griddepcontrol.wait before touching the predecessor's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Timing events: inside a stream capture they must be external record nodes so
 // that every graph replay records them.
@@ -170,123 +223,118 @@ cudaError_t record_time(moe_layer* L, int which, cudaStream_t st) {
   return cudaEventRecord(L->ev_time[which], st);
 }
 
-RouterArgs router_args(moe_layer* L, const void* x, int B, int32_t* idx, float* w) {
-  RouterArgs a;
-  a.x = static_cast<const uint16_t*>(x);
-  a.wr = static_cast<const uint16_t*>(L->w.router_w);
-  a.bias = L->w.router_bias;
-  a.B = B;
-  a.d = L->dims.d;
-  a.E = L->dims.n_experts;
+StreamArgs base_args(moe_layer* L) {
+  StreamArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.k = L->dims.top_k;
-  a.routed_scale = L->dims.routed_scale;
-  a.logits = L->ws.logits;
-  a.done = L->ws.done;
   a.x_shift = L->ws.x_shift;
-  a.topk_idx = idx;
-  a.topk_w = w;
   a.n_active = L->ws.n_active;
   a.active_expert = L->ws.active_expert;
   a.active_off = L->ws.active_off;
   a.pair_list = L->ws.pair_list;
-  a.h_amax = L->ws.h_amax;
-  a.work = L->ws.work;
+  a.status = L->ws.status;
   return a;
+}
+
+template <typename K>
+int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_items_cap,
+                cudaStream_t st, bool pdl) {
+  a.NS = p.NS;
+  a.stage_bytes = p.stage_bytes;
+  const int grid = n_items_cap > 0 ? std::min(p.grid, n_items_cap) : p.grid;
+  MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, pdl, a));
+  return MOE_OK;
 }
 
 int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* idx, float* w) {
-  const RouterArgs a = router_args(L, x, B, idx, w);
-  const int grid = (L->dims.n_experts + kRouterExpertsPerCta - 1) / kRouterExpertsPerCta;
-  const int threads = kRouterWarps * 32;
-  if (B == 1) router_topk_kernel<1><<<grid, threads, 0, st>>>(a);
-  else if (B == 2) router_topk_kernel<2><<<grid, threads, 0, st>>>(a);
-  else if (B <= 4) router_topk_kernel<4><<<grid, threads, 0, st>>>(a);
-  else router_topk_kernel<8><<<grid, threads, 0, st>>>(a);
-  MOE_CUDA(cudaGetLastError());
-  return MOE_OK;
-}
-
-RoutedArgs routed_args(moe_layer* L, const void* x, bool fc1) {
-  RoutedArgs a;
   const moe_dims_t& d = L->dims;
-  a.q = fc1 ? L->w.w_gu_q : L->w.w_d_q;
-  a.s = fc1 ? L->w.w_gu_s : L->w.w_d_s;
-  a.q_stride = fc1 ? L->q_gu_stride : L->q_d_stride;
-  a.s_stride = fc1 ? L->s_gu_stride : L->s_d_stride;
-  a.K = fc1 ? d.d : d.f;
-  a.N = fc1 ? d.f : d.d;
-  a.k = d.top_k;
+  StreamArgs a = base_args(L);
+  a.q = static_cast<const uint8_t*>(L->w.router_w);
+  a.K = d.d;
+  a.N = d.n_experts;
+  a.B = B;
   a.x = static_cast<const uint16_t*>(x);
-  a.x_shift = L->ws.x_shift;
-  a.h = L->ws.h;
-  a.h_amax = L->ws.h_amax;
-  a.out = fc1 ? L->ws.h : L->ws.y_pair;
-  a.out_amax = L->ws.h_amax;
-  a.n_active = L->ws.n_active;
-  a.active_expert = L->ws.active_expert;
-  a.active_off = L->ws.active_off;
-  a.pair_list = L->ws.pair_list;
-  a.work = L->ws.work + (fc1 ? 0 : 1);
-  return a;
+  a.out = L->ws.logits;
+  int rc = launch_step(L, MOE_ROUTER_KERNEL(4), L->plan[kStepRouter][2], a,
+                       (d.n_experts + 1) / 2, st, false);
+  if (rc) return rc;
+  TopkArgs t;
+  t.logits = L->ws.logits;
+  t.bias = L->w.router_bias;
+  t.x = static_cast<const uint16_t*>(x);
+  t.B = B;
+  t.d = d.d;
+  t.E = d.n_experts;
+  t.k = d.top_k;
+  t.routed_scale = d.routed_scale;
+  t.topk_idx = idx;
+  t.topk_w = w;
+  t.x_shift = L->ws.x_shift;
+  t.done = L->ws.done;
+  t.n_active = L->ws.n_active;
+  t.active_expert = L->ws.active_expert;
+  t.active_off = L->ws.active_off;
+  t.pair_list = L->ws.pair_list;
+  t.h_amax = L->ws.h_amax;
+  MOE_CUDA(launch_ex(topk_kernel, dim3(B), dim3(kTopkThreads), 0, st, true, t));
+  return MOE_OK;
 }
 
 int launch_routed(moe_layer* L, cudaStream_t st, const void* x, int B) {
-  const RoutedArgs a1 = routed_args(L, x, true);
-  switch (rmax_fc1(B)) {
-    case 1: routed_fc1_kernel<1><<<L->fc1_grid[0], L->fc1_threads, 0, st>>>(a1); break;
-    case 2: routed_fc1_kernel<2><<<L->fc1_grid[1], L->fc1_threads, 0, st>>>(a1); break;
-    default: routed_fc1_kernel<4><<<L->fc1_grid[2], L->fc1_threads, 0, st>>>(a1); break;
-  }
-  MOE_CUDA(cudaGetLastError());
+  const moe_dims_t& d = L->dims;
+  const bool one = B == 1;
+  StreamArgs a = base_args(L);
+  a.q = L->w.w_gu_q;
+  a.s = L->w.w_gu_s;
+  a.q_stride = L->q_gu_stride;
+  a.s_stride = L->s_gu_stride;
+  a.K = d.d;
+  a.N = d.f;
+  a.x = static_cast<const uint16_t*>(x);
+  a.out = L->ws.h;
+  a.out_amax = L->ws.h_amax;
+  int rc = one ? launch_step(L, MOE_FC1_KERNEL(1), L->plan[kStepFc1][0], a, 0, st, true)
+               : launch_step(L, MOE_FC1_KERNEL(2), L->plan[kStepFc1][1], a, 0, st, true);
+  if (rc) return rc;
   if (L->timing) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  const RoutedArgs a2 = routed_args(L, x, false);
-  if (rmax_fc2(B) == 1) routed_fc2_kernel<1><<<L->fc2_grid[0], L->fc2_threads, 0, st>>>(a2);
-  else routed_fc2_kernel<2><<<L->fc2_grid[1], L->fc2_threads, 0, st>>>(a2);
-  MOE_CUDA(cudaGetLastError());
-  return MOE_OK;
+  StreamArgs b = base_args(L);
+  b.q = L->w.w_d_q;
+  b.s = L->w.w_d_s;
+  b.q_stride = L->q_d_stride;
+  b.s_stride = L->s_d_stride;
+  b.K = d.f;
+  b.N = d.d;
+  b.h = L->ws.h;
+  b.h_amax = L->ws.h_amax;
+  b.out = L->ws.y_pair;
+  return one ? launch_step(L, MOE_FC2_KERNEL(1), L->plan[kStepFc2][0], b, 0, st, true)
+             : launch_step(L, MOE_FC2_KERNEL(2), L->plan[kStepFc2][1], b, 0, st, true);
 }
 
 int launch_shared(moe_layer* L, cudaStream_t st, const void* x, int B) {
   const moe_dims_t& d = L->dims;
-  SharedArgs a1;
-  a1.w = static_cast<const uint16_t*>(L->w.shared_gu);
-  a1.K = d.d;
-  a1.N = d.f_shared;
-  a1.B = B;
-  a1.x = static_cast<const uint16_t*>(x);
-  a1.hs = nullptr;
-  a1.out = L->ws.hs;
-  SharedArgs a2;
-  a2.w = static_cast<const uint16_t*>(L->w.shared_d);
-  a2.K = d.f_shared;
-  a2.N = d.d;
-  a2.B = B;
-  a2.x = nullptr;
-  a2.hs = L->ws.hs;
-  a2.out = L->ws.y_s;
-  switch (rmax_shared(B)) {
-    case 1:
-      shared_fc1_kernel<1><<<L->sh1_grid[0], L->sh1_threads, 0, st>>>(a1);
-      MOE_CUDA(cudaGetLastError());
-      shared_fc2_kernel<1><<<L->sh2_grid[0], L->sh2_threads, 0, st>>>(a2);
-      break;
-    case 2:
-      shared_fc1_kernel<2><<<L->sh1_grid[1], L->sh1_threads, 0, st>>>(a1);
-      MOE_CUDA(cudaGetLastError());
-      shared_fc2_kernel<2><<<L->sh2_grid[1], L->sh2_threads, 0, st>>>(a2);
-      break;
-    default:
-      shared_fc1_kernel<4><<<L->sh1_grid[2], L->sh1_threads, 0, st>>>(a1);
-      MOE_CUDA(cudaGetLastError());
-      shared_fc2_kernel<4><<<L->sh2_grid[2], L->sh2_threads, 0, st>>>(a2);
-      break;
-  }
-  MOE_CUDA(cudaGetLastError());
-  return MOE_OK;
+  StreamArgs a = base_args(L);
+  a.q = static_cast<const uint8_t*>(L->w.shared_gu);
+  a.K = d.d;
+  a.N = d.f_shared;
+  a.B = B;
+  a.x = static_cast<const uint16_t*>(x);
+  a.out = L->ws.hs;
+  int rc = launch_step(L, MOE_SH1_KERNEL(4), L->plan[kStepSh1][2], a, (d.f_shared + 3) / 4, st,
+                       false);
+  if (rc) return rc;
+  StreamArgs b = base_args(L);
+  b.q = static_cast<const uint8_t*>(L->w.shared_d);
+  b.K = d.f_shared;
+  b.N = d.d;
+  b.B = B;
+  b.h = L->ws.hs;
+  b.out = L->ws.y_s;
+  return launch_step(L, MOE_SH2_KERNEL(4), L->plan[kStepSh2][2], b, (d.d + 15) / 16, st, true);
 }
 
 int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg,
-                float* out_dbg) {
+                float* z_dbg, float* out_dbg, bool pdl) {
   TailArgs a;
   a.y_pair = L->ws.y_pair;
   a.topk_w = L->ws.topk_w;
@@ -294,17 +342,14 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.gamma = static_cast<const uint16_t*>(L->w.rms_gamma);
   a.residual = static_cast<uint16_t*>(residual);
   a.out = static_cast<uint16_t*>(out);
-  a.z = L->ws.z;
-  a.psum = L->ws.psum;
-  a.ticket = L->ws.ticket;
   a.y_r_dbg = y_r_dbg;
+  a.z_dbg = z_dbg;
   a.out_dbg = out_dbg;
   a.B = B;
   a.d = L->dims.d;
   a.k = L->dims.top_k;
   a.eps = L->dims.rms_eps;
-  tail_kernel<<<dim3(L->tail_slices, B), kTailThreads, 0, st>>>(a);
-  MOE_CUDA(cudaGetLastError());
+  MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
   return MOE_OK;
 }
 
@@ -334,7 +379,6 @@ int check_forward_args(moe_layer* L, const void* x, int B) {
   return MOE_OK;
 }
 
-
 int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* residual, void* out,
                  float* y_r_dbg, float* y_s_dbg, float* h_dbg, float* z_dbg, float* out_dbg) {
   int rc = check_forward_args(L, x, B);
@@ -346,7 +390,7 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-  // side stream: shared expert, overlapping router + routed experts
+  // side stream: shared expert, overlapping the router and the routed experts
   MOE_CUDA(cudaStreamWaitEvent(L->side, L->ev_fork, 0));
   if (tm) MOE_CUDA(record_time(L, kTimeSharedStart, L->side));
   if ((rc = launch_shared(L, L->side, x, B))) return rc;
@@ -357,7 +401,7 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   MOE_CUDA(cudaStreamWaitEvent(st, L->ev_join, 0));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
-  if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, out_dbg))) return rc;
+  if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
   if (tm) {
     MOE_CUDA(record_time(L, kTimeTailEnd, st));
     L->timed_once = true;
@@ -368,9 +412,6 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
                              cudaMemcpyDeviceToDevice, st));
   if (h_dbg)
     MOE_CUDA(cudaMemcpyAsync(h_dbg, L->ws.h, P * L->dims.f * 4, cudaMemcpyDeviceToDevice, st));
-  if (z_dbg)
-    MOE_CUDA(cudaMemcpyAsync(z_dbg, L->ws.z, (size_t)B * L->dims.d * 4, cudaMemcpyDeviceToDevice,
-                             st));
   return MOE_OK;
 }
 
@@ -416,19 +457,18 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   L->w = w;
   L->device = dev;
   L->n_sm = prop.multiProcessorCount;
-  L->tail_slices = (dims->d + kTailThreads - 1) / kTailThreads;
   const size_t f = dims->f, dd = dims->d;
   L->q_gu_stride = 2 * f * dd / 2;
   L->s_gu_stride = 2 * f * dd / 32;
   L->q_d_stride = dd * f / 2;
   L->s_d_stride = dd * f / 32;
-  const size_t bytes = workspace_bytes(*dims, L->tail_slices, nullptr, nullptr);
+  const size_t bytes = workspace_bytes(*dims, nullptr, nullptr);
   if (cudaMalloc(&L->ws_base, bytes) != cudaSuccess) {
     cudaGetLastError();
     delete L;
     return MOE_ERR_ALLOC;
   }
-  workspace_bytes(*dims, L->tail_slices, &L->ws, static_cast<char*>(L->ws_base));
+  workspace_bytes(*dims, &L->ws, static_cast<char*>(L->ws_base));
   auto fail = [&](cudaError_t e) {
     moe_layer_destroy(L);
     return cuda_fail(e);
@@ -442,26 +482,9 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
-  L->fc1_threads = shape_threads(dims->d, 1024);
-  L->fc2_threads = shape_threads(dims->f, 512);
-  L->sh1_threads = shape_threads(dims->d, 1024);
-  L->sh2_threads = shape_threads(dims->f_shared, 512);
-  L->fc1_grid[0] = grid_for(routed_fc1_kernel<1>, L->fc1_threads, L->n_sm);
-  L->fc1_grid[1] = grid_for(routed_fc1_kernel<2>, L->fc1_threads, L->n_sm);
-  L->fc1_grid[2] = grid_for(routed_fc1_kernel<4>, L->fc1_threads, L->n_sm);
-  L->fc2_grid[0] = grid_for(routed_fc2_kernel<1>, L->fc2_threads, L->n_sm);
-  L->fc2_grid[1] = grid_for(routed_fc2_kernel<2>, L->fc2_threads, L->n_sm);
-  {
-    const int rows1 = (L->sh1_threads / 32 / ((dims->d + 1023) / 1024)) * kSh1RPW;
-    const int items1 = (dims->f_shared + rows1 - 1) / rows1;
-    const int rows2 = (L->sh2_threads / 32 / ((dims->f_shared + 511) / 512)) * kSh2RPW;
-    const int items2 = (dims->d + rows2 - 1) / rows2;
-    L->sh1_grid[0] = std::min(items1, grid_for(shared_fc1_kernel<1>, L->sh1_threads, L->n_sm));
-    L->sh1_grid[1] = std::min(items1, grid_for(shared_fc1_kernel<2>, L->sh1_threads, L->n_sm));
-    L->sh1_grid[2] = std::min(items1, grid_for(shared_fc1_kernel<4>, L->sh1_threads, L->n_sm));
-    L->sh2_grid[0] = std::min(items2, grid_for(shared_fc2_kernel<1>, L->sh2_threads, L->n_sm));
-    L->sh2_grid[1] = std::min(items2, grid_for(shared_fc2_kernel<2>, L->sh2_threads, L->n_sm));
-    L->sh2_grid[2] = std::min(items2, grid_for(shared_fc2_kernel<4>, L->sh2_threads, L->n_sm));
+  if ((rc = plan_all(L))) {
+    moe_layer_destroy(L);
+    return rc;
   }
   *out = L;
   return MOE_OK;
@@ -582,7 +605,7 @@ int moe_get_timing(moe_layer_t L, float* us, int n) {
 
 int moe_launches_per_forward(moe_layer_t L, int B) {
   if (!L || B < 1 || B > L->dims.max_batch) return -1;
-  return 6;   // router, shared FC1, shared FC2, routed FC1, routed FC2, tail
+  return 7;   // router, top-k, shared FC1, shared FC2, routed FC1, routed FC2, tail
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {

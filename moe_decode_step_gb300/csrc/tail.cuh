@@ -3,12 +3,16 @@
 // section "What the fused path changes": the tail folds the down-projection
 // reduction and the next norm together; at one GPU the reduction is local).
 //
-// Grid (S, B): CTA (s, b) owns 256 elements of row b.  It forms
-//   z = residual + sum_j w[b][j] * y_pair[b*k + j] + y_s,
-// writes residual <- bf16(z) and the fp32 z, and a partial sum of squares.
-// The last CTA of the row (atomic ticket, no waiting) adds the S partials in
-// slice order and writes out = bf16(z / sqrt(mean z^2 + eps) * gamma).
+// Each row is handled by one thread-block cluster of kTailCluster CTAs; CTA c
+// owns d / kTailCluster elements, four per thread.  A thread forms
+//   z = residual + sum_j w[b][j] * y_pair[b*k + j] + y_s
+// for its elements (all k partial loads issued before use), the CTAs exchange
+// their sums of squares through distributed shared memory, and every CTA
+// normalises its own elements: out = bf16(z / sqrt(mean z^2 + eps) * gamma).
+// The partial sums are added in CTA-rank order, so the result is deterministic.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
@@ -21,65 +25,91 @@ struct TailArgs {
   const uint16_t* gamma;   // bf16 [d]
   uint16_t* residual;      // bf16 [B][d] in / out
   uint16_t* out;           // bf16 [B][d]
-  float* z;                // workspace [B][d]
-  float* psum;             // workspace [B][S]
-  unsigned* ticket;        // workspace [B], 0 at rest
   float* y_r_dbg;          // optional export [B][d]
+  float* z_dbg;            // optional export of z before bf16 rounding [B][d]
   float* out_dbg;          // optional export of out before bf16 rounding [B][d]
   int B, d, k;
   float eps;
 };
 
-constexpr int kTailThreads = 256;
+constexpr int kTailCluster = 8;
+constexpr int kTailBatch = 16;   // y_pair loads in flight per thread
 
-__global__ void __launch_bounds__(kTailThreads)
+__global__ void __cluster_dims__(kTailCluster, 1, 1) __launch_bounds__(256)
 tail_kernel(const TailArgs a) {
-  const int s = blockIdx.x, b = blockIdx.y, S = gridDim.x;
-  const int n = s * kTailThreads + threadIdx.x;
-  __shared__ float s_ws[32];
-  __shared__ float s_warp[kTailThreads / 32];
-  __shared__ unsigned s_last;
-  if (threadIdx.x < a.k) s_ws[threadIdx.x] = a.topk_w[b * a.k + threadIdx.x];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank(), b = blockIdx.y;
+  const int per_cta = a.d / kTailCluster;
+  const int n = c * per_cta + (int)threadIdx.x * 4;
+  const bool ok = (int)threadIdx.x * 4 < per_cta;
+  __shared__ float s_w[32];
+  __shared__ float s_warp[8];
+  __shared__ float s_ss;
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
+  for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_w[i] = __ldcg(a.topk_w + b * a.k + i);
   __syncthreads();
-  float zz = 0.f;
-  if (n < a.d) {
-    float yr = 0.f;
-    const float* yp = a.y_pair + (size_t)b * a.k * a.d + n;
-    for (int j = 0; j < a.k; ++j) yr = fmaf(s_ws[j], __ldcg(yp + (size_t)j * a.d), yr);
+  float z[4] = {0.f, 0.f, 0.f, 0.f};
+  float yr[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ok) {
     const size_t o = (size_t)b * a.d + n;
-    const float z = bf16_bits_to_f32(a.residual[o]) + yr + __ldcg(a.y_s + o);
-    a.residual[o] = f32_to_bf16_bits(z);
-    a.z[o] = z;
-    if (a.y_r_dbg) a.y_r_dbg[o] = yr;
-    zz = z * z;
+    const float* yp = a.y_pair + (size_t)b * a.k * a.d + n;
+    for (int j0 = 0; j0 < a.k; j0 += kTailBatch) {
+      float4 v[kTailBatch];
+#pragma unroll
+      for (int j = 0; j < kTailBatch; ++j)
+        v[j] = (j0 + j < a.k) ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)(j0 + j) * a.d))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kTailBatch; ++j) {
+        const float w = (j0 + j < a.k) ? s_w[j0 + j] : 0.f;
+        yr[0] = fmaf(w, v[j].x, yr[0]);
+        yr[1] = fmaf(w, v[j].y, yr[1]);
+        yr[2] = fmaf(w, v[j].z, yr[2]);
+        yr[3] = fmaf(w, v[j].w, yr[3]);
+      }
+    }
+    const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.y_s + o));
+    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
+    z[0] = bf16_bits_to_f32(rb.x & 0xFFFFu) + yr[0] + ys.x;
+    z[1] = bf16_bits_to_f32(rb.x >> 16) + yr[1] + ys.y;
+    z[2] = bf16_bits_to_f32(rb.y & 0xFFFFu) + yr[2] + ys.z;
+    z[3] = bf16_bits_to_f32(rb.y >> 16) + yr[3] + ys.w;
+    uint2 ro;
+    ro.x = (uint32_t)f32_to_bf16_bits(z[0]) | ((uint32_t)f32_to_bf16_bits(z[1]) << 16);
+    ro.y = (uint32_t)f32_to_bf16_bits(z[2]) | ((uint32_t)f32_to_bf16_bits(z[3]) << 16);
+    *reinterpret_cast<uint2*>(a.residual + o) = ro;
+    if (a.y_r_dbg) *reinterpret_cast<float4*>(a.y_r_dbg + o) = make_float4(yr[0], yr[1], yr[2], yr[3]);
+    if (a.z_dbg) *reinterpret_cast<float4*>(a.z_dbg + o) = make_float4(z[0], z[1], z[2], z[3]);
   }
-  const float ws = warp_sum(zz);
-  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ws;
+  const float ss = warp_sum(z[0] * z[0] + z[1] * z[1] + z[2] * z[2] + z[3] * z[3]);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < kTailThreads / 32; ++w) t += s_warp[w];
-    a.psum[b * S + s] = t;
-    __threadfence();
-    s_last = (atomicAdd(a.ticket + b, 1u) == (unsigned)(S - 1)) ? 1u : 0u;
+    for (int w = 0; w < (int)((blockDim.x + 31) >> 5); ++w) t += s_warp[w];
+    s_ss = t;
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int i = 0; i < S; ++i) t += __ldcg(a.psum + b * S + i);
-    s_warp[0] = 1.0f / sqrtf(t / (float)a.d + a.eps);
-    a.ticket[b] = 0u;
+  cluster.sync();
+  float total = 0.f;
+  for (int r = 0; r < kTailCluster; ++r) total += *cluster.map_shared_rank(&s_ss, r);
+  const float inv = 1.0f / sqrtf(total / (float)a.d + a.eps);
+  if (ok) {
+    const size_t o = (size_t)b * a.d + n;
+    const uint2 g = *reinterpret_cast<const uint2*>(a.gamma + n);
+    float v[4];
+    v[0] = z[0] * inv * bf16_bits_to_f32(g.x & 0xFFFFu);
+    v[1] = z[1] * inv * bf16_bits_to_f32(g.x >> 16);
+    v[2] = z[2] * inv * bf16_bits_to_f32(g.y & 0xFFFFu);
+    v[3] = z[3] * inv * bf16_bits_to_f32(g.y >> 16);
+    uint2 oo;
+    oo.x = (uint32_t)f32_to_bf16_bits(v[0]) | ((uint32_t)f32_to_bf16_bits(v[1]) << 16);
+    oo.y = (uint32_t)f32_to_bf16_bits(v[2]) | ((uint32_t)f32_to_bf16_bits(v[3]) << 16);
+    *reinterpret_cast<uint2*>(a.out + o) = oo;
+    if (a.out_dbg) *reinterpret_cast<float4*>(a.out_dbg + o) = make_float4(v[0], v[1], v[2], v[3]);
   }
-  __syncthreads();
-  const float inv = s_warp[0];
-  for (int i = threadIdx.x; i < a.d; i += kTailThreads) {
-    const size_t o = (size_t)b * a.d + i;
-    const float v = __ldcg(a.z + o) * inv * bf16_bits_to_f32(a.gamma[i]);
-    a.out[o] = f32_to_bf16_bits(v);
-    if (a.out_dbg) a.out_dbg[o] = v;
-  }
+  cluster.sync();   // no CTA leaves while a peer may still read its s_ss
 }
 
 // L2 prefetch of upcoming weights ("What the fused path changes": a small

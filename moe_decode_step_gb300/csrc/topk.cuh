@@ -1,0 +1,184 @@
+// Router selection: sigmoid scores, biased top-k per row, combine weights, and
+// the routing tables the expert kernels consume.
+//
+// One CTA per row, one thread per expert (E <= 1024).  The k-th largest key is
+// found by a bitwise radix select with __syncthreads_count (32 steps over the
+// order-preserving unsigned image of the fp32 key); ties at the threshold go
+// to the lowest expert ids.  Selection compares fp32 (score + bias); the
+// combine weights use the unbiased scores, normalised to routed_scale.
+// The last CTA to finish (atomic ticket, no waiting) groups the (row, slot)
+// pairs by expert.  ("Kimi K3 on GB300: 13 kernels a layer...", section "What
+// one decode step of Kimi K3 does": 16 of 896 experts per token.)
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct TopkArgs {
+  const float* logits;    // [B][E]
+  const float* bias;      // [E]
+  const uint16_t* x;      // bf16 [B][d] (for the f16 scaling shift of each row)
+  int B, d, E, k;
+  float routed_scale;
+  int32_t* topk_idx;      // [B][k], descending by biased score
+  float* topk_w;          // [B][k]
+  int* x_shift;           // [B]
+  unsigned* done;         // ticket, 0 at rest
+  int* n_active;          // routing tables (see RoutedArgs)
+  int* active_expert;
+  int* active_off;
+  int* pair_list;
+  unsigned* h_amax;       // [B*k] reset to 0
+};
+
+constexpr int kTopkThreads = 1024;
+
+__device__ __forceinline__ uint32_t float_order_bits(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Exclusive block scan of one int per thread (1024 threads); returns the
+// exclusive prefix, writes the total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+    int winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += t;
+    }
+    if (lane < nw) s_warp[lane] = winc - w;
+    if (lane == nw - 1) s_warp[32] = winc;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + inc - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
+  const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ int s_warp[33];
+  __shared__ uint64_t s_key[32];
+  __shared__ float s_score[32];
+  __shared__ int s_cnt;
+  __shared__ unsigned s_last;
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
+
+  // ---- scores and keys ----
+  const bool valid = t < a.E;
+  float score = 0.f;
+  uint32_t u = 0;
+  if (valid) {
+    const float l = __ldcg(a.logits + (size_t)b * a.E + t);
+    score = 1.0f / (1.0f + expf(-l));
+    u = float_order_bits(score + __ldg(a.bias + t));
+  }
+  // ---- k-th largest u (with multiplicity) ----
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    if (__syncthreads_count(valid && u >= cand) >= a.k) T = cand;
+  }
+  const int c_gt = __syncthreads_count(valid && u > T);
+  // ties at T: lowest ids first
+  const bool eq = valid && u == T;
+  const unsigned bal = __ballot_sync(0xffffffffu, eq);
+  if (lane == 0) s_warp[warp] = __popc(bal);
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
+  int before = __popc(bal & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  const bool sel = valid && (u > T || (eq && before < a.k - c_gt));
+  __syncthreads();
+  if (sel) {
+    const int slot = atomicAdd(&s_cnt, 1);
+    s_key[slot] = ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
+  }
+  __syncthreads();
+  if (sel) {
+    const uint64_t mine = ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
+    int rank = 0;
+    for (int i = 0; i < a.k; ++i) rank += s_key[i] > mine;
+    a.topk_idx[b * a.k + rank] = t;
+    s_score[rank] = score;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float ssum = 0.f;
+    for (int i = 0; i < a.k; ++i) ssum += s_score[i];   // picks summed in rank order
+    if (lane < a.k) a.topk_w[b * a.k + lane] = a.routed_scale * s_score[lane] / ssum;
+    if (lane < a.k) a.h_amax[b * a.k + lane] = 0u;
+  }
+  // ---- f16 scaling shift of x row b ----
+  {
+    uint32_t m = 0;
+    const uint16_t* xr = a.x + (size_t)b * a.d;
+    for (int i = t; i < a.d; i += blockDim.x) m = max(m, (uint32_t)(xr[i] & 0x7FFFu));
+    m = __reduce_max_sync(0xffffffffu, m);
+    __syncthreads();
+    if (lane == 0) s_warp[warp] = (int)m;
+    __syncthreads();
+    if (t == 0) {
+      uint32_t mm = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mm = max(mm, (uint32_t)s_warp[w]);
+      a.x_shift[b] = f16_shift_for_amax(bf16_bits_to_f32(mm));
+    }
+  }
+
+  // ---- the last CTA groups pairs by expert ----
+  __threadfence();
+  __syncthreads();
+  if (t == 0) s_last = (atomicAdd(a.done, 1u) == (unsigned)(gridDim.x - 1)) ? 1u : 0u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  __shared__ unsigned long long s_mask[1024];
+  __shared__ int32_t s_idx[64 * 32];
+  const int P = a.B * a.k;
+  for (int p = t; p < P; p += blockDim.x) s_idx[p] = __ldcg(a.topk_idx + p);
+  if (valid) s_mask[t] = 0ull;
+  __syncthreads();
+  for (int p = t; p < P; p += blockDim.x) atomicOr(&s_mask[s_idx[p]], 1ull << (p / a.k));
+  __syncthreads();
+  const unsigned long long mask = valid ? s_mask[t] : 0ull;
+  const int cnt = __popcll(mask);
+  int total_pairs, n_act;
+  const int off = block_exclusive_scan(cnt, s_warp, &total_pairs);
+  const int slot = block_exclusive_scan(cnt > 0 ? 1 : 0, s_warp, &n_act);
+  if (cnt > 0) {
+    a.active_expert[slot] = t;
+    a.active_off[slot] = off;
+    unsigned long long mm = mask;
+    int pos = off;
+    while (mm) {
+      const int row = __ffsll((long long)mm) - 1;
+      mm &= mm - 1;
+      int j = 0;
+      while (j < a.k && s_idx[row * a.k + j] != t) ++j;
+      a.pair_list[pos++] = row * a.k + j;
+    }
+  }
+  if (t == 0) {
+    *a.n_active = n_act;
+    a.active_off[n_act] = total_pairs;
+    *a.done = 0u;
+  }
+}
+
+}  // namespace moe
