@@ -166,29 +166,33 @@ int plan_stream(int K, int n_sm, int smem_budget, StreamPlan* p) {
 #define MOE_SH1_KERNEL(R) stream_gemv_kernel<kWfBf16, true, false, false, 1, 4, R>
 #define MOE_SH2_KERNEL(R) stream_gemv_kernel<kWfBf16, false, true, false, 8, 16, R>
 
-constexpr int kBudgetOne = 220 * 1024;   // one CTA per SM
-constexpr int kBudgetTwo = 110 * 1024;   // two CTAs per SM
+// Shared-memory budget per CTA: how many CTAs of a step share an SM, chosen
+// from each instantiation's register footprint.
+constexpr int kBudget1 = 220 * 1024;   // one CTA per SM
+constexpr int kBudget2 = 110 * 1024;   // two
+constexpr int kBudget3 = 72 * 1024;    // three
+constexpr int kBudget4 = 54 * 1024;    // four
 
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
   int rc;
-#define MOE_PLAN(step, slot, expr) \
+#define MOE_PLAN(expr) \
   if ((rc = (expr))) return rc;
-  MOE_PLAN(kStepRouter, 2, (plan_stream<kWfBf16, false, false, false, 1, 2, 4>(
-                               d.d, n, kBudgetTwo, &L->plan[kStepRouter][2])));
-  MOE_PLAN(kStepFc1, 0, (plan_stream<kWfMx, true, false, true, 4, 16, 1>(
-                            d.d, n, kBudgetOne, &L->plan[kStepFc1][0])));
-  MOE_PLAN(kStepFc1, 1, (plan_stream<kWfMx, true, false, true, 4, 16, 2>(
-                            d.d, n, kBudgetOne, &L->plan[kStepFc1][1])));
-  MOE_PLAN(kStepFc2, 0, (plan_stream<kWfMx, false, true, true, 16, 32, 1>(
-                            d.f, n, kBudgetTwo, &L->plan[kStepFc2][0])));
-  MOE_PLAN(kStepFc2, 1, (plan_stream<kWfMx, false, true, true, 16, 32, 2>(
-                            d.f, n, kBudgetTwo, &L->plan[kStepFc2][1])));
-  MOE_PLAN(kStepSh1, 2, (plan_stream<kWfBf16, true, false, false, 1, 4, 4>(
-                            d.d, n, kBudgetOne, &L->plan[kStepSh1][2])));
-  MOE_PLAN(kStepSh2, 2, (plan_stream<kWfBf16, false, true, false, 8, 16, 4>(
-                            d.f_shared, n, kBudgetTwo, &L->plan[kStepSh2][2])));
+  MOE_PLAN((plan_stream<kWfBf16, false, false, false, 1, 2, 4>(d.d, n, kBudget2,
+                                                                &L->plan[kStepRouter][2])));
+  MOE_PLAN((plan_stream<kWfMx, true, false, true, 4, 16, 1>(d.d, n, kBudget2,
+                                                             &L->plan[kStepFc1][0])));
+  MOE_PLAN((plan_stream<kWfMx, true, false, true, 4, 16, 2>(d.d, n, kBudget1,
+                                                             &L->plan[kStepFc1][1])));
+  MOE_PLAN((plan_stream<kWfMx, false, true, true, 16, 32, 1>(d.f, n, kBudget4,
+                                                              &L->plan[kStepFc2][0])));
+  MOE_PLAN((plan_stream<kWfMx, false, true, true, 16, 32, 2>(d.f, n, kBudget3,
+                                                              &L->plan[kStepFc2][1])));
+  MOE_PLAN((plan_stream<kWfBf16, true, false, false, 1, 4, 4>(d.d, n, kBudget1,
+                                                               &L->plan[kStepSh1][2])));
+  MOE_PLAN((plan_stream<kWfBf16, false, true, false, 8, 16, 4>(d.f_shared, n, kBudget3,
+                                                                &L->plan[kStepSh2][2])));
 #undef MOE_PLAN
   return MOE_OK;
 }

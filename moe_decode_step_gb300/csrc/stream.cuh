@@ -298,6 +298,26 @@ __device__ __forceinline__ int stream_pass_rows(int left) {
   return (RMAX >= 4 && left >= 4) ? 4 : ((RMAX >= 2 && left >= 2) ? 2 : 1);
 }
 
+// CTA c owns the contiguous item range [lo, hi).  Items are ordered expert by
+// expert, so a range is a few runs of tiles that share one activation set:
+// the consumers load activations once per (run, pass), not once per item.
+__device__ __forceinline__ void stream_range(int n_items, int& lo, int& hi) {
+  lo = (int)(((long long)blockIdx.x * n_items) / gridDim.x);
+  hi = (int)(((long long)(blockIdx.x + 1) * n_items) / gridDim.x);
+}
+
+// End of the run that starts at item `it` (same expert for routed steps; a
+// dense step is one run).
+template <bool ROUTED>
+__device__ __forceinline__ int stream_run_end(int it, int hi, int tiles) {
+  return ROUTED ? min(hi, (it / tiles + 1) * tiles) : hi;
+}
+
+template <bool ROUTED, int RW>
+__device__ __forceinline__ int stream_row0(int it, int tiles) {
+  return ROUTED ? (it % tiles) * RW : it * RW;
+}
+
 // Producer: lane 0 of warp 0 walks the CTA's items and issues the bulk copies.
 template <int WF, bool GLU, bool ROUTED, int SP, int RW, int RMAX>
 __device__ __forceinline__ void stream_produce(const StreamArgs& a, uint8_t* stages, uint64_t* full,
@@ -311,40 +331,49 @@ __device__ __forceinline__ void stream_produce(const StreamArgs& a, uint8_t* sta
   int tiles;
   const int n_items = stream_n_items<ROUTED, RW>(a, tiles);
   uint32_t stage = 0;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const StreamItem m = stream_item<ROUTED, RW>(a, it, tiles);
+  int lo, hi;
+  stream_range(n_items, lo, hi);
+  for (int it0 = lo; it0 < hi;) {
+    const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
+    const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
     const uint8_t* qe = a.q + (size_t)m.e * a.q_stride;
     for (int done = 0; done < m.pr; done += stream_pass_rows<RMAX>(m.pr - done)) {
-      for (int st = 0; st < SPI; ++st, ++stage) {
-        const int buf = (int)(stage % (uint32_t)a.NS);
-        const uint32_t use = stage / (uint32_t)a.NS;
-        if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, a.status);
-        const int r0 = m.row0 + st * SP;
-        const int nv = max(0, min(SP, a.N - r0));
-        uint8_t* dst = stages + (size_t)buf * a.stage_bytes;
-        if (WF == kWfMx) {
-          const uint8_t* se = a.s + (size_t)m.e * a.s_stride;
-          const uint32_t qb = (uint32_t)nv * (a.K / 2), sb = (uint32_t)nv * (a.K / 32);
-          mbar_arrive_expect_tx(&full[buf], G * (qb + sb));
-          if (nv > 0) {
-            bulk_g2s(dst, qe + (size_t)r0 * (a.K / 2), qb, &full[buf], pol);
-            bulk_g2s(dst + s_off, se + (size_t)r0 * (a.K / 32), sb, &full[buf], pol);
-            if (GLU) {
-              bulk_g2s(dst + half_bytes, qe + (size_t)(a.N + r0) * (a.K / 2), qb, &full[buf], pol);
-              bulk_g2s(dst + s_off + (size_t)SP * (a.K / 32), se + (size_t)(a.N + r0) * (a.K / 32),
-                       sb, &full[buf], pol);
+      for (int it = it0; it < run_end; ++it) {
+        const int row0 = stream_row0<ROUTED, RW>(it, tiles);
+        for (int st = 0; st < SPI; ++st, ++stage) {
+          const int buf = (int)(stage % (uint32_t)a.NS);
+          const uint32_t use = stage / (uint32_t)a.NS;
+          if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, a.status);
+          const int r0 = row0 + st * SP;
+          const int nv = max(0, min(SP, a.N - r0));
+          uint8_t* dst = stages + (size_t)buf * a.stage_bytes;
+          if (WF == kWfMx) {
+            const uint8_t* se = a.s + (size_t)m.e * a.s_stride;
+            const uint32_t qb = (uint32_t)nv * (a.K / 2), sb = (uint32_t)nv * (a.K / 32);
+            mbar_arrive_expect_tx(&full[buf], G * (qb + sb));
+            if (nv > 0) {
+              bulk_g2s(dst, qe + (size_t)r0 * (a.K / 2), qb, &full[buf], pol);
+              bulk_g2s(dst + s_off, se + (size_t)r0 * (a.K / 32), sb, &full[buf], pol);
+              if (GLU) {
+                bulk_g2s(dst + half_bytes, qe + (size_t)(a.N + r0) * (a.K / 2), qb, &full[buf],
+                         pol);
+                bulk_g2s(dst + s_off + (size_t)SP * (a.K / 32),
+                         se + (size_t)(a.N + r0) * (a.K / 32), sb, &full[buf], pol);
+              }
             }
-          }
-        } else {
-          const uint32_t wb = (uint32_t)nv * a.K * 2;
-          mbar_arrive_expect_tx(&full[buf], G * wb);
-          if (nv > 0) {
-            bulk_g2s(dst, qe + (size_t)r0 * a.K * 2, wb, &full[buf], pol);
-            if (GLU) bulk_g2s(dst + half_bytes, qe + (size_t)(a.N + r0) * a.K * 2, wb, &full[buf], pol);
+          } else {
+            const uint32_t wb = (uint32_t)nv * a.K * 2;
+            mbar_arrive_expect_tx(&full[buf], G * wb);
+            if (nv > 0) {
+              bulk_g2s(dst, qe + (size_t)r0 * a.K * 2, wb, &full[buf], pol);
+              if (GLU)
+                bulk_g2s(dst + half_bytes, qe + (size_t)(a.N + r0) * a.K * 2, wb, &full[buf], pol);
+            }
           }
         }
       }
     }
+    it0 = run_end;
   }
   // Drain: wait until the last use of every buffer has been consumed, so no
   // copy is still landing in this CTA's shared memory when it exits.
@@ -368,12 +397,15 @@ __device__ __forceinline__ int stream_shift(const StreamArgs& a, int pid) {
   return __ldcg(a.x_shift + stream_x_row<ROUTED>(a, pid));
 }
 
-// Consumers: one pass of R activation rows over one item.
+// Consumers: one pass of R activation rows over the run [it0, run_end) of
+// items that share them.  Activation slices, pair ids and scale shifts are
+// loaded once; every item then streams its SPI stages, reduces and finalises.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int R>
-__device__ __forceinline__ void stream_consume_pass(const StreamArgs& a, const StreamItem& m,
-                                                    int done, uint8_t* stages, uint64_t* full,
-                                                    uint64_t* empty, float* red, uint32_t& stage,
-                                                    int pp, int kw, int KW, int lane) {
+__device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const StreamItem& m,
+                                                   int done, int it0, int run_end, int tiles,
+                                                   uint8_t* stages, uint64_t* full,
+                                                   uint64_t* empty, float* red, uint32_t& stage,
+                                                   int& pp, int kw, int KW, int lane) {
   using Sh = StreamShape<WF, ACTH>;
   constexpr int G = GLU ? 2 : 1;
   constexpr int SPI = RW / SP;
@@ -385,88 +417,97 @@ __device__ __forceinline__ void stream_consume_pass(const StreamArgs& a, const S
   const int blk = kw * 32 + lane;
   const bool ok = blk * Sh::EPL < a.K;
   const int slab = kw * Sh::WARP_K;
+  const int cthreads = KW * 32;
+  const int ct = (int)threadIdx.x - 32;
 
+  int pid[R], shift[R];
   uint32_t act[R][Sh::AW];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int pid = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
+    pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
+    shift[r] = stream_shift<WF, ACTH, ROUTED>(a, pid[r]);
     if constexpr (WF == kWfMx && !ACTH) {
-      const int xr = stream_x_row<ROUTED>(a, pid);
-      act_load_mx_x(a.x + (size_t)xr * a.K, blk, ok, __ldcg(a.x_shift + xr), act[r]);
-    } else if constexpr (WF == kWfMx && ACTH) {
-      act_load_mx_h(a.h + (size_t)pid * a.K, blk, ok, stream_shift<WF, ACTH, ROUTED>(a, pid),
+      act_load_mx_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, blk, ok, shift[r],
                     act[r]);
+    } else if constexpr (WF == kWfMx && ACTH) {
+      act_load_mx_h(a.h + (size_t)pid[r] * a.K, blk, ok, shift[r], act[r]);
     } else if constexpr (!ACTH) {
-      act_load_bf_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid) * a.K, slab, lane, a.K, act[r]);
+      act_load_bf_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K, act[r]);
     } else {
-      act_load_bf_h(a.h + (size_t)pid * a.K, slab, lane, a.K, act[r]);
+      act_load_bf_h(a.h + (size_t)pid[r] * a.K, slab, lane, a.K, act[r]);
     }
   }
 
-  float v[V];
+  for (int it = it0; it < run_end; ++it) {
+    const int row0 = stream_row0<ROUTED, RW>(it, tiles);
+    float v[V];
 #pragma unroll
-  for (int st = 0; st < SPI; ++st) {
-    const int buf = (int)(stage % (uint32_t)a.NS);
-    mbar_wait(&full[buf], (stage / (uint32_t)a.NS) & 1u, a.status);
-    const uint8_t* sb = stages + (size_t)buf * a.stage_bytes;
+    for (int st = 0; st < SPI; ++st) {
+      const int buf = (int)(stage % (uint32_t)a.NS);
+      mbar_wait(&full[buf], (stage / (uint32_t)a.NS) & 1u, a.status);
+      const uint8_t* sb = stages + (size_t)buf * a.stage_bytes;
 #pragma unroll
-    for (int rr = 0; rr < SP; ++rr) {
-      const int j = st * SP + rr;
+      for (int rr = 0; rr < SP; ++rr) {
+        const int j = st * SP + rr;
 #pragma unroll
-      for (int gu = 0; gu < G; ++gu) {
-        float o[R];
-        if constexpr (WF == kWfMx) {
-          const uint8_t* qrow = sb + gu * half_bytes + (size_t)rr * (a.K / 2);
-          const uint8_t* srow = sb + s_off + (size_t)(gu * SP + rr) * (a.K / 32);
-          if constexpr (ACTH) row_dot_mx_h<R>(qrow, srow, blk, ok, act, o);
-          else row_dot_mx_x<R>(qrow, srow, blk, ok, act, o);
-        } else {
-          const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
-          if constexpr (ACTH) row_dot_bf_h<R>(wrow, slab, lane, a.K, act, o);
-          else row_dot_bf_x<R>(wrow, slab, lane, a.K, act, o);
+        for (int gu = 0; gu < G; ++gu) {
+          float o[R];
+          if constexpr (WF == kWfMx) {
+            const uint8_t* qrow = sb + gu * half_bytes + (size_t)rr * (a.K / 2);
+            const uint8_t* srow = sb + s_off + (size_t)(gu * SP + rr) * (a.K / 32);
+            if constexpr (ACTH) row_dot_mx_h<R>(qrow, srow, blk, ok, act, o);
+            else row_dot_mx_x<R>(qrow, srow, blk, ok, act, o);
+          } else {
+            const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
+            if constexpr (ACTH) row_dot_bf_h<R>(wrow, slab, lane, a.K, act, o);
+            else row_dot_bf_x<R>(wrow, slab, lane, a.K, act, o);
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
         }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[buf]);
+      ++stage;
+    }
+
+    // combine: lanes -> one value per lane group, then K slabs through shared memory
+    float second;
+    const float first = stream_reduce<V>(v, lane, second);
+    float* rb = red + (size_t)pp * 64 * KW;
+    if ((lane & ((1 << (5 - M)) - 1)) == 0) {
+      const int vi = lane >> (5 - M);
+      rb[vi * KW + kw] = first;
+      if (V > 32) rb[(32 + vi) * KW + kw] = second;
+    }
+    consumer_sync(cthreads);
+    for (int t = ct; t < RW * R; t += cthreads) {
+      const int j = t / R, r = t % R;
+      const int row = row0 + j;
+      if (row >= a.N) continue;
+      int p = pid[0], sh = shift[0];
 #pragma unroll
-        for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
+      for (int q = 1; q < R; ++q)
+        if (q == r) { p = pid[q]; sh = shift[q]; }
+      const float back = pow2f(sh);
+      float* dst = a.out + (size_t)p * a.N + row;
+      if constexpr (GLU) {
+        const float* pg = rb + ((j * R + r) * 2) * KW;
+        float g = 0.f, u = 0.f;
+        for (int w = 0; w < KW; ++w) { g += pg[w]; u += pg[KW + w]; }
+        g *= back;
+        u *= back;
+        const float hv = g / (1.0f + expf(-g)) * u;
+        *dst = hv;
+        if (a.out_amax) atomicMax(a.out_amax + p, __float_as_uint(fabsf(hv)));
+      } else {
+        const float* pv = rb + (j * R + r) * KW;
+        float acc = 0.f;
+        for (int w = 0; w < KW; ++w) acc += pv[w];
+        *dst = acc * back;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[buf]);
-    ++stage;
-  }
-
-  // combine: lanes -> one value per lane group, then K slabs through shared memory
-  float second;
-  const float first = stream_reduce<V>(v, lane, second);
-  float* rb = red + (size_t)pp * 64 * KW;
-  if ((lane & ((1 << (5 - M)) - 1)) == 0) {
-    const int vi = lane >> (5 - M);
-    rb[vi * KW + kw] = first;
-    if (V > 32) rb[(32 + vi) * KW + kw] = second;
-  }
-  const int cthreads = KW * 32;
-  consumer_sync(cthreads);
-  for (int t = (int)threadIdx.x - 32; t < RW * R; t += cthreads) {
-    const int j = t / R, r = t % R;
-    const int row = m.row0 + j;
-    if (row >= a.N) continue;
-    const int pid = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
-    const float back = pow2f(stream_shift<WF, ACTH, ROUTED>(a, pid));
-    float* dst = a.out + (size_t)pid * a.N + row;
-    if constexpr (GLU) {
-      const float* pg = rb + ((j * R + r) * 2) * KW;
-      float g = 0.f, u = 0.f;
-      for (int w = 0; w < KW; ++w) { g += pg[w]; u += pg[KW + w]; }
-      g *= back;
-      u *= back;
-      const float hv = g / (1.0f + expf(-g)) * u;
-      *dst = hv;
-      if (a.out_amax) atomicMax(a.out_amax + pid, __float_as_uint(fabsf(hv)));
-    } else {
-      const float* pv = rb + (j * R + r) * KW;
-      float acc = 0.f;
-      for (int w = 0; w < KW; ++w) acc += pv[w];
-      *dst = acc * back;
-    }
+    pp ^= 1;
   }
 }
 
@@ -500,27 +541,33 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   const int kw = warp - 1;
   int tiles;
   const int n_items = stream_n_items<ROUTED, RW>(a, tiles);
+  int lo, hi;
+  stream_range(n_items, lo, hi);
   uint32_t stage = 0;
   int pp = 0;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const StreamItem m = stream_item<ROUTED, RW>(a, it, tiles);
+  for (int it0 = lo; it0 < hi;) {
+    const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
+    const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
     for (int done = 0; done < m.pr;) {
       const int R = stream_pass_rows<RMAX>(m.pr - done);
       if (R == 1) {
-        stream_consume_pass<WF, GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, stages, full, empty, red,
-                                                               stage, pp, kw, KW, lane);
+        stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, it0, run_end, tiles,
+                                                              stages, full, empty, red, stage, pp,
+                                                              kw, KW, lane);
       } else if constexpr (RMAX >= 2) {
         if (R == 2) {
-          stream_consume_pass<WF, GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, stages, full, empty,
-                                                                 red, stage, pp, kw, KW, lane);
+          stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, it0, run_end, tiles,
+                                                                stages, full, empty, red, stage,
+                                                                pp, kw, KW, lane);
         } else if constexpr (RMAX >= 4) {
-          stream_consume_pass<WF, GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, stages, full, empty,
-                                                                 red, stage, pp, kw, KW, lane);
+          stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, it0, run_end, tiles,
+                                                                stages, full, empty, red, stage,
+                                                                pp, kw, KW, lane);
         }
       }
       done += R;
-      pp ^= 1;
     }
+    it0 = run_end;
   }
 }
 

@@ -43,35 +43,39 @@ tail_kernel(const TailArgs a) {
   const int per_cta = a.d / kTailCluster;
   const int n = c * per_cta + (int)threadIdx.x * 4;
   const bool ok = (int)threadIdx.x * 4 < per_cta;
-  __shared__ float s_w[32];
   __shared__ float s_warp[8];
   __shared__ float s_ss;
+  // gamma is a static weight: it may be read before the predecessor finishes
+  uint2 g = make_uint2(0, 0);
+  if (ok) g = *reinterpret_cast<const uint2*>(a.gamma + n);
   pdl_launch_dependents();
   pdl_wait_prerequisites();
-  for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_w[i] = __ldcg(a.topk_w + b * a.k + i);
-  __syncthreads();
   float z[4] = {0.f, 0.f, 0.f, 0.f};
   float yr[4] = {0.f, 0.f, 0.f, 0.f};
   if (ok) {
     const size_t o = (size_t)b * a.d + n;
+    // every load of this thread is issued before the first use
+    const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.y_s + o));
+    const uint2 rb = __ldcg(reinterpret_cast<const uint2*>(a.residual + o));
     const float* yp = a.y_pair + (size_t)b * a.k * a.d + n;
     for (int j0 = 0; j0 < a.k; j0 += kTailBatch) {
       float4 v[kTailBatch];
-#pragma unroll
-      for (int j = 0; j < kTailBatch; ++j)
-        v[j] = (j0 + j < a.k) ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)(j0 + j) * a.d))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      float w[kTailBatch];
 #pragma unroll
       for (int j = 0; j < kTailBatch; ++j) {
-        const float w = (j0 + j < a.k) ? s_w[j0 + j] : 0.f;
-        yr[0] = fmaf(w, v[j].x, yr[0]);
-        yr[1] = fmaf(w, v[j].y, yr[1]);
-        yr[2] = fmaf(w, v[j].z, yr[2]);
-        yr[3] = fmaf(w, v[j].w, yr[3]);
+        const bool in = j0 + j < a.k;
+        v[j] = in ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)(j0 + j) * a.d))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[j] = in ? __ldcg(a.topk_w + b * a.k + j0 + j) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kTailBatch; ++j) {
+        yr[0] = fmaf(w[j], v[j].x, yr[0]);
+        yr[1] = fmaf(w[j], v[j].y, yr[1]);
+        yr[2] = fmaf(w[j], v[j].z, yr[2]);
+        yr[3] = fmaf(w[j], v[j].w, yr[3]);
       }
     }
-    const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.y_s + o));
-    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
     z[0] = bf16_bits_to_f32(rb.x & 0xFFFFu) + yr[0] + ys.x;
     z[1] = bf16_bits_to_f32(rb.x >> 16) + yr[1] + ys.y;
     z[2] = bf16_bits_to_f32(rb.y & 0xFFFFu) + yr[2] + ys.z;
@@ -97,7 +101,6 @@ tail_kernel(const TailArgs a) {
   const float inv = 1.0f / sqrtf(total / (float)a.d + a.eps);
   if (ok) {
     const size_t o = (size_t)b * a.d + n;
-    const uint2 g = *reinterpret_cast<const uint2*>(a.gamma + n);
     float v[4];
     v[0] = z[0] * inv * bf16_bits_to_f32(g.x & 0xFFFFu);
     v[1] = z[1] * inv * bf16_bits_to_f32(g.x >> 16);

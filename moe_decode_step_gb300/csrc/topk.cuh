@@ -77,17 +77,32 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   __shared__ float s_score[32];
   __shared__ int s_cnt;
   __shared__ unsigned s_last;
+  // the bias is a static weight: it may be read before the predecessor finishes
+  const bool valid = t < a.E;
+  const float bias = valid ? __ldg(a.bias + t) : 0.f;
   pdl_launch_dependents();
   pdl_wait_prerequisites();
 
-  // ---- scores and keys ----
-  const bool valid = t < a.E;
+  // ---- scores and keys (the x row for the f16 shift is loaded alongside) ----
+  constexpr int kXPer = 8;   // d <= 8192 = kXPer * 1024
+  uint32_t xm = 0;
+  {
+    const uint16_t* xr = a.x + (size_t)b * a.d;
+    uint16_t xv[kXPer];
+#pragma unroll
+    for (int i = 0; i < kXPer; ++i) {
+      const int e = t + i * (int)blockDim.x;
+      xv[i] = e < a.d ? xr[e] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int i = 0; i < kXPer; ++i) xm = max(xm, (uint32_t)(xv[i] & 0x7FFFu));
+  }
   float score = 0.f;
   uint32_t u = 0;
   if (valid) {
     const float l = __ldcg(a.logits + (size_t)b * a.E + t);
     score = 1.0f / (1.0f + expf(-l));
-    u = float_order_bits(score + __ldg(a.bias + t));
+    u = float_order_bits(score + bias);
   }
   // ---- k-th largest u (with multiplicity) ----
   uint32_t T = 0;
@@ -127,10 +142,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   }
   // ---- f16 scaling shift of x row b ----
   {
-    uint32_t m = 0;
-    const uint16_t* xr = a.x + (size_t)b * a.d;
-    for (int i = t; i < a.d; i += blockDim.x) m = max(m, (uint32_t)(xr[i] & 0x7FFFu));
-    m = __reduce_max_sync(0xffffffffu, m);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, xm);
     __syncthreads();
     if (lane == 0) s_warp[warp] = (int)m;
     __syncthreads();
@@ -142,12 +154,16 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   }
 
   // ---- the last CTA groups pairs by expert ----
-  __threadfence();
-  __syncthreads();
-  if (t == 0) s_last = (atomicAdd(a.done, 1u) == (unsigned)(gridDim.x - 1)) ? 1u : 0u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  if (gridDim.x > 1) {
+    __threadfence();
+    __syncthreads();
+    if (t == 0) s_last = (atomicAdd(a.done, 1u) == (unsigned)(gridDim.x - 1)) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  } else {
+    __syncthreads();
+  }
   __shared__ unsigned long long s_mask[1024];
   __shared__ int32_t s_idx[64 * 32];
   const int P = a.B * a.k;
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   if (t == 0) {
     *a.n_active = n_act;
     a.active_off[n_act] = total_pairs;
-    *a.done = 0u;
+    if (gridDim.x > 1) *a.done = 0u;
   }
 }
 
