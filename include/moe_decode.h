@@ -172,6 +172,24 @@ int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, 
 int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
                       uint8_t* s, int layout);
 
+/* Router + top-k that allocates nothing (no counterpart in the paper: it
+ * exists for callers that cannot call cudaMalloc, e.g. code running inside a
+ * stream capture it does not own, runtimes that hand over a fixed memory pool,
+ * or callers that must not synchronise the device).  It needs no layer handle:
+ * router_w device bf16 [E][d], router_bias device fp32 [E], x device bf16
+ * [B][d]; outputs idx device int32 [B][k] and w device fp32 [B][k], exactly
+ * as moe_router_topk.  Its scratch (logits, ticket, routing tables; 284,928
+ * bytes) is one static device array that every GPU loading this library holds
+ * until the process exits.  Limits: B <= 64, E <= 1024, k <= 32, d % 256 == 0,
+ * d <= 8192; larger sizes return MOE_ERR_UNSUPPORTED.  The first call on each
+ * device (and the first with a new d) does a one-time set-up (fetches the
+ * array's device address, sizes the launch): make that call before any stream
+ * capture.  Every call shares the one array, so calls that overlap on the GPU
+ * (two streams, or two threads) race; calls in one stream are safe. */
+int moe_router_topk_noalloc(void* stream, const void* router_w, const float* router_bias,
+                            const void* x, int B, int d, int n_experts, int top_k,
+                            float routed_scale, int32_t* idx, float* w);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 

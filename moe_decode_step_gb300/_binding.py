@@ -64,6 +64,9 @@ _PROTOS = {
     "mxfp4_pack": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, ctypes.c_int]),
     "mxfp4_pack_device": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int64, _P, _P,
                                          ctypes.c_int]),
+    "moe_router_topk_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
+                                               _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_int, []),
 }

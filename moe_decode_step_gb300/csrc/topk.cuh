@@ -70,7 +70,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
+static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   __shared__ int s_warp[33];
   __shared__ uint64_t s_key[32];
