@@ -142,11 +142,13 @@ int moe_set_prefetch_next(moe_layer_t layer, moe_layer_t next);
  * (0 = ok, else a moe_status such as MOE_ERR_TIMEOUT); clears it. */
 int moe_layer_status(moe_layer_t layer, int* device_status);
 
-/* Per-phase timing of forward calls (CUDA events on the launching streams).
+/* Per-phase timing of forward calls (CUDA events on the launching stream;
+ * under stream capture they become event-record nodes of the graph).
  * enable != 0 records events around each phase from the next forward on.
  * moe_get_timing synchronises and writes up to n floats (microseconds) for
- * the last forward: [0] router+top-k, [1] routed FC1, [2] routed FC2,
- * [3] shared expert (side stream), [4] tail, [5] whole layer. */
+ * the last forward: [0] router + top-k, [1] FC1 (shared then routed gate/up),
+ * [2] FC2 (shared then routed down), [3] always 0 (the shared expert has no
+ * phase of its own), [4] tail, [5] whole layer. */
 int moe_set_timing(moe_layer_t layer, int enable);
 int moe_get_timing(moe_layer_t layer, float* us, int n);
 

@@ -1,11 +1,15 @@
 // C ABI of the MoE decode layer (see include/moe_decode.h for the contract).
 //
-// One forward, main stream (kernels chained with programmatic dependent launch):
-//   router GEMV (streamed bf16) -> top-k + routing tables -> routed FC1
-//   (streamed MXFP4, SwiGLU) -> routed FC2 (streamed MXFP4) -> [join] -> tail
-// side stream, forked at entry: shared FC1 -> shared FC2 (streamed bf16)
-// third stream (chained layers only): L2 prefetch of the next layer's router
-// and shared-expert weights.
+// One forward = five kernels on the caller's stream, chained with programmatic
+// dependent launch:
+//   router GEMV (streamed bf16) -> top-k + routing tables
+//   -> FC1: shared gate/up (bf16) then routed gate/up (MXFP4), SwiGLU
+//   -> FC2: shared down (bf16) then routed down (MXFP4)
+//   -> tail (combine + residual + RMSNorm)
+// The shared expert streams first inside FC1/FC2: its weights do not depend on
+// the routing, so FC1 starts them while top-k is still finishing.
+// Optional second stream (chained layers only): L2 prefetch of the next
+// layer's router and shared-expert weights.
 // No allocation, no host synchronisation: capturable into a CUDA graph.
 #include <cuda_runtime.h>
 
@@ -40,8 +44,7 @@ inline int cuda_fail(cudaError_t e) {
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-enum { kTimeRouterStart, kTimeRouterEnd, kTimeFc1End, kTimeFc2End, kTimeTailEnd, kTimeSharedStart,
-       kTimeSharedEnd, kNumTimeEvents };
+enum { kTimeRouterStart, kTimeRouterEnd, kTimeFc1End, kTimeFc2End, kTimeTailEnd, kNumTimeEvents };
 
 struct Workspace {
   float* logits;
@@ -69,7 +72,7 @@ struct StreamPlan {
   int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0;
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kStepSh1, kStepSh2, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kNumSteps };
 
 }  // namespace
 
@@ -80,12 +83,12 @@ struct moe_layer {
   int n_sm = 0;
   void* ws_base = nullptr;
   Workspace ws{};
-  cudaStream_t side = nullptr, pref = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_pref = nullptr;
+  cudaStream_t pref = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_pref = nullptr;
   cudaEvent_t ev_time[kNumTimeEvents] = {};
   bool timing = false, timed_once = false;
   moe_layer* next = nullptr;
-  StreamPlan plan[kNumSteps][3];   // by RMAX slot (1, 2, 4)
+  StreamPlan plan[kNumSteps][3];   // by batch class (B = 1, B <= 8, B > 8)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
 };
 
@@ -136,20 +139,43 @@ int validate_dims(const moe_dims_t& d) {
   return MOE_OK;
 }
 
-// Size the stage ring for one instantiation and record its launch shape.
-template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
-int plan_stream(int K, int n_sm, int smem_budget, StreamPlan* p) {
-  using Sh = StreamShape<WF, ACTH>;
-  const int KW = (K + Sh::WARP_K - 1) / Sh::WARP_K;
-  const int G = GLU ? 2 : 1;
+// Kernel instantiations.  FC1 and FC2 each stream the shared expert (dense
+// bf16, segment A) and the routed experts (MXFP4, segment B) in one launch;
+// the variant is picked by batch class (B = 1, B <= 8, B > 8), which sets how
+// many activation rows one pass carries.
+using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 2, 4>;
+template <int R> using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R>;
+template <int R> using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 4, 16, R>;
+template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 4, 16, R>;
+template <int R> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16, 32, R>;
+#define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 2, 4>
+#define MOE_FC1_KERNEL(RS, RR) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg<RR>, false>
+#define MOE_FC2_KERNEL(RS, RR) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<RR>, true>
+
+int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
+
+// Shared-memory budget per CTA: how many CTAs of a step share an SM, chosen
+// from each instantiation's register footprint.
+constexpr int kBudget1 = 220 * 1024;   // one CTA per SM
+constexpr int kBudget2 = 110 * 1024;   // two
+constexpr int kBudget3 = 72 * 1024;    // three
+constexpr int kBudget4 = 54 * 1024;    // four
+
+// Launch shape for a kernel whose segments have the given row lengths.
+template <class A, class B, typename Kern>
+int plan_kernel(Kern kern, int KA, int KB, int n_sm, int budget, StreamPlan* p) {
+  using ShA = StreamShape<A::WF, A::ACTH>;
+  using ShB = StreamShape<B::WF, B::ACTH>;
+  const int KW = std::max((KA + ShA::WARP_K - 1) / ShA::WARP_K, (KB + ShB::WARP_K - 1) / ShB::WARP_K);
+  const size_t sa = (A::GLU ? 2 : 1) * stream_rows_bytes(A::WF, KA, A::SP);
+  const size_t sb = (B::GLU ? 2 : 1) * stream_rows_bytes(B::WF, KB, B::SP);
   StreamPlan r;
   r.threads = 32 * (KW + 1);
-  r.stage_bytes = (int)((G * stream_rows_bytes(WF, K, SP) + 127) / 128 * 128);
+  r.stage_bytes = (int)((std::max(sa, sb) + 127) / 128 * 128);
   const int red_bytes = 2 * 64 * KW * 4;
-  r.NS = std::min(8, (smem_budget - red_bytes) / (r.stage_bytes + 16));
+  r.NS = std::min(8, (budget - red_bytes) / (r.stage_bytes + 16));
   if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
-  auto kern = stream_gemv_kernel<WF, GLU, ACTH, ROUTED, SP, RW, RMAX>;
   MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
   int occ = 0;
   MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, r.threads, r.smem));
@@ -159,40 +185,26 @@ int plan_stream(int K, int n_sm, int smem_budget, StreamPlan* p) {
   return MOE_OK;
 }
 
-// Kernel instantiations of the five streaming steps.
-#define MOE_ROUTER_KERNEL(R) stream_gemv_kernel<kWfBf16, false, false, false, 1, 2, R>
-#define MOE_FC1_KERNEL(R) stream_gemv_kernel<kWfMx, true, false, true, 4, 16, R>
-#define MOE_FC2_KERNEL(R) stream_gemv_kernel<kWfMx, false, true, true, 16, 32, R>
-#define MOE_SH1_KERNEL(R) stream_gemv_kernel<kWfBf16, true, false, false, 1, 4, R>
-#define MOE_SH2_KERNEL(R) stream_gemv_kernel<kWfBf16, false, true, false, 8, 16, R>
-
-// Shared-memory budget per CTA: how many CTAs of a step share an SM, chosen
-// from each instantiation's register footprint.
-constexpr int kBudget1 = 220 * 1024;   // one CTA per SM
-constexpr int kBudget2 = 110 * 1024;   // two
-constexpr int kBudget3 = 72 * 1024;    // three
-constexpr int kBudget4 = 54 * 1024;    // four
-
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
   int rc;
 #define MOE_PLAN(expr) \
   if ((rc = (expr))) return rc;
-  MOE_PLAN((plan_stream<kWfBf16, false, false, false, 1, 2, 4>(d.d, n, kBudget2,
-                                                                &L->plan[kStepRouter][2])));
-  MOE_PLAN((plan_stream<kWfMx, true, false, true, 4, 16, 1>(d.d, n, kBudget2,
-                                                             &L->plan[kStepFc1][0])));
-  MOE_PLAN((plan_stream<kWfMx, true, false, true, 4, 16, 2>(d.d, n, kBudget1,
-                                                             &L->plan[kStepFc1][1])));
-  MOE_PLAN((plan_stream<kWfMx, false, true, true, 16, 32, 1>(d.f, n, kBudget4,
-                                                              &L->plan[kStepFc2][0])));
-  MOE_PLAN((plan_stream<kWfMx, false, true, true, 16, 32, 2>(d.f, n, kBudget3,
-                                                              &L->plan[kStepFc2][1])));
-  MOE_PLAN((plan_stream<kWfBf16, true, false, false, 1, 4, 4>(d.d, n, kBudget1,
-                                                               &L->plan[kStepSh1][2])));
-  MOE_PLAN((plan_stream<kWfBf16, false, true, false, 8, 16, 4>(d.f_shared, n, kBudget3,
-                                                                &L->plan[kStepSh2][2])));
+  MOE_PLAN((plan_kernel<RouterCfg, RouterCfg>(MOE_ROUTER_KERNEL, d.d, d.d, n, kBudget2,
+                                              &L->plan[kStepRouter][0])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg<1>>(MOE_FC1_KERNEL(1, 1), d.d, d.d, n, kBudget2,
+                                              &L->plan[kStepFc1][0])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg<2>>(MOE_FC1_KERNEL(2, 2), d.d, d.d, n, kBudget1,
+                                              &L->plan[kStepFc1][1])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg<2>>(MOE_FC1_KERNEL(4, 2), d.d, d.d, n, kBudget1,
+                                              &L->plan[kStepFc1][2])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<1>, Fc2Cfg<1>>(MOE_FC2_KERNEL(1, 1), d.f_shared, d.f, n, kBudget4,
+                                              &L->plan[kStepFc2][0])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<2>, Fc2Cfg<2>>(MOE_FC2_KERNEL(2, 2), d.f_shared, d.f, n, kBudget3,
+                                              &L->plan[kStepFc2][1])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<4>, Fc2Cfg<2>>(MOE_FC2_KERNEL(4, 2), d.f_shared, d.f, n, kBudget3,
+                                              &L->plan[kStepFc2][2])));
 #undef MOE_PLAN
   return MOE_OK;
 }
@@ -259,8 +271,8 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.B = B;
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
-  int rc = launch_step(L, MOE_ROUTER_KERNEL(4), L->plan[kStepRouter][2], a,
-                       (d.n_experts + 1) / 2, st, false);
+  int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, (d.n_experts + 1) / 2,
+                       st, false);
   if (rc) return rc;
   TopkArgs t;
   t.logits = L->ws.logits;
@@ -284,57 +296,66 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   return MOE_OK;
 }
 
-int launch_routed(moe_layer* L, cudaStream_t st, const void* x, int B) {
-  const moe_dims_t& d = L->dims;
-  const bool one = B == 1;
-  StreamArgs a = base_args(L);
-  a.q = L->w.w_gu_q;
-  a.s = L->w.w_gu_s;
-  a.q_stride = L->q_gu_stride;
-  a.s_stride = L->s_gu_stride;
-  a.K = d.d;
-  a.N = d.f;
-  a.x = static_cast<const uint16_t*>(x);
-  a.out = L->ws.h;
-  a.out_amax = L->ws.h_amax;
-  int rc = one ? launch_step(L, MOE_FC1_KERNEL(1), L->plan[kStepFc1][0], a, 0, st, true)
-               : launch_step(L, MOE_FC1_KERNEL(2), L->plan[kStepFc1][1], a, 0, st, true);
-  if (rc) return rc;
-  if (L->timing) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  StreamArgs b = base_args(L);
-  b.q = L->w.w_d_q;
-  b.s = L->w.w_d_s;
-  b.q_stride = L->q_d_stride;
-  b.s_stride = L->s_d_stride;
-  b.K = d.f;
-  b.N = d.d;
-  b.h = L->ws.h;
-  b.h_amax = L->ws.h_amax;
-  b.out = L->ws.y_pair;
-  return one ? launch_step(L, MOE_FC2_KERNEL(1), L->plan[kStepFc2][0], b, 0, st, true)
-             : launch_step(L, MOE_FC2_KERNEL(2), L->plan[kStepFc2][1], b, 0, st, true);
+template <typename K>
+int launch_dual(K kern, const StreamPlan& p, StreamArgs a0, StreamArgs a1, cudaStream_t st) {
+  a0.NS = a1.NS = p.NS;
+  a0.stage_bytes = a1.stage_bytes = p.stage_bytes;
+  MOE_CUDA(launch_ex(kern, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, a0, a1));
+  return MOE_OK;
 }
 
-int launch_shared(moe_layer* L, cudaStream_t st, const void* x, int B) {
+// FC1: shared gate/up (bf16) then routed gate/up (MXFP4), SwiGLU epilogues.
+int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   const moe_dims_t& d = L->dims;
-  StreamArgs a = base_args(L);
-  a.q = static_cast<const uint8_t*>(L->w.shared_gu);
-  a.K = d.d;
-  a.N = d.f_shared;
-  a.B = B;
-  a.x = static_cast<const uint16_t*>(x);
-  a.out = L->ws.hs;
-  int rc = launch_step(L, MOE_SH1_KERNEL(4), L->plan[kStepSh1][2], a, (d.f_shared + 3) / 4, st,
-                       false);
-  if (rc) return rc;
-  StreamArgs b = base_args(L);
-  b.q = static_cast<const uint8_t*>(L->w.shared_d);
-  b.K = d.f_shared;
-  b.N = d.d;
-  b.B = B;
-  b.h = L->ws.hs;
-  b.out = L->ws.y_s;
-  return launch_step(L, MOE_SH2_KERNEL(4), L->plan[kStepSh2][2], b, (d.d + 15) / 16, st, true);
+  StreamArgs sa = base_args(L);
+  sa.q = static_cast<const uint8_t*>(L->w.shared_gu);
+  sa.K = d.d;
+  sa.N = d.f_shared;
+  sa.B = B;
+  sa.x = static_cast<const uint16_t*>(x);
+  sa.out = L->ws.hs;
+  StreamArgs ra = base_args(L);
+  ra.q = L->w.w_gu_q;
+  ra.s = L->w.w_gu_s;
+  ra.q_stride = L->q_gu_stride;
+  ra.s_stride = L->s_gu_stride;
+  ra.K = d.d;
+  ra.N = d.f;
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.out = L->ws.h;
+  ra.out_amax = L->ws.h_amax;
+  switch (batch_class(B)) {
+    case 0: return launch_dual(MOE_FC1_KERNEL(1, 1), L->plan[kStepFc1][0], sa, ra, st);
+    case 1: return launch_dual(MOE_FC1_KERNEL(2, 2), L->plan[kStepFc1][1], sa, ra, st);
+    default: return launch_dual(MOE_FC1_KERNEL(4, 2), L->plan[kStepFc1][2], sa, ra, st);
+  }
+}
+
+// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).
+int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
+  const moe_dims_t& d = L->dims;
+  StreamArgs sa = base_args(L);
+  sa.q = static_cast<const uint8_t*>(L->w.shared_d);
+  sa.K = d.f_shared;
+  sa.N = d.d;
+  sa.B = B;
+  sa.h = L->ws.hs;
+  sa.out = L->ws.y_s;
+  StreamArgs ra = base_args(L);
+  ra.q = L->w.w_d_q;
+  ra.s = L->w.w_d_s;
+  ra.q_stride = L->q_d_stride;
+  ra.s_stride = L->s_d_stride;
+  ra.K = d.f;
+  ra.N = d.d;
+  ra.h = L->ws.h;
+  ra.h_amax = L->ws.h_amax;
+  ra.out = L->ws.y_pair;
+  switch (batch_class(B)) {
+    case 0: return launch_dual(MOE_FC2_KERNEL(1, 1), L->plan[kStepFc2][0], sa, ra, st);
+    case 1: return launch_dual(MOE_FC2_KERNEL(2, 2), L->plan[kStepFc2][1], sa, ra, st);
+    default: return launch_dual(MOE_FC2_KERNEL(4, 2), L->plan[kStepFc2][2], sa, ra, st);
+  }
 }
 
 int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg,
@@ -394,16 +415,11 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-  // side stream: shared expert, overlapping the router and the routed experts
-  MOE_CUDA(cudaStreamWaitEvent(L->side, L->ev_fork, 0));
-  if (tm) MOE_CUDA(record_time(L, kTimeSharedStart, L->side));
-  if ((rc = launch_shared(L, L->side, x, B))) return rc;
-  if (tm) MOE_CUDA(record_time(L, kTimeSharedEnd, L->side));
-  MOE_CUDA(cudaEventRecord(L->ev_join, L->side));
   if ((rc = launch_prefetch(L))) return rc;
-  if ((rc = launch_routed(L, st, x, B))) return rc;
+  if ((rc = launch_fc1(L, st, x, B))) return rc;
+  if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
+  if ((rc = launch_fc2(L, st, B))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
-  MOE_CUDA(cudaStreamWaitEvent(st, L->ev_join, 0));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
   if (tm) {
@@ -479,10 +495,8 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   };
   cudaError_t e;
   if ((e = cudaMemset(L->ws_base, 0, bytes)) != cudaSuccess) return fail(e);
-  if ((e = cudaStreamCreateWithFlags(&L->side, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamCreateWithFlags(&L->pref, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
   if ((e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
-  if ((e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
@@ -500,10 +514,8 @@ int moe_layer_destroy(moe_layer_t L) {
   cudaGetDevice(&prev);
   cudaSetDevice(L->device);
   cudaDeviceSynchronize();
-  if (L->side) cudaStreamDestroy(L->side);
   if (L->pref) cudaStreamDestroy(L->pref);
   if (L->ev_fork) cudaEventDestroy(L->ev_fork);
-  if (L->ev_join) cudaEventDestroy(L->ev_join);
   if (L->ev_pref) cudaEventDestroy(L->ev_pref);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if (L->ev_time[i]) cudaEventDestroy(L->ev_time[i]);
@@ -574,7 +586,6 @@ int moe_set_prefetch_next(moe_layer_t L, moe_layer_t next) {
 
 int moe_layer_status(moe_layer_t L, int* device_status) {
   if (!L || !device_status) return MOE_ERR_INVALID_ARG;
-  MOE_CUDA(cudaStreamSynchronize(L->side));
   MOE_CUDA(cudaStreamSynchronize(L->pref));
   MOE_CUDA(cudaDeviceSynchronize());
   int v = 0;
@@ -595,12 +606,11 @@ int moe_get_timing(moe_layer_t L, float* us, int n) {
   if (!L || !us || n < 0) return MOE_ERR_INVALID_ARG;
   if (!L->timed_once) return MOE_ERR_INVALID_ARG;
   MOE_CUDA(cudaEventSynchronize(L->ev_time[kTimeTailEnd]));
-  MOE_CUDA(cudaEventSynchronize(L->ev_time[kTimeSharedEnd]));
   float t[6];
   MOE_CUDA(cudaEventElapsedTime(&t[0], L->ev_time[kTimeRouterStart], L->ev_time[kTimeRouterEnd]));
   MOE_CUDA(cudaEventElapsedTime(&t[1], L->ev_time[kTimeRouterEnd], L->ev_time[kTimeFc1End]));
   MOE_CUDA(cudaEventElapsedTime(&t[2], L->ev_time[kTimeFc1End], L->ev_time[kTimeFc2End]));
-  MOE_CUDA(cudaEventElapsedTime(&t[3], L->ev_time[kTimeSharedStart], L->ev_time[kTimeSharedEnd]));
+  t[3] = 0.f;   // the shared expert streams inside FC1 and FC2
   MOE_CUDA(cudaEventElapsedTime(&t[4], L->ev_time[kTimeFc2End], L->ev_time[kTimeTailEnd]));
   MOE_CUDA(cudaEventElapsedTime(&t[5], L->ev_time[kTimeRouterStart], L->ev_time[kTimeTailEnd]));
   for (int i = 0; i < n && i < 6; ++i) us[i] = t[i] * 1000.f;
@@ -609,7 +619,7 @@ int moe_get_timing(moe_layer_t L, float* us, int n) {
 
 int moe_launches_per_forward(moe_layer_t L, int B) {
   if (!L || B < 1 || B > L->dims.max_batch) return -1;
-  return 7;   // router, top-k, shared FC1, shared FC2, routed FC1, routed FC2, tail
+  return 5;   // router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {

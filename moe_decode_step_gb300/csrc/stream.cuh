@@ -318,21 +318,17 @@ __device__ __forceinline__ int stream_row0(int it, int tiles) {
   return ROUTED ? (it % tiles) * RW : it * RW;
 }
 
-// Producer: lane 0 of warp 0 walks the CTA's items and issues the bulk copies.
+// Producer: lane 0 of warp 0 issues the bulk copies for items [lo, hi) of one
+// step, continuing the CTA's running stage counter.
 template <int WF, bool GLU, bool ROUTED, int SP, int RW, int RMAX>
-__device__ __forceinline__ void stream_produce(const StreamArgs& a, uint8_t* stages, uint64_t* full,
-                                               uint64_t* empty) {
+__device__ __forceinline__ void stream_produce_range(const StreamArgs& a, int lo, int hi, int tiles,
+                                                     uint8_t* stages, uint64_t* full,
+                                                     uint64_t* empty, uint32_t& stage) {
   constexpr int G = GLU ? 2 : 1;
   constexpr int SPI = RW / SP;
-  if (ROUTED) pdl_wait_prerequisites();
   const uint64_t pol = policy_evict_first();
   const size_t half_bytes = WF == kWfMx ? (size_t)SP * (a.K / 2) : (size_t)SP * a.K * 2;
   const size_t s_off = (size_t)G * half_bytes;
-  int tiles;
-  const int n_items = stream_n_items<ROUTED, RW>(a, tiles);
-  uint32_t stage = 0;
-  int lo, hi;
-  stream_range(n_items, lo, hi);
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
@@ -375,8 +371,11 @@ __device__ __forceinline__ void stream_produce(const StreamArgs& a, uint8_t* sta
     }
     it0 = run_end;
   }
-  // Drain: wait until the last use of every buffer has been consumed, so no
-  // copy is still landing in this CTA's shared memory when it exits.
+}
+
+// Drain: wait until the last use of every buffer has been consumed, so no copy
+// is still landing in this CTA's shared memory when it exits.
+__device__ __forceinline__ void stream_drain(const StreamArgs& a, uint64_t* empty, uint32_t stage) {
   for (int b = 0; b < a.NS && (uint32_t)b < stage; ++b) {
     const uint32_t uses = (stage - (uint32_t)b + (uint32_t)a.NS - 1) / (uint32_t)a.NS;
     mbar_wait(&empty[b], (uses - 1) & 1u, a.status);
@@ -511,40 +510,12 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
   }
 }
 
-// Kernel: warp 0 produces, warps 1..KW consume (KW = blockDim.x / 32 - 1).
-// Dynamic shared memory: NS stages, NS full + NS empty mbarriers, 2 x 64 x KW
-// floats of cross-slab partials.
+// Consumers: items [lo, hi) of one step, run by run, pass by pass.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
-__global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a) {
-  static_assert(RW % SP == 0, "an item is a whole number of stages");
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KW = (int)(blockDim.x >> 5) - 1;
-  uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.NS * a.stage_bytes);
-  uint64_t* empty = full + a.NS;
-  float* red = reinterpret_cast<float*>(empty + a.NS);
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < a.NS; ++b) {
-      mbar_init(&full[b], 1);
-      mbar_init(&empty[b], (uint32_t)KW);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-  pdl_launch_dependents();
-  if (warp == 0) {
-    if (lane == 0) stream_produce<WF, GLU, ROUTED, SP, RW, RMAX>(a, stages, full, empty);
-    return;
-  }
-  pdl_wait_prerequisites();
-  const int kw = warp - 1;
-  int tiles;
-  const int n_items = stream_n_items<ROUTED, RW>(a, tiles);
-  int lo, hi;
-  stream_range(n_items, lo, hi);
-  uint32_t stage = 0;
-  int pp = 0;
+__device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
+                                                     uint8_t* stages, uint64_t* full,
+                                                     uint64_t* empty, float* red, uint32_t& stage,
+                                                     int& pp, int kw, int KW, int lane) {
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
@@ -569,6 +540,118 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
     }
     it0 = run_end;
   }
+}
+
+// Compile-time description of one streaming step.
+template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_>
+struct StreamCfg {
+  static constexpr int WF = WF_;
+  static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_;
+  static constexpr int SP = SP_, RW = RW_, RMAX = RMAX_;
+  static_assert(RW % SP == 0, "an item is a whole number of stages");
+};
+
+template <class C>
+__device__ __forceinline__ void cfg_produce(const StreamArgs& a, uint8_t* stages, uint64_t* full,
+                                            uint64_t* empty, uint32_t& stage) {
+  int tiles, lo, hi;
+  const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
+  stream_range(n, lo, hi);
+  stream_produce_range<C::WF, C::GLU, C::ROUTED, C::SP, C::RW, C::RMAX>(a, lo, hi, tiles, stages,
+                                                                       full, empty, stage);
+}
+
+template <class C>
+__device__ __forceinline__ void cfg_consume(const StreamArgs& a, uint8_t* stages, uint64_t* full,
+                                            uint64_t* empty, float* red, uint32_t& stage, int& pp,
+                                            int kw, int KW, int lane) {
+  int tiles, lo, hi;
+  const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
+  stream_range(n, lo, hi);
+  stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX>(
+      a, lo, hi, tiles, stages, full, empty, red, stage, pp, kw, KW, lane);
+}
+
+// Shared-memory carve-up common to both kernels.
+struct StreamSmem {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  float* red;
+};
+
+__device__ __forceinline__ StreamSmem stream_smem_init(uint8_t* smem, int NS, int stage_bytes,
+                                                       int KW) {
+  StreamSmem m;
+  m.stages = smem;
+  m.full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
+  m.empty = m.full + NS;
+  m.red = reinterpret_cast<float*>(m.empty + NS);
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NS; ++b) {
+      mbar_init(&m.full[b], 1);
+      mbar_init(&m.empty[b], (uint32_t)KW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  return m;
+}
+
+// Single step.  Warp 0 produces, warps 1..KW consume (KW = blockDim.x/32 - 1).
+// Dynamic shared memory: NS stages, NS full + NS empty mbarriers, 2 x 64 x KW
+// floats of cross-slab partials.
+template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
+__global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a) {
+  using C = StreamCfg<WF, GLU, ACTH, ROUTED, SP, RW, RMAX>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = (int)(blockDim.x >> 5) - 1;
+  const StreamSmem m = stream_smem_init(smem, a.NS, a.stage_bytes, KW);
+  pdl_launch_dependents();
+  uint32_t stage = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      if (ROUTED) pdl_wait_prerequisites();
+      cfg_produce<C>(a, m.stages, m.full, m.empty, stage);
+      stream_drain(a, m.empty, stage);
+    }
+    return;
+  }
+  pdl_wait_prerequisites();
+  int pp = 0;
+  cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+}
+
+// Two steps in one launch sharing the stage ring: segment A (a dense step on
+// static weights, e.g. the shared expert) then segment B (a routed step).  The
+// producer streams A's weights before waiting for the predecessor kernel;
+// A's consumers wait first only when A_WAITS (A's activations come from the
+// predecessor).  The stage buffers are sized for the larger segment.
+template <class A, class B, bool A_WAITS>
+__global__ void __launch_bounds__(288, 1) stream_dual_kernel(const StreamArgs a0,
+                                                             const StreamArgs a1) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = (int)(blockDim.x >> 5) - 1;
+  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, KW);
+  pdl_launch_dependents();
+  uint32_t stage = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      if (A::ROUTED) pdl_wait_prerequisites();
+      cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
+      pdl_wait_prerequisites();
+      cfg_produce<B>(a1, m.stages, m.full, m.empty, stage);
+      stream_drain(a0, m.empty, stage);
+    }
+    return;
+  }
+  if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
+  int pp = 0;
+  cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+  pdl_wait_prerequisites();
+  cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
 }
 
 }  // namespace moe
