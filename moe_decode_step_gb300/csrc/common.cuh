@@ -72,6 +72,17 @@ __device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float c) {
   return c;
 }
 
+// Same with the activation already split into its two f16 halves (lets the
+// compiler keep them in 16-bit registers across rows).
+__device__ __forceinline__ float fma2_f16s(uint32_t a, unsigned short bl, unsigned short bh,
+                                           float c) {
+  asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %1;\n\t"
+      "fma.rn.f32.f16 %0, al, %2, %0;\n\tfma.rn.f32.f16 %0, ah, %3, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "h"(bl), "h"(bh));
+  return c;
+}
+
 // Same with bf16 inputs.
 __device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float c) {
   asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"

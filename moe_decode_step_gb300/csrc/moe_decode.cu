@@ -143,12 +143,12 @@ int validate_dims(const moe_dims_t& d) {
 // bf16, segment A) and the routed experts (MXFP4, segment B) in one launch;
 // the variant is picked by batch class (B = 1, B <= 8, B > 8), which sets how
 // many activation rows one pass carries.
-using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 2, 4>;
+using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 4>;
 template <int R> using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R>;
 template <int R> using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 4, 16, R>;
 template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 4, 16, R>;
 template <int R> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16, 32, R>;
-#define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 2, 4>
+#define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 #define MOE_FC1_KERNEL(RS, RR) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg<RR>, false>
 #define MOE_FC2_KERNEL(RS, RR) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<RR>, true>
 
@@ -271,7 +271,7 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.B = B;
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
-  int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, (d.n_experts + 1) / 2,
+  int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts,
                        st, false);
   if (rc) return rc;
   TopkArgs t;

@@ -160,7 +160,11 @@ __device__ __forceinline__ void row_dot_mx_x(const uint8_t* q, const uint8_t* s,
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int t = 0; t < 4; ++t) out[r] = fma2_f16(hq[t], a[r][w * 4 + t], out[r]);
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t xv = a[r][w * 4 + t];
+        out[r] = fma2_f16s(hq[t], (unsigned short)(xv & 0xFFFFu), (unsigned short)(xv >> 16),
+                           out[r]);
+      }
     }
   }
 #pragma unroll
@@ -184,7 +188,11 @@ __device__ __forceinline__ void row_dot_mx_h(const uint8_t* q, const uint8_t* s,
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int t = 0; t < 4; ++t) out[r] = fma2_f16(hq[t], a[r][w * 4 + t], out[r]);
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t xv = a[r][w * 4 + t];
+        out[r] = fma2_f16s(hq[t], (unsigned short)(xv & 0xFFFFu), (unsigned short)(xv >> 16),
+                           out[r]);
+      }
     }
   }
 #pragma unroll

@@ -44,7 +44,10 @@ tail_kernel(const TailArgs a) {
   const int n = c * per_cta + (int)threadIdx.x * 4;
   const bool ok = (int)threadIdx.x * 4 < per_cta;
   __shared__ float s_warp[8];
-  __shared__ float s_ss;
+  __shared__ float s_part[kTailCluster];
+  // first cluster phase: every CTA of the cluster has started (required before
+  // any remote shared-memory store); arrive now, wait just before the stores
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // gamma is a static weight: it may be read before the predecessor finishes
   uint2 g = make_uint2(0, 0);
   if (ok) g = *reinterpret_cast<const uint2*>(a.gamma + n);
@@ -90,14 +93,16 @@ tail_kernel(const TailArgs a) {
   const float ss = warp_sum(z[0] * z[0] + z[1] * z[1] + z[2] * z[2] + z[3] * z[3]);
   if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (threadIdx.x < kTailCluster) {
+    // every CTA pushes its partial sum into slot c of every peer's s_part
     float t = 0.f;
     for (int w = 0; w < (int)((blockDim.x + 31) >> 5); ++w) t += s_warp[w];
-    s_ss = t;
+    *cluster.map_shared_rank(&s_part[c], (int)threadIdx.x) = t;
   }
-  cluster.sync();
+  cluster.sync();   // all pushes have landed; nothing remote is touched after this
   float total = 0.f;
-  for (int r = 0; r < kTailCluster; ++r) total += *cluster.map_shared_rank(&s_ss, r);
+  for (int r = 0; r < kTailCluster; ++r) total += s_part[r];
   const float inv = 1.0f / sqrtf(total / (float)a.d + a.eps);
   if (ok) {
     const size_t o = (size_t)b * a.d + n;
@@ -112,7 +117,6 @@ tail_kernel(const TailArgs a) {
     *reinterpret_cast<uint2*>(a.out + o) = oo;
     if (a.out_dbg) *reinterpret_cast<float4*>(a.out_dbg + o) = make_float4(v[0], v[1], v[2], v[3]);
   }
-  cluster.sync();   // no CTA leaves while a peer may still read its s_ss
 }
 
 // L2 prefetch of upcoming weights ("What the fused path changes": a small

@@ -1,10 +1,13 @@
 // Router selection: sigmoid scores, biased top-k per row, combine weights, and
 // the routing tables the expert kernels consume.
 //
-// One CTA per row, one thread per expert (E <= 1024).  The k-th largest key is
-// found by a bitwise radix select with __syncthreads_count (32 steps over the
-// order-preserving unsigned image of the fp32 key); ties at the threshold go
-// to the lowest expert ids.  Selection compares fp32 (score + bias); the
+// One CTA per row, one thread per expert (E <= 1024).  Each key is the
+// order-preserving unsigned image of the fp32 (score + bias) in the high word
+// and the complemented expert id in the low word, so keys are distinct and a
+// larger key means a better expert, ties going to the lower id.  Every warp
+// sorts its 32 keys (bitonic network over shuffles); the largest of the warps'
+// k-th keys is a lower bound on the block's k-th key, so only keys at or above
+// it (at most k per warp, usually about k in all) are ranked exactly.  Selection compares fp32 (score + bias); the
 // combine weights use the unbiased scores, normalised to routed_scale.
 // The last CTA to finish (atomic ticket, no waiting) groups the (row, slot)
 // pairs by expert.  ("Kimi K3 on GB300: 13 kernels a layer...", section "What
@@ -73,9 +76,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   __shared__ int s_warp[33];
-  __shared__ uint64_t s_key[32];
   __shared__ float s_score[32];
-  __shared__ int s_cnt;
   __shared__ unsigned s_last;
   // the bias is a static weight: it may be read before the predecessor finishes
   const bool valid = t < a.E;
@@ -104,34 +105,52 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     score = 1.0f / (1.0f + expf(-l));
     u = float_order_bits(score + bias);
   }
-  // ---- k-th largest u (with multiplicity) ----
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    if (__syncthreads_count(valid && u >= cand) >= a.k) T = cand;
+  // ---- per-warp bitonic sort, descending ----
+  uint64_t key = valid ? (((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t)) : 0ull;
+  float sc = score;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      const float os = __shfl_xor_sync(0xffffffffu, sc, stride);
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool lower = (lane & stride) == 0;
+      const bool take = (lower == desc) ? (ok > key) : (ok < key);
+      if (take) { key = ok; sc = os; }
+    }
   }
-  const int c_gt = __syncthreads_count(valid && u > T);
-  // ties at T: lowest ids first
-  const bool eq = valid && u == T;
-  const unsigned bal = __ballot_sync(0xffffffffu, eq);
+  // ---- lower bound on the block's k-th key, then exact ranks above it ----
+  const uint64_t kth = __shfl_sync(0xffffffffu, key, a.k - 1);
+  __shared__ uint64_t s_kth[32];
+  __shared__ uint64_t s_cand[32 * 32];
+  __shared__ float s_cand_score[32 * 32];
+  if (lane == 0) s_kth[warp] = kth;
+  __syncthreads();
+  uint64_t lb = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) lb = s_kth[w] > lb ? s_kth[w] : lb;
+  const bool cand = key >= lb && key != 0ull;
+  const unsigned bal = __ballot_sync(0xffffffffu, cand);   // a prefix of the sorted lanes
   if (lane == 0) s_warp[warp] = __popc(bal);
-  if (t == 0) s_cnt = 0;
   __syncthreads();
-  int before = __popc(bal & ((1u << lane) - 1u));
-  for (int w = 0; w < warp; ++w) before += s_warp[w];
-  const bool sel = valid && (u > T || (eq && before < a.k - c_gt));
-  __syncthreads();
-  if (sel) {
-    const int slot = atomicAdd(&s_cnt, 1);
-    s_key[slot] = ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
+  int base = 0, total = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    if (w < warp) base += s_warp[w];
+    total += s_warp[w];
+  }
+  if (cand) {
+    s_cand[base + lane] = key;
+    s_cand_score[base + lane] = sc;
   }
   __syncthreads();
-  if (sel) {
-    const uint64_t mine = ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
+  if (t < total) {
+    const uint64_t mine = s_cand[t];
     int rank = 0;
-    for (int i = 0; i < a.k; ++i) rank += s_key[i] > mine;
-    a.topk_idx[b * a.k + rank] = t;
-    s_score[rank] = score;
+    for (int i = 0; i < total; ++i) rank += s_cand[i] > mine;
+    if (rank < a.k) {
+      a.topk_idx[b * a.k + rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+      s_score[rank] = s_cand_score[t];
+    }
   }
   __syncthreads();
   if (warp == 0) {
