@@ -152,6 +152,14 @@ int moe_layer_status(moe_layer_t layer, int* device_status);
 int moe_set_timing(moe_layer_t layer, int enable);
 int moe_get_timing(moe_layer_t layer, float* us, int n);
 
+/* Device-side kernel trace.  enable != 0 makes every later forward record,
+ * per kernel, the earliest CTA start and the latest CTA end (globaltimer,
+ * nanoseconds).  moe_get_trace synchronises the device and writes up to n
+ * values: [start, end] of router, top-k, FC1, FC2, tail, in that order (ten
+ * values); a kernel that did not run reports start > end. */
+int moe_set_trace(moe_layer_t layer, int enable);
+int moe_get_trace(moe_layer_t layer, unsigned long long* ns, int n);
+
 /* Number of kernel launches one forward makes for batch B (excluding the
  * optional prefetch kernel, which adds one when enabled). */
 int moe_launches_per_forward(moe_layer_t layer, int B);

@@ -159,6 +159,18 @@ class MoELayer:
         check(lib().moe_get_timing(self._h, arr, 6), "moe_get_timing")
         return list(arr)
 
+    def set_trace(self, enable):
+        check(lib().moe_set_trace(self._h, int(bool(enable))), "moe_set_trace")
+
+    def get_trace(self):
+        """{kernel: (start_us, end_us)} relative to the router's start, last forward."""
+        arr = (ctypes.c_ulonglong * 10)()
+        check(lib().moe_get_trace(self._h, arr, 10), "moe_get_trace")
+        names = ["router", "topk", "fc1", "fc2", "tail"]
+        t0 = arr[0]
+        return {n: ((arr[2 * i] - t0) / 1e3, (arr[2 * i + 1] - t0) / 1e3)
+                for i, n in enumerate(names)}
+
     def launches_per_forward(self, B):
         return lib().moe_launches_per_forward(self._h, int(B))
 

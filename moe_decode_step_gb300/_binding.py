@@ -59,6 +59,8 @@ _PROTOS = {
     "moe_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_get_timing": (ctypes.c_int, [_P, _P, ctypes.c_int]),
     "moe_launches_per_forward": (ctypes.c_int, [_P, ctypes.c_int]),
+    "moe_set_trace": (ctypes.c_int, [_P, ctypes.c_int]),
+    "moe_get_trace": (ctypes.c_int, [_P, _P, ctypes.c_int]),
     "mxfp4_packed_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_size_t)]),
     "mxfp4_pack": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, ctypes.c_int]),

@@ -266,4 +266,17 @@ __device__ __forceinline__ void pdl_wait_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Optional kernel trace: slot id holds the earliest CTA start and slot 8 + id
+// the latest CTA end (globaltimer ns) of kernel `id` in one forward.
+constexpr int kTraceSlots = 16;
+__device__ __forceinline__ void trace_begin(unsigned long long* trace, int id) {
+  if (trace && threadIdx.x == 0) atomicMin(trace + id, global_ns());
+}
+__device__ __forceinline__ void trace_end(unsigned long long* trace, int id) {
+  if (trace) {
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(trace + 8 + id, global_ns());
+  }
+}
+
 }  // namespace moe

@@ -62,6 +62,7 @@ struct Workspace {
   float* hs;
   float* y_s;
   int* status;
+  unsigned long long* trace;
   uint16_t* x_stage;
   uint16_t* res_stage;
   uint16_t* out_stage;
@@ -86,7 +87,7 @@ struct moe_layer {
   cudaStream_t pref = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_pref = nullptr;
   cudaEvent_t ev_time[kNumTimeEvents] = {};
-  bool timing = false, timed_once = false;
+  bool timing = false, timed_once = false, tracing = false;
   moe_layer* next = nullptr;
   StreamPlan plan[kNumSteps][3];   // by batch class (B = 1, B <= 8, B > 8)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
@@ -120,6 +121,7 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.hs = carve<float>(p, B * d.f_shared);
   w.y_s = carve<float>(p, B * d.d);
   w.status = carve<int>(p, 1);
+  w.trace = carve<unsigned long long>(p, kTraceSlots);
   w.x_stage = carve<uint16_t>(p, B * d.d);
   w.res_stage = carve<uint16_t>(p, B * d.d);
   w.out_stage = carve<uint16_t>(p, B * d.d);
@@ -249,6 +251,7 @@ StreamArgs base_args(moe_layer* L) {
   a.active_off = L->ws.active_off;
   a.pair_list = L->ws.pair_list;
   a.status = L->ws.status;
+  a.trace = L->tracing ? L->ws.trace : nullptr;
   return a;
 }
 
@@ -271,10 +274,11 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.B = B;
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
+  a.trace_id = 0;
   int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts,
                        st, false);
   if (rc) return rc;
-  TopkArgs t;
+  TopkArgs t{};
   t.logits = L->ws.logits;
   t.bias = L->w.router_bias;
   t.x = static_cast<const uint16_t*>(x);
@@ -292,6 +296,7 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   t.active_off = L->ws.active_off;
   t.pair_list = L->ws.pair_list;
   t.h_amax = L->ws.h_amax;
+  t.trace = L->tracing ? L->ws.trace : nullptr;
   MOE_CUDA(launch_ex(topk_kernel, dim3(B), dim3(kTopkThreads), 0, st, true, t));
   return MOE_OK;
 }
@@ -324,6 +329,7 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   ra.x = static_cast<const uint16_t*>(x);
   ra.out = L->ws.h;
   ra.out_amax = L->ws.h_amax;
+  sa.trace_id = ra.trace_id = 2;
   switch (batch_class(B)) {
     case 0: return launch_dual(MOE_FC1_KERNEL(1, 1), L->plan[kStepFc1][0], sa, ra, st);
     case 1: return launch_dual(MOE_FC1_KERNEL(2, 2), L->plan[kStepFc1][1], sa, ra, st);
@@ -351,6 +357,7 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   ra.h = L->ws.h;
   ra.h_amax = L->ws.h_amax;
   ra.out = L->ws.y_pair;
+  sa.trace_id = ra.trace_id = 3;
   switch (batch_class(B)) {
     case 0: return launch_dual(MOE_FC2_KERNEL(1, 1), L->plan[kStepFc2][0], sa, ra, st);
     case 1: return launch_dual(MOE_FC2_KERNEL(2, 2), L->plan[kStepFc2][1], sa, ra, st);
@@ -360,7 +367,7 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
 
 int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg,
                 float* z_dbg, float* out_dbg, bool pdl) {
-  TailArgs a;
+  TailArgs a{};
   a.y_pair = L->ws.y_pair;
   a.topk_w = L->ws.topk_w;
   a.y_s = L->ws.y_s;
@@ -374,6 +381,7 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.d = L->dims.d;
   a.k = L->dims.top_k;
   a.eps = L->dims.rms_eps;
+  a.trace = L->tracing ? L->ws.trace : nullptr;
   MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
   return MOE_OK;
 }
@@ -381,7 +389,7 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
 int launch_prefetch(moe_layer* L) {
   moe_layer* n = L->next;
   if (!n) return MOE_OK;
-  PrefetchArgs a;
+  PrefetchArgs a{};
   a.n = 3;
   a.ptr[0] = static_cast<const char*>(n->w.router_w);
   a.bytes[0] = (size_t)n->dims.n_experts * n->dims.d * 2;
@@ -411,6 +419,10 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (!residual || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(residual) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   const bool tm = L->timing;
+  if (L->tracing) {
+    MOE_CUDA(cudaMemsetAsync(L->ws.trace, 0xFF, 8 * sizeof(unsigned long long), st));
+    MOE_CUDA(cudaMemsetAsync(L->ws.trace + 8, 0, 8 * sizeof(unsigned long long), st));
+  }
   MOE_CUDA(cudaEventRecord(L->ev_fork, st));
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
@@ -614,6 +626,21 @@ int moe_get_timing(moe_layer_t L, float* us, int n) {
   MOE_CUDA(cudaEventElapsedTime(&t[4], L->ev_time[kTimeFc2End], L->ev_time[kTimeTailEnd]));
   MOE_CUDA(cudaEventElapsedTime(&t[5], L->ev_time[kTimeRouterStart], L->ev_time[kTimeTailEnd]));
   for (int i = 0; i < n && i < 6; ++i) us[i] = t[i] * 1000.f;
+  return MOE_OK;
+}
+
+int moe_set_trace(moe_layer_t L, int enable) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  L->tracing = enable != 0;
+  return MOE_OK;
+}
+
+int moe_get_trace(moe_layer_t L, unsigned long long* ns, int n) {
+  if (!L || !ns || n < 0) return MOE_ERR_INVALID_ARG;
+  unsigned long long t[kTraceSlots];
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(t, L->ws.trace, sizeof(t), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < n && i < 10; ++i) ns[i] = (i % 2 == 0) ? t[i / 2] : t[8 + i / 2];
   return MOE_OK;
 }
 

@@ -140,7 +140,7 @@ extern "C" int moe_router_topk_noalloc(void* stream, const void* router_w, const
   NOALLOC_ROUTER_KERNEL<<<grid, s.threads, s.smem, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
-  TopkArgs t;
+  TopkArgs t{};
   t.logits = reinterpret_cast<const float*>(s.scratch + kOffLogits);
   t.bias = router_bias;
   t.x = static_cast<const uint16_t*>(x);

@@ -50,6 +50,8 @@ struct StreamArgs {
   int* status;               // device status word (bounded-wait timeouts)
   int NS;                    // stage buffers in the ring
   int stage_bytes;           // bytes per stage buffer (multiple of 128)
+  unsigned long long* trace; // optional kernel trace (see trace_begin), or null
+  int trace_id;
 };
 
 // Elements per lane and activation registers per row, by format.
@@ -615,6 +617,7 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
+  trace_begin(a.trace, a.trace_id);
   const StreamSmem m = stream_smem_init(smem, a.NS, a.stage_bytes, KW);
   pdl_launch_dependents();
   uint32_t stage = 0;
@@ -624,11 +627,13 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
       cfg_produce<C>(a, m.stages, m.full, m.empty, stage);
       stream_drain(a, m.empty, stage);
     }
-    return;
+    __syncwarp();
+  } else {
+    pdl_wait_prerequisites();
+    int pp = 0;
+    cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
   }
-  pdl_wait_prerequisites();
-  int pp = 0;
-  cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+  trace_end(a.trace, a.trace_id);
 }
 
 // Two steps in one launch sharing the stage ring: segment A (a dense step on
@@ -642,6 +647,7 @@ __global__ void __launch_bounds__(288, 1) stream_dual_kernel(const StreamArgs a0
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
+  trace_begin(a0.trace, a0.trace_id);
   const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, KW);
   pdl_launch_dependents();
   uint32_t stage = 0;
@@ -653,13 +659,15 @@ __global__ void __launch_bounds__(288, 1) stream_dual_kernel(const StreamArgs a0
       cfg_produce<B>(a1, m.stages, m.full, m.empty, stage);
       stream_drain(a0, m.empty, stage);
     }
-    return;
+    __syncwarp();
+  } else {
+    if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
+    int pp = 0;
+    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+    pdl_wait_prerequisites();
+    cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
   }
-  if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
-  int pp = 0;
-  cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
-  pdl_wait_prerequisites();
-  cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+  trace_end(a0.trace, a0.trace_id);
 }
 
 }  // namespace moe

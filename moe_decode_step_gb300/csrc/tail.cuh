@@ -30,6 +30,7 @@ struct TailArgs {
   float* out_dbg;          // optional export of out before bf16 rounding [B][d]
   int B, d, k;
   float eps;
+  unsigned long long* trace;  // optional kernel trace, or null
 };
 
 constexpr int kTailCluster = 8;
@@ -45,6 +46,7 @@ tail_kernel(const TailArgs a) {
   const bool ok = (int)threadIdx.x * 4 < per_cta;
   __shared__ float s_warp[8];
   __shared__ float s_part[kTailCluster];
+  trace_begin(a.trace, 4);
   // first cluster phase: every CTA of the cluster has started (required before
   // any remote shared-memory store); arrive now, wait just before the stores
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -117,6 +119,7 @@ tail_kernel(const TailArgs a) {
     *reinterpret_cast<uint2*>(a.out + o) = oo;
     if (a.out_dbg) *reinterpret_cast<float4*>(a.out_dbg + o) = make_float4(v[0], v[1], v[2], v[3]);
   }
+  trace_end(a.trace, 4);
 }
 
 // L2 prefetch of upcoming weights ("What the fused path changes": a small

@@ -33,6 +33,7 @@ struct TopkArgs {
   int* active_off;
   int* pair_list;
   unsigned* h_amax;       // [B*k] reset to 0
+  unsigned long long* trace;  // optional kernel trace, or null
 };
 
 constexpr int kTopkThreads = 1024;
@@ -78,6 +79,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   __shared__ int s_warp[33];
   __shared__ float s_score[32];
   __shared__ unsigned s_last;
+  trace_begin(a.trace, 1);
   // the bias is a static weight: it may be read before the predecessor finishes
   const bool valid = t < a.E;
   const float bias = valid ? __ldg(a.bias + t) : 0.f;
@@ -178,7 +180,10 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     __syncthreads();
     if (t == 0) s_last = (atomicAdd(a.done, 1u) == (unsigned)(gridDim.x - 1)) ? 1u : 0u;
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last) {
+      trace_end(a.trace, 1);
+      return;
+    }
     __threadfence();
   } else {
     __syncthreads();
@@ -214,6 +219,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     a.active_off[n_act] = total_pairs;
     if (gridDim.x > 1) *a.done = 0u;
   }
+  trace_end(a.trace, 1);
 }
 
 }  // namespace moe
