@@ -174,7 +174,7 @@ int plan_kernel(Kern kern, int KA, int KB, int n_sm, int budget, StreamPlan* p) 
   StreamPlan r;
   r.threads = 32 * (KW + 1);
   r.stage_bytes = (int)((std::max(sa, sb) + 127) / 128 * 128);
-  const int red_bytes = 2 * 64 * KW * 4;
+  const int red_bytes = 2 * 64 * KW * 4 + 32;
   r.NS = std::min(8, (budget - red_bytes) / (r.stage_bytes + 16));
   if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
@@ -281,7 +281,6 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   TopkArgs t{};
   t.logits = L->ws.logits;
   t.bias = L->w.router_bias;
-  t.x = static_cast<const uint16_t*>(x);
   t.B = B;
   t.d = d.d;
   t.E = d.n_experts;
@@ -289,7 +288,6 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   t.routed_scale = d.routed_scale;
   t.topk_idx = idx;
   t.topk_w = w;
-  t.x_shift = L->ws.x_shift;
   t.done = L->ws.done;
   t.n_active = L->ws.n_active;
   t.active_expert = L->ws.active_expert;

@@ -77,7 +77,7 @@ int device_setup(int dev, int d, DeviceSetup* out) {
     using Sh = StreamShape<kWfBf16, false>;
     const int KW = (d + Sh::WARP_K - 1) / Sh::WARP_K;
     const int stage = (int)((stream_rows_bytes(kWfBf16, d, 1) + 127) / 128 * 128);
-    const int red = 2 * 64 * KW * 4;
+    const int red = 2 * 64 * KW * 4 + 32;
     const int budget = 110 * 1024;
     const int NS = std::min(8, (budget - red) / (stage + 16));
     if (NS < 2) return MOE_ERR_UNSUPPORTED;
@@ -143,7 +143,6 @@ extern "C" int moe_router_topk_noalloc(void* stream, const void* router_w, const
   TopkArgs t{};
   t.logits = reinterpret_cast<const float*>(s.scratch + kOffLogits);
   t.bias = router_bias;
-  t.x = static_cast<const uint16_t*>(x);
   t.B = B;
   t.d = d;
   t.E = n_experts;
@@ -151,7 +150,6 @@ extern "C" int moe_router_topk_noalloc(void* stream, const void* router_w, const
   t.routed_scale = routed_scale;
   t.topk_idx = idx;
   t.topk_w = w;
-  t.x_shift = reinterpret_cast<int*>(s.scratch + kOffXShift);
   t.done = reinterpret_cast<unsigned*>(s.scratch + kOffDone);
   t.n_active = reinterpret_cast<int*>(s.scratch + kOffNActive);
   t.active_expert = reinterpret_cast<int*>(s.scratch + kOffActiveExpert);

@@ -91,6 +91,28 @@ __device__ __forceinline__ void act_load_mx_x(const uint16_t* row, int blk, bool
   }
 }
 
+// Raw bf16 pairs of the 32-element slice [blk*32, +32) of an x row.
+__device__ __forceinline__ void act_load_raw_x(const uint16_t* row, int blk, bool ok,
+                                               uint32_t (&a)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(row + blk * 32);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = ok ? p[c] : make_uint4(0, 0, 0, 0);
+    a[c * 4 + 0] = v.x;
+    a[c * 4 + 1] = v.y;
+    a[c * 4 + 2] = v.z;
+    a[c * 4 + 3] = v.w;
+  }
+}
+
+// bf16 pairs -> f16x2 scaled by 2^-shift, in place.
+__device__ __forceinline__ void act_convert_mx_x(int shift, uint32_t (&a)[16]) {
+  const float sc = pow2f(-shift);
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+    a[t] = pack_f16x2(__uint_as_float(a[t] << 16) * sc, __uint_as_float(a[t] & 0xFFFF0000u) * sc);
+}
+
 // MXFP4 h-activation: 16 elements [hb*16, +16) of an fp32 row as f16x2.
 __device__ __forceinline__ void act_load_mx_h(const float* row, int hb, bool ok, int shift,
                                               uint32_t (&a)[8]) {
@@ -414,7 +436,7 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
                                                    int done, int it0, int run_end, int tiles,
                                                    uint8_t* stages, uint64_t* full,
                                                    uint64_t* empty, float* red, uint32_t& stage,
-                                                   int& pp, int kw, int KW, int lane) {
+                                                   int& pp, int& rp, int kw, int KW, int lane) {
   using Sh = StreamShape<WF, ACTH>;
   constexpr int G = GLU ? 2 : 1;
   constexpr int SPI = RW / SP;
@@ -431,20 +453,43 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
 
   int pid[R], shift[R];
   uint32_t act[R][Sh::AW];
+  if constexpr (WF == kWfMx && !ACTH) {
+    // x rows: the f16 scaling shift needs the whole row's max |x|; the KW
+    // consumer warps together hold the whole row, so reduce across them.
+    unsigned* s_amax = reinterpret_cast<unsigned*>(red + (size_t)2 * 64 * KW);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
+      act_load_raw_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, blk, ok, act[r]);
+      uint32_t mx = 0;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        mx = max(mx, max(act[r][q] & 0x7FFFu, (act[r][q] >> 16) & 0x7FFFu));
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0) atomicMax(&s_amax[(rp & 1) * 4 + r], mx);
+    }
+    consumer_sync(KW * 32);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      shift[r] = f16_shift_for_amax(bf16_bits_to_f32(s_amax[(rp & 1) * 4 + r]));
+      act_convert_mx_x(shift[r], act[r]);
+    }
+    // the other parity's slots are free: every consumer is past this barrier
+    if (kw == 0 && lane < 4) s_amax[((rp & 1) ^ 1) * 4 + lane] = 0u;
+    rp ^= 1;
+  } else {
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
     shift[r] = stream_shift<WF, ACTH, ROUTED>(a, pid[r]);
-    if constexpr (WF == kWfMx && !ACTH) {
-      act_load_mx_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, blk, ok, shift[r],
-                    act[r]);
-    } else if constexpr (WF == kWfMx && ACTH) {
+    if constexpr (WF == kWfMx && ACTH) {
       act_load_mx_h(a.h + (size_t)pid[r] * a.K, blk, ok, shift[r], act[r]);
     } else if constexpr (!ACTH) {
       act_load_bf_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K, act[r]);
     } else {
       act_load_bf_h(a.h + (size_t)pid[r] * a.K, slab, lane, a.K, act[r]);
     }
+  }
   }
 
   for (int it = it0; it < run_end; ++it) {
@@ -525,7 +570,7 @@ template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
 __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
-                                                     int& pp, int kw, int KW, int lane) {
+                                                     int& pp, int& rp, int kw, int KW, int lane) {
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
@@ -534,16 +579,16 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
       if (R == 1) {
         stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, it0, run_end, tiles,
                                                               stages, full, empty, red, stage, pp,
-                                                              kw, KW, lane);
+                                                              rp, kw, KW, lane);
       } else if constexpr (RMAX >= 2) {
         if (R == 2) {
           stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, it0, run_end, tiles,
                                                                 stages, full, empty, red, stage,
-                                                                pp, kw, KW, lane);
+                                                                pp, rp, kw, KW, lane);
         } else if constexpr (RMAX >= 4) {
           stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, it0, run_end, tiles,
                                                                 stages, full, empty, red, stage,
-                                                                pp, kw, KW, lane);
+                                                                pp, rp, kw, KW, lane);
         }
       }
       done += R;
@@ -574,12 +619,12 @@ __device__ __forceinline__ void cfg_produce(const StreamArgs& a, uint8_t* stages
 template <class C>
 __device__ __forceinline__ void cfg_consume(const StreamArgs& a, uint8_t* stages, uint64_t* full,
                                             uint64_t* empty, float* red, uint32_t& stage, int& pp,
-                                            int kw, int KW, int lane) {
+                                            int& rp, int kw, int KW, int lane) {
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
   stream_range(n, lo, hi);
   stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX>(
-      a, lo, hi, tiles, stages, full, empty, red, stage, pp, kw, KW, lane);
+      a, lo, hi, tiles, stages, full, empty, red, stage, pp, rp, kw, KW, lane);
 }
 
 // Shared-memory carve-up common to both kernels.
@@ -604,13 +649,14 @@ __device__ __forceinline__ StreamSmem stream_smem_init(uint8_t* smem, int NS, in
     }
     fence_barrier_init();
   }
+  if (threadIdx.x < 8) reinterpret_cast<unsigned*>(m.red + (size_t)2 * 64 * KW)[threadIdx.x] = 0u;
   __syncthreads();
   return m;
 }
 
 // Single step.  Warp 0 produces, warps 1..KW consume (KW = blockDim.x/32 - 1).
 // Dynamic shared memory: NS stages, NS full + NS empty mbarriers, 2 x 64 x KW
-// floats of cross-slab partials.
+// floats of cross-slab partials, 8 words of per-run activation maxima.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
 __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a) {
   using C = StreamCfg<WF, GLU, ACTH, ROUTED, SP, RW, RMAX>;
@@ -630,8 +676,8 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
     __syncwarp();
   } else {
     pdl_wait_prerequisites();
-    int pp = 0;
-    cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+    int pp = 0, rp = 0;
+    cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
   }
   trace_end(a.trace, a.trace_id);
 }
@@ -662,10 +708,10 @@ __global__ void __launch_bounds__(288, 1) stream_dual_kernel(const StreamArgs a0
     __syncwarp();
   } else {
     if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
-    int pp = 0;
-    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+    int pp = 0, rp = 0;
+    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
     pdl_wait_prerequisites();
-    cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, warp - 1, KW, lane);
+    cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
   }
   trace_end(a0.trace, a0.trace_id);
 }

@@ -21,12 +21,10 @@ namespace moe {
 struct TopkArgs {
   const float* logits;    // [B][E]
   const float* bias;      // [E]
-  const uint16_t* x;      // bf16 [B][d] (for the f16 scaling shift of each row)
   int B, d, E, k;
   float routed_scale;
   int32_t* topk_idx;      // [B][k], descending by biased score
   float* topk_w;          // [B][k]
-  int* x_shift;           // [B]
   unsigned* done;         // ticket, 0 at rest
   int* n_active;          // routing tables (see RoutedArgs)
   int* active_expert;
@@ -78,6 +76,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   __shared__ int s_warp[33];
   __shared__ float s_score[32];
+  __shared__ int32_t s_idx[64 * 32];
   __shared__ unsigned s_last;
   trace_begin(a.trace, 1);
   // the bias is a static weight: it may be read before the predecessor finishes
@@ -86,20 +85,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   pdl_launch_dependents();
   pdl_wait_prerequisites();
 
-  // ---- scores and keys (the x row for the f16 shift is loaded alongside) ----
-  constexpr int kXPer = 8;   // d <= 8192 = kXPer * 1024
-  uint32_t xm = 0;
-  {
-    const uint16_t* xr = a.x + (size_t)b * a.d;
-    uint16_t xv[kXPer];
-#pragma unroll
-    for (int i = 0; i < kXPer; ++i) {
-      const int e = t + i * (int)blockDim.x;
-      xv[i] = e < a.d ? xr[e] : (uint16_t)0;
-    }
-#pragma unroll
-    for (int i = 0; i < kXPer; ++i) xm = max(xm, (uint32_t)(xv[i] & 0x7FFFu));
-  }
+  // ---- scores and keys ----
   float score = 0.f;
   uint32_t u = 0;
   if (valid) {
@@ -150,7 +136,9 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     int rank = 0;
     for (int i = 0; i < total; ++i) rank += s_cand[i] > mine;
     if (rank < a.k) {
-      a.topk_idx[b * a.k + rank] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)mine);
+      a.topk_idx[b * a.k + rank] = e;
+      s_idx[b * a.k + rank] = e;
       s_score[rank] = s_cand_score[t];
     }
   }
@@ -161,19 +149,6 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     if (lane < a.k) a.topk_w[b * a.k + lane] = a.routed_scale * s_score[lane] / ssum;
     if (lane < a.k) a.h_amax[b * a.k + lane] = 0u;
   }
-  // ---- f16 scaling shift of x row b ----
-  {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, xm);
-    __syncthreads();
-    if (lane == 0) s_warp[warp] = (int)m;
-    __syncthreads();
-    if (t == 0) {
-      uint32_t mm = 0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mm = max(mm, (uint32_t)s_warp[w]);
-      a.x_shift[b] = f16_shift_for_amax(bf16_bits_to_f32(mm));
-    }
-  }
-
   // ---- the last CTA groups pairs by expert ----
   if (gridDim.x > 1) {
     __threadfence();
@@ -189,9 +164,9 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     __syncthreads();
   }
   __shared__ unsigned long long s_mask[1024];
-  __shared__ int32_t s_idx[64 * 32];
   const int P = a.B * a.k;
-  for (int p = t; p < P; p += blockDim.x) s_idx[p] = __ldcg(a.topk_idx + p);
+  if (gridDim.x > 1)   // other rows were selected by other CTAs
+    for (int p = t; p < P; p += blockDim.x) s_idx[p] = __ldcg(a.topk_idx + p);
   if (valid) s_mask[t] = 0ull;
   __syncthreads();
   for (int p = t; p < P; p += blockDim.x) atomicOr(&s_mask[s_idx[p]], 1ull << (p / a.k));
