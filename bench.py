@@ -45,7 +45,17 @@ def parse_args():
     p.add_argument("--config", default="full_b1")
     p.add_argument("--no-batches", action="store_true", help="skip the B=8 / B=64 extras")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    p.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                   help="run --warmup untimed forwards of a profiling workload (L2 flushed "
+                        "between them) and exit; for ncu captures, prints no JSON line")
     return p.parse_args()
+
+
+# Profiling workloads.  "full_b1_e128" is the full_b1 layer with 128 experts
+# held instead of 896 (2.2 GB of expert weights instead of 15.7 GB): at B = 1
+# the 16 selected experts make its FC1 and FC2 launches the same size as
+# full_b1's, while the device holds a few GB, as a many-pass capture needs.
+PROFILE_CASES = {"full_b1": ("full_b1", None), "full_b1_e128": ("full_b1", 128)}
 
 
 def dist_env():
@@ -116,9 +126,22 @@ def fc1_bytes(cfg, n_distinct, B):
             + 4 * B * cfg.top_k * cfg.f)
 
 
-def traffic_from_profile(kernel_file):
-    """dram bytes per launch recorded by the ncu summary of the routed FC1
-    kernel, or None when missing or taken on a different kernel source."""
+KERNEL_SOURCES = ("common.cuh", "stream.cuh", "moe_decode.cu")
+
+
+def kernel_source_sha256():
+    """sha256 over the FC1 kernel's sources (the dot, the streaming kernel and
+    its launch plan), concatenated in that order."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "moe_decode_step_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_from_profile():
+    """dram bytes per launch recorded by the ncu summary of the FC1 streaming
+    kernel, or None when missing or taken on different kernel sources."""
     summ = os.path.join(ROOT, "profiles", "fc1_stream_full_b1.md")
     try:
         text = open(summ).read()
@@ -128,8 +151,7 @@ def traffic_from_profile(kernel_file):
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
-    return float(m.group(1)) if cur == h.group(1) else None
+    return float(m.group(1)) if kernel_source_sha256() == h.group(1) else None
 
 
 # ---------------------------------------------------------------------------
@@ -376,8 +398,7 @@ def run_ours(args, rank, world, local):
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
     fc1_us = statistics.median(p[1] for p in phases)
     fc1_b = fc1_bytes(cfg, n_distinct, cfg.B)
-    kernel_src = os.path.join(ROOT, "moe_decode_step_gb300", "csrc", "stream.cuh")
-    traffic = traffic_from_profile(kernel_src)
+    traffic = traffic_from_profile()
     if traffic is not None:
         traffic = traffic * n_distinct / 16.0
     phase_names = ["router_topk", "fc1_shared_then_routed", "fc2_shared_then_routed",
@@ -461,8 +482,37 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def run_profile_case(args):
+    import dataclasses
+    import torch
+    from gen.configs import CONFIGS
+    from moe_decode_step_gb300 import synthetic
+
+    base, n_experts = PROFILE_CASES[args.profile_case]
+    cfg = CONFIGS[base]
+    if n_experts is not None:
+        cfg = dataclasses.replace(cfg, name=args.profile_case, n_experts=n_experts)
+    dev = torch.device("cuda", 0)
+    flush = L2Flush(dev)
+    layer = synthetic.make_layer(cfg)
+    x, res0 = synthetic.make_activations(cfg)
+    res = res0.clone()
+    out = torch.empty_like(x)
+    for _ in range(max(1, args.warmup)):
+        res.copy_(res0)
+        flush()
+        layer.forward(x, res, out)
+    torch.cuda.synchronize()
+    rc = layer.status()
+    layer.close()
+    print(f"profile case {args.profile_case}: {max(1, args.warmup)} forwards, status {rc}")
+    return 0 if rc == 0 else 1
+
+
 def main():
     args = parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)

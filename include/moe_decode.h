@@ -60,9 +60,13 @@ typedef enum {
 
 typedef struct moe_layer* moe_layer_t;
 
-/* Layer dimensions.  d % 256 == 0 and d <= 8192; f % 256 == 0 and f <= 4096;
+/* Layer dimensions.  d % 256 == 0 and d <= 7680; f % 256 == 0 and f <= 4096;
  * f_shared % 256 == 0 and f_shared <= 4096; 1 <= top_k <= 32; top_k <= n_experts
- * <= 1024; 1 <= max_batch <= 64.  mxfp4_layout must be 0 (canonical). */
+ * <= 1024; 1 <= max_batch <= 64.  mxfp4_layout is 0 (expert weights in the
+ * canonical layout: moe_layer_create copies them into the kernels' tiled
+ * layouts, E * 3 * d * f * 17/32 bytes of extra device memory owned by the
+ * handle) or 1 (expert weights already tiled: FC1 matrices in layout 2, FC2
+ * matrices in layout 1, see mxfp4_pack; used in place). */
 typedef struct {
   int32_t d;              /* hidden size */
   int32_t f;              /* routed-expert intermediate size */
@@ -72,7 +76,7 @@ typedef struct {
   int32_t max_batch;      /* largest B forward will be called with */
   float routed_scale;     /* combine weights sum to this (2.5 for the Kimi-style router) */
   float rms_eps;          /* RMSNorm epsilon (1e-6) */
-  int32_t mxfp4_layout;   /* 0: canonical layout, see mxfp4_pack */
+  int32_t mxfp4_layout;   /* 0: canonical expert weights, 1: tiled (see above) */
 } moe_dims_t;
 
 /* Device pointers to the layer's weights (borrowed, never freed).
@@ -81,10 +85,10 @@ typedef struct {
 typedef struct {
   const void* router_w;        /* device bf16 [E][d] */
   const float* router_bias;    /* device fp32 [E], used for selection only */
-  const uint8_t* w_gu_q;       /* device [E][2f][d/2]  E2M1 nibbles, canonical layout */
-  const uint8_t* w_gu_s;       /* device [E][2f][d/32] E8M0 scale bytes */
-  const uint8_t* w_d_q;        /* device [E][d][f/2] */
-  const uint8_t* w_d_s;        /* device [E][d][f/32] */
+  const uint8_t* w_gu_q;       /* device [E][2f][d/2]  E2M1 nibbles (layout 0, or 2) */
+  const uint8_t* w_gu_s;       /* device [E][2f][d/32] E8M0 scale bytes (layout 0, or 2) */
+  const uint8_t* w_d_q;        /* device [E][d][f/2]  (layout 0, or 1) */
+  const uint8_t* w_d_s;        /* device [E][d][f/32] (layout 0, or 1) */
   const void* shared_gu;       /* device bf16 [2 f_shared][d] (gate rows, then up rows) */
   const void* shared_d;        /* device bf16 [d][f_shared] */
   const void* rms_gamma;       /* device bf16 [d] */
@@ -129,8 +133,11 @@ int moe_decode_forward_debug(moe_layer_t layer, void* stream, const void* x, int
                              void* out, float* y_routed, float* y_shared, float* h, float* z,
                              float* out_f32);
 
-/* Dequantise one expert matrix on the GPU with the kernels' own decode path:
- * which = 0 -> FC1 [2f][d], which = 1 -> FC2 [d][f]; out device fp32. */
+/* Dequantise one expert matrix on the GPU from the handle's tiled copy, with
+ * the kernels' element decode (cvt.rn.f16x2.e2m1x2) and the exact scale value:
+ * which = 0 -> FC1 [2f][d], which = 1 -> FC2 [d][f], canonical row order;
+ * out device fp32.  (The matmul kernels read scale code 0, 2^-127, as 0: the
+ * products it scales are below 6 * 2^-127 * |activation|.) */
 int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, float* out);
 
 /* Chain layers: while this layer's routed experts run, an L2-prefetch kernel on
@@ -171,8 +178,22 @@ int moe_launches_per_forward(moe_layer_t layer, int B);
  * (all-zero block: -127); element code = nearest E2M1 value to w / 2^exp,
  * ties to the even code, magnitudes past 6 saturate to 6, sign bit = sign of w. */
 
-/* Bytes of nibbles for rows x k (k % 32 == 0); *scale_bytes gets the scale
- * bytes when non-NULL.  Returns 0 on bad arguments. */
+/* Tiled layouts 1 and 2 hold the same bytes for the tensor-core kernels.
+ * Rows form tiles of 16 "mma rows": layout 1 puts rows 16T..16T+15 in tile T;
+ * layout 2 (a [2n][k] gate/up matrix, row i pairing with row n + i) puts rows
+ * 8T..8T+7 as mma rows 0..7 and rows n+8T..n+8T+7 as mma rows 8..15.  Tile T's
+ * nibbles occupy bytes [8kT, 8k(T+1)): for K blocks 2P and 2P+1 (32 elements
+ * each) and lane L = 4g + t (g < 8, t < 4), 16 bytes at 8kT + (32P + L) * 16
+ * hold canonical bytes [4t, 4t+4) of block 2P of mma row g, then of mma row
+ * g + 8, then the same two for block 2P+1.  Tile T's scales occupy bytes
+ * [kT/2, k(T+1)/2): for block group Q (blocks 4Q..4Q+3) and g, 8 bytes at
+ * kT/2 + (8Q + g) * 8 hold, per block 4Q+j, the scale of mma row g (byte 2j)
+ * and of mma row g + 8 (byte 2j + 1).  Tiled layouts need k % 128 == 0 and
+ * rows % 16 == 0. */
+
+/* Bytes of nibbles for rows x k (k % 32 == 0, and the layout's rules);
+ * *scale_bytes gets the scale bytes when non-NULL.  The same for every
+ * layout.  Returns 0 on bad arguments. */
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes);
 
 /* Host packer: w host fp32 [rows][k] -> q host [rows][k/2], s host [rows][k/32]. */
@@ -182,13 +203,20 @@ int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, 
 int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
                       uint8_t* s, int layout);
 
+/* Canonical packed bytes -> tiled layout 1 or 2, asynchronous on stream, for
+ * n_mat matrices stored back to back (rows x k each): q_in, s_in device
+ * canonical; q_out, s_out device, the same sizes, must not overlap the input.
+ * Errors: INVALID_ARG, UNSUPPORTED (layout rules, 16-byte alignment), CUDA. */
+int mxfp4_retile_device(void* stream, const uint8_t* q_in, const uint8_t* s_in, int64_t n_mat,
+                        int64_t rows, int64_t k, int layout, uint8_t* q_out, uint8_t* s_out);
+
 /* Router + top-k that allocates nothing (no counterpart in the paper: it
  * exists for callers that cannot call cudaMalloc, e.g. code running inside a
  * stream capture it does not own, runtimes that hand over a fixed memory pool,
  * or callers that must not synchronise the device).  It needs no layer handle:
  * router_w device bf16 [E][d], router_bias device fp32 [E], x device bf16
  * [B][d]; outputs idx device int32 [B][k] and w device fp32 [B][k], exactly
- * as moe_router_topk.  Its scratch (logits, ticket, routing tables; 284,928
+ * as moe_router_topk.  Its scratch (logits, ticket, routing tables; 284,672
  * bytes) is one static device array that every GPU loading this library holds
  * until the process exits.  Limits: B <= 64, E <= 1024, k <= 32, d % 256 == 0,
  * d <= 8192; larger sizes return MOE_ERR_UNSUPPORTED.  The first call on each

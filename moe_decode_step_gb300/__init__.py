@@ -14,6 +14,7 @@ from ._binding import (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR
                        status_string)
 
 __all__ = ["MoELayer", "MoEDims", "MoEWeights", "MoEError", "mxfp4_pack", "mxfp4_pack_device",
+           "mxfp4_retile_device",
            "mxfp4_packed_bytes", "status_string", "lib", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_ALLOC", "MOE_ERR_TIMEOUT"]
 
@@ -42,11 +43,17 @@ class MoELayer:
     weights: dict with router_w bf16 [E,d], router_bias f32 [E], w_gu_q u8
     [E,2f,d/2], w_gu_s u8 [E,2f,d/32], w_d_q u8 [E,d,f/2], w_d_s u8 [E,d,f/32],
     shared_gu bf16 [2fs,d], shared_d bf16 [d,fs], rms_gamma bf16 [d].
+    mxfp4_layout: 0 if the expert bytes are canonical (the layer keeps a tiled
+    copy), 1 if FC1 is already in tiled layout 2 and FC2 in layout 1; by
+    default the dict's "mxfp4_layout" entry, else 0.
     """
 
     def __init__(self, d, f, n_experts, top_k, f_shared, max_batch, weights,
-                 routed_scale=2.5, rms_eps=1e-6):
-        self.dims = MoEDims(d, f, n_experts, top_k, f_shared, max_batch, routed_scale, rms_eps, 0)
+                 routed_scale=2.5, rms_eps=1e-6, mxfp4_layout=None):
+        if mxfp4_layout is None:
+            mxfp4_layout = int(weights.get("mxfp4_layout", 0))
+        self.dims = MoEDims(d, f, n_experts, top_k, f_shared, max_batch, routed_scale, rms_eps,
+                            mxfp4_layout)
         E, fs = n_experts, f_shared
         spec = {
             "router_w": (torch.bfloat16, (E, d)), "router_bias": (torch.float32, (E,)),
@@ -181,19 +188,20 @@ def mxfp4_packed_bytes(rows, k, layout=0):
     return qb, sb.value
 
 
-def mxfp4_pack(w):
-    """Host packer: w CPU float32 [rows, k] -> (q uint8 [rows, k/2], s uint8 [rows, k/32])."""
+def mxfp4_pack(w, layout=0):
+    """Host packer: w CPU float32 [rows, k] -> (q uint8 [rows, k/2], s uint8 [rows, k/32])
+    in the given layout (0 canonical, 1 tiled rows, 2 tiled gate/up pairs)."""
     if w.is_cuda or w.dtype != torch.float32 or w.dim() != 2:
         raise ValueError("mxfp4_pack wants a CPU float32 matrix")
     w = w.contiguous()
     rows, k = w.shape
     q = torch.empty((rows, k // 2), dtype=torch.uint8)
     s = torch.empty((rows, k // 32), dtype=torch.uint8)
-    check(lib().mxfp4_pack(_ptr(w), rows, k, _ptr(q), _ptr(s), 0), "mxfp4_pack")
+    check(lib().mxfp4_pack(_ptr(w), rows, k, _ptr(q), _ptr(s), int(layout)), "mxfp4_pack")
     return q, s
 
 
-def mxfp4_pack_device(w, q=None, s=None, stream=None):
+def mxfp4_pack_device(w, q=None, s=None, stream=None, layout=0):
     """Device packer: w CUDA float32 [rows, k] -> q, s on the same device."""
     if not w.is_cuda or w.dtype != torch.float32 or w.dim() != 2:
         raise ValueError("mxfp4_pack_device wants a CUDA float32 matrix")
@@ -203,6 +211,22 @@ def mxfp4_pack_device(w, q=None, s=None, stream=None):
         q = torch.empty((rows, k // 2), dtype=torch.uint8, device=w.device)
     if s is None:
         s = torch.empty((rows, k // 32), dtype=torch.uint8, device=w.device)
-    check(lib().mxfp4_pack_device(_stream(stream), _ptr(w), rows, k, _ptr(q), _ptr(s), 0),
-          "mxfp4_pack_device")
+    check(lib().mxfp4_pack_device(_stream(stream), _ptr(w), rows, k, _ptr(q), _ptr(s),
+                                  int(layout)), "mxfp4_pack_device")
     return q, s
+
+
+def mxfp4_retile_device(q, s, layout, stream=None):
+    """Canonical packed bytes (CUDA uint8 [..., rows, k/2] and [..., rows, k/32],
+    matrices stacked on the leading dims) -> new tensors in tiled layout 1 or 2."""
+    if not (q.is_cuda and s.is_cuda) or q.dtype != torch.uint8 or s.dtype != torch.uint8:
+        raise ValueError("mxfp4_retile_device wants CUDA uint8 tensors")
+    q = q.contiguous()
+    s = s.contiguous()
+    rows, k = q.shape[-2], q.shape[-1] * 2
+    n_mat = q.numel() // (rows * (k // 2))
+    qo = torch.empty_like(q)
+    so = torch.empty_like(s)
+    check(lib().mxfp4_retile_device(_stream(stream), _ptr(q), _ptr(s), n_mat, rows, k, int(layout),
+                                    _ptr(qo), _ptr(so)), "mxfp4_retile_device")
+    return qo, so

@@ -48,6 +48,33 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
       : "r"(w));
 }
 
+// D += A * B on the tensor cores: one m16n8k16 tile, f16 operands, fp32
+// accumulators, in the register fragments of PTX mma.sync .row.col: with
+// g = lane/4, t = lane%4, a0/a2 hold row g at k = 2t, 2t+1 / 2t+8, 2t+9 and
+// a1/a3 the same k of row g+8; b0/b1 hold column g at k = 2t, 2t+1 /
+// 2t+8, 2t+9; d0, d1 are (row g, columns 2t, 2t+1), d2, d3 the same for
+// row g+8.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same with zero accumulators: D = A * B.
+__device__ __forceinline__ void mma_f16_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
 }

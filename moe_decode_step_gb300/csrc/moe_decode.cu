@@ -49,7 +49,6 @@ enum { kTimeRouterStart, kTimeRouterEnd, kTimeFc1End, kTimeFc2End, kTimeTailEnd,
 struct Workspace {
   float* logits;
   unsigned* done;
-  int* x_shift;
   int32_t* topk_idx;
   float* topk_w;
   int* n_active;
@@ -70,7 +69,8 @@ struct Workspace {
 
 // Launch shape of one streaming-GEMV step.
 struct StreamPlan {
-  int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0;
+  int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0, red_pp = 0;
+  int kc = 1;   // K chunks per item of the MXFP4 segment
 };
 
 enum { kStepRouter, kStepFc1, kStepFc2, kNumSteps };
@@ -91,6 +91,11 @@ struct moe_layer {
   moe_layer* next = nullptr;
   StreamPlan plan[kNumSteps][3];   // by batch class (B = 1, B <= 8, B > 8)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
+  // expert weights in the kernels' tiled layouts (FC1 gate/up pairs, FC2
+  // rows): the caller's when created with mxfp4_layout 1, else a copy
+  // retiled at create time that the handle owns
+  const uint8_t *gu_q = nullptr, *gu_s = nullptr, *d_q = nullptr, *d_s = nullptr;
+  void* owned_w = nullptr;
 };
 
 namespace {
@@ -108,7 +113,6 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   Workspace w;
   w.logits = carve<float>(p, B * E);
   w.done = carve<unsigned>(p, 1);
-  w.x_shift = carve<int>(p, B);
   w.topk_idx = carve<int32_t>(p, P);
   w.topk_w = carve<float>(p, P);
   w.n_active = carve<int>(p, 1);
@@ -130,29 +134,33 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
 }
 
 int validate_dims(const moe_dims_t& d) {
-  if (d.d <= 0 || d.d % 256 != 0 || d.d > 8192) return MOE_ERR_INVALID_ARG;
+  if (d.d <= 0 || d.d % 256 != 0 || d.d > 7680) return MOE_ERR_INVALID_ARG;
   if (d.f <= 0 || d.f % 256 != 0 || d.f > 4096) return MOE_ERR_INVALID_ARG;
   if (d.f_shared <= 0 || d.f_shared % 256 != 0 || d.f_shared > 4096) return MOE_ERR_INVALID_ARG;
   if (d.top_k < 1 || d.top_k > 32) return MOE_ERR_INVALID_ARG;
   if (d.n_experts < d.top_k || d.n_experts > 1024) return MOE_ERR_INVALID_ARG;
   if (d.max_batch < 1 || d.max_batch > 64) return MOE_ERR_INVALID_ARG;
   if (!(d.routed_scale > 0.f) || !(d.rms_eps >= 0.f)) return MOE_ERR_INVALID_ARG;
-  if (d.mxfp4_layout != 0) return MOE_ERR_UNSUPPORTED;
+  if (d.mxfp4_layout != 0 && d.mxfp4_layout != 1) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
 // Kernel instantiations.  FC1 and FC2 each stream the shared expert (dense
-// bf16, segment A) and the routed experts (MXFP4, segment B) in one launch;
-// the variant is picked by batch class (B = 1, B <= 8, B > 8), which sets how
-// many activation rows one pass carries.
+// bf16, segment A) and the routed experts (MXFP4 on the tensor cores, segment
+// B) in one launch; the variant is picked by batch class (B = 1, B <= 8,
+// B > 8), which sets how many activation rows one pass of the shared expert
+// carries (the routed segment takes up to 8 per pass at any batch).
+// Routed FC1: items of one tile (8 gate/up row pairs), at most 16 K blocks
+// per warp (d <= 7680 with 15 consumer warps).  Routed FC2: items of two
+// tiles (32 rows), at most 12 K blocks per warp (f <= 4096).
 using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 4>;
 template <int R> using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R>;
-template <int R> using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 4, 16, R>;
-template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 4, 16, R>;
-template <int R> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16, 32, R>;
+using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 8, true, 1, 16>;
+template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R>;
+using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 32, 32, 8, true, 2, 12>;
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
-#define MOE_FC1_KERNEL(RS, RR) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg<RR>, false>
-#define MOE_FC2_KERNEL(RS, RR) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<RR>, true>
+#define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
+#define MOE_FC2_KERNEL(RS) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg, true>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -160,22 +168,64 @@ int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 // from each instantiation's register footprint.
 constexpr int kBudget1 = 220 * 1024;   // one CTA per SM
 constexpr int kBudget2 = 110 * 1024;   // two
-constexpr int kBudget3 = 72 * 1024;    // three
-constexpr int kBudget4 = 54 * 1024;    // four
 
-// Launch shape for a kernel whose segments have the given row lengths.
+// Consumer warps one segment needs for row length K.
+template <class C>
+int seg_warps(int K) {
+  if constexpr (C::MMA) return kMmaWarps;
+  else return (K + StreamShape<C::ACTH>::WARP_K - 1) / StreamShape<C::ACTH>::WARP_K;
+}
+
+// K chunks per item of a tensor-core segment: the fewest that keep a stage
+// within 32 KB while every warp's blocks stay inside one chunk.
+template <class C>
+int seg_kc(int K, int KW) {
+  if constexpr (C::MMA) {
+    const int nblk = K / 32, NB = mx_warp_blocks(K, KW);
+    for (int kc = 1; kc <= 8; kc *= 2) {
+      if (nblk % kc != 0) break;
+      const int CB = nblk / kc;
+      if (kc > 1 && CB % NB != 0) break;
+      if (mx_stage_bytes(K, C::TM, kc) <= 32 * 1024) return kc;
+    }
+    return 1;
+  } else {
+    return 1;
+  }
+}
+
+template <class C>
+size_t seg_stage_bytes(int K, int kc) {
+  if constexpr (C::MMA) return mx_stage_bytes(K, C::TM, kc);
+  else return (size_t)(C::GLU ? 2 : 1) * stream_rows_bytes(K, C::SP);
+}
+
+// A tensor-core segment fits the launch: its K blocks per warp within NBMAX,
+// one epilogue thread per item output, whole tiles of rows.
+template <class C>
+bool seg_fits(int K, int N, int KW) {
+  if constexpr (C::MMA) {
+    return mx_warp_blocks(K, KW) <= C::NBMAX && C::RW * C::RMAX <= 32 * KW &&
+           N % (C::GLU ? 8 : 16) == 0 && K % 128 == 0;
+  } else {
+    return true;
+  }
+}
+
+// Launch shape for a kernel whose segments have row lengths KA, KB and output
+// rows NA, NB (segment B is the routed one).
 template <class A, class B, typename Kern>
-int plan_kernel(Kern kern, int KA, int KB, int n_sm, int budget, StreamPlan* p) {
-  using ShA = StreamShape<A::WF, A::ACTH>;
-  using ShB = StreamShape<B::WF, B::ACTH>;
-  const int KW = std::max((KA + ShA::WARP_K - 1) / ShA::WARP_K, (KB + ShB::WARP_K - 1) / ShB::WARP_K);
-  const size_t sa = (A::GLU ? 2 : 1) * stream_rows_bytes(A::WF, KA, A::SP);
-  const size_t sb = (B::GLU ? 2 : 1) * stream_rows_bytes(B::WF, KB, B::SP);
+int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget, StreamPlan* p) {
+  const int KW = std::max(seg_warps<A>(KA), seg_warps<B>(KB));
+  if (!seg_fits<A>(KA, NA, KW) || !seg_fits<B>(KB, NB, KW)) return MOE_ERR_UNSUPPORTED;
   StreamPlan r;
   r.threads = 32 * (KW + 1);
+  r.kc = seg_kc<B>(KB, KW);
+  const size_t sa = seg_stage_bytes<A>(KA, 1), sb = seg_stage_bytes<B>(KB, r.kc);
   r.stage_bytes = (int)((std::max(sa, sb) + 127) / 128 * 128);
-  const int red_bytes = 2 * 64 * KW * 4 + 32;
-  r.NS = std::min(8, (budget - red_bytes) / (r.stage_bytes + 16));
+  r.red_pp = stream_red_pp(KW, std::max(A::TM, B::TM));
+  const int red_bytes = 2 * r.red_pp * 4 + 64;
+  r.NS = std::min(16, (budget - red_bytes) / (r.stage_bytes + 16));
   if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
   MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
@@ -193,20 +243,21 @@ int plan_all(moe_layer* L) {
   int rc;
 #define MOE_PLAN(expr) \
   if ((rc = (expr))) return rc;
-  MOE_PLAN((plan_kernel<RouterCfg, RouterCfg>(MOE_ROUTER_KERNEL, d.d, d.d, n, kBudget2,
+  MOE_PLAN((plan_kernel<RouterCfg, RouterCfg>(MOE_ROUTER_KERNEL, d.d, d.n_experts, d.d,
+                                              d.n_experts, n, kBudget2,
                                               &L->plan[kStepRouter][0])));
-  MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg<1>>(MOE_FC1_KERNEL(1, 1), d.d, d.d, n, kBudget2,
-                                              &L->plan[kStepFc1][0])));
-  MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg<2>>(MOE_FC1_KERNEL(2, 2), d.d, d.d, n, kBudget1,
-                                              &L->plan[kStepFc1][1])));
-  MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg<2>>(MOE_FC1_KERNEL(4, 2), d.d, d.d, n, kBudget1,
-                                              &L->plan[kStepFc1][2])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<1>, Fc2Cfg<1>>(MOE_FC2_KERNEL(1, 1), d.f_shared, d.f, n, kBudget4,
-                                              &L->plan[kStepFc2][0])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<2>, Fc2Cfg<2>>(MOE_FC2_KERNEL(2, 2), d.f_shared, d.f, n, kBudget3,
-                                              &L->plan[kStepFc2][1])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<4>, Fc2Cfg<2>>(MOE_FC2_KERNEL(4, 2), d.f_shared, d.f, n, kBudget3,
-                                              &L->plan[kStepFc2][2])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg>(MOE_FC1_KERNEL(1), d.d, d.f_shared, d.d, d.f, n,
+                                           kBudget1, &L->plan[kStepFc1][0])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg>(MOE_FC1_KERNEL(2), d.d, d.f_shared, d.d, d.f, n,
+                                           kBudget1, &L->plan[kStepFc1][1])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg>(MOE_FC1_KERNEL(4), d.d, d.f_shared, d.d, d.f, n,
+                                           kBudget1, &L->plan[kStepFc1][2])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<1>, Fc2Cfg>(MOE_FC2_KERNEL(1), d.f_shared, d.d, d.f, d.d, n,
+                                           kBudget1, &L->plan[kStepFc2][0])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<2>, Fc2Cfg>(MOE_FC2_KERNEL(2), d.f_shared, d.d, d.f, d.d, n,
+                                           kBudget1, &L->plan[kStepFc2][1])));
+  MOE_PLAN((plan_kernel<Sh2Cfg<4>, Fc2Cfg>(MOE_FC2_KERNEL(4), d.f_shared, d.d, d.f, d.d, n,
+                                           kBudget1, &L->plan[kStepFc2][2])));
 #undef MOE_PLAN
   return MOE_OK;
 }
@@ -245,7 +296,6 @@ StreamArgs base_args(moe_layer* L) {
   StreamArgs a;
   std::memset(&a, 0, sizeof(a));
   a.k = L->dims.top_k;
-  a.x_shift = L->ws.x_shift;
   a.n_active = L->ws.n_active;
   a.active_expert = L->ws.active_expert;
   a.active_off = L->ws.active_off;
@@ -260,6 +310,8 @@ int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_i
                 cudaStream_t st, bool pdl) {
   a.NS = p.NS;
   a.stage_bytes = p.stage_bytes;
+  a.red_pp = p.red_pp;
+  a.kc = p.kc;
   const int grid = n_items_cap > 0 ? std::min(p.grid, n_items_cap) : p.grid;
   MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, pdl, a));
   return MOE_OK;
@@ -303,6 +355,8 @@ template <typename K>
 int launch_dual(K kern, const StreamPlan& p, StreamArgs a0, StreamArgs a1, cudaStream_t st) {
   a0.NS = a1.NS = p.NS;
   a0.stage_bytes = a1.stage_bytes = p.stage_bytes;
+  a0.red_pp = a1.red_pp = p.red_pp;
+  a0.kc = a1.kc = p.kc;
   MOE_CUDA(launch_ex(kern, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, a0, a1));
   return MOE_OK;
 }
@@ -318,8 +372,8 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   sa.x = static_cast<const uint16_t*>(x);
   sa.out = L->ws.hs;
   StreamArgs ra = base_args(L);
-  ra.q = L->w.w_gu_q;
-  ra.s = L->w.w_gu_s;
+  ra.q = L->gu_q;
+  ra.s = L->gu_s;
   ra.q_stride = L->q_gu_stride;
   ra.s_stride = L->s_gu_stride;
   ra.K = d.d;
@@ -329,9 +383,9 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   ra.out_amax = L->ws.h_amax;
   sa.trace_id = ra.trace_id = 2;
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC1_KERNEL(1, 1), L->plan[kStepFc1][0], sa, ra, st);
-    case 1: return launch_dual(MOE_FC1_KERNEL(2, 2), L->plan[kStepFc1][1], sa, ra, st);
-    default: return launch_dual(MOE_FC1_KERNEL(4, 2), L->plan[kStepFc1][2], sa, ra, st);
+    case 0: return launch_dual(MOE_FC1_KERNEL(1), L->plan[kStepFc1][0], sa, ra, st);
+    case 1: return launch_dual(MOE_FC1_KERNEL(2), L->plan[kStepFc1][1], sa, ra, st);
+    default: return launch_dual(MOE_FC1_KERNEL(4), L->plan[kStepFc1][2], sa, ra, st);
   }
 }
 
@@ -346,8 +400,8 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   sa.h = L->ws.hs;
   sa.out = L->ws.y_s;
   StreamArgs ra = base_args(L);
-  ra.q = L->w.w_d_q;
-  ra.s = L->w.w_d_s;
+  ra.q = L->d_q;
+  ra.s = L->d_s;
   ra.q_stride = L->q_d_stride;
   ra.s_stride = L->s_d_stride;
   ra.K = d.f;
@@ -357,9 +411,9 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   ra.out = L->ws.y_pair;
   sa.trace_id = ra.trace_id = 3;
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC2_KERNEL(1, 1), L->plan[kStepFc2][0], sa, ra, st);
-    case 1: return launch_dual(MOE_FC2_KERNEL(2, 2), L->plan[kStepFc2][1], sa, ra, st);
-    default: return launch_dual(MOE_FC2_KERNEL(4, 2), L->plan[kStepFc2][2], sa, ra, st);
+    case 0: return launch_dual(MOE_FC2_KERNEL(1), L->plan[kStepFc2][0], sa, ra, st);
+    case 1: return launch_dual(MOE_FC2_KERNEL(2), L->plan[kStepFc2][1], sa, ra, st);
+    default: return launch_dual(MOE_FC2_KERNEL(4), L->plan[kStepFc2][2], sa, ra, st);
   }
 }
 
@@ -510,6 +564,37 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
+  if (dims->mxfp4_layout == 1) {
+    L->gu_q = w.w_gu_q;
+    L->gu_s = w.w_gu_s;
+    L->d_q = w.w_d_q;
+    L->d_s = w.w_d_s;
+  } else {
+    const size_t E = dims->n_experts;
+    const size_t total = E * (L->q_gu_stride + L->s_gu_stride + L->q_d_stride + L->s_d_stride);
+    if (cudaMalloc(&L->owned_w, total) != cudaSuccess) {
+      cudaGetLastError();
+      moe_layer_destroy(L);
+      return MOE_ERR_ALLOC;
+    }
+    uint8_t* p = static_cast<uint8_t*>(L->owned_w);
+    uint8_t* gq = p;
+    uint8_t* gs = gq + E * L->q_gu_stride;
+    uint8_t* dq = gs + E * L->s_gu_stride;
+    uint8_t* ds = dq + E * L->q_d_stride;
+    if ((rc = mxfp4_retile_device(nullptr, w.w_gu_q, w.w_gu_s, (int64_t)E, 2 * (int64_t)f,
+                                  (int64_t)dd, 2, gq, gs)) ||
+        (rc = mxfp4_retile_device(nullptr, w.w_d_q, w.w_d_s, (int64_t)E, (int64_t)dd, (int64_t)f,
+                                  1, dq, ds))) {
+      moe_layer_destroy(L);
+      return rc;
+    }
+    if ((e = cudaStreamSynchronize(nullptr)) != cudaSuccess) return fail(e);
+    L->gu_q = gq;
+    L->gu_s = gs;
+    L->d_q = dq;
+    L->d_s = ds;
+  }
   if ((rc = plan_all(L))) {
     moe_layer_destroy(L);
     return rc;
@@ -530,6 +615,7 @@ int moe_layer_destroy(moe_layer_t L) {
   for (int i = 0; i < kNumTimeEvents; ++i)
     if (L->ev_time[i]) cudaEventDestroy(L->ev_time[i]);
   if (L->ws_base) cudaFree(L->ws_base);
+  if (L->owned_w) cudaFree(L->owned_w);
   cudaSetDevice(prev);
   delete L;
   return MOE_OK;
@@ -576,13 +662,14 @@ int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float*
     return MOE_ERR_INVALID_ARG;
   const int64_t rows = which == 0 ? 2LL * L->dims.f : L->dims.d;
   const int64_t k = which == 0 ? L->dims.d : L->dims.f;
-  const uint8_t* q = (which == 0 ? L->w.w_gu_q : L->w.w_d_q) +
+  const uint8_t* q = (which == 0 ? L->gu_q : L->d_q) +
                      (size_t)expert * (which == 0 ? L->q_gu_stride : L->q_d_stride);
-  const uint8_t* s = (which == 0 ? L->w.w_gu_s : L->w.w_d_s) +
+  const uint8_t* s = (which == 0 ? L->gu_s : L->d_s) +
                      (size_t)expert * (which == 0 ? L->s_gu_stride : L->s_d_stride);
+  const int layout = which == 0 ? kMxTiledPairs : kMxTiled;
   const int64_t blocks = std::min<int64_t>((rows * (k / 32) + 255) / 256, 4096);
-  mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(q, s, rows,
-                                                                                       k, out);
+  mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      q, s, rows, k, layout, out);
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -648,32 +735,54 @@ int moe_launches_per_forward(moe_layer_t L, int B) {
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {
-  if (rows < 0 || k <= 0 || k % 32 != 0 || layout != 0) return 0;
+  if (!mx_layout_ok(rows, k, layout)) return 0;
   if (scale_bytes) *scale_bytes = (size_t)(rows * (k / 32));
   return (size_t)(rows * (k / 2));
 }
 
 int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, int layout) {
   if (!w || !q || !s || rows < 0 || k <= 0 || k % 32 != 0) return MOE_ERR_INVALID_ARG;
-  if (layout != 0) return MOE_ERR_UNSUPPORTED;
+  if (!mx_layout_ok(rows, k, layout)) return MOE_ERR_UNSUPPORTED;
   const int64_t nb = k / 32;
   for (int64_t r = 0; r < rows; ++r)
-    for (int64_t b = 0; b < nb; ++b)
-      s[r * nb + b] = mx_pack_block(w + r * k + b * 32, q + r * (k / 2) + b * 16);
+    for (int64_t b = 0; b < nb; ++b) {
+      uint8_t qb[16];
+      const uint8_t sb = mx_pack_block(w + r * k + b * 32, qb);
+      mx_store_block(q, s, r, b, rows, k, layout, qb, sb);
+    }
   return MOE_OK;
 }
 
 int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
                       uint8_t* s, int layout) {
   if (!w || !q || !s || rows < 0 || k <= 0 || k % 32 != 0) return MOE_ERR_INVALID_ARG;
-  if (layout != 0) return MOE_ERR_UNSUPPORTED;
+  if (!mx_layout_ok(rows, k, layout)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(w) || !aligned16(q)) return MOE_ERR_UNSUPPORTED;
   const int64_t total = rows * (k / 32);
   if (total == 0) return MOE_OK;
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
   mxfp4_pack_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(w, rows, k, q,
-                                                                                     s);
+                                                                                     s, layout);
   MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int mxfp4_retile_device(void* stream, const uint8_t* q_in, const uint8_t* s_in, int64_t n_mat,
+                        int64_t rows, int64_t k, int layout, uint8_t* q_out, uint8_t* s_out) {
+  if (!q_in || !s_in || !q_out || !s_out || n_mat < 0 || rows < 0 || k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (layout == kMxCanonical || !mx_layout_ok(rows, k, layout)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(q_in) || !aligned16(q_out)) return MOE_ERR_UNSUPPORTED;
+  const int64_t qb = rows * (k / 2), sb = rows * (k / 32);
+  const int64_t total = rows * (k / 32);
+  if (total == 0) return MOE_OK;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int64_t m = 0; m < n_mat; ++m) {
+    mxfp4_retile_kernel<<<(unsigned)blocks, 256, 0, st>>>(q_in + m * qb, s_in + m * sb, rows, k,
+                                                         q_out + m * qb, s_out + m * sb, layout);
+    MOE_CUDA(cudaGetLastError());
+  }
   return MOE_OK;
 }
 

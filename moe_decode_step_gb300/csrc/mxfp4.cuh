@@ -7,6 +7,15 @@
 // the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} to nearest, ties to the even code,
 // saturating at 6; the sign bit is the sign of w.  Canonical layout: byte j of
 // a row holds elements 2j (low nibble) and 2j + 1 (high nibble).
+//
+// Kernel (tiled) layouts keep the same bytes, rearranged for the tensor-core
+// consumers: rows go in tiles of 16 mma rows (layout 1: 16 consecutive rows;
+// layout 2, for a [2n][k] gate/up matrix: gate rows 8T..8T+7 as mma rows 0..7
+// and the matching up rows n+8T.. as mma rows 8..15).  Within a tile, the 16
+// bytes lane L = 4g + t loads for K blocks 2P and 2P+1 are adjacent: bytes
+// [4t, 4t+4) of mma rows g and g+8 in block 2P, then the same in block 2P+1.
+// The scales of a tile are grouped by 4 blocks: for group Q and g < 8, eight
+// bytes hold (row g, row g+8) for blocks 4Q..4Q+3.
 #pragma once
 
 #include <math.h>
@@ -63,8 +72,61 @@ __host__ __device__ inline uint8_t mx_pack_block(const float* w, uint8_t* q16) {
   return (uint8_t)(e + 127);
 }
 
+enum { kMxCanonical = 0, kMxTiled = 1, kMxTiledPairs = 2 };
+
+// Tile T and mma row r (0..15) of canonical row `row` in a tiled layout.
+__host__ __device__ inline void mx_tile_of_row(int64_t row, int64_t rows, int layout, int64_t& T,
+                                               int& r) {
+  if (layout == kMxTiledPairs) {
+    const int64_t n = rows / 2;
+    const int64_t i = row < n ? row : row - n;
+    T = i / 8;
+    r = (int)(i % 8) + (row < n ? 0 : 8);
+  } else {
+    T = row / 16;
+    r = (int)(row % 16);
+  }
+}
+
+// Byte offset of nibble bytes [4u, 4u+4) of K block b of (tile T, mma row r).
+__host__ __device__ inline int64_t mx_tiled_word_offset(int64_t T, int r, int64_t b, int u,
+                                                        int64_t k) {
+  const int g = r & 7, half = r >> 3;
+  return T * 8 * k + ((b / 2) * 32 + 4 * g + u) * 16 + (b % 2) * 8 + half * 4;
+}
+
+// Byte offset of the scale of K block b of (tile T, mma row r).
+__host__ __device__ inline int64_t mx_tiled_scale_offset(int64_t T, int r, int64_t b, int64_t k) {
+  const int g = r & 7, half = r >> 3;
+  return T * (k / 2) + ((b / 4) * 8 + g) * 8 + (b % 4) * 2 + half;
+}
+
+// Where the 16 nibble bytes and the scale byte of (row, block b) go.
+__host__ __device__ inline void mx_store_block(uint8_t* q, uint8_t* s, int64_t row, int64_t b,
+                                               int64_t rows, int64_t k, int layout,
+                                               const uint8_t (&qb)[16], uint8_t sb) {
+  if (layout == kMxCanonical) {
+    memcpy(q + row * (k / 2) + b * 16, qb, 16);
+    s[row * (k / 32) + b] = sb;
+    return;
+  }
+  int64_t T;
+  int r;
+  mx_tile_of_row(row, rows, layout, T, r);
+  for (int u = 0; u < 4; ++u) memcpy(q + mx_tiled_word_offset(T, r, b, u, k), qb + 4 * u, 4);
+  s[mx_tiled_scale_offset(T, r, b, k)] = sb;
+}
+
+// A layout's shape rules: k % 32 (canonical); tiled also k % 128 and whole tiles.
+__host__ __device__ inline bool mx_layout_ok(int64_t rows, int64_t k, int layout) {
+  if (rows < 0 || k <= 0 || k % 32 != 0) return false;
+  if (layout == kMxCanonical) return true;
+  if (layout != kMxTiled && layout != kMxTiledPairs) return false;
+  return k % 128 == 0 && rows % 16 == 0;
+}
+
 __global__ void mxfp4_pack_kernel(const float* __restrict__ w, int64_t rows, int64_t k,
-                                  uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+                                  uint8_t* __restrict__ q, uint8_t* __restrict__ s, int layout) {
   const int64_t nb = k / 32;
   const int64_t total = rows * nb;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
@@ -81,25 +143,54 @@ __global__ void mxfp4_pack_kernel(const float* __restrict__ w, int64_t rows, int
       blk[4 * i + 3] = v.w;
     }
     uint8_t qb[16];
-    s[r * nb + b] = mx_pack_block(blk, qb);
-    uint4 out;
-    memcpy(&out, qb, 16);
-    *reinterpret_cast<uint4*>(q + r * (k / 2) + b * 16) = out;
+    const uint8_t sb = mx_pack_block(blk, qb);
+    mx_store_block(q, s, r, b, rows, k, layout, qb, sb);
   }
 }
 
-// Dequantise rows x k through the GEMV kernels' decode path
-// (cvt.rn.f16x2.e2m1x2 and the E8M0 scale) into fp32.
-__global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
-                                     int64_t rows, int64_t k, float* __restrict__ out) {
+// Canonical packed bytes -> a tiled layout (a byte permutation).
+__global__ void mxfp4_retile_kernel(const uint8_t* __restrict__ qc, const uint8_t* __restrict__ sc,
+                                    int64_t rows, int64_t k, uint8_t* __restrict__ q,
+                                    uint8_t* __restrict__ s, int layout) {
   const int64_t nb = k / 32;
   const int64_t total = rows * nb;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / nb, b = t % nb;
-    const uint4 v = *reinterpret_cast<const uint4*>(q + r * (k / 2) + b * 16);
-    const float sc = e8m0_to_f32(s[r * nb + b]);
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    uint8_t qb[16];
+    const uint4 v = *reinterpret_cast<const uint4*>(qc + r * (k / 2) + b * 16);
+    memcpy(qb, &v, 16);
+    mx_store_block(q, s, r, b, rows, k, layout, qb, sc[r * nb + b]);
+  }
+}
+
+// Dequantise rows x k (any layout) into canonical fp32 rows with the
+// consumers' element decode (cvt.rn.f16x2.e2m1x2) and the exact E8M0 value.
+__global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
+                                     int64_t rows, int64_t k, int layout,
+                                     float* __restrict__ out) {
+  const int64_t nb = k / 32;
+  const int64_t total = rows * nb;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / nb, b = t % nb;
+    uint32_t words[4];
+    float sc;
+    if (layout == kMxCanonical) {
+      const uint4 v = *reinterpret_cast<const uint4*>(q + r * (k / 2) + b * 16);
+      words[0] = v.x;
+      words[1] = v.y;
+      words[2] = v.z;
+      words[3] = v.w;
+      sc = e8m0_to_f32(s[r * nb + b]);
+    } else {
+      int64_t T;
+      int mr;
+      mx_tile_of_row(r, rows, layout, T, mr);
+      for (int u = 0; u < 4; ++u)
+        words[u] = *reinterpret_cast<const uint32_t*>(q + mx_tiled_word_offset(T, mr, b, u, k));
+      sc = e8m0_to_f32(s[mx_tiled_scale_offset(T, mr, b, k)]);
+    }
     float* o = out + r * k + b * 32;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {

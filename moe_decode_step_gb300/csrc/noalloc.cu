@@ -38,14 +38,13 @@ constexpr size_t kPairs = (size_t)kMaxRows * kMaxTopK;
 // Layout of the scratch array (byte offsets, each 256-aligned).
 constexpr size_t kOffLogits = 0;
 constexpr size_t kOffDone = kOffLogits + kLogitsBytes;
-constexpr size_t kOffXShift = kOffDone + 256;
-constexpr size_t kOffNActive = kOffXShift + 256;
+constexpr size_t kOffNActive = kOffDone + 256;
 constexpr size_t kOffActiveExpert = kOffNActive + 256;
 constexpr size_t kOffActiveOff = kOffActiveExpert + kMaxExperts * 4;
 constexpr size_t kOffPairList = kOffActiveOff + (kMaxExperts + 64) * 4;
 constexpr size_t kOffHAmax = kOffPairList + kPairs * 4;
 constexpr size_t kOffStatus = kOffHAmax + kPairs * 4;
-constexpr size_t kScratchBytes = kOffStatus + 256;   // 284,928 bytes
+constexpr size_t kScratchBytes = kOffStatus + 256;   // 284,672 bytes
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -55,7 +54,7 @@ inline bool aligned16_noalloc(const void* p) { return ((uintptr_t)p & 15u) == 0;
 
 struct DeviceSetup {
   unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
-  int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0;
+  int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0, red_pp = 0;
   int d = 0;                          // hidden size the launch shape was sized for
 };
 
@@ -74,10 +73,11 @@ int device_setup(int dev, int d, DeviceSetup* out) {
     s.scratch = static_cast<unsigned char*>(p);
   }
   if (s.d != d) {
-    using Sh = StreamShape<kWfBf16, false>;
+    using Sh = StreamShape<false>;
     const int KW = (d + Sh::WARP_K - 1) / Sh::WARP_K;
-    const int stage = (int)((stream_rows_bytes(kWfBf16, d, 1) + 127) / 128 * 128);
-    const int red = 2 * 64 * KW * 4 + 32;
+    const int stage = (int)((stream_rows_bytes(d, 1) + 127) / 128 * 128);
+    const int red_pp = stream_red_pp(KW, 1);
+    const int red = 2 * red_pp * 4 + 64;
     const int budget = 110 * 1024;
     const int NS = std::min(8, (budget - red) / (stage + 16));
     if (NS < 2) return MOE_ERR_UNSUPPORTED;
@@ -96,6 +96,7 @@ int device_setup(int dev, int d, DeviceSetup* out) {
     s.NS = NS;
     s.stage_bytes = stage;
     s.smem = smem;
+    s.red_pp = red_pp;
     s.d = d;
   }
   *out = s;
@@ -136,6 +137,8 @@ extern "C" int moe_router_topk_noalloc(void* stream, const void* router_w, const
   a.status = reinterpret_cast<int*>(s.scratch + kOffStatus);
   a.NS = s.NS;
   a.stage_bytes = s.stage_bytes;
+  a.red_pp = s.red_pp;
+  a.kc = 1;
   const int grid = std::min(s.grid, (n_experts + 1) / 2);
   NOALLOC_ROUTER_KERNEL<<<grid, s.threads, s.smem, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;

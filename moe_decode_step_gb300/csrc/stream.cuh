@@ -1,6 +1,6 @@
 // Persistent streaming GEMV: one producer thread feeds a ring of shared-memory
-// stages with bulk copies (cp.async.bulk + mbarrier), consumer warps compute
-// from shared memory with their activation slice in registers.
+// stages with bulk copies (cp.async.bulk + mbarrier); consumer warps compute
+// from shared memory.
 //
 // It serves every weight-streaming step of the layer:
 //   routed FC1   MXFP4 gate/up rows x x (bf16 -> f16), SwiGLU epilogue
@@ -15,12 +15,23 @@
 //
 // Work: an item is RW consecutive output rows (row pairs for gate/up) of one
 // matrix; for routed steps the matrix is an active expert and the activation
-// rows are that expert's (row, slot) pairs, taken R <= RMAX at a time.  Items
-// are dealt to CTAs round-robin, so the producer knows its whole sequence and
-// runs ahead across item boundaries; the only coupling is the stage ring.
-// Consumer warps split K (warp w owns a K slab); partial sums stay in
-// registers for the whole item, then a butterfly reduce-scatter and one
-// shared-memory combine across the K slabs, in a fixed order (deterministic).
+// rows are that expert's (row, slot) pairs, taken R <= RMAX at a time.  CTA c
+// owns a contiguous range of items, so the producer knows its whole sequence
+// and runs ahead across item boundaries; the only coupling is the stage ring.
+// Consumer warps split K (warp w owns a K slab), then combine their partial
+// sums through shared memory in a fixed order (deterministic).
+//
+// Two consumer formulations:
+//  * bf16 weights (router, shared expert): every lane owns a run of K
+//    elements and keeps one fp32 partial per row; a butterfly reduce-scatter
+//    then folds the lanes.
+//  * MXFP4 weights (routed experts): the tensor cores (mma.sync m16n8k16,
+//    f16 x f16 -> fp32) take the products, 16 weight rows by up to 8
+//    activation rows per instruction.  Dequantising a nibble pair is one
+//    cvt.rn.f16x2.e2m1x2; the per-row, per-block E8M0 scale is applied to the
+//    fp32 result of the block's two MMAs.  Doing the products on the CUDA
+//    cores instead costs about two issue slots per weight, which at 0.53
+//    bytes per weight is more than an SM can issue at HBM speed.
 #pragma once
 
 #include "common.cuh"
@@ -28,6 +39,9 @@
 namespace moe {
 
 enum { kWfMx = 0, kWfBf16 = 1 };
+
+// Consumer warps of the MXFP4 (tensor-core) steps.
+constexpr int kMmaWarps = 15;
 
 struct StreamArgs {
   const uint8_t* q;          // MXFP4 nibbles (or bf16 weights) of matrix 0
@@ -38,7 +52,6 @@ struct StreamArgs {
   int k;                     // top-k: pair p belongs to activation row p / k (routed)
   int B;                     // dense steps: activation rows
   const uint16_t* x;         // bf16 activations [rows][K]
-  const int* x_shift;        // f16 scaling shift per x row (MXFP4 x-activation steps)
   const float* h;            // fp32 activations [rows][K]
   const unsigned* h_amax;    // max |h| bits per row (MXFP4 h-activation steps)
   float* out;                // [rows][N]
@@ -50,86 +63,46 @@ struct StreamArgs {
   int* status;               // device status word (bounded-wait timeouts)
   int NS;                    // stage buffers in the ring
   int stage_bytes;           // bytes per stage buffer (multiple of 128)
+  int red_pp;                // floats per cross-slab partial buffer (two of them)
+  int kc;                    // MXFP4 steps: K chunks (stages) per tile group
   unsigned long long* trace; // optional kernel trace (see trace_begin), or null
   int trace_id;
 };
 
-// Elements per lane and activation registers per row, by format.
-template <int WF, bool ACTH>
+// Elements per lane and activation registers per row of the bf16 steps.
+template <bool ACTH>
 struct StreamShape {
   static constexpr int EPL = ACTH ? 16 : 32;                 // K elements per lane
-  static constexpr int AW = (WF == kWfBf16 && ACTH) ? 16 : EPL / 2;  // u32 registers per row
+  static constexpr int AW = 16;                              // u32 registers per row
   static constexpr int WARP_K = 32 * EPL;                    // K elements per consumer warp
 };
 
-// Bytes of one stage holding `rows` rows (per half for gate/up).
-__host__ __device__ inline size_t stream_rows_bytes(int wf, int K, int rows) {
-  return wf == kWfMx ? (size_t)rows * (K / 2 + K / 32) : (size_t)rows * K * 2;
+// Bytes of one bf16 stage holding `rows` rows (per half for gate/up).
+__host__ __device__ inline size_t stream_rows_bytes(int K, int rows) {
+  return (size_t)rows * K * 2;
 }
 
-// ---- activation slices (registers) --------------------------------------
-
-// MXFP4 x-activation: 32 elements [blk*32, +32) of a bf16 row as f16x2,
-// scaled by 2^-shift.
-__device__ __forceinline__ void act_load_mx_x(const uint16_t* row, int blk, bool ok, int shift,
-                                              uint32_t (&a)[16]) {
-  if (!ok) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) a[t] = 0;
-    return;
-  }
-  const float sc = pow2f(-shift);
-  const uint4* p = reinterpret_cast<const uint4*>(row + blk * 32);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 v = p[c];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      a[c * 4 + t] = pack_f16x2(__uint_as_float(w[t] << 16) * sc,
-                                __uint_as_float(w[t] & 0xFFFF0000u) * sc);
-  }
+// MXFP4 steps read the tiled layouts (16 mma rows per tile, see mxfp4.cuh).
+// An item is TM consecutive tiles; its K blocks are split into kc chunks of
+// CB = K/32/kc blocks, one stage each.  A stage holds, per tile, the chunk's
+// nibbles (CB * 256 bytes: 512 bytes per block pair, 16 per lane), then per
+// tile the chunk's scales (CB * 16 bytes: 64 per group of 4 blocks).
+__host__ __device__ inline size_t mx_stage_bytes(int K, int TM, int kc) {
+  return (size_t)TM * (K / 32 / kc) * 272;
 }
 
-// Raw bf16 pairs of the 32-element slice [blk*32, +32) of an x row.
-__device__ __forceinline__ void act_load_raw_x(const uint16_t* row, int blk, bool ok,
-                                               uint32_t (&a)[16]) {
-  const uint4* p = reinterpret_cast<const uint4*>(row + blk * 32);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 v = ok ? p[c] : make_uint4(0, 0, 0, 0);
-    a[c * 4 + 0] = v.x;
-    a[c * 4 + 1] = v.y;
-    a[c * 4 + 2] = v.z;
-    a[c * 4 + 3] = v.w;
-  }
+// K blocks per consumer warp of an MXFP4 step: whole groups of 4.
+__host__ __device__ inline int mx_warp_blocks(int K, int KW) {
+  const int nblk = K / 32;
+  return ((nblk + KW - 1) / KW + 3) / 4 * 4;
 }
 
-// bf16 pairs -> f16x2 scaled by 2^-shift, in place.
-__device__ __forceinline__ void act_convert_mx_x(int shift, uint32_t (&a)[16]) {
-  const float sc = pow2f(-shift);
-#pragma unroll
-  for (int t = 0; t < 16; ++t)
-    a[t] = pack_f16x2(__uint_as_float(a[t] << 16) * sc, __uint_as_float(a[t] & 0xFFFF0000u) * sc);
+// Cross-slab partial buffer size (floats, one of two) for KW consumer warps.
+__host__ __device__ inline int stream_red_pp(int KW, int TM) {
+  return (TM * 128 > 64 ? TM * 128 : 64) * KW;
 }
 
-// MXFP4 h-activation: 16 elements [hb*16, +16) of an fp32 row as f16x2.
-__device__ __forceinline__ void act_load_mx_h(const float* row, int hb, bool ok, int shift,
-                                              uint32_t (&a)[8]) {
-  if (!ok) {
-#pragma unroll
-    for (int t = 0; t < 8; ++t) a[t] = 0;
-    return;
-  }
-  const float sc = pow2f(-shift);
-  const float4* p = reinterpret_cast<const float4*>(row + hb * 16);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float4 v = __ldcg(p + c);
-    a[c * 2 + 0] = pack_f16x2(v.x * sc, v.y * sc);
-    a[c * 2 + 1] = pack_f16x2(v.z * sc, v.w * sc);
-  }
-}
+// ---- activation slices of the bf16 steps (registers) ----------------------
 
 // bf16 x-activation for bf16 weights: elements slab + q*256 + lane*8 + [0,8),
 // q < 4, kept as raw bf16 pairs.
@@ -165,63 +138,7 @@ __device__ __forceinline__ void act_load_bf_h(const float* row, int slab, int la
   }
 }
 
-// ---- one weight row (in shared memory) against R activation slices -------
-
-// MXFP4, 32-element block per lane: nibbles at q + blk*16, scale byte at s + blk.
-template <int R>
-__device__ __forceinline__ void row_dot_mx_x(const uint8_t* q, const uint8_t* s, int blk, bool ok,
-                                             const uint32_t (&a)[R][16], float (&out)[R]) {
-#pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = 0.f;
-  if (!ok) return;
-  const uint4 wq = *reinterpret_cast<const uint4*>(q + blk * 16);
-  const float sc = e8m0_to_f32(s[blk]);
-  const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t hq[4];
-    e2m1x8_to_f16x2(words[w], hq);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t xv = a[r][w * 4 + t];
-        out[r] = fma2_f16s(hq[t], (unsigned short)(xv & 0xFFFFu), (unsigned short)(xv >> 16),
-                           out[r]);
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) out[r] *= sc;
-}
-
-// MXFP4, 16-element half block per lane: nibbles at q + hb*8, scale at s + hb/2.
-template <int R>
-__device__ __forceinline__ void row_dot_mx_h(const uint8_t* q, const uint8_t* s, int hb, bool ok,
-                                             const uint32_t (&a)[R][8], float (&out)[R]) {
-#pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = 0.f;
-  if (!ok) return;
-  const uint2 wq = *reinterpret_cast<const uint2*>(q + hb * 8);
-  const float sc = e8m0_to_f32(s[hb >> 1]);
-  const uint32_t words[2] = {wq.x, wq.y};
-#pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    uint32_t hq[4];
-    e2m1x8_to_f16x2(words[w], hq);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t xv = a[r][w * 4 + t];
-        out[r] = fma2_f16s(hq[t], (unsigned short)(xv & 0xFFFFu), (unsigned short)(xv >> 16),
-                           out[r]);
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) out[r] *= sc;
-}
+// ---- one bf16 weight row (in shared memory) against R activation slices ----
 
 // bf16 row (as bytes), x activation: 4 chunks of 8 at slab + q*256 + lane*8.
 template <int R>
@@ -325,8 +242,12 @@ __device__ __forceinline__ StreamItem stream_item(const StreamArgs& a, int it, i
   return m;
 }
 
-template <int RMAX>
+// Activation rows of the next pass: the bf16 steps take 4, 2 or 1 (a
+// template parameter of their consumer); the tensor-core steps any count up
+// to RMAX (mma columns).
+template <int RMAX, bool MMA>
 __device__ __forceinline__ int stream_pass_rows(int left) {
+  if (MMA) return min(left, RMAX);
   return (RMAX >= 4 && left >= 4) ? 4 : ((RMAX >= 2 && left >= 2) ? 2 : 1);
 }
 
@@ -351,45 +272,56 @@ __device__ __forceinline__ int stream_row0(int it, int tiles) {
 }
 
 // Producer: lane 0 of warp 0 issues the bulk copies for items [lo, hi) of one
-// step, continuing the CTA's running stage counter.
-template <int WF, bool GLU, bool ROUTED, int SP, int RW, int RMAX>
+// step, continuing the CTA's running stage counter.  A bf16 stage holds SP
+// rows (gate/up: SP gate rows then the SP matching up rows); an MXFP4 stage
+// holds one K chunk of an item's TM tiles.
+template <int WF, bool GLU, bool ROUTED, int SP, int RW, int RMAX, bool MMA, int TM>
 __device__ __forceinline__ void stream_produce_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, uint32_t& stage) {
   constexpr int G = GLU ? 2 : 1;
-  constexpr int SPI = RW / SP;
+  const int SPI = MMA ? a.kc : RW / SP;
   const uint64_t pol = policy_evict_first();
-  const size_t half_bytes = WF == kWfMx ? (size_t)SP * (a.K / 2) : (size_t)SP * a.K * 2;
-  const size_t s_off = (size_t)G * half_bytes;
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
     const uint8_t* qe = a.q + (size_t)m.e * a.q_stride;
-    for (int done = 0; done < m.pr; done += stream_pass_rows<RMAX>(m.pr - done)) {
+    for (int done = 0; done < m.pr; done += stream_pass_rows<RMAX, MMA>(m.pr - done)) {
       for (int it = it0; it < run_end; ++it) {
         const int row0 = stream_row0<ROUTED, RW>(it, tiles);
         for (int st = 0; st < SPI; ++st, ++stage) {
           const int buf = (int)(stage % (uint32_t)a.NS);
           const uint32_t use = stage / (uint32_t)a.NS;
           if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, a.status);
-          const int r0 = row0 + st * SP;
-          const int nv = max(0, min(SP, a.N - r0));
           uint8_t* dst = stages + (size_t)buf * a.stage_bytes;
-          if (WF == kWfMx) {
+          if constexpr (MMA) {
+            // tiles T0.. of the item, K chunk st: per tile its nibbles and scales
             const uint8_t* se = a.s + (size_t)m.e * a.s_stride;
-            const uint32_t qb = (uint32_t)nv * (a.K / 2), sb = (uint32_t)nv * (a.K / 32);
-            mbar_arrive_expect_tx(&full[buf], G * (qb + sb));
-            if (nv > 0) {
-              bulk_g2s(dst, qe + (size_t)r0 * (a.K / 2), qb, &full[buf], pol);
-              bulk_g2s(dst + s_off, se + (size_t)r0 * (a.K / 32), sb, &full[buf], pol);
-              if (GLU) {
-                bulk_g2s(dst + half_bytes, qe + (size_t)(a.N + r0) * (a.K / 2), qb, &full[buf],
+            const int rows_per_tile = GLU ? 8 : 16;
+            const int T0 = row0 / rows_per_tile;
+            const int nvt = max(0, min(TM, a.N / rows_per_tile - T0));
+            const uint32_t CB = (uint32_t)(a.K / 32 / a.kc);
+            const size_t tq = (size_t)a.K * 8, ts = (size_t)a.K / 2;
+            mbar_arrive_expect_tx(&full[buf], (uint32_t)nvt * CB * 272u);
+            if (a.kc == 1) {   // the item's tiles are contiguous: one copy each part
+              if (nvt > 0) {
+                bulk_g2s(dst, qe + (size_t)T0 * tq, (uint32_t)nvt * CB * 256u, &full[buf], pol);
+                bulk_g2s(dst + (size_t)TM * CB * 256, se + (size_t)T0 * ts,
+                         (uint32_t)nvt * CB * 16u, &full[buf], pol);
+              }
+            } else {
+              for (int t = 0; t < nvt; ++t) {
+                bulk_g2s(dst + (size_t)t * CB * 256, qe + (size_t)(T0 + t) * tq + (size_t)st * CB * 256,
+                         CB * 256u, &full[buf], pol);
+                bulk_g2s(dst + (size_t)TM * CB * 256 + (size_t)t * CB * 16,
+                         se + (size_t)(T0 + t) * ts + (size_t)st * CB * 16, CB * 16u, &full[buf],
                          pol);
-                bulk_g2s(dst + s_off + (size_t)SP * (a.K / 32),
-                         se + (size_t)(a.N + r0) * (a.K / 32), sb, &full[buf], pol);
               }
             }
           } else {
+            const int r0 = row0 + st * SP;
+            const int nv = max(0, min(SP, a.N - r0));
+            const size_t half_bytes = (size_t)SP * a.K * 2;
             const uint32_t wb = (uint32_t)nv * a.K * 2;
             mbar_arrive_expect_tx(&full[buf], G * wb);
             if (nv > 0) {
@@ -421,75 +353,35 @@ __device__ __forceinline__ int stream_x_row(const StreamArgs& a, int pid) {
   return ROUTED ? pid / a.k : pid;
 }
 
-template <int WF, bool ACTH, bool ROUTED>
-__device__ __forceinline__ int stream_shift(const StreamArgs& a, int pid) {
-  if (WF != kWfMx) return 0;
-  if (ACTH) return f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + pid)));
-  return __ldcg(a.x_shift + stream_x_row<ROUTED>(a, pid));
-}
-
-// Consumers: one pass of R activation rows over the run [it0, run_end) of
-// items that share them.  Activation slices, pair ids and scale shifts are
+// Consumers of a bf16 step: one pass of R activation rows over the run
+// [it0, run_end) of items that share them.  Activation slices and pair ids are
 // loaded once; every item then streams its SPI stages, reduces and finalises.
-template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int R>
+template <bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int R>
 __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const StreamItem& m,
                                                    int done, int it0, int run_end, int tiles,
                                                    uint8_t* stages, uint64_t* full,
                                                    uint64_t* empty, float* red, uint32_t& stage,
-                                                   int& pp, int& rp, int kw, int KW, int lane) {
-  using Sh = StreamShape<WF, ACTH>;
+                                                   int& pp, int kw, int KW, int lane) {
+  using Sh = StreamShape<ACTH>;
   constexpr int G = GLU ? 2 : 1;
   constexpr int SPI = RW / SP;
   constexpr int V = RW * G * R;
   constexpr int VM = V < 32 ? V : 32;
   constexpr int M = VM == 1 ? 0 : VM == 2 ? 1 : VM == 4 ? 2 : VM == 8 ? 3 : VM == 16 ? 4 : 5;
-  const size_t half_bytes = WF == kWfMx ? (size_t)SP * (a.K / 2) : (size_t)SP * a.K * 2;
-  const size_t s_off = (size_t)G * half_bytes;
-  const int blk = kw * 32 + lane;
-  const bool ok = blk * Sh::EPL < a.K;
+  const size_t half_bytes = (size_t)SP * a.K * 2;
   const int slab = kw * Sh::WARP_K;
   const int cthreads = KW * 32;
   const int ct = (int)threadIdx.x - 32;
 
-  int pid[R], shift[R];
+  int pid[R];
   uint32_t act[R][Sh::AW];
-  if constexpr (WF == kWfMx && !ACTH) {
-    // x rows: the f16 scaling shift needs the whole row's max |x|; the KW
-    // consumer warps together hold the whole row, so reduce across them.
-    unsigned* s_amax = reinterpret_cast<unsigned*>(red + (size_t)2 * 64 * KW);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
-      act_load_raw_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, blk, ok, act[r]);
-      uint32_t mx = 0;
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        mx = max(mx, max(act[r][q] & 0x7FFFu, (act[r][q] >> 16) & 0x7FFFu));
-      mx = __reduce_max_sync(0xffffffffu, mx);
-      if (lane == 0) atomicMax(&s_amax[(rp & 1) * 4 + r], mx);
-    }
-    consumer_sync(KW * 32);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      shift[r] = f16_shift_for_amax(bf16_bits_to_f32(s_amax[(rp & 1) * 4 + r]));
-      act_convert_mx_x(shift[r], act[r]);
-    }
-    // the other parity's slots are free: every consumer is past this barrier
-    if (kw == 0 && lane < 4) s_amax[((rp & 1) ^ 1) * 4 + lane] = 0u;
-    rp ^= 1;
-  } else {
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
-    shift[r] = stream_shift<WF, ACTH, ROUTED>(a, pid[r]);
-    if constexpr (WF == kWfMx && ACTH) {
-      act_load_mx_h(a.h + (size_t)pid[r] * a.K, blk, ok, shift[r], act[r]);
-    } else if constexpr (!ACTH) {
+    if constexpr (!ACTH)
       act_load_bf_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K, act[r]);
-    } else {
+    else
       act_load_bf_h(a.h + (size_t)pid[r] * a.K, slab, lane, a.K, act[r]);
-    }
-  }
   }
 
   for (int it = it0; it < run_end; ++it) {
@@ -506,16 +398,9 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
 #pragma unroll
         for (int gu = 0; gu < G; ++gu) {
           float o[R];
-          if constexpr (WF == kWfMx) {
-            const uint8_t* qrow = sb + gu * half_bytes + (size_t)rr * (a.K / 2);
-            const uint8_t* srow = sb + s_off + (size_t)(gu * SP + rr) * (a.K / 32);
-            if constexpr (ACTH) row_dot_mx_h<R>(qrow, srow, blk, ok, act, o);
-            else row_dot_mx_x<R>(qrow, srow, blk, ok, act, o);
-          } else {
-            const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
-            if constexpr (ACTH) row_dot_bf_h<R>(wrow, slab, lane, a.K, act, o);
-            else row_dot_bf_x<R>(wrow, slab, lane, a.K, act, o);
-          }
+          const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
+          if constexpr (ACTH) row_dot_bf_h<R>(wrow, slab, lane, a.K, act, o);
+          else row_dot_bf_x<R>(wrow, slab, lane, a.K, act, o);
 #pragma unroll
           for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
         }
@@ -528,7 +413,7 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
     // combine: lanes -> one value per lane group, then K slabs through shared memory
     float second;
     const float first = stream_reduce<V>(v, lane, second);
-    float* rb = red + (size_t)pp * 64 * KW;
+    float* rb = red + (size_t)pp * a.red_pp;
     if ((lane & ((1 << (5 - M)) - 1)) == 0) {
       const int vi = lane >> (5 - M);
       rb[vi * KW + kw] = first;
@@ -539,18 +424,15 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
       const int j = t / R, r = t % R;
       const int row = row0 + j;
       if (row >= a.N) continue;
-      int p = pid[0], sh = shift[0];
+      int p = pid[0];
 #pragma unroll
       for (int q = 1; q < R; ++q)
-        if (q == r) { p = pid[q]; sh = shift[q]; }
-      const float back = pow2f(sh);
+        if (q == r) p = pid[q];
       float* dst = a.out + (size_t)p * a.N + row;
       if constexpr (GLU) {
         const float* pg = rb + ((j * R + r) * 2) * KW;
         float g = 0.f, u = 0.f;
         for (int w = 0; w < KW; ++w) { g += pg[w]; u += pg[KW + w]; }
-        g *= back;
-        u *= back;
         const float hv = g / (1.0f + expf(-g)) * u;
         *dst = hv;
         if (a.out_amax) atomicMax(a.out_amax + p, __float_as_uint(fabsf(hv)));
@@ -558,7 +440,208 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
         const float* pv = rb + (j * R + r) * KW;
         float acc = 0.f;
         for (int w = 0; w < KW; ++w) acc += pv[w];
-        *dst = acc * back;
+        *dst = acc;
+      }
+    }
+    pp ^= 1;
+  }
+}
+
+// One K block of a lane's two mma rows against its activation column: wa, wb
+// are nibble bytes [4t, 4t+4) of mma rows g and g+8 (elements 8t..8t+7 of the
+// block), bytes 0 and 1 going to the first MMA and 2, 3 to the second, one
+// f16 pair each; x holds the same eight elements of column g.  Both operands
+// see one k permutation, which leaves the dot products unchanged.  The two
+// MMAs sum the block from zero; the rows' block scales fa, fb then multiply
+// the result into the fp32 accumulators (c1, c3: column 2t+1, skipped when
+// ONE, i.e. a single activation row).
+template <bool ONE>
+__device__ __forceinline__ void mx_block_mma(uint32_t wa, uint32_t wb, float fa, float fb,
+                                             const uint32_t (&x)[4], float& c0, float& c1,
+                                             float& c2, float& c3) {
+  uint32_t ha[4], hb[4];
+  e2m1x8_to_f16x2(wa, ha);
+  e2m1x8_to_f16x2(wb, hb);
+  float d[4];
+  mma_f16_16816_zero(d, ha[0], hb[0], ha[1], hb[1], x[0], x[1]);
+  mma_f16_16816(d, ha[2], hb[2], ha[3], hb[3], x[2], x[3]);
+  c0 = fmaf(fa, d[0], c0);
+  c2 = fmaf(fb, d[2], c2);
+  if (!ONE) {
+    c1 = fmaf(fa, d[1], c1);
+    c3 = fmaf(fb, d[3], c3);
+  }
+}
+
+// E8M0 scale bytes at bit offset 8j of a word -> fp32 2^(code - 127) through
+// the exponent field; code 0 (2^-127) becomes 0, which only drops products
+// below 6 * 2^-127 * |activation|.
+__device__ __forceinline__ float e8m0_byte0(uint32_t w) { return __uint_as_float((w << 23) & 0x7F800000u); }
+__device__ __forceinline__ float e8m0_byte1(uint32_t w) { return __uint_as_float((w << 15) & 0x7F800000u); }
+__device__ __forceinline__ float e8m0_byte2(uint32_t w) { return __uint_as_float((w << 7) & 0x7F800000u); }
+__device__ __forceinline__ float e8m0_byte3(uint32_t w) { return __uint_as_float((w >> 1) & 0x7F800000u); }
+
+// Consumers of an MXFP4 step (tensor cores): one pass of R <= 8 activation
+// rows, the mma columns, over the run [it0, run_end) of items of one expert.
+//
+// An item is TM tiles of 16 mma rows (tiled layouts, see mxfp4.cuh): plain
+// steps put 16 consecutive output rows in a tile, gate/up steps 8 row pairs
+// with gate row g in mma row g and its up row in mma row g + 8, so one lane
+// ends with both halves of a pair.  Warp kw owns the NB K blocks from
+// b0 = kw * NB (NB a multiple of 4, all in one K chunk) and reads, per pair of
+// blocks, 16 bytes (lane-ordered, conflict-free) and per group of four, 8
+// scale bytes.
+template <bool GLU, bool ACTH, int TM, int NBMAX, bool ONE>
+__device__ __forceinline__ void stream_consume_run_mma(
+    const StreamArgs& a, const StreamItem& m, int done, int R, int it0, int run_end, int tiles,
+    uint8_t* stages, uint64_t* full, uint64_t* empty, float* red, uint32_t& stage, int& pp,
+    int& rp, int kw, int KW, int lane) {
+  constexpr int TR = GLU ? TM * 8 : TM * 16;   // output rows (pairs) per item
+  const int g = lane >> 2, t = lane & 3;
+  const int nblk = a.K >> 5;
+  const int NB = mx_warp_blocks(a.K, KW);
+  const int b0 = kw * NB;
+  const int nb = max(0, min(NB, nblk - b0));
+  const int CB = nblk / a.kc;
+  const int chunk = nb > 0 ? b0 / CB : 0;
+  const int lb0 = b0 - chunk * CB;
+  const int cthreads = KW * 32;
+  const int ct = (int)threadIdx.x - 32;
+
+  // the column this lane feeds, and this thread's output column in the epilogue
+  const int ci = min(g, R - 1);
+  const int ei = ct % R;
+  const int cpid = __ldcg(a.pair_list + m.p0 + done + ci);
+  const int epid = __ldcg(a.pair_list + m.p0 + done + ei);
+
+  uint32_t X[NBMAX][4];
+  int eshift;
+  if constexpr (!ACTH) {
+    // x rows (bf16): the f16 scaling shift needs max |x| over the whole row,
+    // which the KW warps hold together: reduce through shared memory.
+    unsigned* s_amax = reinterpret_cast<unsigned*>(red + 2 * (size_t)a.red_pp);
+    unsigned* slots = s_amax + (rp & 1) * 8;
+    const uint16_t* xr = a.x + (size_t)(cpid / a.k) * a.K + 8 * t;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int b = 0; b < NBMAX; ++b) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (b < nb) v = *reinterpret_cast<const uint4*>(xr + (size_t)(b0 + b) * 32);
+      X[b][0] = v.x;
+      X[b][1] = v.y;
+      X[b][2] = v.z;
+      X[b][3] = v.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = max(mx, max(X[b][j] & 0x7FFFu, (X[b][j] >> 16) & 0x7FFFu));
+    }
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (t == 0) atomicMax(slots + ci, mx);
+    consumer_sync(cthreads);
+    const int cshift = f16_shift_for_amax(bf16_bits_to_f32(slots[ci]));
+    eshift = f16_shift_for_amax(bf16_bits_to_f32(slots[ei]));
+    const float sc = pow2f(-cshift);
+#pragma unroll
+    for (int b = 0; b < NBMAX; ++b)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        X[b][j] = pack_f16x2(__uint_as_float(X[b][j] << 16) * sc,
+                             __uint_as_float(X[b][j] & 0xFFFF0000u) * sc);
+    // the other parity's slots are free: every consumer is past this barrier
+    if (kw == 0 && lane < 8) s_amax[((rp & 1) ^ 1) * 8 + lane] = 0u;
+    rp ^= 1;
+  } else {
+    // h rows (fp32): the shift comes from FC1's per-pair max |h|
+    const int cshift = f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + cpid)));
+    eshift = f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + epid)));
+    const float sc = pow2f(-cshift);
+    const float* hr = a.h + (size_t)cpid * a.K + 8 * t;
+#pragma unroll
+    for (int b = 0; b < NBMAX; ++b) {
+      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+      if (b < nb) {
+        v0 = __ldcg(reinterpret_cast<const float4*>(hr + (size_t)(b0 + b) * 32));
+        v1 = __ldcg(reinterpret_cast<const float4*>(hr + (size_t)(b0 + b) * 32 + 4));
+      }
+      X[b][0] = pack_f16x2(v0.x * sc, v0.y * sc);
+      X[b][1] = pack_f16x2(v0.z * sc, v0.w * sc);
+      X[b][2] = pack_f16x2(v1.x * sc, v1.y * sc);
+      X[b][3] = pack_f16x2(v1.z * sc, v1.w * sc);
+    }
+  }
+  const float back = pow2f(eshift);
+  const size_t nib_tile = (size_t)CB * 256, scl_base = (size_t)TM * CB * 256;
+
+  for (int it = it0; it < run_end; ++it) {
+    const int row0 = stream_row0<true, TR>(it, tiles);
+    const uint32_t st = stage + (uint32_t)chunk;
+    const int buf = (int)(st % (uint32_t)a.NS);
+    if (nb > 0) mbar_wait(&full[buf], (st / (uint32_t)a.NS) & 1u, a.status);
+    const uint8_t* sp = stages + (size_t)buf * a.stage_bytes;
+    float acc[TM][4];
+#pragma unroll
+    for (int mb = 0; mb < TM; ++mb) {
+      const uint8_t* nib = sp + mb * nib_tile + (size_t)(lb0 >> 1) * 512 + lane * 16;
+      const uint8_t* scl = sp + scl_base + (size_t)mb * CB * 16 + (size_t)(lb0 >> 2) * 64 + g * 8;
+      float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+      for (int q = 0; q < NBMAX / 4; ++q) {
+        if (4 * q < nb) {
+          const uint2 sv = *reinterpret_cast<const uint2*>(scl + q * 64);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(nib + (2 * q) * 512);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(nib + (2 * q + 1) * 512);
+          mx_block_mma<ONE>(w0.x, w0.y, e8m0_byte0(sv.x), e8m0_byte1(sv.x), X[4 * q], c0, c1, c2, c3);
+          mx_block_mma<ONE>(w0.z, w0.w, e8m0_byte2(sv.x), e8m0_byte3(sv.x), X[4 * q + 1], c0, c1, c2,
+                            c3);
+          mx_block_mma<ONE>(w1.x, w1.y, e8m0_byte0(sv.y), e8m0_byte1(sv.y), X[4 * q + 2], c0, c1, c2,
+                            c3);
+          mx_block_mma<ONE>(w1.z, w1.w, e8m0_byte2(sv.y), e8m0_byte3(sv.y), X[4 * q + 3], c0, c1, c2,
+                            c3);
+        }
+      }
+      acc[mb][0] = c0;
+      acc[mb][1] = c1;
+      acc[mb][2] = c2;
+      acc[mb][3] = c3;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int s = 0; s < a.kc; ++s) mbar_arrive(&empty[(stage + (uint32_t)s) % (uint32_t)a.NS]);
+    }
+    stage += (uint32_t)a.kc;
+
+    // cross-slab combine: partial of (mma row, column) from warp kw at
+    // ((mb*16 + row)*8 + column)*KW + kw
+    float* rbuf = red + (size_t)pp * a.red_pp;
+#pragma unroll
+    for (int mb = 0; mb < TM; ++mb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
+        if (col < R) rbuf[((mb * 16 + row) * 8 + col) * KW + kw] = acc[mb][i];
+      }
+    consumer_sync(cthreads);
+    if (ct < TR * R) {
+      const int j = ct / R;   // output row (pair) within the item; column ei
+      const int row = row0 + j;
+      if (row < a.N) {
+        float* dst = a.out + (size_t)epid * a.N + row;
+        if constexpr (GLU) {
+          const float* pg = rbuf + (((j >> 3) * 16 + (j & 7)) * 8 + ei) * KW;
+          const float* pu = pg + 64 * KW;
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < KW; ++w) { gs += pg[w]; us += pu[w]; }
+          gs *= back;
+          us *= back;
+          const float hv = gs / (1.0f + expf(-gs)) * us;
+          *dst = hv;
+          if (a.out_amax) atomicMax(a.out_amax + epid, __float_as_uint(fabsf(hv)));
+        } else {
+          const float* pv = rbuf + (((j >> 4) * 16 + (j & 15)) * 8 + ei) * KW;
+          float sum = 0.f;
+          for (int w = 0; w < KW; ++w) sum += pv[w];
+          *dst = sum * back;
+        }
       }
     }
     pp ^= 1;
@@ -566,7 +649,8 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
 }
 
 // Consumers: items [lo, hi) of one step, run by run, pass by pass.
-template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
+template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX, bool MMA, int TM,
+          int NBMAX>
 __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
@@ -575,20 +659,31 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
     for (int done = 0; done < m.pr;) {
-      const int R = stream_pass_rows<RMAX>(m.pr - done);
-      if (R == 1) {
-        stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, it0, run_end, tiles,
+      const int R = stream_pass_rows<RMAX, MMA>(m.pr - done);
+      if constexpr (MMA) {
+        if (R == 1)
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, true>(a, m, done, R, it0, run_end, tiles,
+                                                             stages, full, empty, red, stage, pp,
+                                                             rp, kw, KW, lane);
+        else
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, false>(a, m, done, R, it0, run_end, tiles,
                                                               stages, full, empty, red, stage, pp,
                                                               rp, kw, KW, lane);
-      } else if constexpr (RMAX >= 2) {
-        if (R == 2) {
-          stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, it0, run_end, tiles,
-                                                                stages, full, empty, red, stage,
-                                                                pp, rp, kw, KW, lane);
-        } else if constexpr (RMAX >= 4) {
-          stream_consume_run<WF, GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, it0, run_end, tiles,
-                                                                stages, full, empty, red, stage,
-                                                                pp, rp, kw, KW, lane);
+      } else {
+        if (R == 1) {
+          stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, it0, run_end, tiles,
+                                                           stages, full, empty, red, stage, pp,
+                                                           kw, KW, lane);
+        } else if constexpr (RMAX >= 2) {
+          if (R == 2) {
+            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, it0, run_end, tiles,
+                                                             stages, full, empty, red, stage, pp,
+                                                             kw, KW, lane);
+          } else if constexpr (RMAX >= 4) {
+            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, it0, run_end, tiles,
+                                                             stages, full, empty, red, stage, pp,
+                                                             kw, KW, lane);
+          }
         }
       }
       done += R;
@@ -597,13 +692,19 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
   }
 }
 
-// Compile-time description of one streaming step.
-template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_>
+// Compile-time description of one streaming step.  MMA steps (MXFP4, routed)
+// use tiles of TM x 16 mma rows (RW = 16 TM rows, or 8 TM pairs for gate/up)
+// and at most NBMAX K blocks per consumer warp.
+template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_,
+          bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1>
 struct StreamCfg {
   static constexpr int WF = WF_;
-  static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_;
-  static constexpr int SP = SP_, RW = RW_, RMAX = RMAX_;
+  static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_, MMA = MMA_;
+  static constexpr int SP = SP_, RW = RW_, RMAX = RMAX_, TM = TM_, NBMAX = NBMAX_;
   static_assert(RW % SP == 0, "an item is a whole number of stages");
+  static_assert(!MMA || (WF == kWfMx && ROUTED && RW == (GLU ? 8 : 16) * TM && RMAX <= 8),
+                "tensor-core steps: routed MXFP4, one tile per item, at most 8 columns");
+  static_assert(MMA || WF == kWfBf16, "MXFP4 steps run on the tensor cores");
 };
 
 template <class C>
@@ -612,8 +713,8 @@ __device__ __forceinline__ void cfg_produce(const StreamArgs& a, uint8_t* stages
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
   stream_range(n, lo, hi);
-  stream_produce_range<C::WF, C::GLU, C::ROUTED, C::SP, C::RW, C::RMAX>(a, lo, hi, tiles, stages,
-                                                                       full, empty, stage);
+  stream_produce_range<C::WF, C::GLU, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM>(
+      a, lo, hi, tiles, stages, full, empty, stage);
 }
 
 template <class C>
@@ -623,8 +724,9 @@ __device__ __forceinline__ void cfg_consume(const StreamArgs& a, uint8_t* stages
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
   stream_range(n, lo, hi);
-  stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX>(
-      a, lo, hi, tiles, stages, full, empty, red, stage, pp, rp, kw, KW, lane);
+  stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM,
+                       C::NBMAX>(a, lo, hi, tiles, stages, full, empty, red, stage, pp, rp, kw,
+                                 KW, lane);
 }
 
 // Shared-memory carve-up common to both kernels.
@@ -636,7 +738,7 @@ struct StreamSmem {
 };
 
 __device__ __forceinline__ StreamSmem stream_smem_init(uint8_t* smem, int NS, int stage_bytes,
-                                                       int KW) {
+                                                       int red_pp, int KW) {
   StreamSmem m;
   m.stages = smem;
   m.full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
@@ -649,14 +751,15 @@ __device__ __forceinline__ StreamSmem stream_smem_init(uint8_t* smem, int NS, in
     }
     fence_barrier_init();
   }
-  if (threadIdx.x < 8) reinterpret_cast<unsigned*>(m.red + (size_t)2 * 64 * KW)[threadIdx.x] = 0u;
+  if (threadIdx.x < 16) reinterpret_cast<unsigned*>(m.red + (size_t)2 * red_pp)[threadIdx.x] = 0u;
   __syncthreads();
   return m;
 }
 
 // Single step.  Warp 0 produces, warps 1..KW consume (KW = blockDim.x/32 - 1).
-// Dynamic shared memory: NS stages, NS full + NS empty mbarriers, 2 x 64 x KW
-// floats of cross-slab partials, 8 words of per-run activation maxima.
+// Dynamic shared memory: NS stages, NS full + NS empty mbarriers, two buffers
+// of red_pp floats of cross-slab partials, 16 words of per-run activation
+// maxima.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX>
 __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a) {
   using C = StreamCfg<WF, GLU, ACTH, ROUTED, SP, RW, RMAX>;
@@ -664,7 +767,7 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
   trace_begin(a.trace, a.trace_id);
-  const StreamSmem m = stream_smem_init(smem, a.NS, a.stage_bytes, KW);
+  const StreamSmem m = stream_smem_init(smem, a.NS, a.stage_bytes, a.red_pp, KW);
   pdl_launch_dependents();
   uint32_t stage = 0;
   if (warp == 0) {
@@ -688,13 +791,13 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
 // A's consumers wait first only when A_WAITS (A's activations come from the
 // predecessor).  The stage buffers are sized for the larger segment.
 template <class A, class B, bool A_WAITS>
-__global__ void __launch_bounds__(288, 1) stream_dual_kernel(const StreamArgs a0,
-                                                             const StreamArgs a1) {
+__global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
+    stream_dual_kernel(const StreamArgs a0, const StreamArgs a1) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
   trace_begin(a0.trace, a0.trace_id);
-  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, KW);
+  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
   pdl_launch_dependents();
   uint32_t stage = 0;
   if (warp == 0) {

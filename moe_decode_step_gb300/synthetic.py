@@ -24,8 +24,10 @@ def _normal(seed, tensor, sub, shape, mean, std, device, scratch=None):
     return out
 
 
-def make_weights(cfg, layer=0, device="cuda"):
-    """Device tensors of one seeded layer (dict in MoELayer's naming)."""
+def make_weights(cfg, layer=0, device="cuda", layout=1):
+    """Device tensors of one seeded layer (dict in MoELayer's naming).  layout 1
+    packs the experts straight into the kernels' tiled layouts (FC1 gate/up
+    pairs: layout 2, FC2: layout 1); layout 0 keeps them canonical."""
     c = cfg
     s = c.seeds[layer]
     dev = torch.device(device)
@@ -44,10 +46,11 @@ def make_weights(cfg, layer=0, device="cuda"):
     scratch = torch.empty(2 * f * d, dtype=torch.float32, device=dev)
     for e in range(E):
         gu = _normal(s, T_EXPERT_GU, e, (2 * f, d), 0.0, c.std_gu(), dev, scratch)
-        mxfp4_pack_device(gu, w["w_gu_q"][e], w["w_gu_s"][e])
+        mxfp4_pack_device(gu, w["w_gu_q"][e], w["w_gu_s"][e], layout=2 if layout else 0)
         dn = _normal(s, T_EXPERT_D, e, (d, f), 0.0, c.std_down(), dev, scratch)
-        mxfp4_pack_device(dn, w["w_d_q"][e], w["w_d_s"][e])
+        mxfp4_pack_device(dn, w["w_d_q"][e], w["w_d_s"][e], layout=1 if layout else 0)
     del scratch
+    w["mxfp4_layout"] = 1 if layout else 0
     return w
 
 

@@ -49,7 +49,7 @@ def test_device_packer_matches_oracle_bytes(which):
 def test_decode_of_all_256_bytes_matches_oracle_tables():
     """Every byte value through the kernels' cvt-based decode, at several scales."""
     cfg = CONFIGS["tiny_b1"]
-    w = synthetic.make_weights(cfg)
+    w = synthetic.make_weights(cfg, layout=0)   # canonical bytes, retiled by the layer
     rng = np.random.default_rng(0)
     q = w["w_gu_q"][0]
     s = w["w_gu_s"][0]
@@ -78,3 +78,34 @@ def test_layer_dequant_matches_oracle_packing_of_the_same_draws():
         assert np.array_equal(got0, oracle.mxfp4_dequant(q_gu, s_gu))
         assert np.array_equal(got1, oracle.mxfp4_dequant(q_d, s_d))
     layer.close()
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_device_tiled_pack_and_retile_match_host_tiled_pack(layout):
+    w = np.random.default_rng(layout).standard_normal((64, 512)).astype(np.float32)
+    qh, sh = M.mxfp4_pack(torch.from_numpy(w), layout=layout)
+    qd, sd = M.mxfp4_pack_device(torch.from_numpy(w).cuda(), layout=layout)
+    assert torch.equal(qd.cpu(), qh) and torch.equal(sd.cpu(), sh)
+    qc, sc = M.mxfp4_pack_device(torch.from_numpy(np.stack([w, -w])).cuda().view(128, 512))
+    qr, sr = M.mxfp4_retile_device(qc.view(2, 64, 256), sc.view(2, 64, 16), layout)
+    qh2, sh2 = M.mxfp4_pack(torch.from_numpy(-w), layout=layout)
+    assert torch.equal(qr[0].cpu(), qh) and torch.equal(sr[0].cpu(), sh)
+    assert torch.equal(qr[1].cpu(), qh2) and torch.equal(sr[1].cpu(), sh2)
+
+
+def test_layer_from_canonical_weights_equals_layer_from_tiled_weights():
+    """moe_layer_create with canonical expert bytes (retiled into the handle's
+    own copy) and with pre-tiled bytes give bit-identical outputs."""
+    cfg = CONFIGS["tiny_b1"]
+    x, r = synthetic.make_activations(cfg, B=5)
+    outs = []
+    for layout in (0, 1):
+        w = synthetic.make_weights(cfg, layout=layout)
+        layer = synthetic.make_layer(cfg, max_batch=5, weights=w)
+        res = r.clone()
+        out = torch.empty_like(x)
+        layer.forward(x, res, out)
+        torch.cuda.synchronize()
+        outs.append((out.cpu(), res.cpu()))
+        layer.close()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

@@ -87,11 +87,12 @@ def test_create_rejects_bad_dims_and_null_weights_before_touching_the_gpu():
     good = dict(d=1024, f=256, n_experts=64, top_k=4, f_shared=256, max_batch=1,
                 routed_scale=2.5, rms_eps=1e-6, mxfp4_layout=0)
     for bad in (dict(d=1000), dict(f=100), dict(f=384), dict(top_k=0), dict(top_k=65), dict(n_experts=2),
-                dict(max_batch=65), dict(max_batch=0), dict(f_shared=0), dict(d=16384)):
+                dict(max_batch=65), dict(max_batch=0), dict(f_shared=0), dict(d=16384),
+                dict(d=7936)):
         dims = M.MoEDims(**{**good, **bad})
         assert L.moe_layer_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(h)) == \
             M.MOE_ERR_INVALID_ARG, bad
-    dims = M.MoEDims(**{**good, "mxfp4_layout": 1})
+    dims = M.MoEDims(**{**good, "mxfp4_layout": 2})
     assert L.moe_layer_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(h)) == \
         M.MOE_ERR_UNSUPPORTED
     dims = M.MoEDims(**good)
