@@ -152,15 +152,15 @@ int validate_dims(const moe_dims_t& d) {
 // carries (the routed segment takes up to 8 per pass at any batch).
 // Routed FC1: items of one tile (8 gate/up row pairs), at most 16 K blocks
 // per warp (d <= 7680 with 15 consumer warps).  Routed FC2: items of two
-// tiles (32 rows), at most 12 K blocks per warp (f <= 4096).
+// tiles (32 rows), 4 K blocks per warp (f <= 1920) or at most 12 (f <= 4096).
 using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 4>;
 template <int R> using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R>;
 using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 8, true, 1, 16>;
 template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R>;
-using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 32, 32, 8, true, 2, 12>;
+template <int NBM> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 32, 32, 8, true, 2, NBM>;
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
-#define MOE_FC2_KERNEL(RS) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg, true>
+#define MOE_FC2_KERNEL(RS, NBM) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM>, true>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -237,6 +237,18 @@ int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget,
   return MOE_OK;
 }
 
+// FC2 comes in two instantiations by K blocks per warp (4 or 12).
+bool fc2_small(const moe_dims_t& d) { return mx_warp_blocks(d.f, kMmaWarps) <= 4; }
+
+template <int RS>
+int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
+  if (fc2_small(d))
+    return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<4>>(MOE_FC2_KERNEL(RS, 4), d.f_shared, d.d, d.f, d.d, n,
+                                              kBudget1, p);
+  return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<12>>(MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n,
+                                             kBudget1, p);
+}
+
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
@@ -252,12 +264,9 @@ int plan_all(moe_layer* L) {
                                            kBudget1, &L->plan[kStepFc1][1])));
   MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg>(MOE_FC1_KERNEL(4), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][2])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<1>, Fc2Cfg>(MOE_FC2_KERNEL(1), d.f_shared, d.d, d.f, d.d, n,
-                                           kBudget1, &L->plan[kStepFc2][0])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<2>, Fc2Cfg>(MOE_FC2_KERNEL(2), d.f_shared, d.d, d.f, d.d, n,
-                                           kBudget1, &L->plan[kStepFc2][1])));
-  MOE_PLAN((plan_kernel<Sh2Cfg<4>, Fc2Cfg>(MOE_FC2_KERNEL(4), d.f_shared, d.d, d.f, d.d, n,
-                                           kBudget1, &L->plan[kStepFc2][2])));
+  MOE_PLAN((plan_fc2<1>(L, d, n, &L->plan[kStepFc2][0])));
+  MOE_PLAN((plan_fc2<2>(L, d, n, &L->plan[kStepFc2][1])));
+  MOE_PLAN((plan_fc2<4>(L, d, n, &L->plan[kStepFc2][2])));
 #undef MOE_PLAN
   return MOE_OK;
 }
@@ -410,10 +419,18 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   ra.h_amax = L->ws.h_amax;
   ra.out = L->ws.y_pair;
   sa.trace_id = ra.trace_id = 3;
+  const StreamPlan& p = L->plan[kStepFc2][batch_class(B)];
+  if (fc2_small(d)) {
+    switch (batch_class(B)) {
+      case 0: return launch_dual(MOE_FC2_KERNEL(1, 4), p, sa, ra, st);
+      case 1: return launch_dual(MOE_FC2_KERNEL(2, 4), p, sa, ra, st);
+      default: return launch_dual(MOE_FC2_KERNEL(4, 4), p, sa, ra, st);
+    }
+  }
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC2_KERNEL(1), L->plan[kStepFc2][0], sa, ra, st);
-    case 1: return launch_dual(MOE_FC2_KERNEL(2), L->plan[kStepFc2][1], sa, ra, st);
-    default: return launch_dual(MOE_FC2_KERNEL(4), L->plan[kStepFc2][2], sa, ra, st);
+    case 0: return launch_dual(MOE_FC2_KERNEL(1, 12), p, sa, ra, st);
+    case 1: return launch_dual(MOE_FC2_KERNEL(2, 12), p, sa, ra, st);
+    default: return launch_dual(MOE_FC2_KERNEL(4, 12), p, sa, ra, st);
   }
 }
 

@@ -481,6 +481,25 @@ __device__ __forceinline__ float e8m0_byte1(uint32_t w) { return __uint_as_float
 __device__ __forceinline__ float e8m0_byte2(uint32_t w) { return __uint_as_float((w << 7) & 0x7F800000u); }
 __device__ __forceinline__ float e8m0_byte3(uint32_t w) { return __uint_as_float((w >> 1) & 0x7F800000u); }
 
+// NQ groups of 4 K blocks of one tile (GUARD: only the first nb blocks):
+// per group 8 scale bytes and two 16-byte nibble loads per lane.
+template <bool ONE, int NQ, bool GUARD>
+__device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* scl,
+                                             const uint32_t (&X)[4 * NQ][4], int nb, float& c0,
+                                             float& c1, float& c2, float& c3) {
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (GUARD && 4 * q >= nb) break;
+    const uint2 sv = *reinterpret_cast<const uint2*>(scl + q * 64);
+    const uint4 w0 = *reinterpret_cast<const uint4*>(nib + (2 * q) * 512);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(nib + (2 * q + 1) * 512);
+    mx_block_mma<ONE>(w0.x, w0.y, e8m0_byte0(sv.x), e8m0_byte1(sv.x), X[4 * q], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w0.z, w0.w, e8m0_byte2(sv.x), e8m0_byte3(sv.x), X[4 * q + 1], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w1.x, w1.y, e8m0_byte0(sv.y), e8m0_byte1(sv.y), X[4 * q + 2], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w1.z, w1.w, e8m0_byte2(sv.y), e8m0_byte3(sv.y), X[4 * q + 3], c0, c1, c2, c3);
+  }
+}
+
 // Consumers of an MXFP4 step (tensor cores): one pass of R <= 8 activation
 // rows, the mma columns, over the run [it0, run_end) of items of one expert.
 //
@@ -584,21 +603,10 @@ __device__ __forceinline__ void stream_consume_run_mma(
       const uint8_t* nib = sp + mb * nib_tile + (size_t)(lb0 >> 1) * 512 + lane * 16;
       const uint8_t* scl = sp + scl_base + (size_t)mb * CB * 16 + (size_t)(lb0 >> 2) * 64 + g * 8;
       float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-      for (int q = 0; q < NBMAX / 4; ++q) {
-        if (4 * q < nb) {
-          const uint2 sv = *reinterpret_cast<const uint2*>(scl + q * 64);
-          const uint4 w0 = *reinterpret_cast<const uint4*>(nib + (2 * q) * 512);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(nib + (2 * q + 1) * 512);
-          mx_block_mma<ONE>(w0.x, w0.y, e8m0_byte0(sv.x), e8m0_byte1(sv.x), X[4 * q], c0, c1, c2, c3);
-          mx_block_mma<ONE>(w0.z, w0.w, e8m0_byte2(sv.x), e8m0_byte3(sv.x), X[4 * q + 1], c0, c1, c2,
-                            c3);
-          mx_block_mma<ONE>(w1.x, w1.y, e8m0_byte0(sv.y), e8m0_byte1(sv.y), X[4 * q + 2], c0, c1, c2,
-                            c3);
-          mx_block_mma<ONE>(w1.z, w1.w, e8m0_byte2(sv.y), e8m0_byte3(sv.y), X[4 * q + 3], c0, c1, c2,
-                            c3);
-        }
-      }
+      if (nb == NBMAX)   // the common case: one straight run the compiler can schedule
+        mx_group_run<ONE, NBMAX / 4, false>(nib, scl, X, nb, c0, c1, c2, c3);
+      else
+        mx_group_run<ONE, NBMAX / 4, true>(nib, scl, X, nb, c0, c1, c2, c3);
       acc[mb][0] = c0;
       acc[mb][1] = c1;
       acc[mb][2] = c2;
