@@ -154,9 +154,11 @@ int validate_dims(const moe_dims_t& d) {
 // per warp (d <= 7680 with 15 consumer warps).  Routed FC2: items of two
 // tiles (32 rows), 4 K blocks per warp (f <= 1920) or at most 12 (f <= 4096).
 using RouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 4>;
-template <int R> using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R>;
+template <int R>
+using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R, false, 1, 1, 8, 2>;
 using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 8, true, 1, 16>;
-template <int R> using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R>;
+template <int R>
+using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R, false, 1, 1, 4, 1>;
 template <int NBM> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 32, 32, 8, true, 2, NBM>;
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
@@ -173,7 +175,10 @@ constexpr int kBudget2 = 110 * 1024;   // two
 template <class C>
 int seg_warps(int K) {
   if constexpr (C::MMA) return kMmaWarps;
-  else return (K + StreamShape<C::ACTH>::WARP_K - 1) / StreamShape<C::ACTH>::WARP_K;
+  else {
+    using Sh = StreamShape<C::ACTH, C::CW, C::NQ>;
+    return (K + Sh::WARP_K - 1) / Sh::WARP_K;
+  }
 }
 
 // K chunks per item of a tensor-core segment: the fewest that keep a stage
@@ -361,12 +366,13 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
 }
 
 template <typename K>
-int launch_dual(K kern, const StreamPlan& p, StreamArgs a0, StreamArgs a1, cudaStream_t st) {
+int launch_dual(K kern, const StreamPlan& p, StreamArgs a0, StreamArgs a1, cudaStream_t st,
+                int grid) {
   a0.NS = a1.NS = p.NS;
   a0.stage_bytes = a1.stage_bytes = p.stage_bytes;
   a0.red_pp = a1.red_pp = p.red_pp;
   a0.kc = a1.kc = p.kc;
-  MOE_CUDA(launch_ex(kern, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, a0, a1));
+  MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, true, a0, a1));
   return MOE_OK;
 }
 
@@ -391,10 +397,14 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   ra.out = L->ws.h;
   ra.out_amax = L->ws.h_amax;
   sa.trace_id = ra.trace_id = 2;
+  // At B = 1 one SM holds the top-k CTA when FC1 launches; a CTA waiting for
+  // it would start (and finish) last, so FC1 leaves that SM out.
+  const StreamPlan& p = L->plan[kStepFc1][batch_class(B)];
+  const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC1_KERNEL(1), L->plan[kStepFc1][0], sa, ra, st);
-    case 1: return launch_dual(MOE_FC1_KERNEL(2), L->plan[kStepFc1][1], sa, ra, st);
-    default: return launch_dual(MOE_FC1_KERNEL(4), L->plan[kStepFc1][2], sa, ra, st);
+    case 0: return launch_dual(MOE_FC1_KERNEL(1), p, sa, ra, st, grid);
+    case 1: return launch_dual(MOE_FC1_KERNEL(2), p, sa, ra, st, grid);
+    default: return launch_dual(MOE_FC1_KERNEL(4), p, sa, ra, st, grid);
   }
 }
 
@@ -422,15 +432,15 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   const StreamPlan& p = L->plan[kStepFc2][batch_class(B)];
   if (fc2_small(d)) {
     switch (batch_class(B)) {
-      case 0: return launch_dual(MOE_FC2_KERNEL(1, 4), p, sa, ra, st);
-      case 1: return launch_dual(MOE_FC2_KERNEL(2, 4), p, sa, ra, st);
-      default: return launch_dual(MOE_FC2_KERNEL(4, 4), p, sa, ra, st);
+      case 0: return launch_dual(MOE_FC2_KERNEL(1, 4), p, sa, ra, st, p.grid);
+      case 1: return launch_dual(MOE_FC2_KERNEL(2, 4), p, sa, ra, st, p.grid);
+      default: return launch_dual(MOE_FC2_KERNEL(4, 4), p, sa, ra, st, p.grid);
     }
   }
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC2_KERNEL(1, 12), p, sa, ra, st);
-    case 1: return launch_dual(MOE_FC2_KERNEL(2, 12), p, sa, ra, st);
-    default: return launch_dual(MOE_FC2_KERNEL(4, 12), p, sa, ra, st);
+    case 0: return launch_dual(MOE_FC2_KERNEL(1, 12), p, sa, ra, st, p.grid);
+    case 1: return launch_dual(MOE_FC2_KERNEL(2, 12), p, sa, ra, st, p.grid);
+    default: return launch_dual(MOE_FC2_KERNEL(4, 12), p, sa, ra, st, p.grid);
   }
 }
 

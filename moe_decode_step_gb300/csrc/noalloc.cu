@@ -73,7 +73,7 @@ int device_setup(int dev, int d, DeviceSetup* out) {
     s.scratch = static_cast<unsigned char*>(p);
   }
   if (s.d != d) {
-    using Sh = StreamShape<false>;
+    using Sh = StreamShape<false, 8, 4>;
     const int KW = (d + Sh::WARP_K - 1) / Sh::WARP_K;
     const int stage = (int)((stream_rows_bytes(d, 1) + 127) / 128 * 128);
     const int red_pp = stream_red_pp(KW, 1);

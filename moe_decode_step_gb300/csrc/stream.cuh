@@ -69,11 +69,14 @@ struct StreamArgs {
   int trace_id;
 };
 
-// Elements per lane and activation registers per row of the bf16 steps.
-template <bool ACTH>
+// Lane layout of the bf16 steps: a lane owns NQ chunks of CW consecutive K
+// elements, chunk q at slab + q*32*CW + lane*CW, so a warp covers WARP_K =
+// 32*CW*NQ elements (narrow chunks spread a short K over more warps).
+template <bool ACTH, int CW, int NQ>
 struct StreamShape {
-  static constexpr int EPL = ACTH ? 16 : 32;                 // K elements per lane
-  static constexpr int AW = 16;                              // u32 registers per row
+  static_assert(CW == 4 || CW == 8, "chunks of 4 or 8 elements");
+  static constexpr int EPL = CW * NQ;                        // K elements per lane
+  static constexpr int AW = ACTH ? EPL : EPL / 2;            // u32 registers per row
   static constexpr int WARP_K = 32 * EPL;                    // K elements per consumer warp
 };
 
@@ -104,86 +107,110 @@ __host__ __device__ inline int stream_red_pp(int KW, int TM) {
 
 // ---- activation slices of the bf16 steps (registers) ----------------------
 
-// bf16 x-activation for bf16 weights: elements slab + q*256 + lane*8 + [0,8),
-// q < 4, kept as raw bf16 pairs.
+// bf16 x-activation for bf16 weights, kept as raw bf16 pairs.
+template <int CW, int NQ>
 __device__ __forceinline__ void act_load_bf_x(const uint16_t* row, int slab, int lane, int K,
-                                              uint32_t (&a)[16]) {
+                                              uint32_t (&a)[CW * NQ / 2]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = slab + q * 256 + lane * 8;
-    const uint4 v = e < K ? *reinterpret_cast<const uint4*>(row + e) : make_uint4(0, 0, 0, 0);
-    a[q * 4 + 0] = v.x;
-    a[q * 4 + 1] = v.y;
-    a[q * 4 + 2] = v.z;
-    a[q * 4 + 3] = v.w;
+  for (int q = 0; q < NQ; ++q) {
+    const int e = slab + q * 32 * CW + lane * CW;
+    if constexpr (CW == 8) {
+      const uint4 v = e < K ? *reinterpret_cast<const uint4*>(row + e) : make_uint4(0, 0, 0, 0);
+      a[q * 4 + 0] = v.x;
+      a[q * 4 + 1] = v.y;
+      a[q * 4 + 2] = v.z;
+      a[q * 4 + 3] = v.w;
+    } else {
+      const uint2 v = e < K ? *reinterpret_cast<const uint2*>(row + e) : make_uint2(0, 0);
+      a[q * 2 + 0] = v.x;
+      a[q * 2 + 1] = v.y;
+    }
   }
 }
 
-// fp32 h-activation for bf16 weights: elements slab + q*256 + lane*8 + [0,8),
-// q < 2, kept as fp32 bit patterns.
+// fp32 h-activation for bf16 weights, kept as fp32 bit patterns.
+template <int CW, int NQ>
 __device__ __forceinline__ void act_load_bf_h(const float* row, int slab, int lane, int K,
-                                              uint32_t (&a)[16]) {
+                                              uint32_t (&a)[CW * NQ]) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int e = slab + q * 256 + lane * 8;
+  for (int q = 0; q < NQ; ++q) {
+    const int e = slab + q * 32 * CW + lane * CW;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < CW / 4; ++c) {
       const float4 v = e < K ? __ldcg(reinterpret_cast<const float4*>(row + e) + c)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      a[q * 8 + c * 4 + 0] = __float_as_uint(v.x);
-      a[q * 8 + c * 4 + 1] = __float_as_uint(v.y);
-      a[q * 8 + c * 4 + 2] = __float_as_uint(v.z);
-      a[q * 8 + c * 4 + 3] = __float_as_uint(v.w);
+      a[q * CW + c * 4 + 0] = __float_as_uint(v.x);
+      a[q * CW + c * 4 + 1] = __float_as_uint(v.y);
+      a[q * CW + c * 4 + 2] = __float_as_uint(v.z);
+      a[q * CW + c * 4 + 3] = __float_as_uint(v.w);
     }
   }
 }
 
 // ---- one bf16 weight row (in shared memory) against R activation slices ----
 
-// bf16 row (as bytes), x activation: 4 chunks of 8 at slab + q*256 + lane*8.
-template <int R>
+// bf16 row (as bytes), x activation.
+template <int R, int CW, int NQ>
 __device__ __forceinline__ void row_dot_bf_x(const uint8_t* wrow, int slab, int lane, int K,
-                                             const uint32_t (&a)[R][16], float (&out)[R]) {
+                                             const uint32_t (&a)[R][CW * NQ / 2], float (&out)[R]) {
 #pragma unroll
   for (int r = 0; r < R; ++r) out[r] = 0.f;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = slab + q * 256 + lane * 8;
+  for (int q = 0; q < NQ; ++q) {
+    const int e = slab + q * 32 * CW + lane * CW;
     if (e < K) {
-      const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
+      uint32_t w[CW / 2];
+      if constexpr (CW == 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(wrow + (size_t)e * 2);
+        w[0] = v.x;
+        w[1] = v.y;
+      }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float acc = out[r];
-        acc = fma2_bf16(v.x, a[r][q * 4 + 0], acc);
-        acc = fma2_bf16(v.y, a[r][q * 4 + 1], acc);
-        acc = fma2_bf16(v.z, a[r][q * 4 + 2], acc);
-        acc = fma2_bf16(v.w, a[r][q * 4 + 3], acc);
+#pragma unroll
+        for (int j = 0; j < CW / 2; ++j) acc = fma2_bf16(w[j], a[r][q * (CW / 2) + j], acc);
         out[r] = acc;
       }
     }
   }
 }
 
-// bf16 row, fp32 activation: 2 chunks of 8 at slab + q*256 + lane*8; the bf16
-// weights widen exactly to fp32.
-template <int R>
+// bf16 row, fp32 activation: the bf16 weights widen exactly to fp32.
+template <int R, int CW, int NQ>
 __device__ __forceinline__ void row_dot_bf_h(const uint8_t* wrow, int slab, int lane, int K,
-                                             const uint32_t (&a)[R][16], float (&out)[R]) {
+                                             const uint32_t (&a)[R][CW * NQ], float (&out)[R]) {
 #pragma unroll
   for (int r = 0; r < R; ++r) out[r] = 0.f;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int e = slab + q * 256 + lane * 8;
+  for (int q = 0; q < NQ; ++q) {
+    const int e = slab + q * 32 * CW + lane * CW;
     if (e < K) {
-      const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
-      const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+      uint32_t w[CW / 2];
+      if constexpr (CW == 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(wrow + (size_t)e * 2);
+        w[0] = v.x;
+        w[1] = v.y;
+      }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float s0 = out[r], s1 = 0.f;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          s0 = fmaf(__uint_as_float(ww[t] << 16), __uint_as_float(a[r][q * 8 + 2 * t]), s0);
-          s1 = fmaf(__uint_as_float(ww[t] & 0xFFFF0000u), __uint_as_float(a[r][q * 8 + 2 * t + 1]),
+        for (int j = 0; j < CW / 2; ++j) {
+          s0 = fmaf(__uint_as_float(w[j] << 16), __uint_as_float(a[r][q * CW + 2 * j]), s0);
+          s1 = fmaf(__uint_as_float(w[j] & 0xFFFF0000u), __uint_as_float(a[r][q * CW + 2 * j + 1]),
                     s1);
         }
         out[r] = s0 + s1;
@@ -356,13 +383,13 @@ __device__ __forceinline__ int stream_x_row(const StreamArgs& a, int pid) {
 // Consumers of a bf16 step: one pass of R activation rows over the run
 // [it0, run_end) of items that share them.  Activation slices and pair ids are
 // loaded once; every item then streams its SPI stages, reduces and finalises.
-template <bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int R>
+template <bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int R, int CW, int NQ>
 __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const StreamItem& m,
                                                    int done, int it0, int run_end, int tiles,
                                                    uint8_t* stages, uint64_t* full,
                                                    uint64_t* empty, float* red, uint32_t& stage,
                                                    int& pp, int kw, int KW, int lane) {
-  using Sh = StreamShape<ACTH>;
+  using Sh = StreamShape<ACTH, CW, NQ>;
   constexpr int G = GLU ? 2 : 1;
   constexpr int SPI = RW / SP;
   constexpr int V = RW * G * R;
@@ -379,9 +406,10 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
   for (int r = 0; r < R; ++r) {
     pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
     if constexpr (!ACTH)
-      act_load_bf_x(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K, act[r]);
+      act_load_bf_x<CW, NQ>(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K,
+                            act[r]);
     else
-      act_load_bf_h(a.h + (size_t)pid[r] * a.K, slab, lane, a.K, act[r]);
+      act_load_bf_h<CW, NQ>(a.h + (size_t)pid[r] * a.K, slab, lane, a.K, act[r]);
   }
 
   for (int it = it0; it < run_end; ++it) {
@@ -399,8 +427,8 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
         for (int gu = 0; gu < G; ++gu) {
           float o[R];
           const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
-          if constexpr (ACTH) row_dot_bf_h<R>(wrow, slab, lane, a.K, act, o);
-          else row_dot_bf_x<R>(wrow, slab, lane, a.K, act, o);
+          if constexpr (ACTH) row_dot_bf_h<R, CW, NQ>(wrow, slab, lane, a.K, act, o);
+          else row_dot_bf_x<R, CW, NQ>(wrow, slab, lane, a.K, act, o);
 #pragma unroll
           for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
         }
@@ -658,7 +686,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
 
 // Consumers: items [lo, hi) of one step, run by run, pass by pass.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX, bool MMA, int TM,
-          int NBMAX>
+          int NBMAX, int CW, int NQ>
 __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
@@ -679,16 +707,16 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
                                                               rp, kw, KW, lane);
       } else {
         if (R == 1) {
-          stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 1>(a, m, done, it0, run_end, tiles,
+          stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 1, CW, NQ>(a, m, done, it0, run_end, tiles,
                                                            stages, full, empty, red, stage, pp,
                                                            kw, KW, lane);
         } else if constexpr (RMAX >= 2) {
           if (R == 2) {
-            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 2>(a, m, done, it0, run_end, tiles,
+            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 2, CW, NQ>(a, m, done, it0, run_end, tiles,
                                                              stages, full, empty, red, stage, pp,
                                                              kw, KW, lane);
           } else if constexpr (RMAX >= 4) {
-            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 4>(a, m, done, it0, run_end, tiles,
+            stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 4, CW, NQ>(a, m, done, it0, run_end, tiles,
                                                              stages, full, empty, red, stage, pp,
                                                              kw, KW, lane);
           }
@@ -704,11 +732,12 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
 // use tiles of TM x 16 mma rows (RW = 16 TM rows, or 8 TM pairs for gate/up)
 // and at most NBMAX K blocks per consumer warp.
 template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_,
-          bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1>
+          bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1, int CW_ = 8, int NQ_ = 4>
 struct StreamCfg {
   static constexpr int WF = WF_;
   static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_, MMA = MMA_;
   static constexpr int SP = SP_, RW = RW_, RMAX = RMAX_, TM = TM_, NBMAX = NBMAX_;
+  static constexpr int CW = CW_, NQ = NQ_;   // bf16 steps: lane chunking (see StreamShape)
   static_assert(RW % SP == 0, "an item is a whole number of stages");
   static_assert(!MMA || (WF == kWfMx && ROUTED && RW == (GLU ? 8 : 16) * TM && RMAX <= 8),
                 "tensor-core steps: routed MXFP4, one tile per item, at most 8 columns");
@@ -733,8 +762,8 @@ __device__ __forceinline__ void cfg_consume(const StreamArgs& a, uint8_t* stages
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
   stream_range(n, lo, hi);
   stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM,
-                       C::NBMAX>(a, lo, hi, tiles, stages, full, empty, red, stage, pp, rp, kw,
-                                 KW, lane);
+                       C::NBMAX, C::CW, C::NQ>(a, lo, hi, tiles, stages, full, empty, red, stage,
+                                               pp, rp, kw, KW, lane);
 }
 
 // Shared-memory carve-up common to both kernels.

@@ -5,13 +5,16 @@
 // order-preserving unsigned image of the fp32 (score + bias) in the high word
 // and the complemented expert id in the low word, so keys are distinct and a
 // larger key means a better expert, ties going to the lower id.  Every warp
-// sorts its 32 keys (bitonic network over shuffles); the largest of the warps'
-// k-th keys is a lower bound on the block's k-th key, so only keys at or above
-// it (at most k per warp, usually about k in all) are ranked exactly.  Selection compares fp32 (score + bias); the
-// combine weights use the unbiased scores, normalised to routed_scale.
-// The last CTA to finish (atomic ticket, no waiting) groups the (row, slot)
-// pairs by expert.  ("Kimi K3 on GB300: 13 kernels a layer...", section "What
-// one decode step of Kimi K3 does": 16 of 896 experts per token.)
+// sorts its 32 keys (bitonic network over shuffles); then the sorted lists
+// meet in a tournament: in each round a warp merges two lists (the elementwise
+// maximum of one list and the other reversed is a bitonic sequence holding the
+// 32 largest keys of both, which five shuffle stages sort), halving the
+// number of lists until one holds the row's 32 best keys in order.  Selection
+// compares fp32 (score + bias); the combine weights use the unbiased scores,
+// normalised to routed_scale.  The last CTA to finish (atomic ticket, no
+// waiting) groups the (row, slot) pairs by expert.  ("Kimi K3 on GB300: 13
+// kernels a layer...", section "What one decode step of Kimi K3 does": 16 of
+// 896 experts per token.)
 #pragma once
 
 #include "common.cuh"
@@ -72,12 +75,26 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
+// Descending bitonic sort of a bitonic sequence of 32 keys held one per lane.
+__device__ __forceinline__ uint64_t warp_bitonic_merge_desc(uint64_t key, int lane) {
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, key, stride);
+    const bool lower = (lane & stride) == 0;
+    key = lower ? (o > key ? o : key) : (o < key ? o : key);
+  }
+  return key;
+}
+
 static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   __shared__ int s_warp[33];
   __shared__ float s_score[32];
+  __shared__ float s_sc[kTopkThreads];             // sigmoid score of expert t
   __shared__ int32_t s_idx[64 * 32];
   __shared__ unsigned s_last;
+  // tournament lists (ping-pong), later reused as the expert masks
+  __shared__ __align__(16) uint64_t s_list[2][32][32];
   trace_begin(a.trace, 1);
   // the bias is a static weight: it may be read before the predecessor finishes
   const bool valid = t < a.E;
@@ -86,64 +103,51 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   pdl_wait_prerequisites();
 
   // ---- scores and keys ----
-  float score = 0.f;
-  uint32_t u = 0;
+  uint64_t key = 0ull;
   if (valid) {
     const float l = __ldcg(a.logits + (size_t)b * a.E + t);
-    score = 1.0f / (1.0f + expf(-l));
-    u = float_order_bits(score + bias);
+    const float score = 1.0f / (1.0f + expf(-l));
+    s_sc[t] = score;
+    key = ((uint64_t)float_order_bits(score + bias) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
   }
   // ---- per-warp bitonic sort, descending ----
-  uint64_t key = valid ? (((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t)) : 0ull;
-  float sc = score;
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
-      const float os = __shfl_xor_sync(0xffffffffu, sc, stride);
       const bool desc = (lane & size) == 0 || size == 32;
       const bool lower = (lane & stride) == 0;
       const bool take = (lower == desc) ? (ok > key) : (ok < key);
-      if (take) { key = ok; sc = os; }
+      if (take) key = ok;
     }
   }
-  // ---- lower bound on the block's k-th key, then exact ranks above it ----
-  const uint64_t kth = __shfl_sync(0xffffffffu, key, a.k - 1);
-  __shared__ uint64_t s_kth[32];
-  __shared__ uint64_t s_cand[32 * 32];
-  __shared__ float s_cand_score[32 * 32];
-  if (lane == 0) s_kth[warp] = kth;
+  // ---- tournament of the sorted warp lists ----
+  int n = (a.E + 31) >> 5;   // lists holding valid keys
+  if (warp < n) s_list[0][warp][lane] = key;
   __syncthreads();
-  uint64_t lb = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) lb = s_kth[w] > lb ? s_kth[w] : lb;
-  const bool cand = key >= lb && key != 0ull;
-  const unsigned bal = __ballot_sync(0xffffffffu, cand);   // a prefix of the sorted lanes
-  if (lane == 0) s_warp[warp] = __popc(bal);
-  __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) base += s_warp[w];
-    total += s_warp[w];
-  }
-  if (cand) {
-    s_cand[base + lane] = key;
-    s_cand_score[base + lane] = sc;
-  }
-  __syncthreads();
-  if (t < total) {
-    const uint64_t mine = s_cand[t];
-    int rank = 0;
-    for (int i = 0; i < total; ++i) rank += s_cand[i] > mine;
-    if (rank < a.k) {
-      const int e = (int)(0xFFFFFFFFu - (uint32_t)mine);
-      a.topk_idx[b * a.k + rank] = e;
-      s_idx[b * a.k + rank] = e;
-      s_score[rank] = s_cand_score[t];
+  int src = 0;
+  while (n > 1) {
+    const int half = n >> 1;
+    if (warp < half) {
+      const uint64_t x = s_list[src][2 * warp][lane];
+      const uint64_t y = s_list[src][2 * warp + 1][31 - lane];
+      s_list[src ^ 1][warp][lane] = warp_bitonic_merge_desc(x > y ? x : y, lane);
+    } else if (warp == half && (n & 1)) {
+      s_list[src ^ 1][warp][lane] = s_list[src][n - 1][lane];
     }
+    n = half + (n & 1);
+    src ^= 1;
+    __syncthreads();
   }
-  __syncthreads();
   if (warp == 0) {
+    if (lane < a.k) {
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)s_list[src][0][lane]);
+      a.topk_idx[b * a.k + lane] = e;
+      s_idx[b * a.k + lane] = e;
+      s_score[lane] = s_sc[e];
+    }
+    __syncwarp();
     float ssum = 0.f;
     for (int i = 0; i < a.k; ++i) ssum += s_score[i];   // picks summed in rank order
     if (lane < a.k) a.topk_w[b * a.k + lane] = a.routed_scale * s_score[lane] / ssum;
@@ -163,7 +167,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   } else {
     __syncthreads();
   }
-  __shared__ unsigned long long s_mask[1024];
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(&s_list[0][0][0]);
   const int P = a.B * a.k;
   if (gridDim.x > 1)   // other rows were selected by other CTAs
     for (int p = t; p < P; p += blockDim.x) s_idx[p] = __ldcg(a.topk_idx + p);
