@@ -231,7 +231,7 @@ int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget,
   r.red_pp = stream_red_pp(KW, std::max(A::TM, B::TM));
   const int red_bytes = 2 * r.red_pp * 4 + 64;
   r.NS = std::min(16, (budget - red_bytes) / (r.stage_bytes + 16));
-  if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
+  if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
   MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
   int occ = 0;

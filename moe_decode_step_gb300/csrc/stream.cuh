@@ -618,13 +618,17 @@ __device__ __forceinline__ void stream_consume_run_mma(
   }
   const float back = pow2f(eshift);
   const size_t nib_tile = (size_t)CB * 256, scl_base = (size_t)TM * CB * 256;
+  // ring position of this warp's chunk and of the item's first stage, advanced
+  // by kc per item without divisions (kc <= NS)
+  const uint32_t NS = (uint32_t)a.NS, KC = (uint32_t)a.kc;
+  uint32_t cbuf = (stage + (uint32_t)chunk) % NS, cph = ((stage + (uint32_t)chunk) / NS) & 1u;
+  uint32_t ibuf = stage % NS;
+  const int ej = ct / R;   // this thread's output row (pair) within an item, column ei
+  int row0 = stream_row0<true, TR>(it0, tiles);
 
-  for (int it = it0; it < run_end; ++it) {
-    const int row0 = stream_row0<true, TR>(it, tiles);
-    const uint32_t st = stage + (uint32_t)chunk;
-    const int buf = (int)(st % (uint32_t)a.NS);
-    if (nb > 0) mbar_wait(&full[buf], (st / (uint32_t)a.NS) & 1u, a.status);
-    const uint8_t* sp = stages + (size_t)buf * a.stage_bytes;
+  for (int it = it0; it < run_end; ++it, row0 += TR) {
+    if (nb > 0) mbar_wait(&full[cbuf], cph, a.status);
+    const uint8_t* sp = stages + (size_t)cbuf * a.stage_bytes;
     float acc[TM][4];
 #pragma unroll
     for (int mb = 0; mb < TM; ++mb) {
@@ -642,9 +646,20 @@ __device__ __forceinline__ void stream_consume_run_mma(
     }
     __syncwarp();
     if (lane == 0) {
-      for (int s = 0; s < a.kc; ++s) mbar_arrive(&empty[(stage + (uint32_t)s) % (uint32_t)a.NS]);
+      uint32_t b = ibuf;
+      for (uint32_t s = 0; s < KC; ++s) {
+        mbar_arrive(&empty[b]);
+        if (++b == NS) b = 0;
+      }
     }
-    stage += (uint32_t)a.kc;
+    stage += KC;
+    ibuf += KC;
+    if (ibuf >= NS) ibuf -= NS;
+    cbuf += KC;
+    if (cbuf >= NS) {
+      cbuf -= NS;
+      cph ^= 1u;
+    }
 
     // cross-slab combine: partial of (mma row, column) from warp kw at
     // ((mb*16 + row)*8 + column)*KW + kw
@@ -658,7 +673,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
       }
     consumer_sync(cthreads);
     if (ct < TR * R) {
-      const int j = ct / R;   // output row (pair) within the item; column ei
+      const int j = ej;
       const int row = row0 + j;
       if (row < a.N) {
         float* dst = a.out + (size_t)epid * a.N + row;
