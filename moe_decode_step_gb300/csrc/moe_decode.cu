@@ -159,10 +159,16 @@ using Sh1Cfg = StreamCfg<kWfBf16, true, false, false, 1, 4, R, false, 1, 1, 8, 2
 using Fc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 8, true, 1, 16>;
 template <int R>
 using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R, false, 1, 1, 4, 1>;
-template <int NBM> using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 32, 32, 8, true, 2, NBM>;
+template <int NBM, int TM, int RM>
+using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, TM, NBM>;
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
-#define MOE_FC2_KERNEL(RS, NBM) stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM>, true>
+// FC2 at batch class 0 (B = 1: one activation row per routed expert) takes
+// items of four tiles with one-column partials.
+#define MOE_FC2_TM(RS) ((RS) == 1 ? 4 : 2)
+#define MOE_FC2_RM(RS) ((RS) == 1 ? 1 : 8)
+#define MOE_FC2_KERNEL(RS, NBM) \
+  stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -228,7 +234,8 @@ int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget,
   r.kc = seg_kc<B>(KB, KW);
   const size_t sa = seg_stage_bytes<A>(KA, 1), sb = seg_stage_bytes<B>(KB, r.kc);
   r.stage_bytes = (int)((std::max(sa, sb) + 127) / 128 * 128);
-  r.red_pp = stream_red_pp(KW, std::max(A::TM, B::TM));
+  r.red_pp = std::max(stream_red_pp(KW, A::MMA, A::TM, A::RMAX),
+                      stream_red_pp(KW, B::MMA, B::TM, B::RMAX));
   const int red_bytes = 2 * r.red_pp * 4 + 64;
   r.NS = std::min(16, (budget - red_bytes) / (r.stage_bytes + 16));
   if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
@@ -248,10 +255,10 @@ bool fc2_small(const moe_dims_t& d) { return mx_warp_blocks(d.f, kMmaWarps) <= 4
 template <int RS>
 int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
   if (fc2_small(d))
-    return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<4>>(MOE_FC2_KERNEL(RS, 4), d.f_shared, d.d, d.f, d.d, n,
-                                              kBudget1, p);
-  return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<12>>(MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n,
-                                             kBudget1, p);
+    return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<4, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>>(
+        MOE_FC2_KERNEL(RS, 4), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
+  return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<12, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>>(
+      MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
 }
 
 int plan_all(moe_layer* L) {

@@ -76,7 +76,7 @@ int device_setup(int dev, int d, DeviceSetup* out) {
     using Sh = StreamShape<false, 8, 4>;
     const int KW = (d + Sh::WARP_K - 1) / Sh::WARP_K;
     const int stage = (int)((stream_rows_bytes(d, 1) + 127) / 128 * 128);
-    const int red_pp = stream_red_pp(KW, 1);
+    const int red_pp = stream_red_pp(KW, false, 1, 4);
     const int red = 2 * red_pp * 4 + 64;
     const int budget = 110 * 1024;
     const int NS = std::min(8, (budget - red) / (stage + 16));

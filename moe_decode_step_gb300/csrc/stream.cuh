@@ -100,9 +100,11 @@ __host__ __device__ inline int mx_warp_blocks(int K, int KW) {
   return ((nblk + KW - 1) / KW + 3) / 4 * 4;
 }
 
-// Cross-slab partial buffer size (floats, one of two) for KW consumer warps.
-__host__ __device__ inline int stream_red_pp(int KW, int TM) {
-  return (TM * 128 > 64 ? TM * 128 : 64) * KW;
+// Cross-slab partials: a bf16 step keeps up to 64 values per warp, a
+// tensor-core step one per (mma row, column) of an item.  Floats per buffer
+// (one of two) for KW consumer warps:
+__host__ __device__ inline int stream_red_pp(int KW, bool mma, int TM, int RMAX) {
+  return (mma ? TM * 16 * RMAX : 64) * KW;
 }
 
 // ---- activation slices of the bf16 steps (registers) ----------------------
@@ -528,7 +530,7 @@ __device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* 
   }
 }
 
-// Consumers of an MXFP4 step (tensor cores): one pass of R <= 8 activation
+// Consumers of an MXFP4 step (tensor cores): one pass of R <= RMAX activation
 // rows, the mma columns, over the run [it0, run_end) of items of one expert.
 //
 // An item is TM tiles of 16 mma rows (tiled layouts, see mxfp4.cuh): plain
@@ -538,7 +540,7 @@ __device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* 
 // b0 = kw * NB (NB a multiple of 4, all in one K chunk) and reads, per pair of
 // blocks, 16 bytes (lane-ordered, conflict-free) and per group of four, 8
 // scale bytes.
-template <bool GLU, bool ACTH, int TM, int NBMAX, bool ONE>
+template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE>
 __device__ __forceinline__ void stream_consume_run_mma(
     const StreamArgs& a, const StreamItem& m, int done, int R, int it0, int run_end, int tiles,
     uint8_t* stages, uint64_t* full, uint64_t* empty, float* red, uint32_t& stage, int& pp,
@@ -662,14 +664,14 @@ __device__ __forceinline__ void stream_consume_run_mma(
     }
 
     // cross-slab combine: partial of (mma row, column) from warp kw at
-    // ((mb*16 + row)*8 + column)*KW + kw
+    // ((mb*16 + row)*RMAX + column)*KW + kw
     float* rbuf = red + (size_t)pp * a.red_pp;
 #pragma unroll
     for (int mb = 0; mb < TM; ++mb)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int col = 2 * t + (i & 1), row = g + 8 * (i >> 1);
-        if (col < R) rbuf[((mb * 16 + row) * 8 + col) * KW + kw] = acc[mb][i];
+        if (col < R) rbuf[((mb * 16 + row) * RMAX + col) * KW + kw] = acc[mb][i];
       }
     consumer_sync(cthreads);
     if (ct < TR * R) {
@@ -678,8 +680,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
       if (row < a.N) {
         float* dst = a.out + (size_t)epid * a.N + row;
         if constexpr (GLU) {
-          const float* pg = rbuf + (((j >> 3) * 16 + (j & 7)) * 8 + ei) * KW;
-          const float* pu = pg + 64 * KW;
+          const float* pg = rbuf + (((j >> 3) * 16 + (j & 7)) * RMAX + ei) * KW;
+          const float* pu = pg + 8 * RMAX * KW;
           float gs = 0.f, us = 0.f;
           for (int w = 0; w < KW; ++w) { gs += pg[w]; us += pu[w]; }
           gs *= back;
@@ -688,7 +690,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
           *dst = hv;
           if (a.out_amax) atomicMax(a.out_amax + epid, __float_as_uint(fabsf(hv)));
         } else {
-          const float* pv = rbuf + (((j >> 4) * 16 + (j & 15)) * 8 + ei) * KW;
+          const float* pv = rbuf + (((j >> 4) * 16 + (j & 15)) * RMAX + ei) * KW;
           float sum = 0.f;
           for (int w = 0; w < KW; ++w) sum += pv[w];
           *dst = sum * back;
@@ -713,13 +715,13 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
       const int R = stream_pass_rows<RMAX, MMA>(m.pr - done);
       if constexpr (MMA) {
         if (R == 1)
-          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, true>(a, m, done, R, it0, run_end, tiles,
-                                                             stages, full, empty, red, stage, pp,
-                                                             rp, kw, KW, lane);
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true>(
+              a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
+              lane);
         else
-          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, false>(a, m, done, R, it0, run_end, tiles,
-                                                              stages, full, empty, red, stage, pp,
-                                                              rp, kw, KW, lane);
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, false>(
+              a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
+              lane);
       } else {
         if (R == 1) {
           stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 1, CW, NQ>(a, m, done, it0, run_end, tiles,
