@@ -203,6 +203,12 @@ int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, 
 int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
                       uint8_t* s, int layout);
 
+/* Host conversion between layouts (0, 1, 2) of one rows x k matrix: q_in, s_in
+ * host in layout `from`; q_out, s_out host in layout `to` (same sizes, must not
+ * overlap the input).  Errors: INVALID_ARG, UNSUPPORTED (a layout's rules). */
+int mxfp4_repack(const uint8_t* q_in, const uint8_t* s_in, int64_t rows, int64_t k, int from,
+                 int to, uint8_t* q_out, uint8_t* s_out);
+
 /* Canonical packed bytes -> tiled layout 1 or 2, asynchronous on stream, for
  * n_mat matrices stored back to back (rows x k each): q_in, s_in device
  * canonical; q_out, s_out device, the same sizes, must not overlap the input.

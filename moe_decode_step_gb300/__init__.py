@@ -14,7 +14,7 @@ from ._binding import (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR
                        status_string)
 
 __all__ = ["MoELayer", "MoEDims", "MoEWeights", "MoEError", "mxfp4_pack", "mxfp4_pack_device",
-           "mxfp4_retile_device",
+           "mxfp4_repack", "mxfp4_retile_device",
            "mxfp4_packed_bytes", "status_string", "lib", "MOE_OK", "MOE_ERR_INVALID_ARG",
            "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_ALLOC", "MOE_ERR_TIMEOUT"]
 
@@ -214,6 +214,21 @@ def mxfp4_pack_device(w, q=None, s=None, stream=None, layout=0):
     check(lib().mxfp4_pack_device(_stream(stream), _ptr(w), rows, k, _ptr(q), _ptr(s),
                                   int(layout)), "mxfp4_pack_device")
     return q, s
+
+
+def mxfp4_repack(q, s, src, dst):
+    """Host conversion of one matrix's packed bytes (CPU uint8 [rows, k/2] and
+    [rows, k/32]) from layout `src` to layout `dst` (0, 1 or 2)."""
+    if q.is_cuda or s.is_cuda or q.dtype != torch.uint8 or s.dtype != torch.uint8:
+        raise ValueError("mxfp4_repack wants CPU uint8 tensors")
+    q = q.contiguous()
+    s = s.contiguous()
+    rows, k = q.shape[0], q.shape[1] * 2
+    qo = torch.empty_like(q)
+    so = torch.empty_like(s)
+    check(lib().mxfp4_repack(_ptr(q), _ptr(s), rows, k, int(src), int(dst), _ptr(qo), _ptr(so)),
+          "mxfp4_repack")
+    return qo, so
 
 
 def mxfp4_retile_device(q, s, layout, stream=None):

@@ -66,6 +66,8 @@ _PROTOS = {
     "mxfp4_pack": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, ctypes.c_int]),
     "mxfp4_pack_device": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int64, _P, _P,
                                          ctypes.c_int]),
+    "mxfp4_repack": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_int, _P, _P]),
     "mxfp4_retile_device": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64, ctypes.c_int, _P, _P]),
     "moe_router_topk_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int,

@@ -801,6 +801,20 @@ int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uin
   return MOE_OK;
 }
 
+int mxfp4_repack(const uint8_t* q_in, const uint8_t* s_in, int64_t rows, int64_t k, int from,
+                 int to, uint8_t* q_out, uint8_t* s_out) {
+  if (!q_in || !s_in || !q_out || !s_out || rows < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (!mx_layout_ok(rows, k, from) || !mx_layout_ok(rows, k, to)) return MOE_ERR_UNSUPPORTED;
+  const int64_t nb = k / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      uint8_t qb[16];
+      const uint8_t sb = mx_load_block(q_in, s_in, r, b, rows, k, from, qb);
+      mx_store_block(q_out, s_out, r, b, rows, k, to, qb, sb);
+    }
+  return MOE_OK;
+}
+
 int mxfp4_retile_device(void* stream, const uint8_t* q_in, const uint8_t* s_in, int64_t n_mat,
                         int64_t rows, int64_t k, int layout, uint8_t* q_out, uint8_t* s_out) {
   if (!q_in || !s_in || !q_out || !s_out || n_mat < 0 || rows < 0 || k <= 0)

@@ -117,6 +117,21 @@ __host__ __device__ inline void mx_store_block(uint8_t* q, uint8_t* s, int64_t r
   s[mx_tiled_scale_offset(T, r, b, k)] = sb;
 }
 
+// The 16 nibble bytes and the scale byte of (row, block b) in a layout.
+__host__ __device__ inline uint8_t mx_load_block(const uint8_t* q, const uint8_t* s, int64_t row,
+                                                 int64_t b, int64_t rows, int64_t k, int layout,
+                                                 uint8_t (&qb)[16]) {
+  if (layout == kMxCanonical) {
+    memcpy(qb, q + row * (k / 2) + b * 16, 16);
+    return s[row * (k / 32) + b];
+  }
+  int64_t T;
+  int r;
+  mx_tile_of_row(row, rows, layout, T, r);
+  for (int u = 0; u < 4; ++u) memcpy(qb + 4 * u, q + mx_tiled_word_offset(T, r, b, u, k), 4);
+  return s[mx_tiled_scale_offset(T, r, b, k)];
+}
+
 // A layout's shape rules: k % 32 (canonical); tiled also k % 128 and whole tiles.
 __host__ __device__ inline bool mx_layout_ok(int64_t rows, int64_t k, int layout) {
   if (rows < 0 || k <= 0 || k % 32 != 0) return false;

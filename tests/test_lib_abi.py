@@ -31,7 +31,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ("moe_layer_create", "moe_layer_destroy", "moe_router_topk", "moe_decode_forward",
-                 "moe_decode_forward_host", "mxfp4_pack", "mxfp4_pack_device"):
+                 "moe_decode_forward_host", "mxfp4_pack", "mxfp4_pack_device", "mxfp4_repack",
+                 "mxfp4_retile_device"):
         assert want in names
 
 

@@ -52,3 +52,17 @@ def test_tiled_layout_shape_rules():
     assert M.mxfp4_packed_bytes(16, 128, 3)[0] == 0
     with pytest.raises(M.MoEError):
         M.mxfp4_pack(torch.zeros(24, 128), layout=1)
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_repack_round_trips_and_matches_the_tiled_packer(layout):
+    w = np.random.default_rng(40 + layout).standard_normal((32, 256)).astype(np.float32)
+    qc, sc = M.mxfp4_pack(torch.from_numpy(w), layout=0)
+    qt, st = M.mxfp4_pack(torch.from_numpy(w), layout=layout)
+    q1, s1 = M.mxfp4_repack(qc, sc, 0, layout)
+    assert torch.equal(q1, qt) and torch.equal(s1, st)
+    q2, s2 = M.mxfp4_repack(qt, st, layout, 0)
+    assert torch.equal(q2, qc) and torch.equal(s2, sc)
+    other = 3 - layout
+    q3, s3 = M.mxfp4_repack(*M.mxfp4_repack(qt, st, layout, other), other, layout)
+    assert torch.equal(q3, qt) and torch.equal(s3, st)
