@@ -39,11 +39,12 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="full_b1")
-    p.add_argument("--no-batches", action="store_true", help="skip the B=8 / B=64 extras")
+    p.add_argument("--no-batches", action="store_true",
+                   help="skip the B=8 / B=64 and four-layer chain extras")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                    help="run --warmup untimed forwards of a profiling workload (L2 flushed "
@@ -289,6 +290,60 @@ def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
     return times, phases
 
 
+def time_chain(layers, x0, res0, steps, warmup, flush):
+    """Device time of a chain of layers (each layer's out is the next one's x,
+    the residual threads through), captured as one CUDA graph; L2 is flushed
+    once before each chain so the side-stream prefetch of the next layer's
+    router and shared weights shows.  Returns per-chain microseconds."""
+    import torch
+    x = x0.clone()
+    res = res0.clone()
+    outs = [torch.empty_like(x0) for _ in layers]
+
+    def chain():
+        xi = x
+        for L, o in zip(layers, outs):
+            L.forward(xi, res, o)
+            xi = o
+
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        chain()
+    cur.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(warmup):
+        res.copy_(res0)
+        flush()
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        res.copy_(res0)
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1000.0)
+    del g
+    return times
+
+
+def percentile(v, q):
+    v = sorted(v)
+    if not v:
+        return None
+    i = min(len(v) - 1, max(0, int(round(q / 100.0 * (len(v) - 1)))))
+    return v[i]
+
+
 def time_e2e(layer, cfg, x, res0, steps, warmup, flush):
     """The same layer through the host-buffer entry point: H2D of x and the
     residual, forward, D2H of residual and out, stream sync, per step."""
@@ -413,6 +468,7 @@ def run_ours(args, rank, world, local):
     del layer
 
     batches = {}
+    chain = None
     if not args.no_batches and args.config == "full_b1":
         for name in ("full_b8", "full_b64"):
             c2 = CONFIGS[name]
@@ -434,10 +490,26 @@ def run_ours(args, rank, world, local):
             L2.close()
             del L2
             torch.cuda.empty_cache()
+        # four chained full-size layers at B = 1 with the next-layer L2 prefetch
+        cc = CONFIGS["chain4_b1"]
+        chain_layers = [synthetic.make_layer(cc, layer=l) for l in range(cc.n_layers)]
+        for l in range(cc.n_layers - 1):
+            chain_layers[l].set_prefetch_next(chain_layers[l + 1])
+        xc, rc = synthetic.make_activations(cc, layer=0)
+        stc = max(5, min(args.steps, 20))
+        tc = time_chain(chain_layers, xc, rc, stc, max(3, args.warmup), flush)
+        vc = reduce_max(statistics.median(tc), world, dev)
+        chain = {"layers": cc.n_layers, "B": cc.B, "us": vc, "us_per_layer": vc / cc.n_layers,
+                 "steps": stc, "l2": "flushed once before each chain",
+                 "prefetch": "next layer's router and shared-expert weights, side stream"}
+        for L in chain_layers:
+            L.close()
+        del chain_layers
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        ts, cores = cpu_oracle_sample(args.config, repeats=1)
+        ts, cores = cpu_oracle_sample(args.config, repeats=10)
         cpu = {"value": statistics.median(ts), "unit": "us", "cores": cores, "kind": "oracle",
                "sample": f"{args.config}: one full layer (router, {cfg.top_k} MXFP4 experts, "
                          "shared expert, tail) in fp64; weight draws and packing excluded"}
@@ -445,6 +517,7 @@ def run_ours(args, rank, world, local):
     agg_tbs = reduce_sum(btouch / us / 1e6, world, dev)
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "p10_us": percentile(times, 10), "p90_us": percentile(times, 90),
         "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": DATA,
         "config": {"workload": f"{args.config}: one MoE decode layer, B={cfg.B}, d={cfg.d}, "
@@ -472,6 +545,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "batches": batches,
+        "chain": chain,
         "wall_s": wall,
     }
     if rank == 0:
