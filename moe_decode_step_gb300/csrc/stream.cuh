@@ -540,11 +540,14 @@ __device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* 
 // b0 = kw * NB (NB a multiple of 4, all in one K chunk) and reads, per pair of
 // blocks, 16 bytes (lane-ordered, conflict-free) and per group of four, 8
 // scale bytes.
+// X holds the pass's activation operand; xkey/xshift remember which single x
+// row it holds (-1: none), so a run of another expert on the same row (every
+// run at B = 1) keeps it instead of reloading and re-reducing it.
 template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE>
 __device__ __forceinline__ void stream_consume_run_mma(
     const StreamArgs& a, const StreamItem& m, int done, int R, int it0, int run_end, int tiles,
     uint8_t* stages, uint64_t* full, uint64_t* empty, float* red, uint32_t& stage, int& pp,
-    int& rp, int kw, int KW, int lane) {
+    int& rp, int kw, int KW, int lane, uint32_t (&X)[NBMAX][4], int& xkey, int& xshift) {
   constexpr int TR = GLU ? TM * 8 : TM * 16;   // output rows (pairs) per item
   const int g = lane >> 2, t = lane & 3;
   const int nblk = a.K >> 5;
@@ -563,9 +566,12 @@ __device__ __forceinline__ void stream_consume_run_mma(
   const int cpid = __ldcg(a.pair_list + m.p0 + done + ci);
   const int epid = __ldcg(a.pair_list + m.p0 + done + ei);
 
-  uint32_t X[NBMAX][4];
   int eshift;
-  if constexpr (!ACTH) {
+  // one x row for the whole pass (R = 1): the same key in every lane and warp
+  const int key = (!ACTH && R == 1) ? cpid / a.k : -1;
+  if (!ACTH && key >= 0 && key == xkey) {
+    eshift = xshift;
+  } else if constexpr (!ACTH) {
     // x rows (bf16): the f16 scaling shift needs max |x| over the whole row,
     // which the KW warps hold together: reduce through shared memory.
     unsigned* s_amax = reinterpret_cast<unsigned*>(red + 2 * (size_t)a.red_pp);
@@ -599,6 +605,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
     // the other parity's slots are free: every consumer is past this barrier
     if (kw == 0 && lane < 8) s_amax[((rp & 1) ^ 1) * 8 + lane] = 0u;
     rp ^= 1;
+    xkey = key;
+    xshift = eshift;
   } else {
     // h rows (fp32): the shift comes from FC1's per-pair max |h|
     const int cshift = f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + cpid)));
@@ -708,6 +716,8 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
                                                      int& pp, int& rp, int kw, int KW, int lane) {
+  uint32_t X[MMA ? NBMAX : 1][4];
+  int xkey = -1, xshift = 0;
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
     const StreamItem m = stream_item<ROUTED, RW>(a, it0, tiles);
@@ -717,11 +727,11 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
         if (R == 1)
           stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
-              lane);
+              lane, X, xkey, xshift);
         else
           stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, false>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
-              lane);
+              lane, X, xkey, xshift);
       } else {
         if (R == 1) {
           stream_consume_run<GLU, ACTH, ROUTED, SP, RW, 1, CW, NQ>(a, m, done, it0, run_end, tiles,
