@@ -149,75 +149,58 @@ __device__ __forceinline__ void act_load_bf_h(const float* row, int slab, int la
   }
 }
 
-// ---- one bf16 weight row (in shared memory) against R activation slices ----
+// ---- one chunk of a bf16 weight row (in shared memory) against R activation
+// slices; the caller has checked that the chunk lies inside K ----
 
-// bf16 row (as bytes), x activation.
+// bf16 weights, x activation (bf16 pairs): acc[r] += w . x_r over CW elements.
 template <int R, int CW, int NQ>
-__device__ __forceinline__ void row_dot_bf_x(const uint8_t* wrow, int slab, int lane, int K,
-                                             const uint32_t (&a)[R][CW * NQ / 2], float (&out)[R]) {
+__device__ __forceinline__ void chunk_dot_bf_x(const uint8_t* wp, int q,
+                                               const uint32_t (&a)[R][CW * NQ / 2],
+                                               float (&acc)[R]) {
+  uint32_t w[CW / 2];
+  if constexpr (CW == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(wp);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(wp);
+    w[0] = v.x;
+    w[1] = v.y;
+  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = 0.f;
+  for (int r = 0; r < R; ++r) {
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    const int e = slab + q * 32 * CW + lane * CW;
-    if (e < K) {
-      uint32_t w[CW / 2];
-      if constexpr (CW == 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(wrow + (size_t)e * 2);
-        w[0] = v.x;
-        w[1] = v.y;
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float acc = out[r];
-#pragma unroll
-        for (int j = 0; j < CW / 2; ++j) acc = fma2_bf16(w[j], a[r][q * (CW / 2) + j], acc);
-        out[r] = acc;
-      }
-    }
+    for (int j = 0; j < CW / 2; ++j) acc[r] = fma2_bf16(w[j], a[r][q * (CW / 2) + j], acc[r]);
   }
 }
 
-// bf16 row, fp32 activation: the bf16 weights widen exactly to fp32.
+// bf16 weights, fp32 activation: the bf16 weights widen exactly to fp32.
 template <int R, int CW, int NQ>
-__device__ __forceinline__ void row_dot_bf_h(const uint8_t* wrow, int slab, int lane, int K,
-                                             const uint32_t (&a)[R][CW * NQ], float (&out)[R]) {
+__device__ __forceinline__ void chunk_dot_bf_h(const uint8_t* wp, int q,
+                                               const uint32_t (&a)[R][CW * NQ], float (&acc)[R]) {
+  uint32_t w[CW / 2];
+  if constexpr (CW == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(wp);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(wp);
+    w[0] = v.x;
+    w[1] = v.y;
+  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = 0.f;
+  for (int r = 0; r < R; ++r) {
+    float s0 = acc[r], s1 = 0.f;
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    const int e = slab + q * 32 * CW + lane * CW;
-    if (e < K) {
-      uint32_t w[CW / 2];
-      if constexpr (CW == 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(wrow + (size_t)e * 2);
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(wrow + (size_t)e * 2);
-        w[0] = v.x;
-        w[1] = v.y;
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float s0 = out[r], s1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < CW / 2; ++j) {
-          s0 = fmaf(__uint_as_float(w[j] << 16), __uint_as_float(a[r][q * CW + 2 * j]), s0);
-          s1 = fmaf(__uint_as_float(w[j] & 0xFFFF0000u), __uint_as_float(a[r][q * CW + 2 * j + 1]),
-                    s1);
-        }
-        out[r] = s0 + s1;
-      }
+    for (int j = 0; j < CW / 2; ++j) {
+      s0 = fmaf(__uint_as_float(w[j] << 16), __uint_as_float(a[r][q * CW + 2 * j]), s0);
+      s1 = fmaf(__uint_as_float(w[j] & 0xFFFF0000u), __uint_as_float(a[r][q * CW + 2 * j + 1]), s1);
     }
+    acc[r] = s0 + s1;
   }
 }
 
@@ -423,16 +406,30 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
       mbar_wait(&full[buf], (stage / (uint32_t)a.NS) & 1u, a.status);
       const uint8_t* sb = stages + (size_t)buf * a.stage_bytes;
 #pragma unroll
-      for (int rr = 0; rr < SP; ++rr) {
-        const int j = st * SP + rr;
+      for (int rr = 0; rr < SP; ++rr)
 #pragma unroll
-        for (int gu = 0; gu < G; ++gu) {
-          float o[R];
-          const uint8_t* wrow = sb + gu * half_bytes + (size_t)rr * a.K * 2;
-          if constexpr (ACTH) row_dot_bf_h<R, CW, NQ>(wrow, slab, lane, a.K, act, o);
-          else row_dot_bf_x<R, CW, NQ>(wrow, slab, lane, a.K, act, o);
+        for (int r = 0; r < R * G; ++r) v[(st * SP + rr) * R * G + r] = 0.f;
+      // one warp-uniform test per chunk (K is a multiple of 32 * CW), then
+      // all SP rows of the stage back to back
 #pragma unroll
-          for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
+      for (int q = 0; q < NQ; ++q) {
+        const int e = slab + q * 32 * CW + lane * CW;
+        if (e < a.K) {
+#pragma unroll
+          for (int rr = 0; rr < SP; ++rr) {
+            const int j = st * SP + rr;
+#pragma unroll
+            for (int gu = 0; gu < G; ++gu) {
+              const uint8_t* wp = sb + gu * half_bytes + ((size_t)rr * a.K + e) * 2;
+              float o[R];
+#pragma unroll
+              for (int r = 0; r < R; ++r) o[r] = v[(j * R + r) * G + gu];
+              if constexpr (ACTH) chunk_dot_bf_h<R, CW, NQ>(wp, q, act, o);
+              else chunk_dot_bf_x<R, CW, NQ>(wp, q, act, o);
+#pragma unroll
+              for (int r = 0; r < R; ++r) v[(j * R + r) * G + gu] = o[r];
+            }
+          }
         }
       }
       __syncwarp();
