@@ -228,6 +228,7 @@ bool seg_fits(int K, int N, int KW) {
 template <class A, class B, typename Kern>
 int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget, StreamPlan* p) {
   const int KW = std::max(seg_warps<A>(KA), seg_warps<B>(KB));
+  if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;   // more consumer warps than a CTA holds
   if (!seg_fits<A>(KA, NA, KW) || !seg_fits<B>(KB, NB, KW)) return MOE_ERR_UNSUPPORTED;
   StreamPlan r;
   r.threads = 32 * (KW + 1);

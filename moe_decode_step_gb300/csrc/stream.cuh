@@ -365,6 +365,18 @@ __device__ __forceinline__ int stream_x_row(const StreamArgs& a, int pid) {
   return ROUTED ? pid / a.k : pid;
 }
 
+// Sum of the n <= kMmaWarps partials at p, in order 0..n-1: the bound is a
+// compile-time constant so every load issues before the dependent adds.
+__device__ __forceinline__ float slab_sum(const float* p, int n) {
+  float v[kMmaWarps];
+#pragma unroll
+  for (int w = 0; w < kMmaWarps; ++w) v[w] = w < n ? p[w] : 0.f;
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMmaWarps; ++w) s += v[w];
+  return s;
+}
+
 // Consumers of a bf16 step: one pass of R activation rows over the run
 // [it0, run_end) of items that share them.  Activation slices and pair ids are
 // loaded once; every item then streams its SPI stages, reduces and finalises.
@@ -459,14 +471,15 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
       if constexpr (GLU) {
         const float* pg = rb + ((j * R + r) * 2) * KW;
         float g = 0.f, u = 0.f;
-        for (int w = 0; w < KW; ++w) { g += pg[w]; u += pg[KW + w]; }
+        g = slab_sum(pg, KW);
+        u = slab_sum(pg + KW, KW);
         const float hv = g / (1.0f + expf(-g)) * u;
         *dst = hv;
         if (a.out_amax) atomicMax(a.out_amax + p, __float_as_uint(fabsf(hv)));
       } else {
         const float* pv = rb + (j * R + r) * KW;
         float acc = 0.f;
-        for (int w = 0; w < KW; ++w) acc += pv[w];
+        acc = slab_sum(pv, KW);
         *dst = acc;
       }
     }
@@ -688,7 +701,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
           const float* pg = rbuf + (((j >> 3) * 16 + (j & 7)) * RMAX + ei) * KW;
           const float* pu = pg + 8 * RMAX * KW;
           float gs = 0.f, us = 0.f;
-          for (int w = 0; w < KW; ++w) { gs += pg[w]; us += pu[w]; }
+          gs = slab_sum(pg, KW);
+          us = slab_sum(pu, KW);
           gs *= back;
           us *= back;
           const float hv = gs / (1.0f + expf(-gs)) * us;
@@ -697,7 +711,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
         } else {
           const float* pv = rbuf + (((j >> 4) * 16 + (j & 15)) * RMAX + ei) * KW;
           float sum = 0.f;
-          for (int w = 0; w < KW; ++w) sum += pv[w];
+          sum = slab_sum(pv, KW);
           *dst = sum * back;
         }
       }
