@@ -62,11 +62,21 @@ typedef struct moe_layer* moe_layer_t;
 
 /* Layer dimensions.  d % 256 == 0 and d <= 7680; f % 256 == 0 and f <= 4096;
  * f_shared % 256 == 0 and f_shared <= 4096; 1 <= top_k <= 32; top_k <= n_experts
- * <= 1024; 1 <= max_batch <= 64.  mxfp4_layout is 0 (expert weights in the
- * canonical layout: moe_layer_create copies them into the kernels' tiled
- * layouts, E * 3 * d * f * 17/32 bytes of extra device memory owned by the
- * handle) or 1 (expert weights already tiled: FC1 matrices in layout 2, FC2
- * matrices in layout 1, see mxfp4_pack; used in place). */
+ * <= 1024; 1 <= max_batch <= 64.
+ *
+ * expert_path picks how the routed experts run: 0 (default) or 2 = the
+ * tcgen05 tensor cores (block-scaled MXFP4 MMAs with tensor-memory
+ * accumulators; the kernels read the UMMA layouts, FC1 matrices in layout 4
+ * and FC2 matrices in layout 3), 1 = mma.sync tensor cores with the weights
+ * converted to f16 in registers (the tiled layouts, FC1 in layout 2 and FC2
+ * in layout 1).  Both give results within the same tolerance of the exact
+ * layer.
+ *
+ * mxfp4_layout says how the caller's expert weights are laid out: 0
+ * (canonical), 1 (tiled: FC1 layout 2, FC2 layout 1) or 3 (UMMA: FC1 layout 4,
+ * FC2 layout 3); see mxfp4_pack.  Weights already in the chosen path's layouts
+ * are used in place; otherwise moe_layer_create relays them into a copy the
+ * handle owns (E * 3 * d * f * 17/32 bytes of extra device memory). */
 typedef struct {
   int32_t d;              /* hidden size */
   int32_t f;              /* routed-expert intermediate size */
@@ -76,7 +86,8 @@ typedef struct {
   int32_t max_batch;      /* largest B forward will be called with */
   float routed_scale;     /* combine weights sum to this (2.5 for the Kimi-style router) */
   float rms_eps;          /* RMSNorm epsilon (1e-6) */
-  int32_t mxfp4_layout;   /* 0: canonical expert weights, 1: tiled (see above) */
+  int32_t mxfp4_layout;   /* 0: canonical, 1: tiled, 3: UMMA expert weights (see above) */
+  int32_t expert_path;    /* 0: default (2), 1: mma.sync, 2: tcgen05 (see above) */
 } moe_dims_t;
 
 /* Device pointers to the layer's weights (borrowed, never freed).
@@ -85,10 +96,10 @@ typedef struct {
 typedef struct {
   const void* router_w;        /* device bf16 [E][d] */
   const float* router_bias;    /* device fp32 [E], used for selection only */
-  const uint8_t* w_gu_q;       /* device [E][2f][d/2]  E2M1 nibbles (layout 0, or 2) */
-  const uint8_t* w_gu_s;       /* device [E][2f][d/32] E8M0 scale bytes (layout 0, or 2) */
-  const uint8_t* w_d_q;        /* device [E][d][f/2]  (layout 0, or 1) */
-  const uint8_t* w_d_s;        /* device [E][d][f/32] (layout 0, or 1) */
+  const uint8_t* w_gu_q;       /* device [E][2f][d/2]  E2M1 nibbles (layout 0, 2 or 4) */
+  const uint8_t* w_gu_s;       /* device [E][2f][d/32] E8M0 scale bytes (layout 0, 2 or 4) */
+  const uint8_t* w_d_q;        /* device [E][d][f/2]  (layout 0, 1 or 3) */
+  const uint8_t* w_d_s;        /* device [E][d][f/32] (layout 0, 1 or 3) */
   const void* shared_gu;       /* device bf16 [2 f_shared][d] (gate rows, then up rows) */
   const void* shared_d;        /* device bf16 [d][f_shared] */
   const void* rms_gamma;       /* device bf16 [d] */
@@ -191,6 +202,16 @@ int moe_launches_per_forward(moe_layer_t layer, int B);
  * and of mma row g + 8 (byte 2j + 1).  Tiled layouts need k % 128 == 0 and
  * rows % 16 == 0. */
 
+/* UMMA layouts 3 and 4 hold the same bytes as tcgen05 block-scaled operands
+ * (no swizzle, K-major core matrices of 8 rows x 16 bytes).  Rows form tiles
+ * of 128 "mma rows": layout 3 puts rows 128T..128T+127 in tile T; layout 4 (a
+ * [2n][k] gate/up matrix) puts rows 64T..64T+63 as mma rows 0..63 and rows
+ * n+64T..n+64T+63 as mma rows 64..127.  Tile T's nibbles occupy bytes
+ * [64kT, 64k(T+1)): the 16 canonical bytes of K block b of mma row m at
+ * 64kT + 2048b + 128(m/8) + 16(m%8).  Tile T's scales occupy bytes [4kT,
+ * 4k(T+1)): the scale of (m, b) at 4kT + 512(b/4) + 16(m%32) + 4(m/32) + b%4.
+ * UMMA layouts need k % 128 == 0 and rows % 128 == 0. */
+
 /* Bytes of nibbles for rows x k (k % 32 == 0, and the layout's rules);
  * *scale_bytes gets the scale bytes when non-NULL.  The same for every
  * layout.  Returns 0 on bad arguments. */
@@ -203,13 +224,13 @@ int mxfp4_pack(const float* w, int64_t rows, int64_t k, uint8_t* q, uint8_t* s, 
 int mxfp4_pack_device(void* stream, const float* w, int64_t rows, int64_t k, uint8_t* q,
                       uint8_t* s, int layout);
 
-/* Host conversion between layouts (0, 1, 2) of one rows x k matrix: q_in, s_in
+/* Host conversion between layouts (0 to 4) of one rows x k matrix: q_in, s_in
  * host in layout `from`; q_out, s_out host in layout `to` (same sizes, must not
  * overlap the input).  Errors: INVALID_ARG, UNSUPPORTED (a layout's rules). */
 int mxfp4_repack(const uint8_t* q_in, const uint8_t* s_in, int64_t rows, int64_t k, int from,
                  int to, uint8_t* q_out, uint8_t* s_out);
 
-/* Canonical packed bytes -> tiled layout 1 or 2, asynchronous on stream, for
+/* Canonical packed bytes -> tiled or UMMA layout 1 to 4, asynchronous on stream, for
  * n_mat matrices stored back to back (rows x k each): q_in, s_in device
  * canonical; q_out, s_out device, the same sizes, must not overlap the input.
  * Errors: INVALID_ARG, UNSUPPORTED (layout rules, 16-byte alignment), CUDA. */

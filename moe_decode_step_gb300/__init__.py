@@ -43,17 +43,20 @@ class MoELayer:
     weights: dict with router_w bf16 [E,d], router_bias f32 [E], w_gu_q u8
     [E,2f,d/2], w_gu_s u8 [E,2f,d/32], w_d_q u8 [E,d,f/2], w_d_s u8 [E,d,f/32],
     shared_gu bf16 [2fs,d], shared_d bf16 [d,fs], rms_gamma bf16 [d].
-    mxfp4_layout: 0 if the expert bytes are canonical (the layer keeps a tiled
-    copy), 1 if FC1 is already in tiled layout 2 and FC2 in layout 1; by
-    default the dict's "mxfp4_layout" entry, else 0.
+    mxfp4_layout: how the expert bytes are laid out: 0 canonical, 1 tiled (FC1
+    in layout 2, FC2 in layout 1), 3 UMMA (FC1 in layout 4, FC2 in layout 3);
+    by default the dict's "mxfp4_layout" entry, else 0.  Weights not in the
+    chosen path's layouts are relaid into a copy the layer owns.
+    expert_path: 0 (default) or 2 = tcgen05 tensor cores (UMMA layouts), 1 =
+    mma.sync tensor cores (tiled layouts).
     """
 
     def __init__(self, d, f, n_experts, top_k, f_shared, max_batch, weights,
-                 routed_scale=2.5, rms_eps=1e-6, mxfp4_layout=None):
+                 routed_scale=2.5, rms_eps=1e-6, mxfp4_layout=None, expert_path=0):
         if mxfp4_layout is None:
             mxfp4_layout = int(weights.get("mxfp4_layout", 0))
         self.dims = MoEDims(d, f, n_experts, top_k, f_shared, max_batch, routed_scale, rms_eps,
-                            mxfp4_layout)
+                            mxfp4_layout, int(expert_path))
         E, fs = n_experts, f_shared
         spec = {
             "router_w": (torch.bfloat16, (E, d)), "router_bias": (torch.float32, (E,)),
@@ -190,7 +193,8 @@ def mxfp4_packed_bytes(rows, k, layout=0):
 
 def mxfp4_pack(w, layout=0):
     """Host packer: w CPU float32 [rows, k] -> (q uint8 [rows, k/2], s uint8 [rows, k/32])
-    in the given layout (0 canonical, 1 tiled rows, 2 tiled gate/up pairs)."""
+    in the given layout (0 canonical, 1 tiled rows, 2 tiled gate/up pairs, 3 UMMA
+    rows, 4 UMMA gate/up pairs)."""
     if w.is_cuda or w.dtype != torch.float32 or w.dim() != 2:
         raise ValueError("mxfp4_pack wants a CPU float32 matrix")
     w = w.contiguous()
@@ -218,7 +222,7 @@ def mxfp4_pack_device(w, q=None, s=None, stream=None, layout=0):
 
 def mxfp4_repack(q, s, src, dst):
     """Host conversion of one matrix's packed bytes (CPU uint8 [rows, k/2] and
-    [rows, k/32]) from layout `src` to layout `dst` (0, 1 or 2)."""
+    [rows, k/32]) from layout `src` to layout `dst` (0 to 4)."""
     if q.is_cuda or s.is_cuda or q.dtype != torch.uint8 or s.dtype != torch.uint8:
         raise ValueError("mxfp4_repack wants CPU uint8 tensors")
     q = q.contiguous()
@@ -233,7 +237,7 @@ def mxfp4_repack(q, s, src, dst):
 
 def mxfp4_retile_device(q, s, layout, stream=None):
     """Canonical packed bytes (CUDA uint8 [..., rows, k/2] and [..., rows, k/32],
-    matrices stacked on the leading dims) -> new tensors in tiled layout 1 or 2."""
+    matrices stacked on the leading dims) -> new tensors in tiled or UMMA layout 1 to 4."""
     if not (q.is_cuda and s.is_cuda) or q.dtype != torch.uint8 or s.dtype != torch.uint8:
         raise ValueError("mxfp4_retile_device wants CUDA uint8 tensors")
     q = q.contiguous()

@@ -23,7 +23,8 @@ class MoEDims(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("f", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("f_shared", ctypes.c_int32),
                 ("max_batch", ctypes.c_int32), ("routed_scale", ctypes.c_float),
-                ("rms_eps", ctypes.c_float), ("mxfp4_layout", ctypes.c_int32)]
+                ("rms_eps", ctypes.c_float), ("mxfp4_layout", ctypes.c_int32),
+                ("expert_path", ctypes.c_int32)]
 
 
 class MoEWeights(ctypes.Structure):

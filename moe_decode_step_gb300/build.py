@@ -6,8 +6,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoe_decode.so")
 SOURCES = ["csrc/moe_decode.cu", "csrc/noalloc.cu"]
-HEADERS = ["csrc/common.cuh", "csrc/mxfp4.cuh", "csrc/stream.cuh", "csrc/topk.cuh",
-           "csrc/tail.cuh"]
+HEADERS = ["csrc/common.cuh", "csrc/mxfp4.cuh", "csrc/planes.cuh", "csrc/stream.cuh",
+           "csrc/tc.cuh", "csrc/topk.cuh", "csrc/tail.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
 

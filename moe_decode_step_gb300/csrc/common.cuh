@@ -119,6 +119,16 @@ __device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float c) {
   return c;
 }
 
+// Nearest E2M1 magnitude code for a >= 0 (E2M1 magnitudes 0, .5, 1, 1.5, 2,
+// 3, 4, 6 are codes 0..7); the midpoints 0.25, 1.25, 2.5, 5 round down (to the
+// even codes 0, 2, 4, 6) and 0.75, 1.75, 3.5 round up (to the even codes 2, 4,
+// 6).  Values above 5 become 6 (code 7), which also saturates everything larger.
+__host__ __device__ inline uint32_t e2m1_magnitude_code(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+         (uint32_t)(a > 5.0f);
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // fp32 -> bf16 bits, round to nearest even (inputs here are finite).

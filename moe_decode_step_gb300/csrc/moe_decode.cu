@@ -23,6 +23,7 @@
 #include "mxfp4.cuh"
 #include "stream.cuh"
 #include "tail.cuh"
+#include "tc.cuh"
 #include "topk.cuh"
 
 using namespace moe;
@@ -65,15 +66,26 @@ struct Workspace {
   uint16_t* x_stage;
   uint16_t* res_stage;
   uint16_t* out_stage;
+  // tensor-core expert path: activation planes of x and h, stream-K partials
+  uint8_t* x_act;
+  uint8_t* x_code;
+  uint8_t* h_act;
+  uint8_t* h_code;
+  float* partial;
+  unsigned* flags;
 };
 
 // Launch shape of one streaming-GEMV step.
 struct StreamPlan {
   int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0, red_pp = 0;
-  int kc = 1;   // K chunks per item of the MXFP4 segment
+  int kc = 1;      // K chunks per item of the MXFP4 segment (CUDA-core path)
+  int tc_kc = 0;   // K elements per stage of the tensor-core segment
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kNumSteps };
+
+// Expert paths: mma.sync on the tiled layouts, or tcgen05 on the UMMA layouts.
+enum { kPathMmaSync = 1, kPathTc = 2 };
 
 }  // namespace
 
@@ -82,6 +94,7 @@ struct moe_layer {
   moe_weights_t w;
   int device = 0;
   int n_sm = 0;
+  int smem_optin = 0;   // largest dynamic shared memory a block may opt into
   void* ws_base = nullptr;
   Workspace ws{};
   cudaStream_t pref = nullptr;
@@ -91,9 +104,11 @@ struct moe_layer {
   moe_layer* next = nullptr;
   StreamPlan plan[kNumSteps][3];   // by batch class (B = 1, B <= 8, B > 8)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
-  // expert weights in the kernels' tiled layouts (FC1 gate/up pairs, FC2
-  // rows): the caller's when created with mxfp4_layout 1, else a copy
-  // retiled at create time that the handle owns
+  int path = kPathTc;
+  int layout_gu = kMxUmmaPairs, layout_d = kMxUmma;
+  // expert weights in the path's layouts (FC1 gate/up pairs, FC2 rows): the
+  // caller's when created in that layout, else a copy relaid at create time
+  // that the handle owns
   const uint8_t *gu_q = nullptr, *gu_s = nullptr, *d_q = nullptr, *d_s = nullptr;
   void* owned_w = nullptr;
 };
@@ -129,6 +144,12 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.x_stage = carve<uint16_t>(p, B * d.d);
   w.res_stage = carve<uint16_t>(p, B * d.d);
   w.out_stage = carve<uint16_t>(p, B * d.d);
+  w.x_act = carve<uint8_t>(p, B * planes_row_bytes(d.d));
+  w.x_code = carve<uint8_t>(p, B * planes_code_bytes(d.d));
+  w.h_act = carve<uint8_t>(p, P * planes_row_bytes(d.f));
+  w.h_code = carve<uint8_t>(p, P * planes_code_bytes(d.f));
+  w.partial = carve<float>(p, (size_t)kTcMaxCtas * kTcRmax * 128);
+  w.flags = carve<unsigned>(p, kTcMaxCtas);
   if (ws) *ws = w;
   return (size_t)(p - base);
 }
@@ -141,7 +162,8 @@ int validate_dims(const moe_dims_t& d) {
   if (d.n_experts < d.top_k || d.n_experts > 1024) return MOE_ERR_INVALID_ARG;
   if (d.max_batch < 1 || d.max_batch > 64) return MOE_ERR_INVALID_ARG;
   if (!(d.routed_scale > 0.f) || !(d.rms_eps >= 0.f)) return MOE_ERR_INVALID_ARG;
-  if (d.mxfp4_layout != 0 && d.mxfp4_layout != 1) return MOE_ERR_UNSUPPORTED;
+  if (d.mxfp4_layout != 0 && d.mxfp4_layout != 1 && d.mxfp4_layout != 3) return MOE_ERR_UNSUPPORTED;
+  if (d.expert_path < 0 || d.expert_path > 2) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -169,6 +191,9 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_FC2_RM(RS) ((RS) == 1 ? 1 : 8)
 #define MOE_FC2_KERNEL(RS, NBM) \
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
+// Tensor-core path: the same shared segments, then the routed step on tcgen05.
+#define MOE_TC1_KERNEL(RS) tc_dual_kernel<Sh1Cfg<RS>, true, false>
+#define MOE_TC2_KERNEL(RS) tc_dual_kernel<Sh2Cfg<RS>, false, true>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -262,6 +287,41 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
       MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
 }
 
+// Launch shape of a tensor-core kernel: segment A's consumer warps (at least
+// the five the routed step's roles need), a stage ring sized for the larger
+// segment, and tensor memory for two accumulators, a scale slot per stage and
+// two activation-scale buffers.  rmax: pairs per pass at this batch class.
+template <class A, typename Kern>
+int plan_tc(Kern kern, int KA, int NA, int K, int rmax, int E, int n_sm, int budget,
+            StreamPlan* p) {
+  const int KW = std::max(seg_warps<A>(KA), 5);
+  if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;
+  if (!seg_fits<A>(KA, NA, KW)) return MOE_ERR_UNSUPPORTED;
+  if (K % 256 != 0 || n_sm > kTcMaxCtas) return MOE_ERR_UNSUPPORTED;
+  StreamPlan r;
+  r.threads = 32 * (KW + 1);
+  r.kc = 1;
+  r.tc_kc = K % 512 == 0 ? 512 : 256;
+  const size_t st = std::max(seg_stage_bytes<A>(KA, 1), tc_stage_bytes(r.tc_kc, rmax));
+  r.stage_bytes = (int)((st + 127) / 128 * 128);
+  r.red_pp = stream_red_pp(KW, A::MMA, A::TM, A::RMAX);
+  const int red_bytes = 2 * r.red_pp * 4 + 64;
+  const int extra = (int)tc_smem_bytes(E);
+  r.NS = std::min(16, (budget - red_bytes - extra) / (r.stage_bytes + 16));
+  auto cols = [&](int ns) { return kTcSfaCol + ns * (r.tc_kc / 32) + 2 * (K / 64); };
+  while (r.NS > 2 && cols(r.NS) > kTcCols) --r.NS;
+  if (r.NS < 2 || cols(r.NS) > kTcCols) return MOE_ERR_UNSUPPORTED;
+  // at least 116 KB: a second CTA on the SM would wait in tcgen05.alloc
+  r.smem = std::max(r.NS * r.stage_bytes + r.NS * 16 + red_bytes + extra, 116 * 1024);
+  MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
+  int occ = 0;
+  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, r.threads, r.smem));
+  if (occ != 1) return MOE_ERR_UNSUPPORTED;
+  r.grid = n_sm;
+  *p = r;
+  return MOE_OK;
+}
+
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
@@ -271,6 +331,24 @@ int plan_all(moe_layer* L) {
   MOE_PLAN((plan_kernel<RouterCfg, RouterCfg>(MOE_ROUTER_KERNEL, d.d, d.n_experts, d.d,
                                               d.n_experts, n, kBudget2,
                                               &L->plan[kStepRouter][0])));
+  if (L->path == kPathTc) {
+    const int E = d.n_experts;
+    // one CTA per SM: all the shared memory a block may opt into
+    const int bud = std::max(kBudget1, L->smem_optin);
+    MOE_PLAN((plan_tc<Sh1Cfg<1>>(MOE_TC1_KERNEL(1), d.d, d.f_shared, d.d, 1, E, n, bud,
+                                 &L->plan[kStepTc1][0])));
+    MOE_PLAN((plan_tc<Sh1Cfg<2>>(MOE_TC1_KERNEL(2), d.d, d.f_shared, d.d, kTcRmax, E, n, bud,
+                                 &L->plan[kStepTc1][1])));
+    MOE_PLAN((plan_tc<Sh1Cfg<4>>(MOE_TC1_KERNEL(4), d.d, d.f_shared, d.d, kTcRmax, E, n, bud,
+                                 &L->plan[kStepTc1][2])));
+    MOE_PLAN((plan_tc<Sh2Cfg<1>>(MOE_TC2_KERNEL(1), d.f_shared, d.d, d.f, 1, E, n, bud,
+                                 &L->plan[kStepTc2][0])));
+    MOE_PLAN((plan_tc<Sh2Cfg<2>>(MOE_TC2_KERNEL(2), d.f_shared, d.d, d.f, kTcRmax, E, n, bud,
+                                 &L->plan[kStepTc2][1])));
+    MOE_PLAN((plan_tc<Sh2Cfg<4>>(MOE_TC2_KERNEL(4), d.f_shared, d.d, d.f, kTcRmax, E, n, bud,
+                                 &L->plan[kStepTc2][2])));
+    return MOE_OK;
+  }
   MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg>(MOE_FC1_KERNEL(1), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][0])));
   MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg>(MOE_FC1_KERNEL(2), d.d, d.f_shared, d.d, d.f, n,
@@ -349,6 +427,10 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
   a.trace_id = 0;
+  if (L->path == kPathTc) {   // the activation planes the tensor-core FC1 streams
+    a.xq = L->ws.x_act;
+    a.xq_code = L->ws.x_code;
+  }
   int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts,
                        st, false);
   if (rc) return rc;
@@ -413,6 +495,103 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
     case 0: return launch_dual(MOE_FC1_KERNEL(1), p, sa, ra, st, grid);
     case 1: return launch_dual(MOE_FC1_KERNEL(2), p, sa, ra, st, grid);
     default: return launch_dual(MOE_FC1_KERNEL(4), p, sa, ra, st, grid);
+  }
+}
+
+// Tensor-core path: the routed step's arguments common to FC1 and FC2.
+TcArgs tc_base_args(moe_layer* L, const StreamPlan& p) {
+  TcArgs b;
+  std::memset(&b, 0, sizeof(b));
+  b.n_active = L->ws.n_active;
+  b.active_expert = L->ws.active_expert;
+  b.active_off = L->ws.active_off;
+  b.pair_list = L->ws.pair_list;
+  b.partial = L->ws.partial;
+  b.flags = L->ws.flags;
+  b.status = L->ws.status;
+  b.NS = p.NS;
+  b.stage_bytes = p.stage_bytes;
+  b.KC = p.tc_kc;
+  return b;
+}
+
+template <typename K>
+int launch_tc(K kern, const StreamPlan& p, StreamArgs a0, const TcArgs& b, cudaStream_t st,
+              int grid) {
+  a0.NS = p.NS;
+  a0.stage_bytes = p.stage_bytes;
+  a0.red_pp = p.red_pp;
+  a0.kc = 1;
+  MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, true, a0, b));
+  return MOE_OK;
+}
+
+// FC1 on the tensor-core path: shared gate/up on the CUDA cores, then routed
+// gate/up (x planes x UMMA-layout weights), SwiGLU, h and its planes.
+int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
+  const moe_dims_t& d = L->dims;
+  StreamArgs sa = base_args(L);
+  sa.q = static_cast<const uint8_t*>(L->w.shared_gu);
+  sa.K = d.d;
+  sa.N = d.f_shared;
+  sa.B = B;
+  sa.x = static_cast<const uint16_t*>(x);
+  sa.out = L->ws.hs;
+  sa.trace_id = 2;
+  const StreamPlan& p = L->plan[kStepTc1][batch_class(B)];
+  TcArgs b = tc_base_args(L, p);
+  b.q = L->gu_q;
+  b.s = L->gu_s;
+  b.q_stride = L->q_gu_stride;
+  b.s_stride = L->s_gu_stride;
+  b.K = d.d;
+  b.tiles = d.f / 64;
+  b.N = d.f;
+  b.act_div = d.top_k;
+  b.act = L->ws.x_act;
+  b.act_code = L->ws.x_code;
+  b.out = L->ws.h;
+  b.out_amax = L->ws.h_amax;
+  b.out_act = L->ws.h_act;
+  b.out_code = L->ws.h_code;
+  // at B = 1 one SM holds the top-k CTA when FC1 launches (see launch_fc1)
+  const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
+  switch (batch_class(B)) {
+    case 0: return launch_tc(MOE_TC1_KERNEL(1), p, sa, b, st, grid);
+    case 1: return launch_tc(MOE_TC1_KERNEL(2), p, sa, b, st, grid);
+    default: return launch_tc(MOE_TC1_KERNEL(4), p, sa, b, st, grid);
+  }
+}
+
+// FC2 on the tensor-core path: shared down on the CUDA cores, then routed
+// down (h planes x UMMA-layout weights).
+int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
+  const moe_dims_t& d = L->dims;
+  StreamArgs sa = base_args(L);
+  sa.q = static_cast<const uint8_t*>(L->w.shared_d);
+  sa.K = d.f_shared;
+  sa.N = d.d;
+  sa.B = B;
+  sa.h = L->ws.hs;
+  sa.out = L->ws.y_s;
+  sa.trace_id = 3;
+  const StreamPlan& p = L->plan[kStepTc2][batch_class(B)];
+  TcArgs b = tc_base_args(L, p);
+  b.q = L->d_q;
+  b.s = L->d_s;
+  b.q_stride = L->q_d_stride;
+  b.s_stride = L->s_d_stride;
+  b.K = d.f;
+  b.tiles = d.d / 128;
+  b.N = d.d;
+  b.act_div = 1;
+  b.act = L->ws.h_act;
+  b.act_code = L->ws.h_code;
+  b.out = L->ws.y_pair;
+  switch (batch_class(B)) {
+    case 0: return launch_tc(MOE_TC2_KERNEL(1), p, sa, b, st, p.grid);
+    case 1: return launch_tc(MOE_TC2_KERNEL(2), p, sa, b, st, p.grid);
+    default: return launch_tc(MOE_TC2_KERNEL(4), p, sa, b, st, p.grid);
   }
 }
 
@@ -515,9 +694,10 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
   if ((rc = launch_prefetch(L))) return rc;
-  if ((rc = launch_fc1(L, st, x, B))) return rc;
+  const bool tc = L->path == kPathTc;
+  if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  if ((rc = launch_fc2(L, st, B))) return rc;
+  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
@@ -531,6 +711,22 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
                              cudaMemcpyDeviceToDevice, st));
   if (h_dbg)
     MOE_CUDA(cudaMemcpyAsync(h_dbg, L->ws.h, P * L->dims.f * 4, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+// n_mat matrices rows x k from layout `from` to layout `to` (default stream).
+int relayout_device(const uint8_t* q_in, const uint8_t* s_in, int64_t n_mat, int64_t rows,
+                    int64_t k, int from, int to, uint8_t* q_out, uint8_t* s_out) {
+  if (!mx_layout_ok(rows, k, from) || !mx_layout_ok(rows, k, to)) return MOE_ERR_UNSUPPORTED;
+  const int64_t qb = rows * (k / 2), sb = rows * (k / 32);
+  const int64_t total = rows * (k / 32);
+  if (total == 0) return MOE_OK;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
+  for (int64_t m = 0; m < n_mat; ++m) {
+    mxfp4_relayout_kernel<<<(unsigned)blocks, 256>>>(q_in + m * qb, s_in + m * sb, rows, k, from,
+                                                     q_out + m * qb, s_out + m * sb, to);
+    MOE_CUDA(cudaGetLastError());
+  }
   return MOE_OK;
 }
 
@@ -576,6 +772,7 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   L->w = w;
   L->device = dev;
   L->n_sm = prop.multiProcessorCount;
+  L->smem_optin = (int)prop.sharedMemPerBlockOptin;
   const size_t f = dims->f, dd = dims->d;
   L->q_gu_stride = 2 * f * dd / 2;
   L->s_gu_stride = 2 * f * dd / 32;
@@ -599,7 +796,13 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
-  if (dims->mxfp4_layout == 1) {
+  // the expert path (tensor cores unless asked otherwise) fixes the layouts
+  // the kernels read; weights given in another layout are relaid into a copy
+  L->path = dims->expert_path == kPathMmaSync ? kPathMmaSync : kPathTc;
+  const int want = L->path == kPathTc ? 3 : 1;
+  L->layout_gu = L->path == kPathTc ? kMxUmmaPairs : kMxTiledPairs;
+  L->layout_d = L->path == kPathTc ? kMxUmma : kMxTiled;
+  if (dims->mxfp4_layout == want) {
     L->gu_q = w.w_gu_q;
     L->gu_s = w.w_gu_s;
     L->d_q = w.w_d_q;
@@ -617,10 +820,14 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
     uint8_t* gs = gq + E * L->q_gu_stride;
     uint8_t* dq = gs + E * L->s_gu_stride;
     uint8_t* ds = dq + E * L->q_d_stride;
-    if ((rc = mxfp4_retile_device(nullptr, w.w_gu_q, w.w_gu_s, (int64_t)E, 2 * (int64_t)f,
-                                  (int64_t)dd, 2, gq, gs)) ||
-        (rc = mxfp4_retile_device(nullptr, w.w_d_q, w.w_d_s, (int64_t)E, (int64_t)dd, (int64_t)f,
-                                  1, dq, ds))) {
+    const int from_gu = dims->mxfp4_layout == 0 ? kMxCanonical
+                        : dims->mxfp4_layout == 1 ? kMxTiledPairs : kMxUmmaPairs;
+    const int from_d = dims->mxfp4_layout == 0 ? kMxCanonical
+                       : dims->mxfp4_layout == 1 ? kMxTiled : kMxUmma;
+    if ((rc = relayout_device(w.w_gu_q, w.w_gu_s, (int64_t)E, 2 * (int64_t)f, (int64_t)dd,
+                              from_gu, L->layout_gu, gq, gs)) ||
+        (rc = relayout_device(w.w_d_q, w.w_d_s, (int64_t)E, (int64_t)dd, (int64_t)f, from_d,
+                              L->layout_d, dq, ds))) {
       moe_layer_destroy(L);
       return rc;
     }
@@ -701,7 +908,7 @@ int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float*
                      (size_t)expert * (which == 0 ? L->q_gu_stride : L->q_d_stride);
   const uint8_t* s = (which == 0 ? L->gu_s : L->d_s) +
                      (size_t)expert * (which == 0 ? L->s_gu_stride : L->s_d_stride);
-  const int layout = which == 0 ? kMxTiledPairs : kMxTiled;
+  const int layout = which == 0 ? L->layout_gu : L->layout_d;
   const int64_t blocks = std::min<int64_t>((rows * (k / 32) + 255) / 256, 4096);
   mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       q, s, rows, k, layout, out);

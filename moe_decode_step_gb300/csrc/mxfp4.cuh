@@ -16,6 +16,16 @@
 // [4t, 4t+4) of mma rows g and g+8 in block 2P, then the same in block 2P+1.
 // The scales of a tile are grouped by 4 blocks: for group Q and g < 8, eight
 // bytes hold (row g, row g+8) for blocks 4Q..4Q+3.
+//
+// UMMA layouts (the tcgen05 block-scaled operand in shared memory, no swizzle,
+// K-major): tiles of 128 mma rows (layout 3: 128 consecutive rows; layout 4,
+// for a [2n][k] gate/up matrix: gate rows 64T..64T+63 as mma rows 0..63 and
+// the matching up rows n+64T.. as mma rows 64..127).  A tile's nibbles are
+// 8-row x 16-byte core matrices: the 16 bytes of K block b of mma row m sit at
+// b*2048 + (m/8)*128 + (m%8)*16 (so one K block of the tile is 2 KB and any
+// run of K blocks is contiguous).  A tile's scales come in atoms of 4 K
+// blocks, 512 bytes each, in the order the 32x128b tensor-memory copy takes
+// them: the scale of (m, b) at (b/4)*512 + (m%32)*16 + (m/32)*4 + b%4.
 #pragma once
 
 #include <math.h>
@@ -44,16 +54,6 @@ __host__ __device__ inline int mx_block_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// Nearest E2M1 magnitude code for a >= 0; the midpoints 0.25, 1.25, 2.5, 5
-// round down (to the even codes 0, 2, 4, 6) and 0.75, 1.75, 3.5 round up (to
-// the even codes 2, 4, 6).  Values above 5 become 6 (code 7), which also
-// saturates everything larger.
-__host__ __device__ inline uint32_t e2m1_magnitude_code(float a) {
-  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-         (uint32_t)(a > 5.0f);
-}
-
 // Pack one 32-element block: 16 nibble bytes and the scale byte.
 __host__ __device__ inline uint8_t mx_pack_block(const float* w, uint8_t* q16) {
   float amax = 0.0f;
@@ -72,12 +72,24 @@ __host__ __device__ inline uint8_t mx_pack_block(const float* w, uint8_t* q16) {
   return (uint8_t)(e + 127);
 }
 
-enum { kMxCanonical = 0, kMxTiled = 1, kMxTiledPairs = 2 };
+enum { kMxCanonical = 0, kMxTiled = 1, kMxTiledPairs = 2, kMxUmma = 3, kMxUmmaPairs = 4 };
 
-// Tile T and mma row r (0..15) of canonical row `row` in a tiled layout.
+__host__ __device__ inline bool mx_is_umma(int layout) {
+  return layout == kMxUmma || layout == kMxUmmaPairs;
+}
+
+// Tile T and mma row r of canonical row `row` in a tiled or UMMA layout.
 __host__ __device__ inline void mx_tile_of_row(int64_t row, int64_t rows, int layout, int64_t& T,
                                                int& r) {
-  if (layout == kMxTiledPairs) {
+  if (layout == kMxUmmaPairs) {
+    const int64_t n = rows / 2;
+    const int64_t i = row < n ? row : row - n;
+    T = i / 64;
+    r = (int)(i % 64) + (row < n ? 0 : 64);
+  } else if (layout == kMxUmma) {
+    T = row / 128;
+    r = (int)(row % 128);
+  } else if (layout == kMxTiledPairs) {
     const int64_t n = rows / 2;
     const int64_t i = row < n ? row : row - n;
     T = i / 8;
@@ -101,6 +113,15 @@ __host__ __device__ inline int64_t mx_tiled_scale_offset(int64_t T, int r, int64
   return T * (k / 2) + ((b / 4) * 8 + g) * 8 + (b % 4) * 2 + half;
 }
 
+// UMMA layouts: byte offset of the 16 nibble bytes / of the scale of K block
+// b of (tile T, mma row m).
+__host__ __device__ inline int64_t mx_umma_block_offset(int64_t T, int m, int64_t b, int64_t k) {
+  return T * 64 * k + b * 2048 + (m / 8) * 128 + (m % 8) * 16;
+}
+__host__ __device__ inline int64_t mx_umma_scale_offset(int64_t T, int m, int64_t b, int64_t k) {
+  return T * 4 * k + (b / 4) * 512 + (m % 32) * 16 + (m / 32) * 4 + b % 4;
+}
+
 // Where the 16 nibble bytes and the scale byte of (row, block b) go.
 __host__ __device__ inline void mx_store_block(uint8_t* q, uint8_t* s, int64_t row, int64_t b,
                                                int64_t rows, int64_t k, int layout,
@@ -108,6 +129,14 @@ __host__ __device__ inline void mx_store_block(uint8_t* q, uint8_t* s, int64_t r
   if (layout == kMxCanonical) {
     memcpy(q + row * (k / 2) + b * 16, qb, 16);
     s[row * (k / 32) + b] = sb;
+    return;
+  }
+  if (mx_is_umma(layout)) {
+    int64_t T;
+    int m;
+    mx_tile_of_row(row, rows, layout, T, m);
+    memcpy(q + mx_umma_block_offset(T, m, b, k), qb, 16);
+    s[mx_umma_scale_offset(T, m, b, k)] = sb;
     return;
   }
   int64_t T;
@@ -125,6 +154,13 @@ __host__ __device__ inline uint8_t mx_load_block(const uint8_t* q, const uint8_t
     memcpy(qb, q + row * (k / 2) + b * 16, 16);
     return s[row * (k / 32) + b];
   }
+  if (mx_is_umma(layout)) {
+    int64_t T;
+    int m;
+    mx_tile_of_row(row, rows, layout, T, m);
+    memcpy(qb, q + mx_umma_block_offset(T, m, b, k), 16);
+    return s[mx_umma_scale_offset(T, m, b, k)];
+  }
   int64_t T;
   int r;
   mx_tile_of_row(row, rows, layout, T, r);
@@ -132,10 +168,12 @@ __host__ __device__ inline uint8_t mx_load_block(const uint8_t* q, const uint8_t
   return s[mx_tiled_scale_offset(T, r, b, k)];
 }
 
-// A layout's shape rules: k % 32 (canonical); tiled also k % 128 and whole tiles.
+// A layout's shape rules: k % 32 (canonical); tiled and UMMA layouts also
+// k % 128 and whole tiles (16 rows tiled, 128 rows UMMA).
 __host__ __device__ inline bool mx_layout_ok(int64_t rows, int64_t k, int layout) {
   if (rows < 0 || k <= 0 || k % 32 != 0) return false;
   if (layout == kMxCanonical) return true;
+  if (mx_is_umma(layout)) return k % 128 == 0 && rows % 128 == 0;
   if (layout != kMxTiled && layout != kMxTiledPairs) return false;
   return k % 128 == 0 && rows % 16 == 0;
 }
@@ -179,6 +217,21 @@ __global__ void mxfp4_retile_kernel(const uint8_t* __restrict__ qc, const uint8_
   }
 }
 
+// Any layout -> any layout (a byte permutation).
+__global__ void mxfp4_relayout_kernel(const uint8_t* __restrict__ qi, const uint8_t* __restrict__ si,
+                                      int64_t rows, int64_t k, int from, uint8_t* __restrict__ q,
+                                      uint8_t* __restrict__ s, int to) {
+  const int64_t nb = k / 32;
+  const int64_t total = rows * nb;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / nb, b = t % nb;
+    uint8_t qb[16];
+    const uint8_t sb = mx_load_block(qi, si, r, b, rows, k, from, qb);
+    mx_store_block(q, s, r, b, rows, k, to, qb, sb);
+  }
+}
+
 // Dequantise rows x k (any layout) into canonical fp32 rows with the
 // consumers' element decode (cvt.rn.f16x2.e2m1x2) and the exact E8M0 value.
 __global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
@@ -198,6 +251,16 @@ __global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ q, const uint8_
       words[2] = v.z;
       words[3] = v.w;
       sc = e8m0_to_f32(s[r * nb + b]);
+    } else if (mx_is_umma(layout)) {
+      int64_t T;
+      int mr;
+      mx_tile_of_row(r, rows, layout, T, mr);
+      const uint4 v = *reinterpret_cast<const uint4*>(q + mx_umma_block_offset(T, mr, b, k));
+      words[0] = v.x;
+      words[1] = v.y;
+      words[2] = v.z;
+      words[3] = v.w;
+      sc = e8m0_to_f32(s[mx_umma_scale_offset(T, mr, b, k)]);
     } else {
       int64_t T;
       int mr;

@@ -35,6 +35,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "planes.cuh"
 
 namespace moe {
 
@@ -67,6 +68,8 @@ struct StreamArgs {
   int kc;                    // MXFP4 steps: K chunks (stages) per tile group
   unsigned long long* trace; // optional kernel trace (see trace_begin), or null
   int trace_id;
+  uint8_t* xq;               // router only: activation planes of x [B][4K] (planes.cuh), or null
+  uint8_t* xq_code;          // and their plane-0 codes [B][K/32]
 };
 
 // Lane layout of the bf16 steps: a lane owns NQ chunks of CW consecutive K
@@ -854,6 +857,19 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
     __syncwarp();
   } else {
     pdl_wait_prerequisites();
+    if (a.xq) {
+      // the activation planes of x for the tensor-core experts: a share of the
+      // B * K/32 blocks per CTA, one block per warp, while the first stages land
+      const int nb = a.K / 32, total = a.B * nb;
+      const int lo = (int)((long long)total * blockIdx.x / gridDim.x);
+      const int hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+      for (int i = lo + warp - 1; i < hi; i += KW) {
+        const int row = i / nb, blk = i - row * nb;
+        const float v = bf16_bits_to_f32(a.x[(size_t)row * a.K + blk * 32 + lane]);
+        planes_block(v, lane, a.xq + (size_t)row * planes_row_bytes(a.K) + blk * 128,
+                     a.xq_code + (size_t)row * planes_code_bytes(a.K) + blk);
+      }
+    }
     int pp = 0, rp = 0;
     cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
   }

@@ -1,0 +1,648 @@
+// Routed experts on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One expert matmul step (routed FC1 gate/up with the SwiGLU epilogue, or
+// routed FC2 down) as a block-scaled MXFP4 x MXFP4 MMA: the weight tile (128
+// rows, UMMA layout, see mxfp4.cuh) is operand A, the activation planes of up
+// to 8 (expert, row) pairs (8 planes each, see planes.cuh) are operand B, the
+// E8M0 scales ride along in tensor memory, and fp32 accumulators live in
+// tensor memory until the epilogue reads them back.  Nothing is converted on
+// the CUDA cores; the stage ring only streams bytes.
+//
+// Work split: units are (run, tile, K chunk) with a run = one pass of <= 8
+// pairs of one active expert.  CTA i takes units [i U / G, (i+1) U / G) (U
+// units, G CTAs), so every CTA streams the same number of weight bytes.  A
+// tile cut by a range boundary is finished by the CTA that holds its first
+// chunk: the later CTAs leave their partial sums in a per-CTA slot and raise
+// a flag at the start of their range; the finisher adds them in K order at the
+// end of its own (so results do not depend on timing).
+//
+// Roles in a CTA (after the shared-expert segment that runs first on the
+// CUDA cores, see stream.cuh): warp 0 lane 0 streams stages; warp 1 builds
+// the run table, then its lane 0 issues the tensor-memory scale copies and
+// MMAs and commits them to the stage's "empty" barrier and, per tile, to an
+// accumulator barrier; warps 2..5 (tensor-memory lane quarters 2, 3, 0, 1)
+// write the activation scales into tensor memory per run and run the
+// epilogues.  Accumulators, scale slots and activation-scale buffers are all
+// double-buffered or ringed, so the MMA warp never waits for an epilogue in
+// steady state.  Every wait is bounded (status 5 on timeout).
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+#include "planes.cuh"
+#include "stream.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// tcgen05 / UMMA wrappers
+// ---------------------------------------------------------------------------
+constexpr int kTcCols = 512;        // tensor-memory columns a CTA allocates (one CTA per SM)
+constexpr int kTcRmax = 8;          // pairs per pass: N = 8 planes x 8 pairs = 64 columns
+constexpr int kTcMaxCtas = 256;     // partial slots / flags in the workspace
+constexpr int kTcSfaCol = 128;      // D buffers take columns [0, 128)
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Whole warp: allocate kTcCols columns, address written to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst)),
+               "n"(kTcCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kTcCols)
+               : "memory");
+}
+// 32 lanes x 32 bits, 2 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 lanes x 32 bits, 16 consecutive columns per thread (no wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Shared-memory matrix descriptor: no swizzle, K-major core matrices of 8
+// rows x 16 bytes; lbo = byte distance between core matrices along K, sbo =
+// between groups of 8 rows.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (uint64_t)((lbo >> 4) & 0x3FFFu) << 16 |
+         (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46;
+}
+// Instruction descriptor, kind::mxf4: E2M1 x E2M1, E8M0 scales, both K-major,
+// M = 128, N columns; a_sf / b_sf select the scale byte pair of the step.
+__device__ __forceinline__ uint32_t umma_idesc_mxf4(uint32_t a_sf, uint32_t b_sf, uint32_t N) {
+  return (b_sf << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | (8u << 24) |
+         (a_sf << 29);
+}
+__device__ __forceinline__ void umma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of scales from shared memory into 4 columns of all
+// four lane quarters.
+__device__ __forceinline__ void umma_sf_copy(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+// The four epilogue warps only (named barrier 2).
+__device__ __forceinline__ void tc_epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Arguments, shared memory, schedule
+// ---------------------------------------------------------------------------
+struct TcArgs {
+  const uint8_t* q;          // UMMA-layout nibbles (layout 4 for gate/up, 3 for down)
+  const uint8_t* s;          // UMMA-layout scales
+  size_t q_stride, s_stride; // bytes between experts
+  int K;                     // row length
+  int KC;                    // K elements per stage (256 or 512)
+  int tiles;                 // 128-row weight tiles per expert
+  int N;                     // outputs per pair (gate/up: f, down: d)
+  int act_div;               // activation row of pair p: p / act_div
+  const uint8_t* act;        // activation planes [rows][4K]
+  const uint8_t* act_code;   // plane-0 codes [rows][K/32]
+  const int* n_active;
+  const int* active_expert;
+  const int* active_off;
+  const int* pair_list;
+  float* out;                // [pairs][N]
+  unsigned* out_amax;        // gate/up: max |h| bits per pair, or null
+  uint8_t* out_act;          // gate/up: h planes [pairs][4N], or null
+  uint8_t* out_code;         // gate/up: h plane-0 codes [pairs][N/32]
+  float* partial;            // [kTcMaxCtas][kTcRmax][128]
+  unsigned* flags;           // [kTcMaxCtas], zero between forwards
+  int* status;
+  int NS, stage_bytes;       // the stage ring (the same as the shared segment's)
+};
+
+// Activation-scale codes a run stages per epilogue warp: kTcRmax rows of at
+// most kTcCodeRow bytes (K <= 8192).
+constexpr int kTcCodeRow = 256;
+
+// Bytes of shared memory after the stream segment's reduction area.
+__host__ __device__ inline size_t tc_smem_bytes(int E) {
+  return 128 + 2 * kTcRmax * 64 * 4 + 4 * kTcRmax * kTcCodeRow +
+         ((size_t)(E + 1) * 4 + 127) / 128 * 128;
+}
+// Bytes of one stage: weight nibbles, weight scales, planes of the pairs (at
+// least two pairs' room: the MMA reads N >= 16 rows).
+__host__ __device__ inline size_t tc_stage_bytes(int KC, int rmax) {
+  return (size_t)KC * 68 + (size_t)(rmax < 2 ? 2 : rmax) * 4 * KC;
+}
+
+struct TcSmem {
+  uint64_t* acc_full;   // [2] accumulator written (commit)
+  uint64_t* acc_empty;  // [2] accumulator read (4 epilogue warps)
+  uint64_t* sfb_full;   // [2] activation scales written (4 epilogue warps)
+  uint64_t* sched;      // run table ready (1)
+  uint32_t* tbase;      // tensor-memory base address
+  int* n_runs;
+  float* xchg;          // [2][kTcRmax][64] up-half sums for the SwiGLU epilogue
+  uint8_t* codes;       // [4 epilogue warps][kTcRmax][kTcCodeRow] staged activation codes
+  int* run_off;         // [n_active + 1] first run of each active slot
+};
+
+__device__ __forceinline__ TcSmem tc_smem(uint8_t* p) {
+  TcSmem t;
+  uint64_t* b = reinterpret_cast<uint64_t*>(p);
+  t.acc_full = b;
+  t.acc_empty = b + 2;
+  t.sfb_full = b + 4;
+  t.sched = b + 6;
+  t.tbase = reinterpret_cast<uint32_t*>(b + 7);
+  t.n_runs = reinterpret_cast<int*>(b + 7) + 1;
+  t.xchg = reinterpret_cast<float*>(p + 128);
+  t.codes = p + 128 + 2 * kTcRmax * 64 * 4;
+  t.run_off = reinterpret_cast<int*>(t.codes + 4 * kTcRmax * kTcCodeRow);
+  return t;
+}
+
+struct TcRun {
+  int e, p0, R;
+};
+
+// Run rho -> (expert, first pair, pairs): the active slot whose runs contain rho.
+__device__ __forceinline__ TcRun tc_run(const TcArgs& b, const int* run_off, int nact, int rho) {
+  int lo = 0, hi = nact;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (run_off[mid] <= rho) lo = mid;
+    else hi = mid;
+  }
+  TcRun r;
+  const int o1 = __ldcg(b.active_off + lo + 1);
+  r.p0 = __ldcg(b.active_off + lo) + (rho - run_off[lo]) * kTcRmax;
+  r.R = min(kTcRmax, o1 - r.p0);
+  r.e = __ldcg(b.active_expert + lo);
+  return r;
+}
+
+// Units [u0, u1) of CTA i out of G.
+__device__ __forceinline__ void tc_range(int U, int i, int G, int& u0, int& u1) {
+  u0 = (int)((long long)U * i / G);
+  u1 = (int)((long long)U * (i + 1) / G);
+}
+
+// Warp 1: first run of every active slot (passes of <= kTcRmax pairs).
+__device__ __forceinline__ void tc_schedule(const TcArgs& b, const TcSmem& t, int lane) {
+  const int nact = __ldcg(b.n_active);
+  int base = 0;
+  if (lane == 0) t.run_off[0] = 0;
+  for (int s0 = 0; s0 < nact; s0 += 32) {
+    const int s = s0 + lane;
+    int passes = 0;
+    if (s < nact) {
+      const int pr = __ldcg(b.active_off + s + 1) - __ldcg(b.active_off + s);
+      passes = (pr + kTcRmax - 1) / kTcRmax;
+    }
+    int incl = passes;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (s < nact) t.run_off[s + 1] = base + incl;
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    *t.n_runs = base;
+    mbar_arrive(t.sched);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Producer (warp 0, lane 0)
+// ---------------------------------------------------------------------------
+// Per unit both loops below do only a handful of adds: the ring position, the
+// chunk index and the source pointers / descriptors advance incrementally, and
+// everything that depends on the run is computed once per run.  (A single
+// thread issues all the copies or all the MMAs of its CTA; with a division or
+// a 64-bit descriptor rebuild per operand, its instruction latency alone
+// would fall behind the HBM stream.)
+__device__ __forceinline__ void tc_produce(const TcArgs& b, const TcSmem& t, uint8_t* stages,
+                                           uint64_t* full, uint64_t* empty, uint32_t& stage) {
+  mbar_wait(t.sched, 0, b.status);
+  const int nact = __ldcg(b.n_active);
+  const int nch = b.K / b.KC, upr = b.tiles * nch;
+  int u0, u1;
+  tc_range(*t.n_runs * upr, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+  const uint32_t abytes = 64u * b.KC, sbytes = 4u * b.KC, pbytes = 4u * b.KC;
+  const uint32_t NS = (uint32_t)b.NS;
+  uint32_t buf = stage % NS, use = stage / NS;
+  int rho = u0 / upr, idx = u0 - rho * upr, c = idx % nch;
+  for (int u = u0; u < u1; ++rho, idx = 0, c = 0) {
+    const TcRun run = tc_run(b, t.run_off, nact, rho);
+    const int n = min(u1 - u, upr - idx);
+    const uint8_t* qs = b.q + (size_t)run.e * b.q_stride + (size_t)idx * abytes;
+    const uint8_t* ss = b.s + (size_t)run.e * b.s_stride + (size_t)idx * sbytes;
+    const uint8_t* as[kTcRmax];
+#pragma unroll
+    for (int r = 0; r < kTcRmax; ++r)
+      as[r] = b.act + (r < run.R ? (size_t)(__ldcg(b.pair_list + run.p0 + r) / b.act_div) *
+                                       planes_row_bytes(b.K)
+                                 : 0);
+    const uint32_t tx = abytes + sbytes + (uint32_t)run.R * pbytes;
+    for (int i = 0; i < n; ++i) {
+      if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, b.status);
+      uint8_t* dst = stages + (size_t)buf * b.stage_bytes;
+      mbar_arrive_expect_tx(&full[buf], tx);
+      bulk_g2s(dst, qs, abytes, &full[buf], pol_w);
+      bulk_g2s(dst + abytes, ss, sbytes, &full[buf], pol_w);
+      const size_t aoff = (size_t)c * pbytes;
+#pragma unroll
+      for (int r = 0; r < kTcRmax; ++r)
+        if (r < run.R)
+          bulk_g2s(dst + abytes + sbytes + r * pbytes, as[r] + aoff, pbytes, &full[buf], pol_a);
+      qs += abytes;
+      ss += sbytes;
+      if (++c == nch) c = 0;
+      if (++buf == NS) {
+        buf = 0;
+        ++use;
+      }
+      ++stage;
+    }
+    u += n;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (warp 1, lane 0)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_t T,
+                                       uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                       uint32_t& stage, int KW) {
+  const int nact = __ldcg(b.n_active);
+  const int nch = b.K / b.KC, upr = b.tiles * nch;
+  int u0, u1;
+  tc_range(*t.n_runs * upr, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint32_t KC = (uint32_t)b.KC, NS = (uint32_t)b.NS;
+  const uint32_t nsteps = KC / 64, natoms = KC / 128;
+  // descriptors of stage 0; stage s, K step j add (s * stage_bytes + step offset) / 16
+  const uint32_t sa0 = smem_addr(stages);
+  const uint32_t st16 = (uint32_t)b.stage_bytes >> 4;
+  const uint64_t dA0 = umma_desc(sa0, 2048, 128);            // weights: K blocks 2 KB apart
+  const uint64_t dB0 = umma_desc(sa0 + 68 * KC, 128, 4 * KC); // planes: pairs 4 KC apart
+  const uint64_t dS0 = umma_desc(sa0 + 64 * KC, 0, 128);      // weight scales: 32 rows x 16 B
+  const uint32_t sfa0 = T + kTcSfaCol;
+  const uint32_t sfb0 = T + kTcSfaCol + NS * (KC / 32);
+  const uint32_t sfb_w = (uint32_t)b.K / 64;
+  uint32_t buf = stage % NS, ph = (stage / NS) & 1u;
+  int rho = u0 / upr, idx = u0 - rho * upr, c = idx % nch;
+  int lr = 0, jobs = 0;
+  uint32_t jb = 0, acc = 0;
+  bool newjob = true;
+  for (int u = u0; u < u1; ++rho, ++lr, idx = 0, c = 0, newjob = true) {
+    const int R = tc_run(b, t.run_off, nact, rho).R;
+    const uint32_t npad = (uint32_t)max(16, (8 * R + 15) & ~15);
+    const uint32_t id0 = umma_idesc_mxf4(0, 0, npad), id1 = umma_idesc_mxf4(2, 2, npad);
+    mbar_wait(&t.sfb_full[lr & 1], (uint32_t)(lr >> 1) & 1u, b.status);
+    tc_fence_after();
+    const uint32_t sfb_run = sfb0 + (uint32_t)(lr & 1) * sfb_w;
+    const int n = min(u1 - u, upr - idx);
+    for (int i = 0; i < n; ++i) {
+      if (newjob) {   // a new tile job: a free accumulator, zero-initialised by its first MMA
+        jb = (uint32_t)jobs & 1u;
+        if (jobs >= 2) {
+          mbar_wait(&t.acc_empty[jb], (uint32_t)((jobs >> 1) - 1) & 1u, b.status);
+          tc_fence_after();
+        }
+        acc = 0;
+      }
+      mbar_wait(&full[buf], ph, b.status);
+      tc_fence_after();
+      const uint64_t off = (uint64_t)(buf * st16);
+      const uint32_t sfa = sfa0 + buf * (KC / 32);
+      for (uint32_t a = 0; a < natoms; ++a) umma_sf_copy(sfa + 4 * a, dS0 + off + 32 * a);
+      const uint32_t sfb = sfb_run + 2 * (uint32_t)c * natoms;
+      const uint32_t dcol = T + 64 * jb;
+#pragma unroll 8
+      for (uint32_t j = 0; j < nsteps; ++j)
+        umma_mxf4(dcol, dA0 + off + 256 * j, dB0 + off + 16 * j, (j & 1) ? id1 : id0,
+                  sfa + 4 * (j >> 1), sfb + 2 * (j >> 1), acc | j);
+      acc = 1;
+      // the stage is free once these MMAs have read it; the other KW - 1
+      // arrivals the barrier counts (one per CUDA-core consumer warp) come now
+      umma_commit(&empty[buf]);
+      mbar_arrive_count(&empty[buf], (uint32_t)(KW - 1));
+      newjob = c == nch - 1;
+      if (newjob || u + i == u1 - 1) {
+        umma_commit(&t.acc_full[jb]);
+        ++jobs;
+      }
+      if (++c == nch) c = 0;
+      if (++buf == NS) {
+        buf = 0;
+        ph ^= 1u;
+      }
+      ++stage;
+    }
+    u += n;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue (warps 2..5)
+// ---------------------------------------------------------------------------
+// Activation scales of run rho into buffer `buf`: rows n = 8 r + p (pair r,
+// plane p) at lane n % 32 of every quarter, column 2A + n / 32 for the atom A
+// of K blocks 4A..4A+3; rows past the run's pairs get scale 1.  The warp first
+// stages the run's plane-0 codes (R rows of K/32 bytes) in its shared scratch
+// with coalesced 16-byte loads, so the global latency is paid once.
+__device__ __forceinline__ void tc_write_sfb(const TcArgs& b, const TcSmem& t, uint32_t T,
+                                             uint32_t qaddr, int q, int nact, int rho, int buf,
+                                             int lane) {
+  const TcRun run = tc_run(b, t.run_off, nact, rho);
+  const int cb = b.K / 32;            // code bytes per row (a multiple of 4)
+  const int chunks = cb % 16 == 0 ? cb / 16 : 0;   // 16-byte loads only when rows stay aligned
+  uint8_t* scratch = t.codes + (size_t)q * (kTcRmax * kTcCodeRow);
+  for (int i = lane; i < run.R * chunks; i += 32) {
+    const int r = i / chunks, c = i - r * chunks;
+    const int arow = __ldcg(b.pair_list + run.p0 + r) / b.act_div;
+    *reinterpret_cast<uint4*>(scratch + r * kTcCodeRow + 16 * c) =
+        __ldcg(reinterpret_cast<const uint4*>(b.act_code + (size_t)arow * cb) + c);
+  }
+  for (int i = chunks * 16 + 4 * lane; i < cb; i += 128) {   // a tail of 4-byte words
+    for (int r = 0; r < run.R; ++r) {
+      const int arow = __ldcg(b.pair_list + run.p0 + r) / b.act_div;
+      *reinterpret_cast<unsigned*>(scratch + r * kTcCodeRow + i) =
+          __ldcg(reinterpret_cast<const unsigned*>(b.act_code + (size_t)arow * cb + i));
+    }
+  }
+  __syncwarp();
+  const int p0 = lane & 7, r0 = lane >> 3, r1 = r0 + 4;   // rows n = lane and lane + 32
+  const uint32_t col0 = kTcSfaCol + (uint32_t)b.NS * ((uint32_t)b.KC / 32) +
+                        (uint32_t)buf * ((uint32_t)b.K / 64);
+  for (int A = 0; A < b.K / 128; ++A) {
+    uint32_t w0 = 0x7F7F7F7Fu, w1 = 0x7F7F7F7Fu;
+    if (r0 < run.R) {
+      const uint32_t c4 = *reinterpret_cast<const unsigned*>(scratch + r0 * kTcCodeRow + 4 * A);
+      w0 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w0 |= planes_code((c4 >> (8 * i)) & 0xFFu, p0) << (8 * i);
+    }
+    if (r1 < run.R) {
+      const uint32_t c4 = *reinterpret_cast<const unsigned*>(scratch + r1 * kTcCodeRow + 4 * A);
+      w1 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w1 |= planes_code((c4 >> (8 * i)) & 0xFFu, p0) << (8 * i);
+    }
+    tmem_st2(T + qaddr + col0 + 2 * (uint32_t)A, w0, w1);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&t.sfb_full[buf]);
+}
+
+__device__ __forceinline__ void tc_wait_flag(const unsigned* f, int* status) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  if (v) return;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    __nanosleep(64);
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v) return;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+template <bool GLU>
+__device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, uint32_t T, int q,
+                                            int lane) {
+  mbar_wait(t.sched, 0, b.status);
+  const int nact = __ldcg(b.n_active);
+  const int nch = b.K / b.KC, upr = b.tiles * nch;
+  const int U = *t.n_runs * upr;
+  int u0, u1;
+  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint32_t qaddr = (uint32_t)(32 * q) << 16;
+  const int m = 32 * q + lane;   // MMA row of this thread
+  const int rho_last = (u1 - 1) / upr;
+  tc_write_sfb(b, t, T, qaddr, q, nact, u0 / upr, 0, lane);
+  if (u0 / upr + 1 <= rho_last) tc_write_sfb(b, t, T, qaddr, q, nact, u0 / upr + 1, 1, lane);
+  int cur = -1, lr = -1, jobs = 0, fin = 0;
+  TcRun run{0, 0, 0};
+  int pid[kTcRmax];
+  for (int u = u0; u < u1;) {
+    const int rho = u / upr, rem = u - rho * upr, tile = rem / nch, cs = rem - tile * nch;
+    const int tile_end = rho * upr + (tile + 1) * nch;
+    const int ue = min(u1, tile_end);
+    const int ce = cs + (ue - u);
+    if (rho != cur) {
+      cur = rho;
+      ++lr;
+      run = tc_run(b, t.run_off, nact, rho);
+#pragma unroll
+      for (int r = 0; r < kTcRmax; ++r) pid[r] = r < run.R ? __ldcg(b.pair_list + run.p0 + r) : 0;
+      // the other buffer last served run lr - 1, whose tiles are all read back
+      if (lr >= 1 && rho + 1 <= rho_last)
+        tc_write_sfb(b, t, T, qaddr, q, nact, rho + 1, (lr + 1) & 1, lane);
+    }
+    const int R = run.R;
+    const int jb = jobs & 1;
+    mbar_wait(&t.acc_full[jb], (uint32_t)(jobs >> 1) & 1u, b.status);
+    tc_fence_after();
+    float v[64];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (16 * i < 8 * R) tmem_ld16(T + qaddr + 64 * (uint32_t)jb + 16 * i, v + 16 * i);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&t.acc_empty[jb]);
+    ++jobs;
+    float y[kTcRmax];
+#pragma unroll
+    for (int r = 0; r < kTcRmax; ++r) {
+      float s = 0.f;
+      if (r < R) {
+#pragma unroll
+        for (int p = 0; p < kPlanes; ++p) s += v[8 * r + p];
+      }
+      y[r] = s;
+    }
+    if (cs > 0) {
+      // the tile's first chunks belong to an earlier CTA: leave the sums to it
+      float* slot = b.partial + (size_t)blockIdx.x * (kTcRmax * 128);
+#pragma unroll
+      for (int r = 0; r < kTcRmax; ++r)
+        if (r < R) slot[r * 128 + m] = y[r];
+      tc_epi_sync();
+      if (m == 0) {
+        __threadfence();
+        atomicExch(b.flags + blockIdx.x, 1u);
+      }
+      u = ue;
+      continue;
+    }
+    if (ce < nch) {
+      // later chunks of this tile were streamed by the next CTAs
+      for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+        int j0, j1;
+        tc_range(U, j, gridDim.x, j0, j1);
+        if (j0 >= tile_end) break;
+        if (j1 <= j0) continue;
+        if (lane == 0) tc_wait_flag(b.flags + j, b.status);
+        __syncwarp();
+        const float* slot = b.partial + (size_t)j * (kTcRmax * 128);
+#pragma unroll
+        for (int r = 0; r < kTcRmax; ++r)
+          if (r < R) y[r] += __ldcg(slot + r * 128 + m);
+      }
+      tc_epi_sync();
+      if (m == 0) {
+        for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+          int j0, j1;
+          tc_range(U, j, gridDim.x, j0, j1);
+          if (j0 >= tile_end) break;
+          b.flags[j] = 0u;
+        }
+      }
+    }
+    if constexpr (GLU) {
+      // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
+      float* xg = t.xchg + (fin & 1) * (kTcRmax * 64);
+      if (q >= 2) {
+#pragma unroll
+        for (int r = 0; r < kTcRmax; ++r)
+          if (r < R) xg[r * 64 + m - 64] = y[r];
+      }
+      tc_epi_sync();
+      if (q < 2) {
+        const int jcol = tile * 64 + m;
+#pragma unroll
+        for (int r = 0; r < kTcRmax; ++r) {
+          if (r < R) {
+            const float g = y[r], uu = xg[r * 64 + m];
+            const float hv = g / (1.0f + expf(-g)) * uu;
+            b.out[(size_t)pid[r] * b.N + jcol] = hv;
+            const float hm = warp_max(fabsf(hv));
+            if (lane == 0 && b.out_amax) atomicMax(b.out_amax + pid[r], __float_as_uint(hm));
+            if (b.out_act)
+              planes_block(hv, lane, b.out_act + (size_t)pid[r] * planes_row_bytes(b.N) + (jcol / 32) * 128,
+                           b.out_code + (size_t)pid[r] * planes_code_bytes(b.N) + jcol / 32);
+          }
+        }
+      }
+      ++fin;
+    } else {
+      const int row = tile * 128 + m;
+#pragma unroll
+      for (int r = 0; r < kTcRmax; ++r)
+        if (r < R) b.out[(size_t)pid[r] * b.N + row] = y[r];
+    }
+    u = ue;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel: segment A (dense, CUDA cores, stream.cuh) then the routed step
+// on the tensor cores through the same stage ring.
+// ---------------------------------------------------------------------------
+template <class A, bool GLU, bool A_WAITS>
+__global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
+    tc_dual_kernel(const StreamArgs a0, const TcArgs b) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = (int)(blockDim.x >> 5) - 1;
+  trace_begin(a0.trace, a0.trace_id);
+  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
+  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp + 16));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&t.acc_full[i], 1);
+      mbar_init(&t.acc_empty[i], 4);
+      mbar_init(&t.sfb_full[i], 4);
+    }
+    mbar_init(t.sched, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(t.tbase);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t T = *t.tbase;
+  pdl_launch_dependents();
+  uint32_t stage = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
+      pdl_wait_prerequisites();
+      tc_produce(b, t, m.stages, m.full, m.empty, stage);
+      stream_drain(a0, m.empty, stage);
+    }
+    __syncwarp();
+  } else {
+    if (A_WAITS) pdl_wait_prerequisites();
+    int pp = 0, rp = 0;
+    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    pdl_wait_prerequisites();
+    // every consumer is past segment A's last shared-memory combine
+    consumer_sync(KW * 32);
+    if (warp == 1) {
+      tc_schedule(b, t, lane);
+      if (lane == 0) tc_mma(b, t, T, m.stages, m.full, m.empty, stage, KW);
+      __syncwarp();
+    } else if (warp < 6) {
+      tc_epilogue<GLU>(b, t, T, warp & 3, lane);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(T);
+  trace_end(a0.trace, a0.trace_id);
+}
+
+}  // namespace moe

@@ -24,10 +24,16 @@ def _normal(seed, tensor, sub, shape, mean, std, device, scratch=None):
     return out
 
 
-def make_weights(cfg, layer=0, device="cuda", layout=1):
-    """Device tensors of one seeded layer (dict in MoELayer's naming).  layout 1
-    packs the experts straight into the kernels' tiled layouts (FC1 gate/up
-    pairs: layout 2, FC2: layout 1); layout 0 keeps them canonical."""
+# weight layout -> (FC1 gate/up layout, FC2 layout)
+_LAYOUTS = {0: (0, 0), 1: (2, 1), 3: (4, 3)}
+
+
+def make_weights(cfg, layer=0, device="cuda", layout=3):
+    """Device tensors of one seeded layer (dict in MoELayer's naming).  layout 3
+    packs the experts straight into the tcgen05 path's UMMA layouts (FC1 gate/up
+    pairs: layout 4, FC2: layout 3), layout 1 into the mma.sync path's tiled
+    layouts (2 and 1); layout 0 keeps them canonical."""
+    gu_layout, d_layout = _LAYOUTS[layout]
     c = cfg
     s = c.seeds[layer]
     dev = torch.device(device)
@@ -46,11 +52,11 @@ def make_weights(cfg, layer=0, device="cuda", layout=1):
     scratch = torch.empty(2 * f * d, dtype=torch.float32, device=dev)
     for e in range(E):
         gu = _normal(s, T_EXPERT_GU, e, (2 * f, d), 0.0, c.std_gu(), dev, scratch)
-        mxfp4_pack_device(gu, w["w_gu_q"][e], w["w_gu_s"][e], layout=2 if layout else 0)
+        mxfp4_pack_device(gu, w["w_gu_q"][e], w["w_gu_s"][e], layout=gu_layout)
         dn = _normal(s, T_EXPERT_D, e, (d, f), 0.0, c.std_down(), dev, scratch)
-        mxfp4_pack_device(dn, w["w_d_q"][e], w["w_d_s"][e], layout=1 if layout else 0)
+        mxfp4_pack_device(dn, w["w_d_q"][e], w["w_d_s"][e], layout=d_layout)
     del scratch
-    w["mxfp4_layout"] = 1 if layout else 0
+    w["mxfp4_layout"] = layout
     return w
 
 
@@ -65,8 +71,10 @@ def make_activations(cfg, layer=0, attempt=0, device="cuda", B=None):
     return x, r
 
 
-def make_layer(cfg, layer=0, device="cuda", max_batch=None, weights=None):
-    w = weights if weights is not None else make_weights(cfg, layer, device)
+def make_layer(cfg, layer=0, device="cuda", max_batch=None, weights=None, expert_path=0):
+    w = weights if weights is not None else make_weights(
+        cfg, layer, device, layout=1 if expert_path == 1 else 3)
     return MoELayer(cfg.d, cfg.f, cfg.n_experts, cfg.top_k, cfg.f_shared,
                     max_batch if max_batch is not None else max(cfg.B, 1), w,
-                    routed_scale=cfg.routed_scale, rms_eps=cfg.rms_eps)
+                    routed_scale=cfg.routed_scale, rms_eps=cfg.rms_eps,
+                    expert_path=expert_path)

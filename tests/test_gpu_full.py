@@ -20,13 +20,14 @@ def _np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("name,rows", [("full_b1", [0]), ("full_b8", [0, 7]),
-                                       ("full_b64", [0, 33, 63])])
-def test_full_layer_sampled_rows(name, rows):
+@pytest.mark.parametrize("name,rows,path", [("full_b1", [0], 2), ("full_b1", [0], 1),
+                                            ("full_b8", [0, 7], 2), ("full_b64", [0, 33, 63], 2)])
+def test_full_layer_sampled_rows(name, rows, path):
+    """path 2: the tcgen05 expert path the benchmark times; 1: mma.sync."""
     cfg = CONFIGS[name]
     inp = oracle.clean_inputs(cfg)
     ref = oracle.forward(inp, rows=rows)
-    layer = synthetic.make_layer(cfg)
+    layer = synthetic.make_layer(cfg, expert_path=path)
     x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
     idx, w = layer.router_topk(x)
     dbg = run_debug(layer, x, res)

@@ -80,32 +80,35 @@ def test_layer_dequant_matches_oracle_packing_of_the_same_draws():
     layer.close()
 
 
-@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("layout", [1, 2, 3, 4])
 def test_device_tiled_pack_and_retile_match_host_tiled_pack(layout):
-    w = np.random.default_rng(layout).standard_normal((64, 512)).astype(np.float32)
+    w = np.random.default_rng(layout).standard_normal((128, 512)).astype(np.float32)
     qh, sh = M.mxfp4_pack(torch.from_numpy(w), layout=layout)
     qd, sd = M.mxfp4_pack_device(torch.from_numpy(w).cuda(), layout=layout)
     assert torch.equal(qd.cpu(), qh) and torch.equal(sd.cpu(), sh)
-    qc, sc = M.mxfp4_pack_device(torch.from_numpy(np.stack([w, -w])).cuda().view(128, 512))
-    qr, sr = M.mxfp4_retile_device(qc.view(2, 64, 256), sc.view(2, 64, 16), layout)
+    qc, sc = M.mxfp4_pack_device(torch.from_numpy(np.stack([w, -w])).cuda().view(256, 512))
+    qr, sr = M.mxfp4_retile_device(qc.view(2, 128, 256), sc.view(2, 128, 16), layout)
     qh2, sh2 = M.mxfp4_pack(torch.from_numpy(-w), layout=layout)
     assert torch.equal(qr[0].cpu(), qh) and torch.equal(sr[0].cpu(), sh)
     assert torch.equal(qr[1].cpu(), qh2) and torch.equal(sr[1].cpu(), sh2)
 
 
-def test_layer_from_canonical_weights_equals_layer_from_tiled_weights():
-    """moe_layer_create with canonical expert bytes (retiled into the handle's
-    own copy) and with pre-tiled bytes give bit-identical outputs."""
+@pytest.mark.parametrize("path", [2, 1])
+def test_layer_output_does_not_depend_on_the_weight_layout_given(path):
+    """moe_layer_create with canonical, tiled or UMMA expert bytes (relaid into
+    the handle's own copy unless already in the path's layouts) gives
+    bit-identical outputs on either expert path."""
     cfg = CONFIGS["tiny_b1"]
     x, r = synthetic.make_activations(cfg, B=5)
     outs = []
-    for layout in (0, 1):
+    for layout in (0, 1, 3):
         w = synthetic.make_weights(cfg, layout=layout)
-        layer = synthetic.make_layer(cfg, max_batch=5, weights=w)
+        layer = synthetic.make_layer(cfg, max_batch=5, weights=w, expert_path=path)
         res = r.clone()
         out = torch.empty_like(x)
         layer.forward(x, res, out)
         torch.cuda.synchronize()
         outs.append((out.cpu(), res.cpu()))
         layer.close()
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0][0], o[0]) and torch.equal(outs[0][1], o[1])

@@ -24,9 +24,10 @@ def tiny_cfg(B):
     return dataclasses.replace(TINY, name=f"tiny_b{B}", B=B)
 
 
-@pytest.fixture(scope="module")
-def tiny_layer():
-    layer = synthetic.make_layer(TINY, max_batch=64)
+@pytest.fixture(scope="module", params=[2, 1], ids=["tcgen05", "mma_sync"])
+def tiny_layer(request):
+    """The tiny layer on each expert path (tcgen05 block-scaled MMAs, mma.sync)."""
+    layer = synthetic.make_layer(TINY, max_batch=64, expert_path=request.param)
     yield layer
     layer.close()
 
