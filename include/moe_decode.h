@@ -64,19 +64,21 @@ typedef struct moe_layer* moe_layer_t;
  * f_shared % 256 == 0 and f_shared <= 4096; 1 <= top_k <= 32; top_k <= n_experts
  * <= 1024; 1 <= max_batch <= 64.
  *
- * expert_path picks how the routed experts run: 0 (default) or 2 = the
- * tcgen05 tensor cores (block-scaled MXFP4 MMAs with tensor-memory
- * accumulators; the kernels read the UMMA layouts, FC1 matrices in layout 4
- * and FC2 matrices in layout 3), 1 = mma.sync tensor cores with the weights
- * converted to f16 in registers (the tiled layouts, FC1 in layout 2 and FC2
- * in layout 1).  Both give results within the same tolerance of the exact
- * layer.
+ * expert_path picks how the routed experts run.  1: mma.sync tensor cores
+ * with the weights converted to f16 in registers (the GEMV regime; the
+ * kernels read the tiled layouts, FC1 matrices in layout 2 and FC2 matrices in
+ * layout 1).  2: tcgen05 tensor cores, block-scaled MXFP4 MMAs with
+ * tensor-memory accumulators (the UMMA layouts, FC1 in layout 4 and FC2 in
+ * layout 3).  0 (default): the layer keeps both layouts and takes path 1 for
+ * B = 1 and path 2 for B >= 2.  All give results within the same tolerance of
+ * the exact layer.
  *
  * mxfp4_layout says how the caller's expert weights are laid out: 0
  * (canonical), 1 (tiled: FC1 layout 2, FC2 layout 1) or 3 (UMMA: FC1 layout 4,
- * FC2 layout 3); see mxfp4_pack.  Weights already in the chosen path's layouts
- * are used in place; otherwise moe_layer_create relays them into a copy the
- * handle owns (E * 3 * d * f * 17/32 bytes of extra device memory). */
+ * FC2 layout 3); see mxfp4_pack.  Weights already in a kept path's layouts
+ * are used in place; for every other kept path moe_layer_create relays them
+ * into a copy the handle owns (E * 3 * d * f * 17/32 bytes of extra device
+ * memory each). */
 typedef struct {
   int32_t d;              /* hidden size */
   int32_t f;              /* routed-expert intermediate size */
@@ -87,7 +89,7 @@ typedef struct {
   float routed_scale;     /* combine weights sum to this (2.5 for the Kimi-style router) */
   float rms_eps;          /* RMSNorm epsilon (1e-6) */
   int32_t mxfp4_layout;   /* 0: canonical, 1: tiled, 3: UMMA expert weights (see above) */
-  int32_t expert_path;    /* 0: default (2), 1: mma.sync, 2: tcgen05 (see above) */
+  int32_t expert_path;    /* 0: both (by batch), 1: mma.sync, 2: tcgen05 (see above) */
 } moe_dims_t;
 
 /* Device pointers to the layer's weights (borrowed, never freed).

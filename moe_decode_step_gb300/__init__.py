@@ -47,8 +47,9 @@ class MoELayer:
     in layout 2, FC2 in layout 1), 3 UMMA (FC1 in layout 4, FC2 in layout 3);
     by default the dict's "mxfp4_layout" entry, else 0.  Weights not in the
     chosen path's layouts are relaid into a copy the layer owns.
-    expert_path: 0 (default) or 2 = tcgen05 tensor cores (UMMA layouts), 1 =
-    mma.sync tensor cores (tiled layouts).
+    expert_path: 1 = mma.sync tensor cores with register dequantisation
+    (tiled layouts), 2 = tcgen05 block-scaled MMAs (UMMA layouts), 0 (default)
+    = both kept, path 1 at B = 1 and path 2 from B = 2.
     """
 
     def __init__(self, d, f, n_experts, top_k, f_shared, max_batch, weights,

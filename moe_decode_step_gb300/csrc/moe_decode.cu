@@ -67,10 +67,10 @@ struct Workspace {
   uint16_t* res_stage;
   uint16_t* out_stage;
   // tensor-core expert path: activation planes of x and h, stream-K partials
-  uint8_t* x_act;
-  uint8_t* x_code;
-  uint8_t* h_act;
-  uint8_t* h_code;
+  uint8_t* x_act;    // x planes [B][4d]
+  uint8_t* x_code;   // their plane-0 code per row [B]
+  uint8_t* h_act;    // h planes [P][4f]
+  uint8_t* h_sfb;    // h plane scales per run, in the tensor-memory copy's atom order [P][4f]
   float* partial;
   unsigned* flags;
 };
@@ -84,8 +84,23 @@ struct StreamPlan {
 
 enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kNumSteps };
 
-// Expert paths: mma.sync on the tiled layouts, or tcgen05 on the UMMA layouts.
-enum { kPathMmaSync = 1, kPathTc = 2 };
+// Expert paths: mma.sync on the tiled layouts (the GEMV regime: weights
+// converted to f16 in registers), or tcgen05 on the UMMA layouts (block-scaled
+// MMAs).  By default a layer keeps both and takes the tensor-core path from
+// kTcMinBatch rows on: at B = 1 every routed expert has one activation row and
+// the register path streams faster; from two rows per forward the MMA path
+// does (measured at full size, B = 8 and 64).
+enum { kPathAuto = 0, kPathMmaSync = 1, kPathTc = 2 };
+constexpr int kTcMinBatch = 2;
+
+// Expert weights in one path's layouts (FC1 gate/up pairs, FC2 rows): the
+// caller's when given in those layouts, else a copy relaid at create time.
+struct ExpertWeights {
+  const uint8_t *gu_q = nullptr, *gu_s = nullptr, *d_q = nullptr, *d_s = nullptr;
+  int layout_gu = 0, layout_d = 0;
+  void* owned = nullptr;
+  bool ok = false;
+};
 
 }  // namespace
 
@@ -104,13 +119,9 @@ struct moe_layer {
   moe_layer* next = nullptr;
   StreamPlan plan[kNumSteps][3];   // by batch class (B = 1, B <= 8, B > 8)
   size_t q_gu_stride = 0, s_gu_stride = 0, q_d_stride = 0, s_d_stride = 0;
-  int path = kPathTc;
-  int layout_gu = kMxUmmaPairs, layout_d = kMxUmma;
-  // expert weights in the path's layouts (FC1 gate/up pairs, FC2 rows): the
-  // caller's when created in that layout, else a copy relaid at create time
-  // that the handle owns
-  const uint8_t *gu_q = nullptr, *gu_s = nullptr, *d_q = nullptr, *d_s = nullptr;
-  void* owned_w = nullptr;
+  ExpertWeights wm;   // mma.sync path (tiled layouts), when kept
+  ExpertWeights wt;   // tcgen05 path (UMMA layouts), when kept
+  int tc_min_batch = kTcMinBatch;
 };
 
 namespace {
@@ -145,9 +156,9 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.res_stage = carve<uint16_t>(p, B * d.d);
   w.out_stage = carve<uint16_t>(p, B * d.d);
   w.x_act = carve<uint8_t>(p, B * planes_row_bytes(d.d));
-  w.x_code = carve<uint8_t>(p, B * planes_code_bytes(d.d));
+  w.x_code = carve<uint8_t>(p, B);
   w.h_act = carve<uint8_t>(p, P * planes_row_bytes(d.f));
-  w.h_code = carve<uint8_t>(p, P * planes_code_bytes(d.f));
+  w.h_sfb = carve<uint8_t>(p, P * 4 * (size_t)d.f);   // at most P runs
   w.partial = carve<float>(p, (size_t)kTcMaxCtas * kTcRmax * 128);
   w.flags = carve<unsigned>(p, kTcMaxCtas);
   if (ws) *ws = w;
@@ -191,7 +202,8 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_FC2_RM(RS) ((RS) == 1 ? 1 : 8)
 #define MOE_FC2_KERNEL(RS, NBM) \
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
-// Tensor-core path: the same shared segments, then the routed step on tcgen05.
+// Tensor-core path: FC1 streams the shared gate/up first (while top-k runs),
+// FC2 the routed down projection first and the shared one last.
 #define MOE_TC1_KERNEL(RS) tc_dual_kernel<Sh1Cfg<RS>, true, false>
 #define MOE_TC2_KERNEL(RS) tc_dual_kernel<Sh2Cfg<RS>, false, true>
 
@@ -292,8 +304,8 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
 // segment, and tensor memory for two accumulators, a scale slot per stage and
 // two activation-scale buffers.  rmax: pairs per pass at this batch class.
 template <class A, typename Kern>
-int plan_tc(Kern kern, int KA, int NA, int K, int rmax, int E, int n_sm, int budget,
-            StreamPlan* p) {
+int plan_tc(Kern kern, int KA, int NA, int K, int rmax, bool rowscale, int E, int n_sm,
+            int budget, StreamPlan* p) {
   const int KW = std::max(seg_warps<A>(KA), 5);
   if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;
   if (!seg_fits<A>(KA, NA, KW)) return MOE_ERR_UNSUPPORTED;
@@ -306,9 +318,9 @@ int plan_tc(Kern kern, int KA, int NA, int K, int rmax, int E, int n_sm, int bud
   r.stage_bytes = (int)((st + 127) / 128 * 128);
   r.red_pp = stream_red_pp(KW, A::MMA, A::TM, A::RMAX);
   const int red_bytes = 2 * r.red_pp * 4 + 64;
-  const int extra = (int)tc_smem_bytes(E);
+  const int extra = (int)tc_smem_bytes(E, K, rowscale);
   r.NS = std::min(16, (budget - red_bytes - extra) / (r.stage_bytes + 16));
-  auto cols = [&](int ns) { return kTcSfaCol + ns * (r.tc_kc / 32) + 2 * (K / 64); };
+  auto cols = [&](int ns) { return tc_tmem_cols(K, r.tc_kc, ns, rowscale); };
   while (r.NS > 2 && cols(r.NS) > kTcCols) --r.NS;
   if (r.NS < 2 || cols(r.NS) > kTcCols) return MOE_ERR_UNSUPPORTED;
   // at least 116 KB: a second CTA on the SM would wait in tcgen05.alloc
@@ -331,24 +343,24 @@ int plan_all(moe_layer* L) {
   MOE_PLAN((plan_kernel<RouterCfg, RouterCfg>(MOE_ROUTER_KERNEL, d.d, d.n_experts, d.d,
                                               d.n_experts, n, kBudget2,
                                               &L->plan[kStepRouter][0])));
-  if (L->path == kPathTc) {
+  if (L->wt.ok) {
     const int E = d.n_experts;
     // one CTA per SM: all the shared memory a block may opt into
     const int bud = std::max(kBudget1, L->smem_optin);
-    MOE_PLAN((plan_tc<Sh1Cfg<1>>(MOE_TC1_KERNEL(1), d.d, d.f_shared, d.d, 1, E, n, bud,
+    MOE_PLAN((plan_tc<Sh1Cfg<1>>(MOE_TC1_KERNEL(1), d.d, d.f_shared, d.d, 1, true, E, n, bud,
                                  &L->plan[kStepTc1][0])));
-    MOE_PLAN((plan_tc<Sh1Cfg<2>>(MOE_TC1_KERNEL(2), d.d, d.f_shared, d.d, kTcRmax, E, n, bud,
+    MOE_PLAN((plan_tc<Sh1Cfg<2>>(MOE_TC1_KERNEL(2), d.d, d.f_shared, d.d, kTcRmax, true, E, n, bud,
                                  &L->plan[kStepTc1][1])));
-    MOE_PLAN((plan_tc<Sh1Cfg<4>>(MOE_TC1_KERNEL(4), d.d, d.f_shared, d.d, kTcRmax, E, n, bud,
+    MOE_PLAN((plan_tc<Sh1Cfg<4>>(MOE_TC1_KERNEL(4), d.d, d.f_shared, d.d, kTcRmax, true, E, n, bud,
                                  &L->plan[kStepTc1][2])));
-    MOE_PLAN((plan_tc<Sh2Cfg<1>>(MOE_TC2_KERNEL(1), d.f_shared, d.d, d.f, 1, E, n, bud,
+    MOE_PLAN((plan_tc<Sh2Cfg<1>>(MOE_TC2_KERNEL(1), d.f_shared, d.d, d.f, 1, false, E, n, bud,
                                  &L->plan[kStepTc2][0])));
-    MOE_PLAN((plan_tc<Sh2Cfg<2>>(MOE_TC2_KERNEL(2), d.f_shared, d.d, d.f, kTcRmax, E, n, bud,
+    MOE_PLAN((plan_tc<Sh2Cfg<2>>(MOE_TC2_KERNEL(2), d.f_shared, d.d, d.f, kTcRmax, false, E, n, bud,
                                  &L->plan[kStepTc2][1])));
-    MOE_PLAN((plan_tc<Sh2Cfg<4>>(MOE_TC2_KERNEL(4), d.f_shared, d.d, d.f, kTcRmax, E, n, bud,
+    MOE_PLAN((plan_tc<Sh2Cfg<4>>(MOE_TC2_KERNEL(4), d.f_shared, d.d, d.f, kTcRmax, false, E, n, bud,
                                  &L->plan[kStepTc2][2])));
-    return MOE_OK;
   }
+  if (!L->wm.ok) return MOE_OK;
   MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg>(MOE_FC1_KERNEL(1), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][0])));
   MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg>(MOE_FC1_KERNEL(2), d.d, d.f_shared, d.d, d.f, n,
@@ -417,6 +429,9 @@ int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_i
   return MOE_OK;
 }
 
+// The tensor-core path for a forward of B rows?
+bool use_tc(const moe_layer* L, int B) { return L->wt.ok && (!L->wm.ok || B >= L->tc_min_batch); }
+
 int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* idx, float* w) {
   const moe_dims_t& d = L->dims;
   StreamArgs a = base_args(L);
@@ -427,7 +442,7 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
   a.trace_id = 0;
-  if (L->path == kPathTc) {   // the activation planes the tensor-core FC1 streams
+  if (use_tc(L, B)) {   // the activation planes the tensor-core FC1 streams
     a.xq = L->ws.x_act;
     a.xq_code = L->ws.x_code;
   }
@@ -477,8 +492,8 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   sa.x = static_cast<const uint16_t*>(x);
   sa.out = L->ws.hs;
   StreamArgs ra = base_args(L);
-  ra.q = L->gu_q;
-  ra.s = L->gu_s;
+  ra.q = L->wm.gu_q;
+  ra.s = L->wm.gu_s;
   ra.q_stride = L->q_gu_stride;
   ra.s_stride = L->s_gu_stride;
   ra.K = d.d;
@@ -540,20 +555,21 @@ int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   sa.trace_id = 2;
   const StreamPlan& p = L->plan[kStepTc1][batch_class(B)];
   TcArgs b = tc_base_args(L, p);
-  b.q = L->gu_q;
-  b.s = L->gu_s;
+  b.q = L->wt.gu_q;
+  b.s = L->wt.gu_s;
   b.q_stride = L->q_gu_stride;
   b.s_stride = L->s_gu_stride;
   b.K = d.d;
   b.tiles = d.f / 64;
   b.N = d.f;
   b.act_div = d.top_k;
+  b.rowscale = 1;
   b.act = L->ws.x_act;
   b.act_code = L->ws.x_code;
   b.out = L->ws.h;
   b.out_amax = L->ws.h_amax;
   b.out_act = L->ws.h_act;
-  b.out_code = L->ws.h_code;
+  b.out_sfb = L->ws.h_sfb;
   // at B = 1 one SM holds the top-k CTA when FC1 launches (see launch_fc1)
   const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
   switch (batch_class(B)) {
@@ -577,16 +593,17 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   sa.trace_id = 3;
   const StreamPlan& p = L->plan[kStepTc2][batch_class(B)];
   TcArgs b = tc_base_args(L, p);
-  b.q = L->d_q;
-  b.s = L->d_s;
+  b.q = L->wt.d_q;
+  b.s = L->wt.d_s;
   b.q_stride = L->q_d_stride;
   b.s_stride = L->s_d_stride;
   b.K = d.f;
   b.tiles = d.d / 128;
   b.N = d.d;
   b.act_div = 1;
+  b.rowscale = 0;
   b.act = L->ws.h_act;
-  b.act_code = L->ws.h_code;
+  b.act_sfb = L->ws.h_sfb;
   b.out = L->ws.y_pair;
   switch (batch_class(B)) {
     case 0: return launch_tc(MOE_TC2_KERNEL(1), p, sa, b, st, p.grid);
@@ -606,8 +623,8 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   sa.h = L->ws.hs;
   sa.out = L->ws.y_s;
   StreamArgs ra = base_args(L);
-  ra.q = L->d_q;
-  ra.s = L->d_s;
+  ra.q = L->wm.d_q;
+  ra.s = L->wm.d_s;
   ra.q_stride = L->q_d_stride;
   ra.s_stride = L->s_d_stride;
   ra.K = d.f;
@@ -694,7 +711,7 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
   if ((rc = launch_prefetch(L))) return rc;
-  const bool tc = L->path == kPathTc;
+  const bool tc = use_tc(L, B);
   if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
   if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
@@ -727,6 +744,50 @@ int relayout_device(const uint8_t* q_in, const uint8_t* s_in, int64_t n_mat, int
                                                      q_out + m * qb, s_out + m * sb, to);
     MOE_CUDA(cudaGetLastError());
   }
+  return MOE_OK;
+}
+
+// One path's expert weights: borrowed when the caller's layout (dims
+// mxfp4_layout) is the path's (`want`: 1 tiled, 3 UMMA), else relaid into a
+// copy the handle owns.
+int setup_weights(moe_layer* L, const moe_weights_t& w, int want, ExpertWeights& ew) {
+  const moe_dims_t& d = L->dims;
+  ew.layout_gu = want == 3 ? kMxUmmaPairs : kMxTiledPairs;
+  ew.layout_d = want == 3 ? kMxUmma : kMxTiled;
+  if (d.mxfp4_layout == want) {
+    ew.gu_q = w.w_gu_q;
+    ew.gu_s = w.w_gu_s;
+    ew.d_q = w.w_d_q;
+    ew.d_s = w.w_d_s;
+    ew.ok = true;
+    return MOE_OK;
+  }
+  const size_t E = d.n_experts, f = d.f, dd = d.d;
+  const size_t total = E * (L->q_gu_stride + L->s_gu_stride + L->q_d_stride + L->s_d_stride);
+  if (cudaMalloc(&ew.owned, total) != cudaSuccess) {
+    cudaGetLastError();
+    ew.owned = nullptr;
+    return MOE_ERR_ALLOC;
+  }
+  uint8_t* gq = static_cast<uint8_t*>(ew.owned);
+  uint8_t* gs = gq + E * L->q_gu_stride;
+  uint8_t* dq = gs + E * L->s_gu_stride;
+  uint8_t* ds = dq + E * L->q_d_stride;
+  const int from_gu = d.mxfp4_layout == 0 ? kMxCanonical
+                      : d.mxfp4_layout == 1 ? kMxTiledPairs : kMxUmmaPairs;
+  const int from_d = d.mxfp4_layout == 0 ? kMxCanonical : d.mxfp4_layout == 1 ? kMxTiled : kMxUmma;
+  int rc;
+  if ((rc = relayout_device(w.w_gu_q, w.w_gu_s, (int64_t)E, 2 * (int64_t)f, (int64_t)dd, from_gu,
+                            ew.layout_gu, gq, gs)) ||
+      (rc = relayout_device(w.w_d_q, w.w_d_s, (int64_t)E, (int64_t)dd, (int64_t)f, from_d,
+                            ew.layout_d, dq, ds)))
+    return rc;
+  MOE_CUDA(cudaStreamSynchronize(nullptr));
+  ew.gu_q = gq;
+  ew.gu_s = gs;
+  ew.d_q = dq;
+  ew.d_s = ds;
+  ew.ok = true;
   return MOE_OK;
 }
 
@@ -796,47 +857,18 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
-  // the expert path (tensor cores unless asked otherwise) fixes the layouts
-  // the kernels read; weights given in another layout are relaid into a copy
-  L->path = dims->expert_path == kPathMmaSync ? kPathMmaSync : kPathTc;
-  const int want = L->path == kPathTc ? 3 : 1;
-  L->layout_gu = L->path == kPathTc ? kMxUmmaPairs : kMxTiledPairs;
-  L->layout_d = L->path == kPathTc ? kMxUmma : kMxTiled;
-  if (dims->mxfp4_layout == want) {
-    L->gu_q = w.w_gu_q;
-    L->gu_s = w.w_gu_s;
-    L->d_q = w.w_d_q;
-    L->d_s = w.w_d_s;
-  } else {
-    const size_t E = dims->n_experts;
-    const size_t total = E * (L->q_gu_stride + L->s_gu_stride + L->q_d_stride + L->s_d_stride);
-    if (cudaMalloc(&L->owned_w, total) != cudaSuccess) {
-      cudaGetLastError();
-      moe_layer_destroy(L);
-      return MOE_ERR_ALLOC;
-    }
-    uint8_t* p = static_cast<uint8_t*>(L->owned_w);
-    uint8_t* gq = p;
-    uint8_t* gs = gq + E * L->q_gu_stride;
-    uint8_t* dq = gs + E * L->s_gu_stride;
-    uint8_t* ds = dq + E * L->q_d_stride;
-    const int from_gu = dims->mxfp4_layout == 0 ? kMxCanonical
-                        : dims->mxfp4_layout == 1 ? kMxTiledPairs : kMxUmmaPairs;
-    const int from_d = dims->mxfp4_layout == 0 ? kMxCanonical
-                       : dims->mxfp4_layout == 1 ? kMxTiled : kMxUmma;
-    if ((rc = relayout_device(w.w_gu_q, w.w_gu_s, (int64_t)E, 2 * (int64_t)f, (int64_t)dd,
-                              from_gu, L->layout_gu, gq, gs)) ||
-        (rc = relayout_device(w.w_d_q, w.w_d_s, (int64_t)E, (int64_t)dd, (int64_t)f, from_d,
-                              L->layout_d, dq, ds))) {
-      moe_layer_destroy(L);
-      return rc;
-    }
-    if ((e = cudaStreamSynchronize(nullptr)) != cudaSuccess) return fail(e);
-    L->gu_q = gq;
-    L->gu_s = gs;
-    L->d_q = dq;
-    L->d_s = ds;
+  // the expert paths kept (both by default, see kTcMinBatch) fix the layouts
+  // the kernels read
+  const int path = dims->expert_path;
+  if (path != kPathTc && (rc = setup_weights(L, w, 1, L->wm))) {
+    moe_layer_destroy(L);
+    return rc;
   }
+  if (path != kPathMmaSync && (rc = setup_weights(L, w, 3, L->wt))) {
+    moe_layer_destroy(L);
+    return rc;
+  }
+  L->tc_min_batch = path == kPathTc ? 1 : kTcMinBatch;
   if ((rc = plan_all(L))) {
     moe_layer_destroy(L);
     return rc;
@@ -857,7 +889,8 @@ int moe_layer_destroy(moe_layer_t L) {
   for (int i = 0; i < kNumTimeEvents; ++i)
     if (L->ev_time[i]) cudaEventDestroy(L->ev_time[i]);
   if (L->ws_base) cudaFree(L->ws_base);
-  if (L->owned_w) cudaFree(L->owned_w);
+  if (L->wm.owned) cudaFree(L->wm.owned);
+  if (L->wt.owned) cudaFree(L->wt.owned);
   cudaSetDevice(prev);
   delete L;
   return MOE_OK;
@@ -904,11 +937,12 @@ int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float*
     return MOE_ERR_INVALID_ARG;
   const int64_t rows = which == 0 ? 2LL * L->dims.f : L->dims.d;
   const int64_t k = which == 0 ? L->dims.d : L->dims.f;
-  const uint8_t* q = (which == 0 ? L->gu_q : L->d_q) +
+  const ExpertWeights& ew = L->wt.ok ? L->wt : L->wm;
+  const uint8_t* q = (which == 0 ? ew.gu_q : ew.d_q) +
                      (size_t)expert * (which == 0 ? L->q_gu_stride : L->q_d_stride);
-  const uint8_t* s = (which == 0 ? L->gu_s : L->d_s) +
+  const uint8_t* s = (which == 0 ? ew.gu_s : ew.d_s) +
                      (size_t)expert * (which == 0 ? L->s_gu_stride : L->s_d_stride);
-  const int layout = which == 0 ? L->layout_gu : L->layout_d;
+  const int layout = which == 0 ? ew.layout_gu : ew.layout_d;
   const int64_t blocks = std::min<int64_t>((rows * (k / 32) + 255) / 256, 4096);
   mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       q, s, rows, k, layout, out);

@@ -1,14 +1,14 @@
 // Activation planes: the activation operand of the block-scaled tensor-core
 // expert matmuls (E2M1 weights x E2M1 activations, E8M0 scales per 32 K).
 //
-// A row v of K activations becomes 8 E2M1 planes q_0..q_7 with per-block
-// scales s_p = 2^(c - 127 - 2p), v = sum_p s_p q_p + r.  c (one E8M0 code per
-// 32-element block) is the smallest power of two with 6 * 2^(c-127) >= max|v|,
-// so plane 0 never saturates.  Each plane rounds the running residual to the
+// A row v of K activations becomes 8 E2M1 planes q_0..q_7 with scales s_p =
+// 2^(c - 127 - 2p), v = sum_p s_p q_p + r.  c is the smallest power of two
+// with 6 * 2^(c-127) >= max|v| over the set it covers (one code per
+// 32-element block, or one per row), so plane 0 never saturates.  Each plane rounds the running residual to the
 // E2M1 grid; the widest grid gap (4 -> 6) bounds that rounding error by s_p =
 // 4 s_{p+1}, so the next plane's input again lies within +-4 of its grid and
 // never saturates either.  After 8 planes |r| <= s_7 = 2^-14 s_0, below
-// max|v| * 2^-14 / 3 per element: products with the exact E2M1 weights then
+// max|v| * 2^-14 / 3 per element (max over the code's block or row): products with the exact E2M1 weights then
 // sum on the tensor cores in fp32 with an error far below the fp32 rounding
 // of the sums themselves.  (A plane's code is clamped at 1, the smallest
 // normal E8M0 scale; a clamped plane repeats the previous scale, which keeps
@@ -18,7 +18,7 @@
 // b * 128: plane p's 16 bytes at + p * 16, element 2j in the low nibble of
 // byte j and element 2j + 1 in the high nibble.  So the 8 planes of one block
 // form one 8-row x 16-byte core matrix of the tensor-core B operand, and any
-// run of blocks is contiguous.  One code byte per block beside it.
+// run of blocks is contiguous.
 #pragma once
 
 #include <stdint.h>
@@ -49,9 +49,9 @@ __device__ __forceinline__ float e2m1_value(uint32_t mag) {
 }
 
 // One warp, one 32-element block: lane i holds element i.  Writes the block's
-// 128 plane bytes at `blk` and its code byte at `code`.
-__device__ __forceinline__ void planes_block(float v, int lane, uint8_t* blk, uint8_t* code) {
-  const int c0 = planes_code0(warp_max(fabsf(v)));
+// 128 plane bytes at `blk` with plane-0 code c0 (which must cover the block:
+// 6 * 2^(c0-127) >= max |v|).
+__device__ __forceinline__ void planes_block_c(float v, int lane, uint8_t* blk, int c0) {
   float r = v;
 #pragma unroll
   for (int p = 0; p < kPlanes; ++p) {
@@ -72,7 +72,13 @@ __device__ __forceinline__ void planes_block(float v, int lane, uint8_t* blk, ui
       *reinterpret_cast<uint32_t*>(blk + p * 16 + lane / 2) =
           (byte & 0xFFu) | (b1 & 0xFFu) << 8 | (b2 & 0xFFu) << 16 | (b3 & 0xFFu) << 24;
   }
-  if (lane == 0) *code = (uint8_t)c0;
+}
+
+// The same with the block's own code (from its max |v|), which it returns.
+__device__ __forceinline__ int planes_block(float v, int lane, uint8_t* blk) {
+  const int c0 = planes_code0(warp_max(fabsf(v)));
+  planes_block_c(v, lane, blk, c0);
+  return c0;
 }
 
 // Scale code of plane p given the block's plane-0 code.

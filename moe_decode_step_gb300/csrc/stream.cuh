@@ -69,7 +69,7 @@ struct StreamArgs {
   unsigned long long* trace; // optional kernel trace (see trace_begin), or null
   int trace_id;
   uint8_t* xq;               // router only: activation planes of x [B][4K] (planes.cuh), or null
-  uint8_t* xq_code;          // and their plane-0 codes [B][K/32]
+  uint8_t* xq_code;          // and their plane-0 codes, one per row [B]
 };
 
 // Lane layout of the bf16 steps: a lane owns NQ chunks of CW consecutive K
@@ -858,16 +858,37 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   } else {
     pdl_wait_prerequisites();
     if (a.xq) {
-      // the activation planes of x for the tensor-core experts: a share of the
-      // B * K/32 blocks per CTA, one block per warp, while the first stages land
+      // the activation planes of x for the tensor-core experts, one plane-0
+      // code per row: a share of the B * K/32 blocks per CTA, one block per
+      // warp, while the first stages land; each row this CTA touches first
+      // gets its max |x| from all consumer warps
       const int nb = a.K / 32, total = a.B * nb;
       const int lo = (int)((long long)total * blockIdx.x / gridDim.x);
       const int hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
-      for (int i = lo + warp - 1; i < hi; i += KW) {
-        const int row = i / nb, blk = i - row * nb;
-        const float v = bf16_bits_to_f32(a.x[(size_t)row * a.K + blk * 32 + lane]);
-        planes_block(v, lane, a.xq + (size_t)row * planes_row_bytes(a.K) + blk * 128,
-                     a.xq_code + (size_t)row * planes_code_bytes(a.K) + blk);
+      unsigned* slots = reinterpret_cast<unsigned*>(m.red);
+      for (int row = lo / nb; lo < hi && row <= (hi - 1) / nb; ++row) {
+        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)row * a.K);
+        uint32_t mx = 0;
+        for (int i = (warp - 1) * 32 + lane; i < a.K / 8; i += KW * 32) {
+          const uint4 v = xr[i];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) slots[warp - 1] = mx;
+        consumer_sync(KW * 32);
+        uint32_t amax = 0;
+        for (int w = 0; w < KW; ++w) amax = max(amax, slots[w]);
+        consumer_sync(KW * 32);
+        const int c0 = planes_code0(bf16_bits_to_f32(amax));
+        if (warp == 1 && lane == 0) a.xq_code[row] = (uint8_t)c0;
+        const int b0 = max(lo, row * nb) - row * nb, b1 = min(hi, (row + 1) * nb) - row * nb;
+        for (int blk = b0 + warp - 1; blk < b1; blk += KW) {
+          const float v = bf16_bits_to_f32(a.x[(size_t)row * a.K + blk * 32 + lane]);
+          planes_block_c(v, lane, a.xq + (size_t)row * planes_row_bytes(a.K) + blk * 128, c0);
+        }
       }
     }
     int pp = 0, rp = 0;

@@ -21,10 +21,19 @@
 // the run table, then its lane 0 issues the tensor-memory scale copies and
 // MMAs and commits them to the stage's "empty" barrier and, per tile, to an
 // accumulator barrier; warps 2..5 (tensor-memory lane quarters 2, 3, 0, 1)
-// write the activation scales into tensor memory per run and run the
-// epilogues.  Accumulators, scale slots and activation-scale buffers are all
-// double-buffered or ringed, so the MMA warp never waits for an epilogue in
-// steady state.  Every wait is bounded (status 5 on timeout).
+// run the epilogues.  Accumulators are double-buffered and scale slots ringed
+// with the stages, so the MMA warp never waits for an epilogue in steady
+// state.  Every wait is bounded (status 5 on timeout).
+//
+// Activation scales: FC1's x planes carry one code per row (planes.cuh), so
+// the MMAs take scale 1 from two constant tensor-memory columns and the
+// epilogue multiplies each plane's column by its scale.  FC2's h planes carry
+// per-block codes (each FC1 epilogue only sees 64 values of an h row); FC1
+// writes them per run in the tensor-memory copy's atom order, and FC2 loads a
+// run's whole set into tensor memory once, at the run's first unit (double
+// buffered by run).  A block-scaled MMA costs about the same whatever N is,
+// and so does each scale copy: per stage the MMA thread issues only the
+// weight-scale copies and the MMAs.
 #pragma once
 
 #include <stdint.h>
@@ -140,8 +149,10 @@ struct TcArgs {
   int tiles;                 // 128-row weight tiles per expert
   int N;                     // outputs per pair (gate/up: f, down: d)
   int act_div;               // activation row of pair p: p / act_div
+  int rowscale;              // 1: one plane-0 code per activation row; 0: per-block scales
   const uint8_t* act;        // activation planes [rows][4K]
-  const uint8_t* act_code;   // plane-0 codes [rows][K/32]
+  const uint8_t* act_code;   // rowscale: plane-0 code per activation row
+  const uint8_t* act_sfb;    // !rowscale: the activation scales of each run, K/128 atoms
   const int* n_active;
   const int* active_expert;
   const int* active_off;
@@ -149,52 +160,73 @@ struct TcArgs {
   float* out;                // [pairs][N]
   unsigned* out_amax;        // gate/up: max |h| bits per pair, or null
   uint8_t* out_act;          // gate/up: h planes [pairs][4N], or null
-  uint8_t* out_code;         // gate/up: h plane-0 codes [pairs][N/32]
+  uint8_t* out_sfb;          // gate/up: h plane scales per run (N/128 atoms), with out_act
   float* partial;            // [kTcMaxCtas][kTcRmax][128]
   unsigned* flags;           // [kTcMaxCtas], zero between forwards
   int* status;
   int NS, stage_bytes;       // the stage ring (the same as the shared segment's)
 };
 
-// Activation-scale codes a run stages per epilogue warp: kTcRmax rows of at
-// most kTcCodeRow bytes (K <= 8192).
-constexpr int kTcCodeRow = 256;
+// A run's activation scales for the block-scaled MMA come as atoms of 4 K
+// blocks (512 bytes, the 32x128b tensor-memory copy's order): the scale of
+// row n = 8 r + p (pair r of the run, plane p) for block 4A + kb at byte
+// 512 A + 16 (n % 32) + 4 (n / 32) + kb.  A run's K/128 atoms are contiguous,
+// run rho's at rho * 4 K.
+__host__ __device__ inline size_t tc_sfb_offset(int A, int n, int kb) {
+  return (size_t)A * 512 + 16 * (n % 32) + 4 * (n / 32) + kb;
+}
 
-// Bytes of shared memory after the stream segment's reduction area.
-__host__ __device__ inline size_t tc_smem_bytes(int E) {
-  return 128 + 2 * kTcRmax * 64 * 4 + 4 * kTcRmax * kTcCodeRow +
+// Bytes of shared memory after the stream segment's reduction area: barriers,
+// the SwiGLU exchange, two runs' activation-scale atoms (per-block steps,
+// 4 K bytes each) and the run table.
+__host__ __device__ inline size_t tc_sfb_smem(int K, bool rowscale) {
+  return rowscale ? 0 : 2 * 4 * (size_t)K;
+}
+__host__ __device__ inline size_t tc_smem_bytes(int E, int K, bool rowscale) {
+  return 128 + 2 * kTcRmax * 64 * 4 + tc_sfb_smem(K, rowscale) +
          ((size_t)(E + 1) * 4 + 127) / 128 * 128;
 }
-// Bytes of one stage: weight nibbles, weight scales, planes of the pairs (at
-// least two pairs' room: the MMA reads N >= 16 rows).
+// One stage: weight nibbles (64 KC), weight scales (4 KC), then the planes of
+// the pairs (4 KC each, room for at least two: the MMA reads N >= 16 rows).
+constexpr int kTcPlaneOff = 68;   // planes start at 68 KC
 __host__ __device__ inline size_t tc_stage_bytes(int KC, int rmax) {
-  return (size_t)KC * 68 + (size_t)(rmax < 2 ? 2 : rmax) * 4 * KC;
+  return (size_t)KC * kTcPlaneOff + (size_t)(rmax < 2 ? 2 : rmax) * 4 * KC;
+}
+// Tensor-memory columns: two accumulators, a weight-scale slot per stage, and
+// either two constant activation-scale columns or two runs' scale sets (4
+// columns per 4 K blocks).
+__host__ __device__ inline int tc_tmem_cols(int K, int KC, int NS, bool rowscale) {
+  return kTcSfaCol + NS * (KC / 32) + (rowscale ? 2 : 2 * (K / 32));
 }
 
 struct TcSmem {
   uint64_t* acc_full;   // [2] accumulator written (commit)
   uint64_t* acc_empty;  // [2] accumulator read (4 epilogue warps)
-  uint64_t* sfb_full;   // [2] activation scales written (4 epilogue warps)
   uint64_t* sched;      // run table ready (1)
+  uint64_t* sfb_full;   // [2] a run's activation-scale atoms landed (bulk copy)
+  uint64_t* sfb_empty;  // [2] and copied into tensor memory (commit)
   uint32_t* tbase;      // tensor-memory base address
   int* n_runs;
+  uint32_t* stage_after;   // the stage count after the routed step (segment A last)
   float* xchg;          // [2][kTcRmax][64] up-half sums for the SwiGLU epilogue
-  uint8_t* codes;       // [4 epilogue warps][kTcRmax][kTcCodeRow] staged activation codes
+  uint8_t* sfb;         // [2][4 K] activation-scale atoms of two runs (per-block steps)
   int* run_off;         // [n_active + 1] first run of each active slot
 };
 
-__device__ __forceinline__ TcSmem tc_smem(uint8_t* p) {
+__device__ __forceinline__ TcSmem tc_smem(uint8_t* p, int K, bool rowscale) {
   TcSmem t;
   uint64_t* b = reinterpret_cast<uint64_t*>(p);
   t.acc_full = b;
   t.acc_empty = b + 2;
-  t.sfb_full = b + 4;
-  t.sched = b + 6;
-  t.tbase = reinterpret_cast<uint32_t*>(b + 7);
-  t.n_runs = reinterpret_cast<int*>(b + 7) + 1;
+  t.sched = b + 4;
+  t.sfb_full = b + 5;
+  t.sfb_empty = b + 7;
+  t.tbase = reinterpret_cast<uint32_t*>(b + 9);
+  t.n_runs = reinterpret_cast<int*>(b + 9) + 1;
+  t.stage_after = reinterpret_cast<uint32_t*>(b + 10);
   t.xchg = reinterpret_cast<float*>(p + 128);
-  t.codes = p + 128 + 2 * kTcRmax * 64 * 4;
-  t.run_off = reinterpret_cast<int*>(t.codes + 4 * kTcRmax * kTcCodeRow);
+  t.sfb = p + 128 + 2 * kTcRmax * 64 * 4;
+  t.run_off = reinterpret_cast<int*>(t.sfb + tc_sfb_smem(K, rowscale));
   return t;
 }
 
@@ -271,21 +303,29 @@ __device__ __forceinline__ void tc_produce(const TcArgs& b, const TcSmem& t, uin
   if (u0 >= u1) return;
   const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
   const uint32_t abytes = 64u * b.KC, sbytes = 4u * b.KC, pbytes = 4u * b.KC;
+  const uint32_t poff = (uint32_t)kTcPlaneOff * b.KC;
   const uint32_t NS = (uint32_t)b.NS;
   uint32_t buf = stage % NS, use = stage / NS;
   int rho = u0 / upr, idx = u0 - rho * upr, c = idx % nch;
-  for (int u = u0; u < u1; ++rho, idx = 0, c = 0) {
+  for (int u = u0, lr = 0; u < u1; ++rho, ++lr, idx = 0, c = 0) {
     const TcRun run = tc_run(b, t.run_off, nact, rho);
     const int n = min(u1 - u, upr - idx);
     const uint8_t* qs = b.q + (size_t)run.e * b.q_stride + (size_t)idx * abytes;
     const uint8_t* ss = b.s + (size_t)run.e * b.s_stride + (size_t)idx * sbytes;
+    if (!b.rowscale) {
+      // the run's activation-scale atoms, once per run (buffer lr & 1)
+      const uint32_t bytes = 4u * b.K, sb = (uint32_t)lr & 1u;
+      if (lr >= 2) mbar_wait(&t.sfb_empty[sb], (uint32_t)((lr >> 1) - 1) & 1u, b.status);
+      mbar_arrive_expect_tx(&t.sfb_full[sb], bytes);
+      bulk_g2s(t.sfb + sb * bytes, b.act_sfb + (size_t)rho * bytes, bytes, &t.sfb_full[sb], pol_a);
+    }
     const uint8_t* as[kTcRmax];
 #pragma unroll
     for (int r = 0; r < kTcRmax; ++r)
       as[r] = b.act + (r < run.R ? (size_t)(__ldcg(b.pair_list + run.p0 + r) / b.act_div) *
                                        planes_row_bytes(b.K)
                                  : 0);
-    const uint32_t tx = abytes + sbytes + (uint32_t)run.R * pbytes;
+    const uint32_t tx = poff + (uint32_t)run.R * pbytes;
     for (int i = 0; i < n; ++i) {
       if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, b.status);
       uint8_t* dst = stages + (size_t)buf * b.stage_bytes;
@@ -295,8 +335,7 @@ __device__ __forceinline__ void tc_produce(const TcArgs& b, const TcSmem& t, uin
       const size_t aoff = (size_t)c * pbytes;
 #pragma unroll
       for (int r = 0; r < kTcRmax; ++r)
-        if (r < run.R)
-          bulk_g2s(dst + abytes + sbytes + r * pbytes, as[r] + aoff, pbytes, &full[buf], pol_a);
+        if (r < run.R) bulk_g2s(dst + poff + r * pbytes, as[r] + aoff, pbytes, &full[buf], pol_a);
       qs += abytes;
       ss += sbytes;
       if (++c == nch) c = 0;
@@ -323,27 +362,41 @@ __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_
   if (u0 >= u1) return;
   const uint32_t KC = (uint32_t)b.KC, NS = (uint32_t)b.NS;
   const uint32_t nsteps = KC / 64, natoms = KC / 128;
+  const bool rows = b.rowscale != 0;
   // descriptors of stage 0; stage s, K step j add (s * stage_bytes + step offset) / 16
   const uint32_t sa0 = smem_addr(stages);
   const uint32_t st16 = (uint32_t)b.stage_bytes >> 4;
-  const uint64_t dA0 = umma_desc(sa0, 2048, 128);            // weights: K blocks 2 KB apart
-  const uint64_t dB0 = umma_desc(sa0 + 68 * KC, 128, 4 * KC); // planes: pairs 4 KC apart
-  const uint64_t dS0 = umma_desc(sa0 + 64 * KC, 0, 128);      // weight scales: 32 rows x 16 B
+  const uint64_t dA0 = umma_desc(sa0, 2048, 128);                     // weights: K blocks 2 KB apart
+  const uint64_t dB0 = umma_desc(sa0 + kTcPlaneOff * KC, 128, 4 * KC); // planes: pairs 4 KC apart
+  const uint64_t dS0 = umma_desc(sa0 + 64 * KC, 0, 128);               // weight scales: 32 rows x 16 B
+  const uint64_t dT0 = umma_desc(smem_addr(t.sfb), 0, 128);            // a run's activation scales
   const uint32_t sfa0 = T + kTcSfaCol;
   const uint32_t sfb0 = T + kTcSfaCol + NS * (KC / 32);
-  const uint32_t sfb_w = (uint32_t)b.K / 64;
+  const uint32_t katoms = (uint32_t)b.K / 128;   // activation-scale atoms of a run
   uint32_t buf = stage % NS, ph = (stage / NS) & 1u;
   int rho = u0 / upr, idx = u0 - rho * upr, c = idx % nch;
-  int lr = 0, jobs = 0;
+  int jobs = 0;
   uint32_t jb = 0, acc = 0;
   bool newjob = true;
-  for (int u = u0; u < u1; ++rho, ++lr, idx = 0, c = 0, newjob = true) {
+  for (int u = u0, lr = 0; u < u1; ++rho, ++lr, idx = 0, c = 0, newjob = true) {
     const int R = tc_run(b, t.run_off, nact, rho).R;
+    uint32_t sfb_run = sfb0;
+    if (!rows) {
+      // the run's activation scales into tensor memory (buffer lr & 1; the
+      // MMAs of run lr - 2, which read it, were issued before these copies)
+      const uint32_t sb = (uint32_t)lr & 1u;
+      mbar_wait(&t.sfb_full[sb], (uint32_t)(lr >> 1) & 1u, b.status);
+      tc_fence_after();
+      sfb_run = sfb0 + sb * 4 * katoms;
+      const uint64_t d = dT0 + (uint64_t)((sb * 4 * (uint32_t)b.K) >> 4);
+      for (uint32_t a = 0; a < katoms; ++a) umma_sf_copy(sfb_run + 4 * a, d + 32 * a);
+      umma_commit(&t.sfb_empty[sb]);
+    }
     const uint32_t npad = (uint32_t)max(16, (8 * R + 15) & ~15);
-    const uint32_t id0 = umma_idesc_mxf4(0, 0, npad), id1 = umma_idesc_mxf4(2, 2, npad);
-    mbar_wait(&t.sfb_full[lr & 1], (uint32_t)(lr >> 1) & 1u, b.status);
-    tc_fence_after();
-    const uint32_t sfb_run = sfb0 + (uint32_t)(lr & 1) * sfb_w;
+    // per K step: the weight scale pair 2 (j & 1); the activation scales the
+    // same pair of the per-block atoms, or the constant columns (byte 0)
+    const uint32_t id0 = umma_idesc_mxf4(0, 0, npad);
+    const uint32_t id1 = umma_idesc_mxf4(2, rows ? 0 : 2, npad);
     const int n = min(u1 - u, upr - idx);
     for (int i = 0; i < n; ++i) {
       if (newjob) {   // a new tile job: a free accumulator, zero-initialised by its first MMA
@@ -359,12 +412,13 @@ __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_
       const uint64_t off = (uint64_t)(buf * st16);
       const uint32_t sfa = sfa0 + buf * (KC / 32);
       for (uint32_t a = 0; a < natoms; ++a) umma_sf_copy(sfa + 4 * a, dS0 + off + 32 * a);
-      const uint32_t sfb = sfb_run + 2 * (uint32_t)c * natoms;
+      const uint32_t sfb = rows ? sfb_run : sfb_run + 4 * (uint32_t)c * natoms;
+      const uint32_t sfb_step = rows ? 0u : 4u;
       const uint32_t dcol = T + 64 * jb;
 #pragma unroll 8
       for (uint32_t j = 0; j < nsteps; ++j)
         umma_mxf4(dcol, dA0 + off + 256 * j, dB0 + off + 16 * j, (j & 1) ? id1 : id0,
-                  sfa + 4 * (j >> 1), sfb + 2 * (j >> 1), acc | j);
+                  sfa + 4 * (j >> 1), sfb + sfb_step * (j >> 1), acc | j);
       acc = 1;
       // the stage is free once these MMAs have read it; the other KW - 1
       // arrivals the barrier counts (one per CUDA-core consumer warp) come now
@@ -389,57 +443,6 @@ __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_
 // ---------------------------------------------------------------------------
 // Epilogue (warps 2..5)
 // ---------------------------------------------------------------------------
-// Activation scales of run rho into buffer `buf`: rows n = 8 r + p (pair r,
-// plane p) at lane n % 32 of every quarter, column 2A + n / 32 for the atom A
-// of K blocks 4A..4A+3; rows past the run's pairs get scale 1.  The warp first
-// stages the run's plane-0 codes (R rows of K/32 bytes) in its shared scratch
-// with coalesced 16-byte loads, so the global latency is paid once.
-__device__ __forceinline__ void tc_write_sfb(const TcArgs& b, const TcSmem& t, uint32_t T,
-                                             uint32_t qaddr, int q, int nact, int rho, int buf,
-                                             int lane) {
-  const TcRun run = tc_run(b, t.run_off, nact, rho);
-  const int cb = b.K / 32;            // code bytes per row (a multiple of 4)
-  const int chunks = cb % 16 == 0 ? cb / 16 : 0;   // 16-byte loads only when rows stay aligned
-  uint8_t* scratch = t.codes + (size_t)q * (kTcRmax * kTcCodeRow);
-  for (int i = lane; i < run.R * chunks; i += 32) {
-    const int r = i / chunks, c = i - r * chunks;
-    const int arow = __ldcg(b.pair_list + run.p0 + r) / b.act_div;
-    *reinterpret_cast<uint4*>(scratch + r * kTcCodeRow + 16 * c) =
-        __ldcg(reinterpret_cast<const uint4*>(b.act_code + (size_t)arow * cb) + c);
-  }
-  for (int i = chunks * 16 + 4 * lane; i < cb; i += 128) {   // a tail of 4-byte words
-    for (int r = 0; r < run.R; ++r) {
-      const int arow = __ldcg(b.pair_list + run.p0 + r) / b.act_div;
-      *reinterpret_cast<unsigned*>(scratch + r * kTcCodeRow + i) =
-          __ldcg(reinterpret_cast<const unsigned*>(b.act_code + (size_t)arow * cb + i));
-    }
-  }
-  __syncwarp();
-  const int p0 = lane & 7, r0 = lane >> 3, r1 = r0 + 4;   // rows n = lane and lane + 32
-  const uint32_t col0 = kTcSfaCol + (uint32_t)b.NS * ((uint32_t)b.KC / 32) +
-                        (uint32_t)buf * ((uint32_t)b.K / 64);
-  for (int A = 0; A < b.K / 128; ++A) {
-    uint32_t w0 = 0x7F7F7F7Fu, w1 = 0x7F7F7F7Fu;
-    if (r0 < run.R) {
-      const uint32_t c4 = *reinterpret_cast<const unsigned*>(scratch + r0 * kTcCodeRow + 4 * A);
-      w0 = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w0 |= planes_code((c4 >> (8 * i)) & 0xFFu, p0) << (8 * i);
-    }
-    if (r1 < run.R) {
-      const uint32_t c4 = *reinterpret_cast<const unsigned*>(scratch + r1 * kTcCodeRow + 4 * A);
-      w1 = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w1 |= planes_code((c4 >> (8 * i)) & 0xFFu, p0) << (8 * i);
-    }
-    tmem_st2(T + qaddr + col0 + 2 * (uint32_t)A, w0, w1);
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&t.sfb_full[buf]);
-}
-
 __device__ __forceinline__ void tc_wait_flag(const unsigned* f, int* status) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
@@ -468,12 +471,10 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
   if (u0 >= u1) return;
   const uint32_t qaddr = (uint32_t)(32 * q) << 16;
   const int m = 32 * q + lane;   // MMA row of this thread
-  const int rho_last = (u1 - 1) / upr;
-  tc_write_sfb(b, t, T, qaddr, q, nact, u0 / upr, 0, lane);
-  if (u0 / upr + 1 <= rho_last) tc_write_sfb(b, t, T, qaddr, q, nact, u0 / upr + 1, 1, lane);
-  int cur = -1, lr = -1, jobs = 0, fin = 0;
+  int cur = -1, jobs = 0, fin = 0;
   TcRun run{0, 0, 0};
   int pid[kTcRmax];
+  float ps[kTcRmax][kPlanes];    // rowscale: the planes' scales of each pair's row
   for (int u = u0; u < u1;) {
     const int rho = u / upr, rem = u - rho * upr, tile = rem / nch, cs = rem - tile * nch;
     const int tile_end = rho * upr + (tile + 1) * nch;
@@ -481,13 +482,16 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
     const int ce = cs + (ue - u);
     if (rho != cur) {
       cur = rho;
-      ++lr;
       run = tc_run(b, t.run_off, nact, rho);
 #pragma unroll
-      for (int r = 0; r < kTcRmax; ++r) pid[r] = r < run.R ? __ldcg(b.pair_list + run.p0 + r) : 0;
-      // the other buffer last served run lr - 1, whose tiles are all read back
-      if (lr >= 1 && rho + 1 <= rho_last)
-        tc_write_sfb(b, t, T, qaddr, q, nact, rho + 1, (lr + 1) & 1, lane);
+      for (int r = 0; r < kTcRmax; ++r) {
+        pid[r] = r < run.R ? __ldcg(b.pair_list + run.p0 + r) : 0;
+        const uint32_t c0 =
+            (b.rowscale && r < run.R) ? (uint32_t)__ldcg(b.act_code + pid[r] / b.act_div) : 127u;
+#pragma unroll
+        for (int p = 0; p < kPlanes; ++p)
+          ps[r][p] = b.rowscale ? __uint_as_float(planes_code(c0, p) << 23) : 1.0f;
+      }
     }
     const int R = run.R;
     const int jb = jobs & 1;
@@ -508,7 +512,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
       float s = 0.f;
       if (r < R) {
 #pragma unroll
-        for (int p = 0; p < kPlanes; ++p) s += v[8 * r + p];
+        for (int p = 0; p < kPlanes; ++p) s = fmaf(ps[r][p], v[8 * r + p], s);
       }
       y[r] = s;
     }
@@ -560,7 +564,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
       }
       tc_epi_sync();
       if (q < 2) {
-        const int jcol = tile * 64 + m;
+        const int jcol = tile * 64 + m, blk = jcol / 32;
 #pragma unroll
         for (int r = 0; r < kTcRmax; ++r) {
           if (r < R) {
@@ -569,9 +573,15 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
             b.out[(size_t)pid[r] * b.N + jcol] = hv;
             const float hm = warp_max(fabsf(hv));
             if (lane == 0 && b.out_amax) atomicMax(b.out_amax + pid[r], __float_as_uint(hm));
-            if (b.out_act)
-              planes_block(hv, lane, b.out_act + (size_t)pid[r] * planes_row_bytes(b.N) + (jcol / 32) * 128,
-                           b.out_code + (size_t)pid[r] * planes_code_bytes(b.N) + jcol / 32);
+            if (b.out_act) {
+              // the down projection's B operand: h planes and their block scales
+              const int c0 = planes_block(hv, lane, b.out_act + (size_t)pid[r] * planes_row_bytes(b.N) + blk * 128);
+              if (lane < kPlanes) {
+                const int n = 8 * r + lane;
+                b.out_sfb[(size_t)rho * 4 * b.N + tc_sfb_offset(blk / 4, n, blk % 4)] =
+                    (uint8_t)planes_code((uint32_t)c0, lane);
+              }
+            }
           }
         }
       }
@@ -587,10 +597,15 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
 }
 
 // ---------------------------------------------------------------------------
-// The kernel: segment A (dense, CUDA cores, stream.cuh) then the routed step
-// on the tensor cores through the same stage ring.
+// The kernel: the routed step on the tensor cores and segment A (dense, CUDA
+// cores, stream.cuh) through one stage ring.  A_LAST = false: A first, its
+// weights streaming before the predecessor kernel is waited for (FC1: the
+// shared gate/up overlaps top-k).  A_LAST = true: the routed step first, right
+// after the predecessor's results land, and A after it, its weights streaming
+// while the routed step's last stages and epilogues drain (FC2: the shared
+// down projection's input is ready long before).
 // ---------------------------------------------------------------------------
-template <class A, bool GLU, bool A_WAITS>
+template <class A, bool GLU, bool A_LAST>
 __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     tc_dual_kernel(const StreamArgs a0, const TcArgs b) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -598,12 +613,14 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   const int KW = (int)(blockDim.x >> 5) - 1;
   trace_begin(a0.trace, a0.trace_id);
   const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
-  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp + 16));
+  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp + 16), b.K,
+                           b.rowscale != 0);
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&t.acc_full[i], 1);
       mbar_init(&t.acc_empty[i], 4);
-      mbar_init(&t.sfb_full[i], 4);
+      mbar_init(&t.sfb_full[i], 1);
+      mbar_init(&t.sfb_empty[i], 1);
     }
     mbar_init(t.sched, 1);
     fence_barrier_init();
@@ -613,29 +630,49 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t T = *t.tbase;
+  if (b.rowscale && warp >= 2 && warp < 6) {
+    // per-row activation scales: the MMAs multiply by 1 (code 127) and the
+    // epilogue applies each plane's scale
+    const uint32_t col = kTcSfaCol + (uint32_t)b.NS * ((uint32_t)b.KC / 32);
+    tmem_st2(T + ((uint32_t)(32 * (warp & 3)) << 16) + col, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    tmem_wait_st();
+    tc_fence_before();
+  }
   pdl_launch_dependents();
   uint32_t stage = 0;
   if (warp == 0) {
     if (lane == 0) {
-      cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
+      if (!A_LAST) cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
       pdl_wait_prerequisites();
       tc_produce(b, t, m.stages, m.full, m.empty, stage);
+      if (A_LAST) cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
       stream_drain(a0, m.empty, stage);
     }
     __syncwarp();
   } else {
-    if (A_WAITS) pdl_wait_prerequisites();
     int pp = 0, rp = 0;
-    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    if (!A_LAST)
+      cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
     pdl_wait_prerequisites();
-    // every consumer is past segment A's last shared-memory combine
+    // every consumer is past segment A's last shared-memory combine (and the
+    // constant activation scales are in tensor memory)
     consumer_sync(KW * 32);
     if (warp == 1) {
       tc_schedule(b, t, lane);
-      if (lane == 0) tc_mma(b, t, T, m.stages, m.full, m.empty, stage, KW);
+      if (lane == 0) {
+        tc_fence_after();
+        tc_mma(b, t, T, m.stages, m.full, m.empty, stage, KW);
+        if (A_LAST) *t.stage_after = stage;
+      }
       __syncwarp();
     } else if (warp < 6) {
       tc_epilogue<GLU>(b, t, T, warp & 3, lane);
+    }
+    if (A_LAST) {
+      // segment A continues the ring where the routed step's MMAs left it
+      consumer_sync(KW * 32);
+      stage = *t.stage_after;
+      cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
     }
   }
   tc_fence_before();

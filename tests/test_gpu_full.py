@@ -20,10 +20,11 @@ def _np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("name,rows,path", [("full_b1", [0], 2), ("full_b1", [0], 1),
-                                            ("full_b8", [0, 7], 2), ("full_b64", [0, 33, 63], 2)])
+@pytest.mark.parametrize("name,rows,path", [("full_b1", [0], 0), ("full_b1", [0], 2),
+                                            ("full_b8", [0, 7], 0), ("full_b64", [0, 33, 63], 0)])
 def test_full_layer_sampled_rows(name, rows, path):
-    """path 2: the tcgen05 expert path the benchmark times; 1: mma.sync."""
+    """path 0, the layer the benchmark times: mma.sync at B = 1, tcgen05 at
+    B = 8 and 64; path 2: tcgen05 at B = 1 as well."""
     cfg = CONFIGS[name]
     inp = oracle.clean_inputs(cfg)
     ref = oracle.forward(inp, rows=rows)

@@ -93,7 +93,7 @@ def test_device_tiled_pack_and_retile_match_host_tiled_pack(layout):
     assert torch.equal(qr[1].cpu(), qh2) and torch.equal(sr[1].cpu(), sh2)
 
 
-@pytest.mark.parametrize("path", [2, 1])
+@pytest.mark.parametrize("path", [0, 2, 1])
 def test_layer_output_does_not_depend_on_the_weight_layout_given(path):
     """moe_layer_create with canonical, tiled or UMMA expert bytes (relaid into
     the handle's own copy unless already in the path's layouts) gives

@@ -24,9 +24,10 @@ def tiny_cfg(B):
     return dataclasses.replace(TINY, name=f"tiny_b{B}", B=B)
 
 
-@pytest.fixture(scope="module", params=[2, 1], ids=["tcgen05", "mma_sync"])
+@pytest.fixture(scope="module", params=[0, 2, 1], ids=["auto", "tcgen05", "mma_sync"])
 def tiny_layer(request):
-    """The tiny layer on each expert path (tcgen05 block-scaled MMAs, mma.sync)."""
+    """The tiny layer on each expert path: both kept (mma.sync at B = 1,
+    tcgen05 from B = 2), tcgen05 block-scaled MMAs only, mma.sync only."""
     layer = synthetic.make_layer(TINY, max_batch=64, expert_path=request.param)
     yield layer
     layer.close()
