@@ -56,7 +56,8 @@ def parse_args():
 # held instead of 896 (2.2 GB of expert weights instead of 15.7 GB): at B = 1
 # the 16 selected experts make its FC1 and FC2 launches the same size as
 # full_b1's, while the device holds a few GB, as a many-pass capture needs.
-PROFILE_CASES = {"full_b1": ("full_b1", None), "full_b1_e128": ("full_b1", 128)}
+PROFILE_CASES = {"full_b1": ("full_b1", None), "full_b1_e128": ("full_b1", 128),
+                 "full_b8_e128": ("full_b8", 128)}
 
 
 def dist_env():
@@ -456,8 +457,7 @@ def run_ours(args, rank, world, local):
     traffic = traffic_from_profile()
     if traffic is not None:
         traffic = traffic * n_distinct / 16.0
-    phase_names = ["router_topk", "fc1_shared_then_routed", "fc2_shared_then_routed",
-                   "unused", "tail", "layer"]
+    phase_names = ["router_topk", "fc1", "fc2", "unused", "tail", "layer"]
     phase_med = {n: statistics.median(p[i] for p in phases) for i, n in enumerate(phase_names)}
 
     e2e_times, h2d, d2h = time_e2e(layer, cfg, x, res0, max(5, args.steps // 2),
@@ -482,9 +482,17 @@ def run_ours(args, rank, world, local):
             _, p2 = time_layer(L2, x2, r2, 5, 3, flush, graph=True, timing=True)
             v2 = reduce_max(statistics.median(t2), world, dev)
             b2 = bytes_touched(c2, nd2, c2.B)
+            f2_us = statistics.median(p[1] for p in p2)
+            f2_b = fc1_bytes(c2, nd2, c2.B)
             batches[str(c2.B)] = {
                 "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
                 "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,
+                "expert_path": "tcgen05 block-scaled MXF4 MMA",
+                "fc1_roofline": {"kernel": "tc_dual_kernel (FC1: shared gate/up on CUDA cores, "
+                                           "routed gate/up on tcgen05)", "bound": "hbm",
+                                 "achieved": f2_b / f2_us / 1e3, "peak": peak, "unit": "GB/s",
+                                 "frac": f2_b / f2_us / 1e3 / peak, "algorithmic_bytes": f2_b,
+                                 "launch_us": f2_us, "peak_kind": peak_kind},
                 "phases_us": {n: statistics.median(p[i] for p in p2)
                               for i, n in enumerate(phase_names)}}
             L2.close()
@@ -529,6 +537,7 @@ def run_ours(args, rank, world, local):
                 "tbs": btouch / us / 1e6, "frac_of_peak": btouch / us / 1e3 / peak,
                 "frac_of_nominal_8tbs": btouch / us / 1e6 / 8.0, "aggregate_tbs": agg_tbs,
                 "peak_gbs": peak, "peak_kind": peak_kind},
+        "expert_path": "mma.sync with register dequantisation (B = 1)",
         "roofline": {"kernel": "stream_dual_kernel (FC1: shared + routed gate/up)", "bound": "hbm",
                      "achieved": fc1_b / fc1_us / 1e3, "peak": peak, "unit": "GB/s",
                      "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,
