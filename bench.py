@@ -488,8 +488,8 @@ def run_ours(args, rank, world, local):
                 "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
                 "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,
                 "expert_path": "tcgen05 block-scaled MXF4 MMA",
-                "fc1_roofline": {"kernel": "tc_dual_kernel (FC1: shared gate/up on CUDA cores, "
-                                           "routed gate/up on tcgen05)", "bound": "hbm",
+                "fc1_roofline": {"kernel": "tc_kernel (FC1: shared gate/up as a bf16 kind::f16 pass, "
+                                           "routed gate/up as block-scaled kind::mxf4)", "bound": "hbm",
                                  "achieved": f2_b / f2_us / 1e3, "peak": peak, "unit": "GB/s",
                                  "frac": f2_b / f2_us / 1e3 / peak, "algorithmic_bytes": f2_b,
                                  "launch_us": f2_us, "peak_kind": peak_kind},

@@ -11,6 +11,7 @@
 // Optional second stream (chained layers only): L2 prefetch of the next
 // layer's router and shared-expert weights.
 // No allocation, no host synchronisation: capturable into a CUDA graph.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -73,13 +74,19 @@ struct Workspace {
   uint8_t* h_sfb;    // h plane scales per run, in the tensor-memory copy's atom order [P][4f]
   float* partial;
   unsigned* flags;
+  // tensor-core dense pass: h_s as (hi, lo) bf16 columns for the shared down
+  // projection, stream-K partials
+  uint8_t* hs_hl;    // [f_shared / 8][2 B padded][16 bytes]
+  float* dpartial;
+  unsigned* dflags;
 };
 
 // Launch shape of one streaming-GEMV step.
 struct StreamPlan {
   int threads = 0, grid = 0, NS = 0, stage_bytes = 0, smem = 0, red_pp = 0;
   int kc = 1;      // K chunks per item of the MXFP4 segment (CUDA-core path)
-  int tc_kc = 0;   // K elements per stage of the tensor-core segment
+  int tc_kc = 0;   // K elements per stage of the tensor-core routed pass
+  int dense_kc = 0;   // K elements per stage of the tensor-core dense pass
 };
 
 enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kNumSteps };
@@ -122,6 +129,11 @@ struct moe_layer {
   ExpertWeights wm;   // mma.sync path (tiled layouts), when kept
   ExpertWeights wt;   // tcgen05 path (UMMA layouts), when kept
   int tc_min_batch = kTcMinBatch;
+  // tcgen05 path: the shared expert's bf16 weights in the dense pass's tiles
+  uint8_t* sh_gu_umma = nullptr;
+  uint8_t* sh_d_umma = nullptr;
+  void* sh_owned = nullptr;
+  void* encode_tiled = nullptr;   // the driver's tensor-map encoder
 };
 
 namespace {
@@ -161,6 +173,9 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.h_sfb = carve<uint8_t>(p, P * 4 * (size_t)d.f);   // at most P runs
   w.partial = carve<float>(p, (size_t)kTcMaxCtas * kTcRmax * 128);
   w.flags = carve<unsigned>(p, kTcMaxCtas);
+  w.hs_hl = carve<uint8_t>(p, (size_t)d.f_shared * dense_np(2 * (int)B) * 2);
+  w.dpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
+  w.dflags = carve<unsigned>(p, kTcMaxCtas);
   if (ws) *ws = w;
   return (size_t)(p - base);
 }
@@ -204,8 +219,8 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
 // Tensor-core path: FC1 streams the shared gate/up first (while top-k runs),
 // FC2 the routed down projection first and the shared one last.
-#define MOE_TC1_KERNEL(RS) tc_dual_kernel<Sh1Cfg<RS>, true, false>
-#define MOE_TC2_KERNEL(RS) tc_dual_kernel<Sh2Cfg<RS>, false, true>
+#define MOE_TC1_KERNEL tc_kernel<true, true>
+#define MOE_TC2_KERNEL tc_kernel<false, false>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -299,33 +314,31 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
       MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
 }
 
-// Launch shape of a tensor-core kernel: segment A's consumer warps (at least
-// the five the routed step's roles need), a stage ring sized for the larger
-// segment, and tensor memory for two accumulators, a scale slot per stage and
-// two activation-scale buffers.  rmax: pairs per pass at this batch class.
-template <class A, typename Kern>
-int plan_tc(Kern kern, int KA, int NA, int K, int rmax, bool rowscale, int E, int n_sm,
+// Launch shape of a tensor-core kernel: six warps, a stage ring sized for the
+// larger pass (routed: rmax pairs; dense: np_max columns), and tensor memory
+// for two accumulators, a scale slot per stage and the activation scales.
+template <typename Kern>
+int plan_tc(Kern kern, int K, int K_dense, int rmax, int np_max, bool rowscale, int E, int n_sm,
             int budget, StreamPlan* p) {
-  const int KW = std::max(seg_warps<A>(KA), 5);
-  if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;
-  if (!seg_fits<A>(KA, NA, KW)) return MOE_ERR_UNSUPPORTED;
-  if (K % 256 != 0 || n_sm > kTcMaxCtas) return MOE_ERR_UNSUPPORTED;
+  if (K % 256 != 0 || K_dense % 128 != 0 || n_sm > kTcMaxCtas) return MOE_ERR_UNSUPPORTED;
+  if (np_max > kTcDenseMaxN) return MOE_ERR_UNSUPPORTED;
   StreamPlan r;
-  r.threads = 32 * (KW + 1);
+  r.threads = kTcThreads;
   r.kc = 1;
   r.tc_kc = K % 512 == 0 ? 512 : 256;
-  const size_t st = std::max(seg_stage_bytes<A>(KA, 1), tc_stage_bytes(r.tc_kc, rmax));
+  r.dense_kc = np_max <= 64 ? 128 : 64;
+  const size_t st = std::max(tc_stage_bytes(r.tc_kc, rmax), dense_stage_bytes(r.dense_kc, np_max));
   r.stage_bytes = (int)((st + 127) / 128 * 128);
-  r.red_pp = stream_red_pp(KW, A::MMA, A::TM, A::RMAX);
-  const int red_bytes = 2 * r.red_pp * 4 + 64;
   const int extra = (int)tc_smem_bytes(E, K, rowscale);
-  r.NS = std::min(16, (budget - red_bytes - extra) / (r.stage_bytes + 16));
+  r.NS = std::min(16, (budget - extra) / (r.stage_bytes + 16));
   auto cols = [&](int ns) { return tc_tmem_cols(K, r.tc_kc, ns, rowscale); };
   while (r.NS > 2 && cols(r.NS) > kTcCols) --r.NS;
   if (r.NS < 2 || cols(r.NS) > kTcCols) return MOE_ERR_UNSUPPORTED;
   // at least 116 KB: a second CTA on the SM would wait in tcgen05.alloc
-  r.smem = std::max(r.NS * r.stage_bytes + r.NS * 16 + red_bytes + extra, 116 * 1024);
-  MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
+  r.smem = std::max((int)tc_kernel_smem(r.NS, r.stage_bytes, E, K, rowscale), 116 * 1024);
+  if (r.smem > budget) return MOE_ERR_UNSUPPORTED;
+  // one instantiation serves every batch class: allow the largest plan's size
+  MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, budget));
   int occ = 0;
   MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, r.threads, r.smem));
   if (occ != 1) return MOE_ERR_UNSUPPORTED;
@@ -333,6 +346,9 @@ int plan_tc(Kern kern, int KA, int NA, int K, int rmax, bool rowscale, int E, in
   *p = r;
   return MOE_OK;
 }
+
+// Largest batch of each batch class (B = 1, B <= 8, B <= 64).
+constexpr int kClassMaxB[3] = {1, 8, 64};
 
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
@@ -347,18 +363,13 @@ int plan_all(moe_layer* L) {
     const int E = d.n_experts;
     // one CTA per SM: all the shared memory a block may opt into
     const int bud = std::max(kBudget1, L->smem_optin);
-    MOE_PLAN((plan_tc<Sh1Cfg<1>>(MOE_TC1_KERNEL(1), d.d, d.f_shared, d.d, 1, true, E, n, bud,
-                                 &L->plan[kStepTc1][0])));
-    MOE_PLAN((plan_tc<Sh1Cfg<2>>(MOE_TC1_KERNEL(2), d.d, d.f_shared, d.d, kTcRmax, true, E, n, bud,
-                                 &L->plan[kStepTc1][1])));
-    MOE_PLAN((plan_tc<Sh1Cfg<4>>(MOE_TC1_KERNEL(4), d.d, d.f_shared, d.d, kTcRmax, true, E, n, bud,
-                                 &L->plan[kStepTc1][2])));
-    MOE_PLAN((plan_tc<Sh2Cfg<1>>(MOE_TC2_KERNEL(1), d.f_shared, d.d, d.f, 1, false, E, n, bud,
-                                 &L->plan[kStepTc2][0])));
-    MOE_PLAN((plan_tc<Sh2Cfg<2>>(MOE_TC2_KERNEL(2), d.f_shared, d.d, d.f, kTcRmax, false, E, n, bud,
-                                 &L->plan[kStepTc2][1])));
-    MOE_PLAN((plan_tc<Sh2Cfg<4>>(MOE_TC2_KERNEL(4), d.f_shared, d.d, d.f, kTcRmax, false, E, n, bud,
-                                 &L->plan[kStepTc2][2])));
+    for (int c = 0; c < 3; ++c) {
+      const int rmax = c == 0 ? 1 : kTcRmax;
+      MOE_PLAN((plan_tc(MOE_TC1_KERNEL, d.d, d.d, rmax, dense_np(kClassMaxB[c]), true, E, n, bud,
+                        &L->plan[kStepTc1][c])));
+      MOE_PLAN((plan_tc(MOE_TC2_KERNEL, d.f, d.f_shared, rmax, dense_np(2 * kClassMaxB[c]), false,
+                        E, n, bud, &L->plan[kStepTc2][c])));
+    }
   }
   if (!L->wm.ok) return MOE_OK;
   MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg>(MOE_FC1_KERNEL(1), d.d, d.f_shared, d.d, d.f, n,
@@ -527,32 +538,51 @@ TcArgs tc_base_args(moe_layer* L, const StreamPlan& p) {
   b.NS = p.NS;
   b.stage_bytes = p.stage_bytes;
   b.KC = p.tc_kc;
+  b.trace = L->tracing ? L->ws.trace : nullptr;
   return b;
 }
 
+// The dense pass's arguments common to FC1 and FC2.
+TcDense dense_base_args(moe_layer* L, const StreamPlan& p, int B) {
+  TcDense dn;
+  std::memset(&dn, 0, sizeof(dn));
+  dn.KC = p.dense_kc;
+  dn.B = B;
+  dn.partial = L->ws.dpartial;
+  dn.flags = L->ws.dflags;
+  return dn;
+}
+
 template <typename K>
-int launch_tc(K kern, const StreamPlan& p, StreamArgs a0, const TcArgs& b, cudaStream_t st,
-              int grid) {
-  a0.NS = p.NS;
-  a0.stage_bytes = p.stage_bytes;
-  a0.red_pp = p.red_pp;
-  a0.kc = 1;
-  MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, true, a0, b));
+int launch_tc(K kern, const StreamPlan& p, const TcArgs& b, const TcDense& dn,
+              const CUtensorMap& xmap, cudaStream_t st, int grid) {
+  MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, true, b, dn, xmap));
   return MOE_OK;
 }
 
-// FC1 on the tensor-core path: shared gate/up on the CUDA cores, then routed
-// gate/up (x planes x UMMA-layout weights), SwiGLU, h and its planes.
+// Tensor map of x [B][d] (bf16, row-major) with a box of 8 K elements x NP
+// rows; rows past B read as zeros.
+int encode_x_map(moe_layer* L, const void* x, int B, int NP, CUtensorMap* map) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  if (!L->encode_tiled) return MOE_ERR_UNSUPPORTED;
+  const cuuint64_t dims[2] = {(cuuint64_t)L->dims.d, (cuuint64_t)B};
+  const cuuint64_t strides[1] = {(cuuint64_t)L->dims.d * 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)NP};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = reinterpret_cast<Encode>(L->encode_tiled)(
+      map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+// FC1 on the tensor-core path: the shared gate/up as a dense pass on x, then
+// routed gate/up (x planes x UMMA-layout weights), SwiGLU, h and its planes.
 int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   const moe_dims_t& d = L->dims;
-  StreamArgs sa = base_args(L);
-  sa.q = static_cast<const uint8_t*>(L->w.shared_gu);
-  sa.K = d.d;
-  sa.N = d.f_shared;
-  sa.B = B;
-  sa.x = static_cast<const uint16_t*>(x);
-  sa.out = L->ws.hs;
-  sa.trace_id = 2;
   const StreamPlan& p = L->plan[kStepTc1][batch_class(B)];
   TcArgs b = tc_base_args(L, p);
   b.q = L->wt.gu_q;
@@ -570,27 +600,28 @@ int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   b.out_amax = L->ws.h_amax;
   b.out_act = L->ws.h_act;
   b.out_sfb = L->ws.h_sfb;
+  b.trace_id = 2;
+  TcDense dn = dense_base_args(L, p, B);
+  dn.w = L->sh_gu_umma;
+  dn.K = d.d;
+  dn.tiles = d.f_shared / 64;
+  dn.N = d.f_shared;
+  dn.NP = dense_np(B);
+  dn.out = L->ws.hs;
+  dn.out_hl = L->ws.hs_hl;
+  dn.out_np = dense_np(2 * B);
+  CUtensorMap xmap;
+  int rc = encode_x_map(L, x, B, dn.NP, &xmap);
+  if (rc) return rc;
   // at B = 1 one SM holds the top-k CTA when FC1 launches (see launch_fc1)
   const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
-  switch (batch_class(B)) {
-    case 0: return launch_tc(MOE_TC1_KERNEL(1), p, sa, b, st, grid);
-    case 1: return launch_tc(MOE_TC1_KERNEL(2), p, sa, b, st, grid);
-    default: return launch_tc(MOE_TC1_KERNEL(4), p, sa, b, st, grid);
-  }
+  return launch_tc(MOE_TC1_KERNEL, p, b, dn, xmap, st, grid);
 }
 
-// FC2 on the tensor-core path: shared down on the CUDA cores, then routed
-// down (h planes x UMMA-layout weights).
+// FC2 on the tensor-core path: routed down (h planes x UMMA-layout weights),
+// then the shared down as a dense pass on h_s's (hi, lo) columns.
 int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   const moe_dims_t& d = L->dims;
-  StreamArgs sa = base_args(L);
-  sa.q = static_cast<const uint8_t*>(L->w.shared_d);
-  sa.K = d.f_shared;
-  sa.N = d.d;
-  sa.B = B;
-  sa.h = L->ws.hs;
-  sa.out = L->ws.y_s;
-  sa.trace_id = 3;
   const StreamPlan& p = L->plan[kStepTc2][batch_class(B)];
   TcArgs b = tc_base_args(L, p);
   b.q = L->wt.d_q;
@@ -605,11 +636,18 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   b.act = L->ws.h_act;
   b.act_sfb = L->ws.h_sfb;
   b.out = L->ws.y_pair;
-  switch (batch_class(B)) {
-    case 0: return launch_tc(MOE_TC2_KERNEL(1), p, sa, b, st, p.grid);
-    case 1: return launch_tc(MOE_TC2_KERNEL(2), p, sa, b, st, p.grid);
-    default: return launch_tc(MOE_TC2_KERNEL(4), p, sa, b, st, p.grid);
-  }
+  b.trace_id = 3;
+  TcDense dn = dense_base_args(L, p, B);
+  dn.w = L->sh_d_umma;
+  dn.act = L->ws.hs_hl;
+  dn.K = d.f_shared;
+  dn.tiles = d.d / 128;
+  dn.N = d.d;
+  dn.NP = dense_np(2 * B);
+  dn.out = L->ws.y_s;
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  return launch_tc(MOE_TC2_KERNEL, p, b, dn, unused, st, p.grid);
 }
 
 // FC2: shared down (bf16, h_s) then routed down (MXFP4, h).
@@ -791,6 +829,38 @@ int setup_weights(moe_layer* L, const moe_weights_t& w, int want, ExpertWeights&
   return MOE_OK;
 }
 
+// The tensor-core path's shared-expert weights: bf16 copies in the dense
+// pass's 128-row tiles (gate/up pairs for FC1, rows for FC2), and the
+// driver's tensor-map encoder for x.
+int setup_dense(moe_layer* L) {
+  const moe_dims_t& d = L->dims;
+  const size_t gu = (size_t)2 * d.f_shared * d.d * 2, dn = (size_t)d.d * d.f_shared * 2;
+  if (cudaMalloc(&L->sh_owned, gu + dn) != cudaSuccess) {
+    cudaGetLastError();
+    L->sh_owned = nullptr;
+    return MOE_ERR_ALLOC;
+  }
+  L->sh_gu_umma = static_cast<uint8_t*>(L->sh_owned);
+  L->sh_d_umma = L->sh_gu_umma + gu;
+  dense_relayout_kernel<<<L->n_sm * 8, 256>>>(static_cast<const uint16_t*>(L->w.shared_gu),
+                                               2LL * d.f_shared, d.d, 1, L->sh_gu_umma);
+  MOE_CUDA(cudaGetLastError());
+  dense_relayout_kernel<<<L->n_sm * 8, 256>>>(static_cast<const uint16_t*>(L->w.shared_d),
+                                               (int64_t)d.d, d.f_shared, 0, L->sh_d_umma);
+  MOE_CUDA(cudaGetLastError());
+  MOE_CUDA(cudaStreamSynchronize(nullptr));
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  L->encode_tiled = fn;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -864,7 +934,8 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
     moe_layer_destroy(L);
     return rc;
   }
-  if (path != kPathMmaSync && (rc = setup_weights(L, w, 3, L->wt))) {
+  if (path != kPathMmaSync &&
+      ((rc = setup_weights(L, w, 3, L->wt)) || (rc = setup_dense(L)))) {
     moe_layer_destroy(L);
     return rc;
   }
@@ -891,6 +962,7 @@ int moe_layer_destroy(moe_layer_t L) {
   if (L->ws_base) cudaFree(L->ws_base);
   if (L->wm.owned) cudaFree(L->wm.owned);
   if (L->wt.owned) cudaFree(L->wt.owned);
+  if (L->sh_owned) cudaFree(L->sh_owned);
   cudaSetDevice(prev);
   delete L;
   return MOE_OK;

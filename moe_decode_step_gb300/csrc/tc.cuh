@@ -1,46 +1,57 @@
-// Routed experts on the 5th-generation tensor cores (tcgen05, sm_103a).
+// The expert matmuls on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One expert matmul step (routed FC1 gate/up with the SwiGLU epilogue, or
-// routed FC2 down) as a block-scaled MXFP4 x MXFP4 MMA: the weight tile (128
-// rows, UMMA layout, see mxfp4.cuh) is operand A, the activation planes of up
-// to 8 (expert, row) pairs (8 planes each, see planes.cuh) are operand B, the
-// E8M0 scales ride along in tensor memory, and fp32 accumulators live in
-// tensor memory until the epilogue reads them back.  Nothing is converted on
-// the CUDA cores; the stage ring only streams bytes.
+// One kernel per projection, two passes through one stage ring:
+//  * routed pass (routed FC1 gate/up with the SwiGLU epilogue, or routed FC2
+//    down): a block-scaled MXFP4 x MXFP4 MMA (kind::mxf4).  The weight tile
+//    (128 rows, UMMA layout, see mxfp4.cuh) is operand A, the activation
+//    planes of up to 8 (expert, row) pairs (8 planes each, see planes.cuh)
+//    are operand B, and the E8M0 scales ride along in tensor memory;
+//  * dense pass (the shared expert): bf16 weights x bf16 activations
+//    (kind::f16), every batch row a column of one MMA, so the shared weights
+//    stream once whatever the batch.  FC1 takes x straight from the caller's
+//    buffer through a tensor map (cp.async.bulk.tensor), so it needs nothing
+//    from the router and runs first, while top-k finishes; its epilogue
+//    writes h_s both as fp32 and as (hi, lo) bf16 pairs, the operand of FC2's
+//    dense pass (h_s = hi + lo to 2^-16 relative, far inside fp32 sums of
+//    bf16 products).  FC2 runs its routed pass first, right after FC1's
+//    results land, and the dense pass after it.
+// fp32 accumulators live in tensor memory until the epilogue reads them back;
+// nothing is converted on the CUDA cores on the way in.
 //
-// Work split: units are (run, tile, K chunk) with a run = one pass of <= 8
-// pairs of one active expert.  CTA i takes units [i U / G, (i+1) U / G) (U
-// units, G CTAs), so every CTA streams the same number of weight bytes.  A
-// tile cut by a range boundary is finished by the CTA that holds its first
-// chunk: the later CTAs leave their partial sums in a per-CTA slot and raise
-// a flag at the start of their range; the finisher adds them in K order at the
-// end of its own (so results do not depend on timing).
+// Work split (both passes): units are (run, tile, K chunk), a run being one
+// pass of <= 8 pairs of one active expert (the dense pass: one run).  CTA i
+// takes units [i U / G, (i+1) U / G) (U units, G CTAs), so every CTA streams
+// the same number of weight bytes.  A tile cut by a range boundary is
+// finished by the CTA that holds its first chunk: the later CTAs leave their
+// partial sums in a per-CTA slot and raise a flag at the start of their
+// range; the finisher adds them in K order at the end of its own (so results
+// do not depend on timing).
 //
-// Roles in a CTA (after the shared-expert segment that runs first on the
-// CUDA cores, see stream.cuh): warp 0 lane 0 streams stages; warp 1 builds
-// the run table, then its lane 0 issues the tensor-memory scale copies and
-// MMAs and commits them to the stage's "empty" barrier and, per tile, to an
-// accumulator barrier; warps 2..5 (tensor-memory lane quarters 2, 3, 0, 1)
-// run the epilogues.  Accumulators are double-buffered and scale slots ringed
-// with the stages, so the MMA warp never waits for an epilogue in steady
-// state.  Every wait is bounded (status 5 on timeout).
+// Roles (6 warps): warp 0 lane 0 streams stages; warp 1 allocates tensor
+// memory, builds the run table, and its lane 0 issues the tensor-memory scale
+// copies and MMAs and commits them to the stage's "empty" barrier and, per
+// tile, to an accumulator barrier; warps 2..5 (tensor-memory lane quarters 2,
+// 3, 0, 1) run the epilogues.  Accumulators are double-buffered and scale
+// slots ringed with the stages, so the MMA thread never waits for an epilogue
+// in steady state.  Every wait is bounded (status 5 on timeout).
 //
-// Activation scales: FC1's x planes carry one code per row (planes.cuh), so
-// the MMAs take scale 1 from two constant tensor-memory columns and the
-// epilogue multiplies each plane's column by its scale.  FC2's h planes carry
-// per-block codes (each FC1 epilogue only sees 64 values of an h row); FC1
-// writes them per run in the tensor-memory copy's atom order, and FC2 loads a
-// run's whole set into tensor memory once, at the run's first unit (double
-// buffered by run).  A block-scaled MMA costs about the same whatever N is,
-// and so does each scale copy: per stage the MMA thread issues only the
-// weight-scale copies and the MMAs.
+// Routed activation scales: FC1's x planes carry one code per row
+// (planes.cuh), so the MMAs take scale 1 from two constant tensor-memory
+// columns and the epilogue multiplies each plane's column by its scale.
+// FC2's h planes carry per-block codes (each FC1 epilogue only sees 64
+// values of an h row); FC1 writes them per run in the tensor-memory copy's
+// atom order, and FC2 loads a run's whole set into tensor memory once, at the
+// run's first unit (double buffered by run).  A block-scaled MMA costs about
+// the same whatever N is (measured: about 158 SM cycles for M = 128, K = 64,
+// any N up to 128, swizzled or not), and so does each scale copy: per stage
+// the MMA thread issues only the weight-scale copies and the MMAs.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "planes.cuh"
-#include "stream.cuh"
 
 namespace moe {
 
@@ -50,7 +61,9 @@ namespace moe {
 constexpr int kTcCols = 512;        // tensor-memory columns a CTA allocates (one CTA per SM)
 constexpr int kTcRmax = 8;          // pairs per pass: N = 8 planes x 8 pairs = 64 columns
 constexpr int kTcMaxCtas = 256;     // partial slots / flags in the workspace
-constexpr int kTcSfaCol = 128;      // D buffers take columns [0, 128)
+constexpr int kTcDStride = 128;     // two accumulators of up to 128 columns
+constexpr int kTcSfaCol = 256;      // D buffers take columns [0, 256)
+constexpr int kTcXchg = 2 * 64 * 16;   // floats of the SwiGLU exchange (two buffers)
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -130,10 +143,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
           smem_addr(bar))
       : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
 // The four epilogue warps only (named barrier 2).
 __device__ __forceinline__ void tc_epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
@@ -164,7 +173,9 @@ struct TcArgs {
   float* partial;            // [kTcMaxCtas][kTcRmax][128]
   unsigned* flags;           // [kTcMaxCtas], zero between forwards
   int* status;
-  int NS, stage_bytes;       // the stage ring (the same as the shared segment's)
+  int NS, stage_bytes;       // the stage ring (shared by both passes)
+  unsigned long long* trace; // optional kernel trace, or null
+  int trace_id;
 };
 
 // A run's activation scales for the block-scaled MMA come as atoms of 4 K
@@ -176,14 +187,14 @@ __host__ __device__ inline size_t tc_sfb_offset(int A, int n, int kb) {
   return (size_t)A * 512 + 16 * (n % 32) + 4 * (n / 32) + kb;
 }
 
-// Bytes of shared memory after the stream segment's reduction area: barriers,
-// the SwiGLU exchange, two runs' activation-scale atoms (per-block steps,
-// 4 K bytes each) and the run table.
+// Bytes of shared memory after the stage ring's barriers: barriers, the
+// SwiGLU exchange (two buffers of 64 rows x 16 columns), two runs'
+// activation-scale atoms (per-block steps, 4 K bytes each) and the run table.
 __host__ __device__ inline size_t tc_sfb_smem(int K, bool rowscale) {
   return rowscale ? 0 : 2 * 4 * (size_t)K;
 }
 __host__ __device__ inline size_t tc_smem_bytes(int E, int K, bool rowscale) {
-  return 128 + 2 * kTcRmax * 64 * 4 + tc_sfb_smem(K, rowscale) +
+  return 128 + kTcXchg * 4 + tc_sfb_smem(K, rowscale) +
          ((size_t)(E + 1) * 4 + 127) / 128 * 128;
 }
 // One stage: weight nibbles (64 KC), weight scales (4 KC), then the planes of
@@ -192,9 +203,9 @@ constexpr int kTcPlaneOff = 68;   // planes start at 68 KC
 __host__ __device__ inline size_t tc_stage_bytes(int KC, int rmax) {
   return (size_t)KC * kTcPlaneOff + (size_t)(rmax < 2 ? 2 : rmax) * 4 * KC;
 }
-// Tensor-memory columns: two accumulators, a weight-scale slot per stage, and
-// either two constant activation-scale columns or two runs' scale sets (4
-// columns per 4 K blocks).
+// Tensor-memory columns: two accumulators (kTcDStride each), a weight-scale
+// slot per stage, and either two constant activation-scale columns or two
+// runs' scale sets (4 columns per 4 K blocks).
 __host__ __device__ inline int tc_tmem_cols(int K, int KC, int NS, bool rowscale) {
   return kTcSfaCol + NS * (KC / 32) + (rowscale ? 2 : 2 * (K / 32));
 }
@@ -207,8 +218,7 @@ struct TcSmem {
   uint64_t* sfb_empty;  // [2] and copied into tensor memory (commit)
   uint32_t* tbase;      // tensor-memory base address
   int* n_runs;
-  uint32_t* stage_after;   // the stage count after the routed step (segment A last)
-  float* xchg;          // [2][kTcRmax][64] up-half sums for the SwiGLU epilogue
+  float* xchg;          // [2][1024] up-half sums for the SwiGLU epilogues
   uint8_t* sfb;         // [2][4 K] activation-scale atoms of two runs (per-block steps)
   int* run_off;         // [n_active + 1] first run of each active slot
 };
@@ -223,9 +233,8 @@ __device__ __forceinline__ TcSmem tc_smem(uint8_t* p, int K, bool rowscale) {
   t.sfb_empty = b + 7;
   t.tbase = reinterpret_cast<uint32_t*>(b + 9);
   t.n_runs = reinterpret_cast<int*>(b + 9) + 1;
-  t.stage_after = reinterpret_cast<uint32_t*>(b + 10);
   t.xchg = reinterpret_cast<float*>(p + 128);
-  t.sfb = p + 128 + 2 * kTcRmax * 64 * 4;
+  t.sfb = p + 128 + kTcXchg * 4;
   t.run_off = reinterpret_cast<int*>(t.sfb + tc_sfb_smem(K, rowscale));
   return t;
 }
@@ -354,7 +363,7 @@ __device__ __forceinline__ void tc_produce(const TcArgs& b, const TcSmem& t, uin
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_t T,
                                        uint8_t* stages, uint64_t* full, uint64_t* empty,
-                                       uint32_t& stage, int KW) {
+                                       uint32_t& stage, int& jobs) {
   const int nact = __ldcg(b.n_active);
   const int nch = b.K / b.KC, upr = b.tiles * nch;
   int u0, u1;
@@ -375,7 +384,6 @@ __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_
   const uint32_t katoms = (uint32_t)b.K / 128;   // activation-scale atoms of a run
   uint32_t buf = stage % NS, ph = (stage / NS) & 1u;
   int rho = u0 / upr, idx = u0 - rho * upr, c = idx % nch;
-  int jobs = 0;
   uint32_t jb = 0, acc = 0;
   bool newjob = true;
   for (int u = u0, lr = 0; u < u1; ++rho, ++lr, idx = 0, c = 0, newjob = true) {
@@ -414,16 +422,14 @@ __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_
       for (uint32_t a = 0; a < natoms; ++a) umma_sf_copy(sfa + 4 * a, dS0 + off + 32 * a);
       const uint32_t sfb = rows ? sfb_run : sfb_run + 4 * (uint32_t)c * natoms;
       const uint32_t sfb_step = rows ? 0u : 4u;
-      const uint32_t dcol = T + 64 * jb;
+      const uint32_t dcol = T + kTcDStride * jb;
 #pragma unroll 8
       for (uint32_t j = 0; j < nsteps; ++j)
         umma_mxf4(dcol, dA0 + off + 256 * j, dB0 + off + 16 * j, (j & 1) ? id1 : id0,
                   sfa + 4 * (j >> 1), sfb + sfb_step * (j >> 1), acc | j);
       acc = 1;
-      // the stage is free once these MMAs have read it; the other KW - 1
-      // arrivals the barrier counts (one per CUDA-core consumer warp) come now
+      // the stage is free once these MMAs have read it
       umma_commit(&empty[buf]);
-      mbar_arrive_count(&empty[buf], (uint32_t)(KW - 1));
       newjob = c == nch - 1;
       if (newjob || u + i == u1 - 1) {
         umma_commit(&t.acc_full[jb]);
@@ -461,7 +467,7 @@ __device__ __forceinline__ void tc_wait_flag(const unsigned* f, int* status) {
 
 template <bool GLU>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, uint32_t T, int q,
-                                            int lane) {
+                                            int lane, int& jobs, int& fin) {
   mbar_wait(t.sched, 0, b.status);
   const int nact = __ldcg(b.n_active);
   const int nch = b.K / b.KC, upr = b.tiles * nch;
@@ -471,7 +477,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
   if (u0 >= u1) return;
   const uint32_t qaddr = (uint32_t)(32 * q) << 16;
   const int m = 32 * q + lane;   // MMA row of this thread
-  int cur = -1, jobs = 0, fin = 0;
+  int cur = -1;
   TcRun run{0, 0, 0};
   int pid[kTcRmax];
   float ps[kTcRmax][kPlanes];    // rowscale: the planes' scales of each pair's row
@@ -500,7 +506,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
     float v[64];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (16 * i < 8 * R) tmem_ld16(T + qaddr + 64 * (uint32_t)jb + 16 * i, v + 16 * i);
+      if (16 * i < 8 * R) tmem_ld16(T + qaddr + kTcDStride * (uint32_t)jb + 16 * i, v + 16 * i);
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
@@ -597,25 +603,334 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
 }
 
 // ---------------------------------------------------------------------------
-// The kernel: the routed step on the tensor cores and segment A (dense, CUDA
-// cores, stream.cuh) through one stage ring.  A_LAST = false: A first, its
-// weights streaming before the predecessor kernel is waited for (FC1: the
-// shared gate/up overlaps top-k).  A_LAST = true: the routed step first, right
-// after the predecessor's results land, and A after it, its weights streaming
-// while the routed step's last stages and epilogues drain (FC2: the shared
-// down projection's input is ready long before).
+// Dense pass: the shared expert, bf16 x bf16 -> fp32 (kind::f16)
 // ---------------------------------------------------------------------------
-template <class A, bool GLU, bool A_LAST>
-__global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
-    tc_dual_kernel(const StreamArgs a0, const TcArgs b) {
+// Operand layouts (no swizzle, K-major core matrices of 8 rows x 16 bytes):
+//  * weights: 128-row tiles, tile T at T * 256 K bytes, element (m, k) of a
+//    tile at (k / 8) * 2048 + m * 16 + (k % 8) * 2.  Gate/up tiles hold 64
+//    gate rows (MMA rows 0..63) and the matching 64 up rows (64..127), so one
+//    lane quarter pair ends with both halves of a feature.
+//  * activations: NP rows (a multiple of 16), element (n, k) at
+//    (k / 8) * NP * 16 + n * 16 + (k % 8) * 2, so a stage's K groups are one
+//    contiguous run (and one 8-element K group of a row-major [rows][K]
+//    matrix is one tensor-map box of 8 x NP).
+constexpr int kTcDenseMaxN = 128;   // MMA columns: 2 x 64 batch rows (hi, lo)
+
+__host__ __device__ inline size_t dense_w_offset(int K, int T, int m, int k) {
+  return (size_t)T * 256 * K + (size_t)(k / 8) * 2048 + (size_t)m * 16 + (size_t)(k % 8) * 2;
+}
+__host__ __device__ inline size_t dense_act_offset(int NP, int n, int k) {
+  return ((size_t)(k / 8) * NP + n) * 16 + (size_t)(k % 8) * 2;
+}
+__host__ __device__ inline int dense_np(int rows) { return (rows + 15) / 16 * 16; }
+__host__ __device__ inline size_t dense_stage_bytes(int KC, int NP) {
+  return (size_t)256 * KC + (size_t)NP * KC * 2;
+}
+
+struct TcDense {
+  const uint8_t* w;      // weight tiles (layout above)
+  const uint8_t* act;    // activation operand (layout above), or null: x through the tensor map
+  int K;                 // row length
+  int KC;                // K elements per stage (64 or 128)
+  int tiles;             // 128-row tiles
+  int N;                 // output features (gate/up: features, 64 per tile; down: rows)
+  int B;                 // batch rows
+  int NP;                // MMA columns: FC1 pad16(B), FC2 pad16(2 B) (row b = columns 2b, 2b+1)
+  float* out;            // [B][N] fp32
+  uint8_t* out_hl;       // gate/up: h_s as (hi, lo) bf16 columns 2b, 2b+1 (out_np columns)
+  int out_np;
+  float* partial;        // [kTcMaxCtas][kTcDenseMaxN][128]
+  unsigned* flags;       // [kTcMaxCtas], zero between forwards
+};
+
+// 2-D tensor-map load: box (8 K elements, NP rows) at (k0, 0) -> NP x 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major,
+// M = 128, N columns.
+__device__ __forceinline__ uint32_t umma_idesc_bf16(uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Producer: per unit the tile's K chunk (one bulk copy) and the activation
+// chunk (one bulk copy, or one tensor-map box per 8-element K group).
+__device__ __forceinline__ void dense_produce(const TcDense& d, const CUtensorMap* xmap,
+                                              uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                              int NS_, int stage_bytes, uint32_t& stage,
+                                              int* status) {
+  const int nch = d.K / d.KC, U = d.tiles * nch;
+  int u0, u1;
+  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+  const uint32_t abytes = 256u * d.KC, bbytes = (uint32_t)d.NP * d.KC * 2u;
+  const uint32_t gbytes = (uint32_t)d.NP * 16u;
+  const uint32_t NS = (uint32_t)NS_;
+  uint32_t buf = stage % NS, use = stage / NS;
+  int c = u0 % nch;
+  // chunk c of tile T at T * 256 K + c * abytes: the units of a range are contiguous
+  const uint8_t* ws = d.w + (size_t)u0 * abytes;
+  for (int u = u0; u < u1; ++u) {
+    if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, status);
+    uint8_t* dst = stages + (size_t)buf * stage_bytes;
+    mbar_arrive_expect_tx(&full[buf], abytes + bbytes);
+    bulk_g2s(dst, ws, abytes, &full[buf], pol_w);
+    if (d.act) {
+      bulk_g2s(dst + abytes, d.act + (size_t)c * bbytes, bbytes, &full[buf], pol_a);
+    } else {
+      for (int g = 0; g < d.KC / 8; ++g)
+        tma_load_2d(dst + abytes + g * gbytes, xmap, c * d.KC + 8 * g, 0, &full[buf], pol_a);
+    }
+    ws += abytes;
+    if (++c == nch) c = 0;
+    if (++buf == NS) {
+      buf = 0;
+      ++use;
+    }
+    ++stage;
+  }
+}
+
+// MMA issuer: KC / 16 MMAs per unit into the job's accumulator.
+__device__ __forceinline__ void dense_mma(const TcDense& d, const TcSmem& t, uint32_t T,
+                                          uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                          int NS_, int stage_bytes, uint32_t& stage, int& jobs,
+                                          int* status) {
+  const int nch = d.K / d.KC, U = d.tiles * nch;
+  int u0, u1;
+  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint32_t NS = (uint32_t)NS_, KC = (uint32_t)d.KC, NP = (uint32_t)d.NP;
+  const uint32_t sa0 = smem_addr(stages);
+  const uint32_t st16 = (uint32_t)stage_bytes >> 4;
+  const uint64_t dA0 = umma_desc(sa0, 2048, 128);              // weights: K groups 2 KB apart
+  const uint64_t dB0 = umma_desc(sa0 + 256 * KC, NP * 16, 128); // activations: K groups NP*16 apart
+  const uint32_t id = umma_idesc_bf16(NP);
+  const uint32_t a_step = 4096u >> 4, b_step = (32u * NP) >> 4;   // per 16 K elements
+  uint32_t buf = stage % NS, ph = (stage / NS) & 1u;
+  int c = u0 % nch;
+  uint32_t jb = 0;
+  bool newjob = true;
+  for (int u = u0; u < u1; ++u) {
+    if (newjob) {   // a new tile job: a free accumulator, zero-initialised by its first MMA
+      jb = (uint32_t)jobs & 1u;
+      if (jobs >= 2) {
+        mbar_wait(&t.acc_empty[jb], (uint32_t)((jobs >> 1) - 1) & 1u, status);
+        tc_fence_after();
+      }
+    }
+    mbar_wait(&full[buf], ph, status);
+    tc_fence_after();
+    const uint64_t off = (uint64_t)(buf * st16);
+    const uint32_t dcol = T + kTcDStride * jb;
+    const uint32_t acc0 = newjob ? 0u : 1u;
+#pragma unroll 8
+    for (uint32_t j = 0; j < KC / 16; ++j)
+      umma_f16(dcol, dA0 + off + a_step * j, dB0 + off + b_step * j, id, acc0 | j);
+    umma_commit(&empty[buf]);
+    newjob = c == nch - 1;
+    if (newjob || u == u1 - 1) {
+      umma_commit(&t.acc_full[jb]);
+      ++jobs;
+    }
+    if (++c == nch) c = 0;
+    if (++buf == NS) {
+      buf = 0;
+      ph ^= 1u;
+    }
+    ++stage;
+  }
+}
+
+// Epilogue: per tile job the NP accumulator columns of this thread's row, the
+// stream-K fix-up, then gate/up: SwiGLU through the exchange (16 columns at a
+// time) to h_s (fp32, and (hi, lo) bf16 for the down projection); down:
+// y_s[b] = column 2b + column 2b + 1.
+template <bool GLU>
+__device__ __forceinline__ void dense_epilogue(const TcDense& d, const TcSmem& t, uint32_t T,
+                                               int q, int lane, int& jobs, int& fin, int* status) {
+  const int nch = d.K / d.KC, U = d.tiles * nch;
+  int u0, u1;
+  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  if (u0 >= u1) return;
+  const uint32_t qaddr = (uint32_t)(32 * q) << 16;
+  const int m = 32 * q + lane;   // MMA row of this thread
+  const int NP = d.NP;
+  constexpr int NCH = kTcDenseMaxN / 16;
+  for (int u = u0; u < u1;) {
+    const int tile = u / nch, cs = u - tile * nch;
+    const int tile_end = (tile + 1) * nch;
+    const int ue = min(u1, tile_end);
+    const int ce = cs + (ue - u);
+    const int jb = jobs & 1;
+    mbar_wait(&t.acc_full[jb], (uint32_t)(jobs >> 1) & 1u, status);
+    tc_fence_after();
+    float v[kTcDenseMaxN];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i)
+      if (16 * i < NP) tmem_ld16(T + qaddr + kTcDStride * (uint32_t)jb + 16 * i, v + 16 * i);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&t.acc_empty[jb]);
+    ++jobs;
+    if (cs > 0) {
+      // the tile's first chunks belong to an earlier CTA: leave the sums to it
+      float* slot = d.partial + (size_t)blockIdx.x * (kTcDenseMaxN * 128);
+#pragma unroll
+      for (int n = 0; n < kTcDenseMaxN; ++n)
+        if (n < NP) slot[n * 128 + m] = v[n];
+      tc_epi_sync();
+      if (m == 0) {
+        __threadfence();
+        atomicExch(d.flags + blockIdx.x, 1u);
+      }
+      u = ue;
+      continue;
+    }
+    if (ce < nch) {
+      // later chunks of this tile were streamed by the next CTAs
+      for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+        int j0, j1;
+        tc_range(U, j, gridDim.x, j0, j1);
+        if (j0 >= tile_end) break;
+        if (j1 <= j0) continue;
+        if (lane == 0) tc_wait_flag(d.flags + j, status);
+        __syncwarp();
+        const float* slot = d.partial + (size_t)j * (kTcDenseMaxN * 128);
+#pragma unroll
+        for (int n = 0; n < kTcDenseMaxN; ++n)
+          if (n < NP) v[n] += __ldcg(slot + n * 128 + m);
+      }
+      tc_epi_sync();
+      if (m == 0) {
+        for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+          int j0, j1;
+          tc_range(U, j, gridDim.x, j0, j1);
+          if (j0 >= tile_end) break;
+          d.flags[j] = 0u;
+        }
+      }
+    }
+    if constexpr (GLU) {
+      // rows 0..63 of the tile are gate rows, 64..127 the matching up rows;
+      // column b is batch row b
+      const int feat = tile * 64 + (m & 63);
+#pragma unroll
+      for (int ci = 0; ci < NCH; ++ci) {
+        if (16 * ci >= NP) break;
+        float* xg = t.xchg + (fin & 1) * 1024;
+        if (q >= 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xg[i * 64 + m - 64] = v[16 * ci + i];
+        }
+        tc_epi_sync();
+        if (q < 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int b = 16 * ci + i;
+            if (b < d.B) {
+              const float g = v[16 * ci + i], uu = xg[i * 64 + m];
+              const float hv = g / (1.0f + expf(-g)) * uu;
+              d.out[(size_t)b * d.N + feat] = hv;
+              if (d.out_hl) {
+                const uint16_t hi = f32_to_bf16_bits(hv);
+                const uint16_t lo = f32_to_bf16_bits(hv - bf16_bits_to_f32(hi));
+                *reinterpret_cast<uint16_t*>(d.out_hl + dense_act_offset(d.out_np, 2 * b, feat)) = hi;
+                *reinterpret_cast<uint16_t*>(d.out_hl + dense_act_offset(d.out_np, 2 * b + 1, feat)) =
+                    lo;
+              }
+            }
+          }
+        }
+        ++fin;
+      }
+    } else {
+      const int row = tile * 128 + m;
+#pragma unroll
+      for (int b = 0; b < kTcDenseMaxN / 2; ++b)
+        if (b < d.B) d.out[(size_t)b * d.N + row] = v[2 * b] + v[2 * b + 1];
+    }
+    u = ue;
+  }
+}
+
+// Shared-expert bf16 weights [rows][K] (row-major) -> 128-row tiles of the
+// layout above.  GLU: rows are the gate half then the up half (rows / 2
+// each), and tile T takes gate rows 64T..64T+63 then the matching up rows.
+static __global__ void dense_relayout_kernel(const uint16_t* src, int64_t rows, int K, int glu,
+                                             uint8_t* dst) {
+  const int64_t G = K / 8, total = rows * G;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / G;
+    const int g = (int)(i - r * G);
+    int64_t T, mrow;
+    if (glu) {
+      const int64_t half = rows / 2, j = r < half ? r : r - half;
+      T = j / 64;
+      mrow = j % 64 + (r < half ? 0 : 64);
+    } else {
+      T = r / 128;
+      mrow = r % 128;
+    }
+    const uint4 v = *reinterpret_cast<const uint4*>(src + r * K + (int64_t)g * 8);
+    *reinterpret_cast<uint4*>(dst + dense_w_offset(K, (int)T, (int)mrow, 8 * g)) = v;
+  }
+}
+
+// Wait until the last use of every stage has been consumed, so no copy is
+// still landing in this CTA's shared memory when it exits.
+__device__ __forceinline__ void tc_drain(uint64_t* empty, int NS, uint32_t stage, int* status) {
+  for (int b = 0; b < NS && (uint32_t)b < stage; ++b) {
+    const uint32_t uses = (stage - (uint32_t)b + (uint32_t)NS - 1) / (uint32_t)NS;
+    mbar_wait(&empty[b], (uses - 1) & 1u, status);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  FC1 (GLU, DENSE_FIRST): the dense gate/up pass on x, which the
+// predecessor kernels do not write, then the wait for top-k, then the routed
+// gate/up pass.  FC2: the wait for FC1, the routed down pass, then the dense
+// down pass on h_s.
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 192;
+
+__host__ __device__ inline size_t tc_kernel_smem(int NS, int stage_bytes, int E, int K,
+                                                 bool rowscale) {
+  return (size_t)NS * stage_bytes + (size_t)NS * 16 + tc_smem_bytes(E, K, rowscale);
+}
+
+template <bool GLU, bool DENSE_FIRST>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_kernel(const TcArgs b, const TcDense dn, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KW = (int)(blockDim.x >> 5) - 1;
-  trace_begin(a0.trace, a0.trace_id);
-  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
-  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp + 16), b.K,
-                           b.rowscale != 0);
+  trace_begin(b.trace, b.trace_id);
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)b.NS * b.stage_bytes);
+  uint64_t* empty = full + b.NS;
+  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(empty + b.NS), b.K, b.rowscale != 0);
   if (threadIdx.x == 0) {
+    for (int i = 0; i < b.NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&t.acc_full[i], 1);
       mbar_init(&t.acc_empty[i], 4);
@@ -630,7 +945,7 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t T = *t.tbase;
-  if (b.rowscale && warp >= 2 && warp < 6) {
+  if (b.rowscale && warp >= 2) {
     // per-row activation scales: the MMAs multiply by 1 (code 127) and the
     // epilogue applies each plane's scale
     const uint32_t col = kTcSfaCol + (uint32_t)b.NS * ((uint32_t)b.KC / 32);
@@ -638,48 +953,58 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     tmem_wait_st();
     tc_fence_before();
   }
+  // the constant columns are written before any MMA is issued
+  __syncthreads();
+  tc_fence_after();
   pdl_launch_dependents();
+  if (!DENSE_FIRST) pdl_wait_prerequisites();
   uint32_t stage = 0;
+  int jobs = 0, fin = 0;
   if (warp == 0) {
     if (lane == 0) {
-      if (!A_LAST) cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
+      if (DENSE_FIRST) {
+        dense_produce(dn, &xmap, stages, full, empty, b.NS, b.stage_bytes, stage, b.status);
+        pdl_wait_prerequisites();
+        tc_produce(b, t, stages, full, empty, stage);
+      } else {
+        tc_produce(b, t, stages, full, empty, stage);
+        dense_produce(dn, &xmap, stages, full, empty, b.NS, b.stage_bytes, stage, b.status);
+      }
+      tc_drain(empty, b.NS, stage, b.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (DENSE_FIRST) {
+      if (lane == 0)
+        dense_mma(dn, t, T, stages, full, empty, b.NS, b.stage_bytes, stage, jobs, b.status);
+      __syncwarp();
       pdl_wait_prerequisites();
-      tc_produce(b, t, m.stages, m.full, m.empty, stage);
-      if (A_LAST) cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
-      stream_drain(a0, m.empty, stage);
+      tc_schedule(b, t, lane);
+      if (lane == 0) tc_mma(b, t, T, stages, full, empty, stage, jobs);
+    } else {
+      tc_schedule(b, t, lane);
+      if (lane == 0) {
+        tc_mma(b, t, T, stages, full, empty, stage, jobs);
+        dense_mma(dn, t, T, stages, full, empty, b.NS, b.stage_bytes, stage, jobs, b.status);
+      }
     }
     __syncwarp();
   } else {
-    int pp = 0, rp = 0;
-    if (!A_LAST)
-      cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
-    pdl_wait_prerequisites();
-    // every consumer is past segment A's last shared-memory combine (and the
-    // constant activation scales are in tensor memory)
-    consumer_sync(KW * 32);
-    if (warp == 1) {
-      tc_schedule(b, t, lane);
-      if (lane == 0) {
-        tc_fence_after();
-        tc_mma(b, t, T, m.stages, m.full, m.empty, stage, KW);
-        if (A_LAST) *t.stage_after = stage;
-      }
-      __syncwarp();
-    } else if (warp < 6) {
-      tc_epilogue<GLU>(b, t, T, warp & 3, lane);
-    }
-    if (A_LAST) {
-      // segment A continues the ring where the routed step's MMAs left it
-      consumer_sync(KW * 32);
-      stage = *t.stage_after;
-      cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    const int q = warp & 3;
+    if (DENSE_FIRST) {
+      dense_epilogue<GLU>(dn, t, T, q, lane, jobs, fin, b.status);
+      pdl_wait_prerequisites();
+      tc_epilogue<GLU>(b, t, T, q, lane, jobs, fin);
+    } else {
+      tc_epilogue<GLU>(b, t, T, q, lane, jobs, fin);
+      dense_epilogue<GLU>(dn, t, T, q, lane, jobs, fin, b.status);
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(T);
-  trace_end(a0.trace, a0.trace_id);
+  trace_end(b.trace, b.trace_id);
 }
 
 }  // namespace moe
