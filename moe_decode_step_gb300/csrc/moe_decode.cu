@@ -218,9 +218,9 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_FC2_KERNEL(RS, NBM) \
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
 // Tensor-core path: FC1 streams the shared gate/up first (while top-k runs),
-// FC2 the routed down projection first and the shared one last.
-#define MOE_TC1_KERNEL tc_kernel<true, true>
-#define MOE_TC2_KERNEL tc_kernel<false, false>
+// FC2 the shared down first (its weights requested before FC1 is waited for).
+#define MOE_TC1_KERNEL tc_kernel<true>
+#define MOE_TC2_KERNEL tc_kernel<false>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -618,8 +618,8 @@ int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   return launch_tc(MOE_TC1_KERNEL, p, b, dn, xmap, st, grid);
 }
 
-// FC2 on the tensor-core path: routed down (h planes x UMMA-layout weights),
-// then the shared down as a dense pass on h_s's (hi, lo) columns.
+// FC2 on the tensor-core path: the shared down as a dense pass on h_s's
+// (hi, lo) columns, then routed down (h planes x UMMA-layout weights).
 int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   const moe_dims_t& d = L->dims;
   const StreamPlan& p = L->plan[kStepTc2][batch_class(B)];

@@ -265,26 +265,34 @@ __device__ __forceinline__ void tc_range(int U, int i, int G, int& u0, int& u1) 
   u1 = (int)((long long)U * (i + 1) / G);
 }
 
-// Warp 1: first run of every active slot (passes of <= kTcRmax pairs).
+// One warp: first run of every active slot (passes of <= kTcRmax pairs).
+// Each lane first loads the pair counts of 8 slots (independent loads, one
+// round trip to L2 per 256 slots), then the warp scans them.
 __device__ __forceinline__ void tc_schedule(const TcArgs& b, const TcSmem& t, int lane) {
   const int nact = __ldcg(b.n_active);
   int base = 0;
   if (lane == 0) t.run_off[0] = 0;
-  for (int s0 = 0; s0 < nact; s0 += 32) {
-    const int s = s0 + lane;
-    int passes = 0;
-    if (s < nact) {
-      const int pr = __ldcg(b.active_off + s + 1) - __ldcg(b.active_off + s);
-      passes = (pr + kTcRmax - 1) / kTcRmax;
-    }
-    int incl = passes;
+  for (int s0 = 0; s0 < nact; s0 += 32 * 8) {
+    int passes[8];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+    for (int i = 0; i < 8; ++i) {
+      const int s = s0 + 32 * i + lane;
+      int pr = 0;
+      if (s < nact) pr = __ldcg(b.active_off + s + 1) - __ldcg(b.active_off + s);
+      passes[i] = (pr + kTcRmax - 1) / kTcRmax;
     }
-    if (s < nact) t.run_off[s + 1] = base + incl;
-    base += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int incl = passes[i];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int s = s0 + 32 * i + lane;
+      if (s < nact) t.run_off[s + 1] = base + incl;
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
   __syncwarp();
   if (lane == 0) {
@@ -364,6 +372,8 @@ __device__ __forceinline__ void tc_produce(const TcArgs& b, const TcSmem& t, uin
 __device__ __forceinline__ void tc_mma(const TcArgs& b, const TcSmem& t, uint32_t T,
                                        uint8_t* stages, uint64_t* full, uint64_t* empty,
                                        uint32_t& stage, int& jobs) {
+  mbar_wait(t.sched, 0, b.status);
+  tc_fence_after();
   const int nact = __ldcg(b.n_active);
   const int nch = b.K / b.KC, upr = b.tiles * nch;
   int u0, u1;
@@ -668,24 +678,47 @@ __device__ __forceinline__ void umma_f16(uint32_t d, uint64_t a, uint64_t b, uin
 }
 
 // Producer: per unit the tile's K chunk (one bulk copy) and the activation
-// chunk (one bulk copy, or one tensor-map box per 8-element K group).
+// chunk (one bulk copy, or one tensor-map box per 8-element K group).  With
+// `wait_between` (the activations come from the predecessor kernel, and the
+// ring is empty: stage 0) the weights of the first NS units are requested
+// first, the predecessor is waited for, and then their activation chunks.
 __device__ __forceinline__ void dense_produce(const TcDense& d, const CUtensorMap* xmap,
                                               uint8_t* stages, uint64_t* full, uint64_t* empty,
                                               int NS_, int stage_bytes, uint32_t& stage,
-                                              int* status) {
+                                              int* status, bool wait_between) {
   const int nch = d.K / d.KC, U = d.tiles * nch;
   int u0, u1;
   tc_range(U, blockIdx.x, gridDim.x, u0, u1);
-  if (u0 >= u1) return;
+  if (u0 >= u1) {
+    if (wait_between) pdl_wait_prerequisites();
+    return;
+  }
   const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
   const uint32_t abytes = 256u * d.KC, bbytes = (uint32_t)d.NP * d.KC * 2u;
   const uint32_t gbytes = (uint32_t)d.NP * 16u;
   const uint32_t NS = (uint32_t)NS_;
-  uint32_t buf = stage % NS, use = stage / NS;
-  int c = u0 % nch;
   // chunk c of tile T at T * 256 K + c * abytes: the units of a range are contiguous
   const uint8_t* ws = d.w + (size_t)u0 * abytes;
-  for (int u = u0; u < u1; ++u) {
+  int npre = 0;
+  if (wait_between) {
+    npre = min(u1 - u0, NS_);
+    for (int i = 0; i < npre; ++i) {
+      uint8_t* dst = stages + (size_t)i * stage_bytes;
+      mbar_arrive_expect_tx(&full[i], abytes + bbytes);
+      bulk_g2s(dst, ws + (size_t)i * abytes, abytes, &full[i], pol_w);
+    }
+    pdl_wait_prerequisites();
+    for (int i = 0; i < npre; ++i) {
+      const int c = (u0 + i) % nch;
+      bulk_g2s(stages + (size_t)i * stage_bytes + abytes, d.act + (size_t)c * bbytes, bbytes,
+               &full[i], pol_a);
+    }
+    ws += (size_t)npre * abytes;
+    stage += (uint32_t)npre;
+  }
+  uint32_t buf = stage % NS, use = stage / NS;
+  int c = (u0 + npre) % nch;
+  for (int u = u0 + npre; u < u1; ++u) {
     if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, status);
     uint8_t* dst = stages + (size_t)buf * stage_bytes;
     mbar_arrive_expect_tx(&full[buf], abytes + bbytes);
@@ -904,19 +937,22 @@ __device__ __forceinline__ void tc_drain(uint64_t* empty, int NS, uint32_t stage
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  FC1 (GLU, DENSE_FIRST): the dense gate/up pass on x, which the
-// predecessor kernels do not write, then the wait for top-k, then the routed
-// gate/up pass.  FC2: the wait for FC1, the routed down pass, then the dense
-// down pass on h_s.
+// The kernel.  FC1 (GLU): the dense gate/up pass on x, which the predecessor
+// kernels do not write, then the routed gate/up pass once top-k's tables are
+// in.  FC2: the dense down pass first, its weight copies requested before
+// FC1 is waited for (they fill the gap while FC1's last CTAs drain), then the
+// routed down pass.  Warp 6 builds the routed run table as soon as the
+// predecessor's tables are visible, while the other roles are still in the
+// dense pass.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 
 __host__ __device__ inline size_t tc_kernel_smem(int NS, int stage_bytes, int E, int K,
                                                  bool rowscale) {
   return (size_t)NS * stage_bytes + (size_t)NS * 16 + tc_smem_bytes(E, K, rowscale);
 }
 
-template <bool GLU, bool DENSE_FIRST>
+template <bool GLU>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_kernel(const TcArgs b, const TcDense dn, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -945,7 +981,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t T = *t.tbase;
-  if (b.rowscale && warp >= 2) {
+  if (b.rowscale && warp >= 2 && warp < 6) {
     // per-row activation scales: the MMAs multiply by 1 (code 127) and the
     // epilogue applies each plane's scale
     const uint32_t col = kTcSfaCol + (uint32_t)b.NS * ((uint32_t)b.KC / 32);
@@ -957,48 +993,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   pdl_launch_dependents();
-  if (!DENSE_FIRST) pdl_wait_prerequisites();
   uint32_t stage = 0;
   int jobs = 0, fin = 0;
   if (warp == 0) {
     if (lane == 0) {
-      if (DENSE_FIRST) {
-        dense_produce(dn, &xmap, stages, full, empty, b.NS, b.stage_bytes, stage, b.status);
-        pdl_wait_prerequisites();
-        tc_produce(b, t, stages, full, empty, stage);
-      } else {
-        tc_produce(b, t, stages, full, empty, stage);
-        dense_produce(dn, &xmap, stages, full, empty, b.NS, b.stage_bytes, stage, b.status);
-      }
+      dense_produce(dn, &xmap, stages, full, empty, b.NS, b.stage_bytes, stage, b.status, !GLU);
+      if (GLU) pdl_wait_prerequisites();
+      tc_produce(b, t, stages, full, empty, stage);
       tc_drain(empty, b.NS, stage, b.status);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (DENSE_FIRST) {
-      if (lane == 0)
-        dense_mma(dn, t, T, stages, full, empty, b.NS, b.stage_bytes, stage, jobs, b.status);
-      __syncwarp();
+    if (lane == 0) {
+      dense_mma(dn, t, T, stages, full, empty, b.NS, b.stage_bytes, stage, jobs, b.status);
       pdl_wait_prerequisites();
-      tc_schedule(b, t, lane);
-      if (lane == 0) tc_mma(b, t, T, stages, full, empty, stage, jobs);
-    } else {
-      tc_schedule(b, t, lane);
-      if (lane == 0) {
-        tc_mma(b, t, T, stages, full, empty, stage, jobs);
-        dense_mma(dn, t, T, stages, full, empty, b.NS, b.stage_bytes, stage, jobs, b.status);
-      }
+      tc_mma(b, t, T, stages, full, empty, stage, jobs);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     const int q = warp & 3;
-    if (DENSE_FIRST) {
-      dense_epilogue<GLU>(dn, t, T, q, lane, jobs, fin, b.status);
-      pdl_wait_prerequisites();
-      tc_epilogue<GLU>(b, t, T, q, lane, jobs, fin);
-    } else {
-      tc_epilogue<GLU>(b, t, T, q, lane, jobs, fin);
-      dense_epilogue<GLU>(dn, t, T, q, lane, jobs, fin, b.status);
-    }
+    dense_epilogue<GLU>(dn, t, T, q, lane, jobs, fin, b.status);
+    pdl_wait_prerequisites();
+    tc_epilogue<GLU>(b, t, T, q, lane, jobs, fin);
+  } else {
+    pdl_wait_prerequisites();
+    tc_schedule(b, t, lane);
   }
   tc_fence_before();
   __syncthreads();
