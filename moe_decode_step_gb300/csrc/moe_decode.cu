@@ -79,6 +79,10 @@ struct Workspace {
   uint8_t* hs_hl;    // [f_shared / 8][2 B padded][16 bytes]
   float* dpartial;
   unsigned* dflags;
+  // the tensor-core router's own stream-K slots (FC1's dense pass may run
+  // while the router's last CTAs finish)
+  float* rpartial;
+  unsigned* rflags;
 };
 
 // Launch shape of one streaming-GEMV step.
@@ -87,9 +91,10 @@ struct StreamPlan {
   int kc = 1;      // K chunks per item of the MXFP4 segment (CUDA-core path)
   int tc_kc = 0;   // K elements per stage of the tensor-core routed pass
   int dense_kc = 0;   // K elements per stage of the tensor-core dense pass
+  int dense_ctas = 0;   // CTAs of the dense pass (0: the whole grid)
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kNumSteps };
 
 // Expert paths: mma.sync on the tiled layouts (the GEMV regime: weights
 // converted to f16 in registers), or tcgen05 on the UMMA layouts (block-scaled
@@ -132,6 +137,7 @@ struct moe_layer {
   // tcgen05 path: the shared expert's bf16 weights in the dense pass's tiles
   uint8_t* sh_gu_umma = nullptr;
   uint8_t* sh_d_umma = nullptr;
+  uint8_t* router_umma = nullptr;   // router weights in 128-row tiles (last one zero-padded)
   void* sh_owned = nullptr;
   void* encode_tiled = nullptr;   // the driver's tensor-map encoder
 };
@@ -176,6 +182,8 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.hs_hl = carve<uint8_t>(p, (size_t)d.f_shared * dense_np(2 * (int)B) * 2);
   w.dpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
   w.dflags = carve<unsigned>(p, kTcMaxCtas);
+  w.rpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
+  w.rflags = carve<unsigned>(p, kTcMaxCtas);
   if (ws) *ws = w;
   return (size_t)(p - base);
 }
@@ -350,6 +358,33 @@ int plan_tc(Kern kern, int K, int K_dense, int rmax, int np_max, bool rowscale, 
 // Largest batch of each batch class (B = 1, B <= 8, B <= 64).
 constexpr int kClassMaxB[3] = {1, 8, 64};
 
+// Launch shape of the tensor-core router: a stage ring of dense stages.
+int plan_tc_router(int K, int np_max, int E, int n_sm, int budget, StreamPlan* p) {
+  if (K % 128 != 0 || n_sm > kTcMaxCtas || np_max > 64) return MOE_ERR_UNSUPPORTED;
+  StreamPlan r;
+  r.threads = kTcThreads;
+  r.dense_kc = 128;
+  r.stage_bytes = (int)((dense_stage_bytes(r.dense_kc, np_max) + 127) / 128 * 128);
+  const int extra = (int)tc_smem_bytes(E, K, true);
+  r.NS = std::min(16, (budget - extra) / (r.stage_bytes + 16));
+  if (r.NS < 2) return MOE_ERR_UNSUPPORTED;
+  r.smem = std::max((int)tc_kernel_smem(r.NS, r.stage_bytes, E, K, true), 116 * 1024);
+  if (r.smem > budget) return MOE_ERR_UNSUPPORTED;
+  MOE_CUDA(cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                budget));
+  int occ = 0;
+  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tc_router_kernel, r.threads,
+                                                         r.smem));
+  if (occ != 1) return MOE_ERR_UNSUPPORTED;
+  r.grid = n_sm;
+  // the logits on at most four CTAs per 128-row tile (each tile's finisher
+  // adds the others' partial sums, one round trip to L2 per CTA); the other
+  // CTAs quantize the x planes
+  r.dense_ctas = std::min(n_sm, (E + 127) / 128 * 4);
+  *p = r;
+  return MOE_OK;
+}
+
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
@@ -369,6 +404,8 @@ int plan_all(moe_layer* L) {
                         &L->plan[kStepTc1][c])));
       MOE_PLAN((plan_tc(MOE_TC2_KERNEL, d.f, d.f_shared, rmax, dense_np(2 * kClassMaxB[c]), false,
                         E, n, bud, &L->plan[kStepTc2][c])));
+      MOE_PLAN((plan_tc_router(d.d, dense_np(kClassMaxB[c]), E, n, bud,
+                               &L->plan[kStepTcRouter][c])));
     }
   }
   if (!L->wm.ok) return MOE_OK;
@@ -443,6 +480,8 @@ int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_i
 // The tensor-core path for a forward of B rows?
 bool use_tc(const moe_layer* L, int B) { return L->wt.ok && (!L->wm.ok || B >= L->tc_min_batch); }
 
+int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B);
+
 int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* idx, float* w) {
   const moe_dims_t& d = L->dims;
   StreamArgs a = base_args(L);
@@ -453,13 +492,20 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.x = static_cast<const uint16_t*>(x);
   a.out = L->ws.logits;
   a.trace_id = 0;
-  if (use_tc(L, B)) {   // the activation planes the tensor-core FC1 streams
-    a.xq = L->ws.x_act;
-    a.xq_code = L->ws.x_code;
+  int rc;
+  if (use_tc(L, B) && batch_class(B) == 2) {
+    // above 8 rows the CUDA-core router is compute-bound (passes of 4 rows):
+    // logits on the tensor cores, plus the activation planes the tensor-core
+    // FC1 streams
+    if ((rc = launch_router_tc(L, st, x, B))) return rc;
+  } else {
+    if (use_tc(L, B)) {   // the activation planes the tensor-core FC1 streams
+      a.xq = L->ws.x_act;
+      a.xq_code = L->ws.x_code;
+    }
+    rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts, st, false);
+    if (rc) return rc;
   }
-  int rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts,
-                       st, false);
-  if (rc) return rc;
   TopkArgs t{};
   t.logits = L->ws.logits;
   t.bias = L->w.router_bias;
@@ -579,6 +625,37 @@ int encode_x_map(moe_layer* L, const void* x, int B, int NP, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
+// The router on the tensor-core path: logits [B][E] as a dense pass on x, and
+// the x planes of the routed FC1.  The first kernel of a forward: no
+// programmatic launch (everything before it in the stream has finished).
+int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
+  const moe_dims_t& d = L->dims;
+  const StreamPlan& p = L->plan[kStepTcRouter][batch_class(B)];
+  TcDense dn = dense_base_args(L, p, B);
+  dn.w = L->router_umma;
+  dn.K = d.d;
+  dn.tiles = (d.n_experts + 127) / 128;
+  dn.N = d.n_experts;
+  dn.NP = dense_np(B);
+  dn.out = L->ws.logits;
+  dn.partial = L->ws.rpartial;
+  dn.flags = L->ws.rflags;
+  dn.ctas = p.dense_ctas;
+  TcXPlanes xp;
+  xp.x = static_cast<const uint16_t*>(x);
+  xp.B = B;
+  xp.K = d.d;
+  xp.xq = L->ws.x_act;
+  xp.xq_code = L->ws.x_code;
+  CUtensorMap xmap;
+  int rc = encode_x_map(L, x, B, dn.NP, &xmap);
+  if (rc) return rc;
+  MOE_CUDA(launch_ex(tc_router_kernel, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, false,
+                     dn, xmap, xp, p.NS, p.stage_bytes, L->ws.status,
+                     L->tracing ? L->ws.trace : (unsigned long long*)nullptr));
+  return MOE_OK;
+}
+
 // FC1 on the tensor-core path: the shared gate/up as a dense pass on x, then
 // routed gate/up (x planes x UMMA-layout weights), SwiGLU, h and its planes.
 int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
@@ -644,6 +721,7 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   dn.tiles = d.d / 128;
   dn.N = d.d;
   dn.NP = dense_np(2 * B);
+  dn.hilo = 1;
   dn.out = L->ws.y_s;
   CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
@@ -835,13 +913,19 @@ int setup_weights(moe_layer* L, const moe_weights_t& w, int want, ExpertWeights&
 int setup_dense(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const size_t gu = (size_t)2 * d.f_shared * d.d * 2, dn = (size_t)d.d * d.f_shared * 2;
-  if (cudaMalloc(&L->sh_owned, gu + dn) != cudaSuccess) {
+  const size_t rt = (size_t)(d.n_experts + 127) / 128 * 128 * d.d * 2;
+  if (cudaMalloc(&L->sh_owned, gu + dn + rt) != cudaSuccess) {
     cudaGetLastError();
     L->sh_owned = nullptr;
     return MOE_ERR_ALLOC;
   }
   L->sh_gu_umma = static_cast<uint8_t*>(L->sh_owned);
   L->sh_d_umma = L->sh_gu_umma + gu;
+  L->router_umma = L->sh_d_umma + dn;
+  MOE_CUDA(cudaMemset(L->router_umma, 0, rt));
+  dense_relayout_kernel<<<L->n_sm * 8, 256>>>(static_cast<const uint16_t*>(L->w.router_w),
+                                               (int64_t)d.n_experts, d.d, 0, L->router_umma);
+  MOE_CUDA(cudaGetLastError());
   dense_relayout_kernel<<<L->n_sm * 8, 256>>>(static_cast<const uint16_t*>(L->w.shared_gu),
                                                2LL * d.f_shared, d.d, 1, L->sh_gu_umma);
   MOE_CUDA(cudaGetLastError());

@@ -368,6 +368,16 @@ __device__ __forceinline__ int stream_x_row(const StreamArgs& a, int pid) {
   return ROUTED ? pid / a.k : pid;
 }
 
+// Epilogue thread index of consumer thread ct when only the first `busy` of
+// the KW consumer warps own K elements: the idle warps take the first
+// outputs, so the per-item finalisation (partial sums, SwiGLU, stores) stays
+// off the critical path of the warps that do the products.
+__device__ __forceinline__ int stream_epi_index(int ct, int busy, int KW) {
+  const int cthreads = 32 * KW, ct0 = busy < KW ? 32 * busy : 0;
+  const int e = ct - ct0;
+  return e < 0 ? e + cthreads : e;
+}
+
 // Sum of the n <= kMmaWarps partials at p, in order 0..n-1: the bound is a
 // compile-time constant so every load issues before the dependent adds.
 __device__ __forceinline__ float slab_sum(const float* p, int n) {
@@ -462,7 +472,8 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
       if (V > 32) rb[(32 + vi) * KW + kw] = second;
     }
     consumer_sync(cthreads);
-    for (int t = ct; t < RW * R; t += cthreads) {
+    const int busy = min(KW, (a.K + Sh::WARP_K - 1) / Sh::WARP_K);
+    for (int t = stream_epi_index(ct, busy, KW); t < RW * R; t += cthreads) {
       const int j = t / R, r = t % R;
       const int row = row0 + j;
       if (row >= a.N) continue;
@@ -575,7 +586,9 @@ __device__ __forceinline__ void stream_consume_run_mma(
 
   // the column this lane feeds, and this thread's output column in the epilogue
   const int ci = min(g, R - 1);
-  const int ei = ct % R;
+  // outputs go first to the consumer warps that own no K blocks
+  const int et = stream_epi_index(ct, min(KW, (nblk + NB - 1) / NB), KW);
+  const int ei = et % R;
   const int cpid = __ldcg(a.pair_list + m.p0 + done + ci);
   const int epid = __ldcg(a.pair_list + m.p0 + done + ei);
 
@@ -646,7 +659,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
   const uint32_t NS = (uint32_t)a.NS, KC = (uint32_t)a.kc;
   uint32_t cbuf = (stage + (uint32_t)chunk) % NS, cph = ((stage + (uint32_t)chunk) / NS) & 1u;
   uint32_t ibuf = stage % NS;
-  const int ej = ct / R;   // this thread's output row (pair) within an item, column ei
+  const int ej = et / R;   // this thread's output row (pair) within an item, column ei
   int row0 = stream_row0<true, TR>(it0, tiles);
 
   for (int it = it0; it < run_end; ++it, row0 += TR) {
@@ -695,7 +708,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
         if (col < R) rbuf[((mb * 16 + row) * RMAX + col) * KW + kw] = acc[mb][i];
       }
     consumer_sync(cthreads);
-    if (ct < TR * R) {
+    if (et < TR * R) {
       const int j = ej;
       const int row = row0 + j;
       if (row < a.N) {

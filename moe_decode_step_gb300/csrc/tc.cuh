@@ -645,13 +645,19 @@ struct TcDense {
   int tiles;             // 128-row tiles
   int N;                 // output features (gate/up: features, 64 per tile; down: rows)
   int B;                 // batch rows
-  int NP;                // MMA columns: FC1 pad16(B), FC2 pad16(2 B) (row b = columns 2b, 2b+1)
+  int NP;                // MMA columns: pad16(B), or pad16(2 B) with hilo
+  int hilo;              // row b is columns 2b, 2b + 1 (a (hi, lo) bf16 pair), else column b
   float* out;            // [B][N] fp32
   uint8_t* out_hl;       // gate/up: h_s as (hi, lo) bf16 columns 2b, 2b+1 (out_np columns)
   int out_np;
   float* partial;        // [kTcMaxCtas][kTcDenseMaxN][128]
   unsigned* flags;       // [kTcMaxCtas], zero between forwards
+  int ctas;              // CTAs 0..ctas-1 share the pass (0: all of the grid)
 };
+
+__device__ __forceinline__ int dense_ctas(const TcDense& d) {
+  return d.ctas > 0 ? min(d.ctas, (int)gridDim.x) : (int)gridDim.x;
+}
 
 // 2-D tensor-map load: box (8 K elements, NP rows) at (k0, 0) -> NP x 16 bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
@@ -687,8 +693,9 @@ __device__ __forceinline__ void dense_produce(const TcDense& d, const CUtensorMa
                                               int NS_, int stage_bytes, uint32_t& stage,
                                               int* status, bool wait_between) {
   const int nch = d.K / d.KC, U = d.tiles * nch;
-  int u0, u1;
-  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  const int G = dense_ctas(d);
+  int u0 = 0, u1 = 0;
+  if ((int)blockIdx.x < G) tc_range(U, blockIdx.x, G, u0, u1);
   if (u0 >= u1) {
     if (wait_between) pdl_wait_prerequisites();
     return;
@@ -745,8 +752,9 @@ __device__ __forceinline__ void dense_mma(const TcDense& d, const TcSmem& t, uin
                                           int NS_, int stage_bytes, uint32_t& stage, int& jobs,
                                           int* status) {
   const int nch = d.K / d.KC, U = d.tiles * nch;
-  int u0, u1;
-  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  const int G = dense_ctas(d);
+  int u0 = 0, u1 = 0;
+  if ((int)blockIdx.x < G) tc_range(U, blockIdx.x, G, u0, u1);
   if (u0 >= u1) return;
   const uint32_t NS = (uint32_t)NS_, KC = (uint32_t)d.KC, NP = (uint32_t)d.NP;
   const uint32_t sa0 = smem_addr(stages);
@@ -792,14 +800,16 @@ __device__ __forceinline__ void dense_mma(const TcDense& d, const TcSmem& t, uin
 
 // Epilogue: per tile job the NP accumulator columns of this thread's row, the
 // stream-K fix-up, then gate/up: SwiGLU through the exchange (16 columns at a
-// time) to h_s (fp32, and (hi, lo) bf16 for the down projection); down:
-// y_s[b] = column 2b + column 2b + 1.
+// time) to h_s (fp32, and (hi, lo) bf16 for the down projection); plain:
+// out[b] = column b, or column 2b + column 2b + 1 with hilo (rows past N,
+// the padding of the last tile, are skipped).
 template <bool GLU>
 __device__ __forceinline__ void dense_epilogue(const TcDense& d, const TcSmem& t, uint32_t T,
                                                int q, int lane, int& jobs, int& fin, int* status) {
   const int nch = d.K / d.KC, U = d.tiles * nch;
-  int u0, u1;
-  tc_range(U, blockIdx.x, gridDim.x, u0, u1);
+  const int G = dense_ctas(d);
+  int u0 = 0, u1 = 0;
+  if ((int)blockIdx.x < G) tc_range(U, blockIdx.x, G, u0, u1);
   if (u0 >= u1) return;
   const uint32_t qaddr = (uint32_t)(32 * q) << 16;
   const int m = 32 * q + lane;   // MMA row of this thread
@@ -837,14 +847,22 @@ __device__ __forceinline__ void dense_epilogue(const TcDense& d, const TcSmem& t
       continue;
     }
     if (ce < nch) {
-      // later chunks of this tile were streamed by the next CTAs
-      for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+      // later chunks of this tile were streamed by the next CTAs: wait for
+      // their flags in parallel (lane l polls CTA blockIdx.x + 1 + l), then
+      // add their sums in K order
+      for (int j0 = blockIdx.x + 1; j0 < G; j0 += 32) {
+        const int j = j0 + lane;
+        int a0 = tile_end, a1 = tile_end;
+        if (j < G) tc_range(U, j, G, a0, a1);
+        if (a0 < tile_end && a1 > a0) tc_wait_flag(d.flags + j, status);
+        if (!__any_sync(0xffffffffu, a0 < tile_end)) break;
+      }
+      __syncwarp();
+      for (int j = blockIdx.x + 1; j < G; ++j) {
         int j0, j1;
-        tc_range(U, j, gridDim.x, j0, j1);
+        tc_range(U, j, G, j0, j1);
         if (j0 >= tile_end) break;
         if (j1 <= j0) continue;
-        if (lane == 0) tc_wait_flag(d.flags + j, status);
-        __syncwarp();
         const float* slot = d.partial + (size_t)j * (kTcDenseMaxN * 128);
 #pragma unroll
         for (int n = 0; n < kTcDenseMaxN; ++n)
@@ -852,9 +870,9 @@ __device__ __forceinline__ void dense_epilogue(const TcDense& d, const TcSmem& t
       }
       tc_epi_sync();
       if (m == 0) {
-        for (int j = blockIdx.x + 1; j < (int)gridDim.x; ++j) {
+        for (int j = blockIdx.x + 1; j < G; ++j) {
           int j0, j1;
-          tc_range(U, j, gridDim.x, j0, j1);
+          tc_range(U, j, G, j0, j1);
           if (j0 >= tile_end) break;
           d.flags[j] = 0u;
         }
@@ -895,9 +913,17 @@ __device__ __forceinline__ void dense_epilogue(const TcDense& d, const TcSmem& t
       }
     } else {
       const int row = tile * 128 + m;
+      if (row < d.N) {
+        if (d.hilo) {
 #pragma unroll
-      for (int b = 0; b < kTcDenseMaxN / 2; ++b)
-        if (b < d.B) d.out[(size_t)b * d.N + row] = v[2 * b] + v[2 * b + 1];
+          for (int b = 0; b < kTcDenseMaxN / 2; ++b)
+            if (b < d.B) d.out[(size_t)b * d.N + row] = v[2 * b] + v[2 * b + 1];
+        } else {
+#pragma unroll
+          for (int b = 0; b < kTcDenseMaxN; ++b)
+            if (b < d.B) d.out[(size_t)b * d.N + row] = v[b];
+        }
+      }
     }
     u = ue;
   }
@@ -1024,6 +1050,116 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(T);
   trace_end(b.trace, b.trace_id);
+}
+
+// ---------------------------------------------------------------------------
+// Router on the tensor cores (tensor-core expert path): the logits as a dense
+// pass (router weights in 128-row tiles, the last one zero-padded, x through
+// the tensor map), and the x activation planes of the routed FC1, one
+// plane-0 code per row (planes.cuh): this CTA's share of the B * K/32
+// blocks, each row it touches getting its max |x| from all five plane warps.
+// ---------------------------------------------------------------------------
+struct TcXPlanes {
+  const uint16_t* x;   // [B][K] bf16
+  int B, K;
+  uint8_t* xq;         // planes [B][4 K], or null
+  uint8_t* xq_code;    // plane-0 code per row
+};
+
+// Warps 2..6 only (named barrier 3).
+__device__ __forceinline__ void tc_plane_sync() { asm volatile("bar.sync 3, 160;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_xplanes(const TcXPlanes& p, int cta, int ncta, int wi, int lane,
+                                           unsigned* slots) {
+  constexpr int NW = 5;
+  const int nb = p.K / 32, total = p.B * nb;
+  const int lo = (int)((long long)total * cta / ncta);
+  const int hi = (int)((long long)total * (cta + 1) / ncta);
+  for (int row = lo / nb; lo < hi && row <= (hi - 1) / nb; ++row) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.K);
+    uint32_t mx = 0;
+    for (int i = wi * 32 + lane; i < p.K / 8; i += NW * 32) {
+      const uint4 v = xr[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) slots[wi] = mx;
+    tc_plane_sync();
+    uint32_t amax = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) amax = max(amax, slots[w]);
+    tc_plane_sync();
+    const int c0 = planes_code0(bf16_bits_to_f32(amax));
+    if (wi == 0 && lane == 0) p.xq_code[row] = (uint8_t)c0;
+    const int b0 = max(lo, row * nb) - row * nb, b1 = min(hi, (row + 1) * nb) - row * nb;
+    for (int blk = b0 + wi; blk < b1; blk += NW) {
+      const float v = bf16_bits_to_f32(p.x[(size_t)row * p.K + blk * 32 + lane]);
+      planes_block_c(v, lane, p.xq + (size_t)row * planes_row_bytes(p.K) + blk * 128, c0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_router_kernel(const TcDense dn, const __grid_constant__ CUtensorMap xmap,
+                     const TcXPlanes xp, int NS, int stage_bytes, int* status,
+                     unsigned long long* trace) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  trace_begin(trace, 0);
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
+  uint64_t* empty = full + NS;
+  const TcSmem t = tc_smem(reinterpret_cast<uint8_t*>(empty + NS), dn.K, true);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&t.acc_full[i], 1);
+      mbar_init(&t.acc_empty[i], 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(t.tbase);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t T = *t.tbase;
+  pdl_launch_dependents();
+  uint32_t stage = 0;
+  int jobs = 0, fin = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      dense_produce(dn, &xmap, stages, full, empty, NS, stage_bytes, stage, status, false);
+      tc_drain(empty, NS, stage, status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) dense_mma(dn, t, T, stages, full, empty, NS, stage_bytes, stage, jobs, status);
+    __syncwarp();
+  } else {
+    // the x planes on the CTAs past the dense pass's (all of them when the
+    // pass takes the whole grid), then the epilogues
+    const int G = dense_ctas(dn), spare = (int)gridDim.x - G;
+    unsigned* slots = reinterpret_cast<unsigned*>(t.xchg);
+    if (xp.xq) {
+      if (spare > 0) {
+        if ((int)blockIdx.x >= G) tc_xplanes(xp, blockIdx.x - G, spare, warp - 2, lane, slots);
+      } else {
+        tc_xplanes(xp, blockIdx.x, gridDim.x, warp - 2, lane, slots);
+      }
+    }
+    if (warp < 6) dense_epilogue<false>(dn, t, T, warp & 3, lane, jobs, fin, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(T);
+  trace_end(trace, 0);
 }
 
 }  // namespace moe
