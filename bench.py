@@ -57,7 +57,7 @@ def parse_args():
 # the 16 selected experts make its FC1 and FC2 launches the same size as
 # full_b1's, while the device holds a few GB, as a many-pass capture needs.
 PROFILE_CASES = {"full_b1": ("full_b1", None), "full_b1_e128": ("full_b1", 128),
-                 "full_b8_e128": ("full_b8", 128)}
+                 "full_b8_e128": ("full_b8", 128), "full_b64_e128": ("full_b64", 128)}
 
 
 def dist_env():
