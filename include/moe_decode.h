@@ -67,11 +67,14 @@ typedef struct moe_layer* moe_layer_t;
  * expert_path picks how the routed experts run.  1: mma.sync tensor cores
  * with the weights converted to f16 in registers (the GEMV regime; the
  * kernels read the tiled layouts, FC1 matrices in layout 2 and FC2 matrices in
- * layout 1).  2: tcgen05 tensor cores, block-scaled MXFP4 MMAs with
- * tensor-memory accumulators (the UMMA layouts, FC1 in layout 4 and FC2 in
- * layout 3).  0 (default): the layer keeps both layouts and takes path 1 for
- * B = 1 and path 2 for B >= 2.  All give results within the same tolerance of
- * the exact layer.
+ * layout 1), the shared expert and the router on the CUDA cores.  2: tcgen05
+ * tensor cores, block-scaled MXFP4 MMAs with tensor-memory accumulators (the
+ * UMMA layouts, FC1 in layout 4 and FC2 in layout 3); the shared expert (and,
+ * for B > 8, the router) as bf16 MMAs on the same tensor cores, from bf16
+ * copies of those weights in 128-row tiles that the handle owns (2 * (3 * d *
+ * f_shared + 128 * ceil(E / 128) * d) bytes of extra device memory).  0
+ * (default): the layer keeps both and takes path 1 for B = 1 and path 2 for
+ * B >= 2.  All give results within the same tolerance of the exact layer.
  *
  * mxfp4_layout says how the caller's expert weights are laid out: 0
  * (canonical), 1 (tiled: FC1 layout 2, FC2 layout 1) or 3 (UMMA: FC1 layout 4,
