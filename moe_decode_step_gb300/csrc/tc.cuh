@@ -13,8 +13,9 @@
 //    from the router and runs first, while top-k finishes; its epilogue
 //    writes h_s both as fp32 and as (hi, lo) bf16 pairs, the operand of FC2's
 //    dense pass (h_s = hi + lo to 2^-16 relative, far inside fp32 sums of
-//    bf16 products).  FC2 runs its routed pass first, right after FC1's
-//    results land, and the dense pass after it.
+//    bf16 products).  FC2 runs its dense pass first too: its weight copies go
+//    out before FC1 is waited for, and the (hi, lo) columns after.
+//    Above 8 rows the router is a dense pass of its own (tc_router_kernel).
 // fp32 accumulators live in tensor memory until the epilogue reads them back;
 // nothing is converted on the CUDA cores on the way in.
 //
@@ -27,11 +28,11 @@
 // range; the finisher adds them in K order at the end of its own (so results
 // do not depend on timing).
 //
-// Roles (6 warps): warp 0 lane 0 streams stages; warp 1 allocates tensor
-// memory, builds the run table, and its lane 0 issues the tensor-memory scale
-// copies and MMAs and commits them to the stage's "empty" barrier and, per
-// tile, to an accumulator barrier; warps 2..5 (tensor-memory lane quarters 2,
-// 3, 0, 1) run the epilogues.  Accumulators are double-buffered and scale
+// Roles (7 warps): warp 0 lane 0 streams stages; warp 1 allocates tensor
+// memory and its lane 0 issues the tensor-memory scale copies and MMAs and
+// commits them to the stage's "empty" barrier and, per tile, to an
+// accumulator barrier; warps 2..5 (tensor-memory lane quarters 2, 3, 0, 1)
+// run the epilogues; warp 6 builds the routed run table.  Accumulators are double-buffered and scale
 // slots ringed with the stages, so the MMA thread never waits for an epilogue
 // in steady state.  Every wait is bounded (status 5 on timeout).
 //
