@@ -470,7 +470,7 @@ def run_ours(args, rank, world, local):
     batches = {}
     chain = None
     if not args.no_batches and args.config == "full_b1":
-        for name in ("full_b8", "full_b64"):
+        for name in ("full_b8", "verify_b16", "full_b64"):
             c2 = CONFIGS[name]
             L2 = synthetic.make_layer(c2)
             x2, r2 = synthetic.make_activations(c2)
@@ -484,7 +484,8 @@ def run_ours(args, rank, world, local):
             b2 = bytes_touched(c2, nd2, c2.B)
             f2_us = statistics.median(p[1] for p in p2)
             f2_b = fc1_bytes(c2, nd2, c2.B)
-            batches[str(c2.B)] = {
+            key = str(c2.B) if c2.drafts == 0 else f"{c2.B} (verify: {c2.B // (1 + c2.drafts)} tokens x {1 + c2.drafts} rows, corr {c2.corr})"
+            batches[key] = {
                 "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
                 "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,
                 "expert_path": "tcgen05 block-scaled MXF4 MMA",

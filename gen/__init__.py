@@ -91,3 +91,27 @@ def normal_device(seed, tensor, sub, out, mean, std, start=0, stream=None):
     if rc != 0:
         raise RuntimeError(f"moegen device launch failed: cudaError {rc}")
     return out
+
+
+def activation_x(cfg, seed, B=None):
+    """x rows [B, d] as float32 (before the bf16 rounding both sides apply).
+
+    Uncorrelated configs: the N(0, 1) draws of tensor T_X, sub-stream 0.  A
+    verify batch (cfg.drafts > 0, correlation rho = cfg.corr): row r of group
+    g = r // (1 + drafts) is rho * z_g + sqrt(1 - rho^2) * n_r, with n_r the
+    same sub-stream-0 draws and z_g the draws of sub-stream 1 (one row per
+    group), each product and the sum rounded to float32 (numpy float32
+    arithmetic, no fused multiply-add), so every row is still N(0, 1) and two
+    rows of a group correlate by rho**2."""
+    B = cfg.B if B is None else B
+    n = normal_host(seed, T_X, 0, B * cfg.d, 0.0, 1.0).reshape(B, cfg.d)
+    if cfg.drafts <= 0 or cfg.corr == 0.0:
+        return n
+    gsize = 1 + cfg.drafts
+    groups = (B + gsize - 1) // gsize
+    z = normal_host(seed, T_X, 1, groups * cfg.d, 0.0, 1.0).reshape(groups, cfg.d)
+    rho = np.float32(cfg.corr)
+    sig = np.float32(np.sqrt(1.0 - float(cfg.corr) ** 2))
+    zr = z[np.arange(B) // gsize]
+    return (rho * zr + sig * n).astype(np.float32)
+

@@ -5,7 +5,10 @@ the Kimi K3 latency-specialised decode write-ups: a tiny layer (d=1024, f=256,
 64 experts, top-4) for fast exact checks, and the full-size layer (d=7168,
 f=1536, 896 experts, top-16; each MXFP4 expert 17,547,264 bytes, the figure
 the teardown page gives in "What one decode step of Kimi K3 does") at B = 1,
-8 and 64 rows, plus a chain of four full-size layers at B = 1.
+8 and 64 rows, plus a chain of four full-size layers at B = 1, plus a
+speculative-decoding verify batch: 4 tokens with 3 drafts each (B = 16) whose
+rows route to mostly the same experts (the teardown page, "What DSpark adds":
+a verify pass loads the union of the experts its rows pick).
 
 Every "N(a, b)" is read as mean a, standard deviation b.
 """
@@ -43,6 +46,8 @@ class LayerConfig:
     seeds: tuple            # one weight seed per layer (chain: several)
     routed_scale: float = 2.5
     rms_eps: float = 1e-6
+    drafts: int = 0         # verify batch: rows come in groups of 1 + drafts
+    corr: float = 0.0       # correlation of x between the rows of a group
 
     @property
     def n_layers(self):
@@ -72,6 +77,8 @@ CONFIGS = {
     "full_b8": LayerConfig("full_b8", 8, 7168, 1536, 896, 16, 1536, (2,)),
     "full_b64": LayerConfig("full_b64", 64, 7168, 1536, 896, 16, 1536, (3,)),
     "chain4_b1": LayerConfig("chain4_b1", 1, 7168, 1536, 896, 16, 1536, (10, 11, 12, 13)),
+    "verify_b16": LayerConfig("verify_b16", 16, 7168, 1536, 896, 16, 1536, (4,), drafts=3,
+                              corr=0.95),
 }
 
 

@@ -66,7 +66,11 @@ def make_activations(cfg, layer=0, attempt=0, device="cuda", B=None):
     B = c.B if B is None else B
     s = activation_seed(c.seeds[layer], attempt)
     dev = torch.device(device)
-    x = _normal(s, T_X, 0, (B, c.d), 0.0, 1.0, dev).to(torch.bfloat16)
+    if c.drafts > 0 and c.corr != 0.0:
+        # a verify batch: the rows mixed on the host (see gen.activation_x)
+        x = torch.from_numpy(gen.activation_x(c, s, B)).to(dev).to(torch.bfloat16)
+    else:
+        x = _normal(s, T_X, 0, (B, c.d), 0.0, 1.0, dev).to(torch.bfloat16)
     r = _normal(s, T_RESIDUAL, 0, (B, c.d), 0.0, 1.0, dev).to(torch.bfloat16)
     return x, r
 

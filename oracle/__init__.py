@@ -234,7 +234,7 @@ class LayerInputs:
                                            c.std_shared_down())).reshape(c.d, c.f_shared)
         self.x_seed = activation_seed(s, x_attempt)
         if x is None:
-            x = bf(gen.normal_host(self.x_seed, T_X, 0, c.B * c.d, 0.0, 1.0)).reshape(c.B, c.d)
+            x = bf(gen.activation_x(c, self.x_seed))
         if residual is None:
             residual = bf(gen.normal_host(self.x_seed, T_RESIDUAL, 0, c.B * c.d, 0.0,
                                           1.0)).reshape(c.B, c.d)

@@ -71,3 +71,47 @@ def test_streams_differ():
     for o in (b, c, d):
         assert not np.array_equal(a, o)
         assert abs(np.corrcoef(a, o)[0, 1]) < 0.15
+
+
+def test_uncorrelated_activation_rows_are_the_plain_stream():
+    from gen.configs import CONFIGS, T_X
+    cfg = CONFIGS["full_b8"]
+    x = gen.activation_x(cfg, 2)
+    n = gen.normal_host(2, T_X, 0, cfg.B * cfg.d, 0.0, 1.0).reshape(cfg.B, cfg.d)
+    assert x.dtype == np.float32 and np.array_equal(x, n)
+
+
+def test_verify_batch_rows_correlate_within_groups_only():
+    """The verify batch's recipe: rows of one group (a token and its 3 drafts)
+    correlate by rho^2, rows of different groups not at all, and every row
+    keeps unit variance."""
+    from gen.configs import CONFIGS
+    cfg = CONFIGS["verify_b16"]
+    x = gen.activation_x(cfg, cfg.seeds[0]).astype(np.float64)
+    assert x.shape == (16, cfg.d)
+    c = np.corrcoef(x)
+    g = np.arange(16) // (1 + cfg.drafts)
+    same = (g[:, None] == g[None, :]) & ~np.eye(16, dtype=bool)
+    diff = g[:, None] != g[None, :]
+    assert abs(c[same].mean() - cfg.corr ** 2) < 0.01
+    assert np.abs(c[diff]).max() < 0.06
+    np.testing.assert_allclose(x.std(axis=1), 1.0, atol=0.03)
+
+
+def test_verify_batch_rows_route_to_shared_experts():
+    """What the correlation is for: the rows of a group pick mostly the same
+    experts (exact routing by the oracle), so the batch touches far fewer
+    distinct experts than 16 independent rows (about 225 of 896)."""
+    import oracle
+    from gen.configs import CONFIGS
+    cfg = CONFIGS["verify_b16"]
+    inp = oracle.LayerInputs(cfg)
+    _, idx, _, _ = oracle.route(inp)
+    sets = [set(r.tolist()) for r in idx]
+    gsize = 1 + cfg.drafts
+    within = [len(sets[a] & sets[b]) for a in range(16) for b in range(16)
+              if a != b and a // gsize == b // gsize]
+    across = [len(sets[a] & sets[b]) for a in range(16) for b in range(16)
+              if a // gsize != b // gsize]
+    assert np.mean(within) >= 8 and np.mean(across) <= 2
+    assert len(set().union(*sets)) <= 140

@@ -21,10 +21,12 @@ def _np(t):
 
 
 @pytest.mark.parametrize("name,rows,path", [("full_b1", [0], 0), ("full_b1", [0], 2),
-                                            ("full_b8", [0, 7], 0), ("full_b64", [0, 33, 63], 0)])
+                                            ("full_b8", [0, 7], 0), ("verify_b16", [0, 5, 15], 0),
+                                            ("verify_b16", [3, 12], 1), ("full_b64", [0, 33, 63], 0)])
 def test_full_layer_sampled_rows(name, rows, path):
     """path 0, the layer the benchmark times: mma.sync at B = 1, tcgen05 at
-    B = 8 and 64; path 2: tcgen05 at B = 1 as well."""
+    B = 8, 16 and 64; path 2: tcgen05 at B = 1 as well; path 1: mma.sync on
+    the verify batch, whose experts take several rows per pass."""
     cfg = CONFIGS[name]
     inp = oracle.clean_inputs(cfg)
     ref = oracle.forward(inp, rows=rows)
