@@ -484,7 +484,8 @@ def run_ours(args, rank, world, local):
             b2 = bytes_touched(c2, nd2, c2.B)
             f2_us = statistics.median(p[1] for p in p2)
             f2_b = fc1_bytes(c2, nd2, c2.B)
-            key = str(c2.B) if c2.drafts == 0 else f"{c2.B} (verify: {c2.B // (1 + c2.drafts)} tokens x {1 + c2.drafts} rows, corr {c2.corr})"
+            key = str(c2.B) if c2.drafts == 0 else (f"{c2.B} (rows in correlated groups of "
+                                                       f"{1 + c2.drafts}, rho {c2.corr})")
             batches[key] = {
                 "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
                 "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,

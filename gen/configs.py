@@ -5,10 +5,13 @@ the Kimi K3 latency-specialised decode write-ups: a tiny layer (d=1024, f=256,
 64 experts, top-4) for fast exact checks, and the full-size layer (d=7168,
 f=1536, 896 experts, top-16; each MXFP4 expert 17,547,264 bytes, the figure
 the teardown page gives in "What one decode step of Kimi K3 does") at B = 1,
-8 and 64 rows, plus a chain of four full-size layers at B = 1, plus a
-speculative-decoding verify batch: 4 tokens with 3 drafts each (B = 16) whose
-rows route to mostly the same experts (the teardown page, "What DSpark adds":
-a verify pass loads the union of the experts its rows pick).
+8 and 64 rows, plus a chain of four full-size layers at B = 1.  The
+teardown's verify steps (section "What DSpark adds": an anchor token and 7
+drafts, 8 rows that route independently, about 120 distinct experts; at most
+64 rows per verify batch) are the B = 8 and B = 64 layers.  verify_b16 adds a
+case the pages do not model: 16 rows in groups of 4 with correlated hidden
+states, so that several rows share an expert (runs of up to 4 rows per
+expert at full size).
 
 Every "N(a, b)" is read as mean a, standard deviation b.
 """
