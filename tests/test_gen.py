@@ -82,9 +82,9 @@ def test_uncorrelated_activation_rows_are_the_plain_stream():
 
 
 def test_verify_batch_rows_correlate_within_groups_only():
-    """The verify batch's recipe: rows of one group (a token and its 3 drafts)
-    correlate by rho^2, rows of different groups not at all, and every row
-    keeps unit variance."""
+    """The correlated 16-row batch's recipe: rows of one group of 4 correlate
+    by rho^2, rows of different groups not at all, and every row keeps unit
+    variance."""
     from gen.configs import CONFIGS
     cfg = CONFIGS["verify_b16"]
     x = gen.activation_x(cfg, cfg.seeds[0]).astype(np.float64)
