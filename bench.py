@@ -18,7 +18,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -128,12 +127,20 @@ def fc1_bytes(cfg, n_distinct, B):
             + 4 * B * cfg.top_k * cfg.f)
 
 
-KERNEL_SOURCES = ("common.cuh", "stream.cuh", "moe_decode.cu")
+def front_bytes(cfg, n_distinct, B):
+    """Algorithmic bytes of the one-row front launch (router + top-k + FC1):
+    FC1's bytes plus the router weights and bias."""
+    return fc1_bytes(cfg, n_distinct, B) + cfg.n_experts * cfg.d * 2 + 4 * cfg.n_experts
+
+
+KERNEL_SOURCES = ("common.cuh", "stream.cuh", "topk.cuh", "front.cuh", "moe_decode.cu")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 
 
 def kernel_source_sha256():
-    """sha256 over the FC1 kernel's sources (the dot, the streaming kernel and
-    its launch plan), concatenated in that order."""
+    """sha256 over the dominant B = 1 kernel's sources (helpers, the streaming
+    kernel, the selection, the front kernel and its launch plan), concatenated
+    in that order."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "moe_decode_step_gb300", "csrc", f), "rb") as fh:
@@ -142,18 +149,17 @@ def kernel_source_sha256():
 
 
 def traffic_from_profile():
-    """dram bytes per launch recorded by the ncu summary of the FC1 streaming
-    kernel, or None when missing or taken on different kernel sources."""
-    summ = os.path.join(ROOT, "profiles", "fc1_stream_full_b1.md")
+    """DRAM bytes (read + write) per launch of the dominant kernel from the ncu
+    record in profiles/roofline_traffic.json, scaled to the timed workload's
+    distinct experts; None when missing or taken on other kernel sources."""
     try:
-        text = open(summ).read()
-    except OSError:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch_full_b1:\s*([0-9.eE+]+)", text)
-    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or not h:
+    if rec.get("kernel_source_sha256") != kernel_source_sha256():
         return None
-    return float(m.group(1)) if kernel_source_sha256() == h.group(1) else None
+    return rec
 
 
 # ---------------------------------------------------------------------------
@@ -337,6 +343,26 @@ def time_chain(layers, x0, res0, steps, warmup, flush):
     return times
 
 
+def trace_layer(layer, x, res0, flush, reps=7):
+    """Device timeline of eager forwards: per kernel, the earliest CTA start and
+    the latest CTA end (globaltimer, us from the first kernel's start), L2
+    flushed before each forward; the median of each over `reps` forwards."""
+    import torch
+    res = res0.clone()
+    out = torch.empty_like(x)
+    layer.set_trace(True)
+    runs = []
+    for _ in range(reps):
+        res.copy_(res0)
+        flush()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        layer.forward(x, res, out)
+        runs.append(layer.get_trace())
+    layer.set_trace(False)
+    return {k: [round(statistics.median(r[k][0] for r in runs), 2),
+                round(statistics.median(r[k][1] for r in runs), 2)] for k in runs[0]}
+
+
 def percentile(v, q):
     v = sorted(v)
     if not v:
@@ -452,11 +478,16 @@ def run_ours(args, rank, world, local):
 
     us = reduce_max(statistics.median(times), world, dev)
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
+    fused_front = layer.launches_per_forward(cfg.B) == 3
     fc1_us = statistics.median(p[1] for p in phases)
-    fc1_b = fc1_bytes(cfg, n_distinct, cfg.B)
-    traffic = traffic_from_profile()
-    if traffic is not None:
-        traffic = traffic * n_distinct / 16.0
+    fc1_b = (front_bytes if fused_front else fc1_bytes)(cfg, n_distinct, cfg.B)
+    rec = traffic_from_profile()
+    traffic = None
+    if rec is not None:
+        # the capture's launch moves the same bytes per touched expert
+        traffic = (rec["dram_bytes_per_launch"] - rec["fixed_bytes"]) * n_distinct \
+            / rec["n_distinct_experts"] + rec["fixed_bytes"]
+    trace = trace_layer(layer, x, res0, flush)
     phase_names = ["router_topk", "fc1", "fc2", "unused", "tail", "layer"]
     phase_med = {n: statistics.median(p[i] for p in phases) for i, n in enumerate(phase_names)}
 
@@ -476,7 +507,7 @@ def run_ours(args, rank, world, local):
             x2, r2 = synthetic.make_activations(c2)
             i2, _ = L2.router_topk(x2)
             nd2 = int(torch.unique(i2).numel())
-            st2 = max(5, min(args.steps, 20))
+            st2 = max(5, args.steps)
             t2, _ = time_layer(L2, x2, r2, st2, max(3, args.warmup), flush, graph=True,
                                timing=False)
             _, p2 = time_layer(L2, x2, r2, 5, 3, flush, graph=True, timing=True)
@@ -484,6 +515,7 @@ def run_ours(args, rank, world, local):
             b2 = bytes_touched(c2, nd2, c2.B)
             f2_us = statistics.median(p[1] for p in p2)
             f2_b = fc1_bytes(c2, nd2, c2.B)
+            tr2 = trace_layer(L2, x2, r2, flush)
             key = str(c2.B) if c2.drafts == 0 else (f"{c2.B} (rows in correlated groups of "
                                                        f"{1 + c2.drafts}, rho {c2.corr})")
             batches[key] = {
@@ -496,7 +528,8 @@ def run_ours(args, rank, world, local):
                                  "frac": f2_b / f2_us / 1e3 / peak, "algorithmic_bytes": f2_b,
                                  "launch_us": f2_us, "peak_kind": peak_kind},
                 "phases_us": {n: statistics.median(p[i] for p in p2)
-                              for i, n in enumerate(phase_names)}}
+                              for i, n in enumerate(phase_names)},
+                "trace_us": tr2}
             L2.close()
             del L2
             torch.cuda.empty_cache()
@@ -506,12 +539,19 @@ def run_ours(args, rank, world, local):
         for l in range(cc.n_layers - 1):
             chain_layers[l].set_prefetch_next(chain_layers[l + 1])
         xc, rc = synthetic.make_activations(cc, layer=0)
-        stc = max(5, min(args.steps, 20))
+        stc = max(5, args.steps)
         tc = time_chain(chain_layers, xc, rc, stc, max(3, args.warmup), flush)
         vc = reduce_max(statistics.median(tc), world, dev)
+        # the same chain with the next-layer prefetch switched off
+        for l in range(cc.n_layers - 1):
+            chain_layers[l].set_prefetch_next(None)
+        tc_off = time_chain(chain_layers, xc, rc, stc, max(3, args.warmup), flush)
+        vc_off = reduce_max(statistics.median(tc_off), world, dev)
         chain = {"layers": cc.n_layers, "B": cc.B, "us": vc, "us_per_layer": vc / cc.n_layers,
                  "steps": stc, "l2": "flushed once before each chain",
-                 "prefetch": "next layer's router and shared-expert weights, side stream"}
+                 "prefetch": "next layer's router and shared-expert weights, side stream",
+                 "us_prefetch_off": vc_off, "us_per_layer_prefetch_off": vc_off / cc.n_layers,
+                 "prefetch_gain_us_per_layer": (vc_off - vc) / cc.n_layers}
         for L in chain_layers:
             L.close()
         del chain_layers
@@ -540,11 +580,16 @@ def run_ours(args, rank, world, local):
                 "frac_of_nominal_8tbs": btouch / us / 1e6 / 8.0, "aggregate_tbs": agg_tbs,
                 "peak_gbs": peak, "peak_kind": peak_kind},
         "expert_path": "mma.sync with register dequantisation (B = 1)",
-        "roofline": {"kernel": "stream_dual_kernel (FC1: shared + routed gate/up)", "bound": "hbm",
+        "roofline": {"kernel": ("stream_front_kernel (router + top-k + shared gate/up + routed "
+                                "gate/up)") if fused_front else
+                               "stream_dual_kernel (FC1: shared + routed gate/up)",
+                     "bound": "hbm",
                      "achieved": fc1_b / fc1_us / 1e3, "peak": peak, "unit": "GB/s",
                      "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,
+                     "traffic_source": None if rec is None else rec.get("source"),
                      "algorithmic_bytes": fc1_b, "launch_us": fc1_us, "peak_kind": peak_kind},
         "phases_us": phase_med,
+        "trace_us": trace,
         "timing_mode": "CUDA graph replay of the forward (value); per-phase events as graph "
                        "nodes on separate replays (phases_us)",
         "eager_us": statistics.median(eager_times),

@@ -248,17 +248,27 @@ int mxfp4_retile_device(void* stream, const uint8_t* q_in, const uint8_t* s_in, 
  * or callers that must not synchronise the device).  It needs no layer handle:
  * router_w device bf16 [E][d], router_bias device fp32 [E], x device bf16
  * [B][d]; outputs idx device int32 [B][k] and w device fp32 [B][k], exactly
- * as moe_router_topk.  Its scratch (logits, ticket, routing tables; 284,672
- * bytes) is one static device array that every GPU loading this library holds
- * until the process exits.  Limits: B <= 64, E <= 1024, k <= 32, d % 256 == 0,
- * d <= 8192; larger sizes return MOE_ERR_UNSUPPORTED.  The first call on each
- * device (and the first with a new d) does a one-time set-up (fetches the
- * array's device address, sizes the launch): make that call before any stream
- * capture.  Every call shares the one array, so calls that overlap on the GPU
+ * as moe_router_topk.  Its scratch (logits, ticket, status word, routing
+ * tables; 284,416 bytes) is one static device array that every GPU loading
+ * this library holds until the process exits; each call looks up the current
+ * device's address of it.  Limits: B <= 64, E <= 1024, k <= 32, d % 256 == 0,
+ * d <= 7680 (as for a layer); larger sizes return MOE_ERR_UNSUPPORTED.  The
+ * first call on each device (and the first with a new d) sizes the launch
+ * (host-side queries, no allocation): make that call before any stream
+ * capture.  A CUDA error already pending when the call starts is returned
+ * (MOE_ERR_CUDA, its code kept for moe_last_cuda_error) and nothing is
+ * launched.  Every call shares the one array, so calls that overlap on the GPU
  * (two streams, or two threads) race; calls in one stream are safe. */
 int moe_router_topk_noalloc(void* stream, const void* router_w, const float* router_bias,
                             const void* x, int B, int d, int n_experts, int top_k,
                             float routed_scale, int32_t* idx, float* w);
+
+/* Status word of the allocation-free router on the current device: 0, or
+ * MOE_ERR_TIMEOUT when a bounded device-side wait of an earlier call expired
+ * (its outputs are then not valid).  Each call clears the word when it
+ * starts, so this reports the calls since the last one started; synchronises
+ * the device, then clears the word. */
+int moe_router_topk_noalloc_status(int* device_status);
 
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);

@@ -174,13 +174,17 @@ class MoELayer:
         check(lib().moe_set_trace(self._h, int(bool(enable))), "moe_set_trace")
 
     def get_trace(self):
-        """{kernel: (start_us, end_us)} relative to the router's start, last forward."""
+        """{kernel: (start_us, end_us)} of the last traced forward, relative to
+        the earliest kernel start; kernels that did not run are left out (the
+        one-row front kernel reports as "fc1", with no router or top-k)."""
         arr = (ctypes.c_ulonglong * 10)()
         check(lib().moe_get_trace(self._h, arr, 10), "moe_get_trace")
         names = ["router", "topk", "fc1", "fc2", "tail"]
-        t0 = arr[0]
-        return {n: ((arr[2 * i] - t0) / 1e3, (arr[2 * i + 1] - t0) / 1e3)
-                for i, n in enumerate(names)}
+        ran = [i for i in range(5) if arr[2 * i] <= arr[2 * i + 1]]
+        if not ran:
+            return {}
+        t0 = min(arr[2 * i] for i in ran)
+        return {names[i]: ((arr[2 * i] - t0) / 1e3, (arr[2 * i + 1] - t0) / 1e3) for i in ran}
 
     def launches_per_forward(self, B):
         return lib().moe_launches_per_forward(self._h, int(B))

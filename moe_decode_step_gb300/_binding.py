@@ -74,6 +74,7 @@ _PROTOS = {
     "moe_router_topk_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
                                                _P]),
+    "moe_router_topk_noalloc_status": (ctypes.c_int, [_P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_int, []),
 }

@@ -35,6 +35,26 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const uint8_t* p) {
   return v;
 }
 
+// Routing-table entries live either in global memory (written by an earlier
+// kernel, or published under a flag) or in the CTA's own shared memory (a
+// kernel that ran the top-k itself).  A generic relaxed load at GPU scope
+// reads either coherently (for global memory it bypasses L1, like ld.cg).
+__device__ __forceinline__ int ld_tab(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Flag and counter accesses between CTAs of one or two kernels in flight.
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // MXFP4 decode.  cvt.rn.f16x2.e2m1x2 turns one byte (two E2M1 codes) into an
 // f16x2; every E2M1 value is exact in f16.  E8M0 byte -> 2^(s-127) as fp32

@@ -1,0 +1,237 @@
+// The front of the layer for one row (B = 1) in a single launch: router GEMV,
+// top-k, shared-expert gate/up and routed gate/up ("Kimi K3 on GB300: 13
+// kernels a layer...", section "What the fused path changes": the MoE front
+// fused into one kernel that starts early, and one persistent routed-expert
+// kernel; section "Why batch 1 on a rack is not only a bandwidth problem":
+// short, dependent steps leave HBM idle).
+//
+// Three steps share one stage ring (stream.cuh):
+//   R  router rows (bf16) -> logits [E] in global memory
+//   A  shared gate/up (bf16) -> h_s, SwiGLU
+//   B  routed gate/up (MXFP4, mma.sync) -> h, SwiGLU
+// Between R and A every CTA's consumers
+//   - make their logits visible and count the CTA in (one atomic per CTA),
+//   - wait, bounded, until all CTAs have counted in,
+//   - select the row's experts themselves from all E logits, with the same
+//     keys, order and weights as topk_kernel, into routing tables in shared
+//     memory (k experts, one pair each, ordered by expert id),
+// and CTA 0 also writes those tables to global memory for FC2 and the tail
+// and raises the route flag.  The producer streams R and A without waiting
+// for anything and learns the routing from a shared-memory barrier before B,
+// so the selection runs while HBM streams the shared expert, and the routed
+// step reads no table from global memory.  The counter and the flag are
+// zeroed again by the tail kernel of the same forward.
+#pragma once
+
+#include "common.cuh"
+#include "stream.cuh"
+#include "topk.cuh"
+
+namespace moe {
+
+struct FrontArgs {
+  const float* bias;      // [E], a static weight
+  int E, k;
+  float routed_scale;
+  unsigned* count;        // CTAs past the router step (zero at rest)
+  unsigned* route_flag;   // raised by CTA 0 once the global tables are written (zero at rest)
+  int32_t* topk_idx;      // [k], descending by biased score
+  float* topk_w;          // [k]
+  int* n_active;          // global routing tables (as topk_kernel writes them)
+  int* active_expert;
+  int* active_off;
+  int* pair_list;
+};
+
+// Routing tables of one row in shared memory, and the barrier the producer
+// waits on for them.
+struct FrontRoute {
+  uint64_t bar;
+  int n_active;
+  int expert[32];
+  int off[33];
+  int pair[32];
+};
+constexpr int kFrontExtraBytes = (int)((sizeof(FrontRoute) + 127) / 128 * 128);
+
+// 32-expert chunks per consumer warp in the selection (E <= 32 * 4 * KW).
+constexpr int kFrontMaxChunks = 4;
+// Shared memory the selection borrows from the cross-slab partial buffers
+// (idle between steps): 2 x 16 sorted lists of 32 keys, then E <= 1024 scores.
+constexpr int kFrontScratchBytes = 2 * 16 * 32 * 8 + 1024 * 4;
+
+__device__ __forceinline__ FrontRoute* front_route(float* red, int red_pp) {
+  return reinterpret_cast<FrontRoute*>(reinterpret_cast<uint8_t*>(red + 2 * (size_t)red_pp) + 64);
+}
+
+// Bounded wait until *c >= target (acquire).
+__device__ __forceinline__ void wait_count(const unsigned* c, unsigned target, int* status) {
+  if (ld_acquire_u32(c) >= target) return;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_u32(c) < target) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+// Selection of one row by the KW consumer warps.  Warp w sorts the 32-expert
+// chunks w, w + KW, ... and merges them into one sorted list of its 32 best
+// keys; the KW lists then meet in a tournament through shared memory, a round
+// per consumer barrier.  Warp 0 turns the winning k keys into the tables.
+__device__ __forceinline__ void front_topk(const FrontArgs& f, const float* logits, float* scratch,
+                                           FrontRoute* rt, const float (&bias)[kFrontMaxChunks],
+                                           int kw, int KW, int lane, int cthreads) {
+  uint64_t* lists = reinterpret_cast<uint64_t*>(scratch);   // [2][16][32]
+  float* s_sc = scratch + 2 * 16 * 32 * 2;                   // [E]
+  const int nch = (f.E + 31) >> 5;
+  float l[kFrontMaxChunks];
+#pragma unroll
+  for (int i = 0; i < kFrontMaxChunks; ++i) {   // every logit load before the first use
+    const int t = (kw + i * KW) * 32 + lane;
+    l[i] = t < f.E ? __ldcg(logits + t) : 0.f;
+  }
+  uint64_t best = 0ull;
+#pragma unroll
+  for (int i = 0; i < kFrontMaxChunks; ++i) {
+    const int ch = kw + i * KW;
+    if (ch < nch) {   // warp-uniform
+      const int t = ch * 32 + lane;
+      uint64_t key = 0ull;
+      if (t < f.E) {
+        const float s = topk_score(l[i]);
+        s_sc[t] = s;
+        key = topk_key(s, bias[i], t);
+      }
+      key = warp_bitonic_sort_desc(key, lane);
+      if (i == 0) {
+        best = key;
+      } else {
+        // the elementwise maximum of one sorted list and the other reversed
+        // is a bitonic sequence holding the 32 largest keys of both
+        const uint64_t y = __shfl_sync(0xffffffffu, key, 31 - lane);
+        best = warp_bitonic_merge_desc(best > y ? best : y, lane);
+      }
+    }
+  }
+  if (kw < 16) lists[kw * 32 + lane] = best;
+  consumer_sync(cthreads);
+  int n = min(KW, 16), src = 0;
+  while (n > 1) {
+    const int half = n >> 1;
+    const uint64_t* s = lists + src * 512;
+    uint64_t* d = lists + (src ^ 1) * 512;
+    if (kw < half) {
+      const uint64_t x = s[(2 * kw) * 32 + lane];
+      const uint64_t y = s[(2 * kw + 1) * 32 + 31 - lane];
+      d[kw * 32 + lane] = warp_bitonic_merge_desc(x > y ? x : y, lane);
+    } else if (kw == half && (n & 1)) {
+      d[kw * 32 + lane] = s[(n - 1) * 32 + lane];
+    }
+    n = half + (n & 1);
+    src ^= 1;
+    consumer_sync(cthreads);
+  }
+  if (kw != 0) return;
+  const int k = f.k;
+  const int e = min(max(topk_key_expert(lists[src * 512 + lane]), 0), f.E - 1);
+  const float s = lane < k ? s_sc[e] : 0.f;
+  float ssum = 0.f;
+  for (int i = 0; i < k; ++i) ssum += __shfl_sync(0xffffffffu, s, i);   // in rank order
+  const float w = f.routed_scale * s / ssum;
+  int slot = 0;   // rank of e among the selected ids: the tables go by expert id
+  for (int i = 0; i < k; ++i) slot += __shfl_sync(0xffffffffu, e, i) < e ? 1 : 0;
+  if (lane < k) {
+    rt->expert[slot] = e;
+    rt->pair[slot] = lane;
+    rt->off[lane] = lane;
+  }
+  if (lane == 0) {
+    rt->n_active = k;
+    rt->off[k] = k;
+  }
+  if (blockIdx.x == 0) {
+    if (lane < k) {
+      f.topk_idx[lane] = e;
+      f.topk_w[lane] = w;
+      f.active_expert[slot] = e;
+      f.pair_list[slot] = lane;
+      f.active_off[lane] = lane;
+    }
+    if (lane == 0) {
+      *f.n_active = k;
+      f.active_off[k] = k;
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_u32(f.route_flag, 1u);
+  }
+}
+
+// Warp 0 lane 0 produces; warps 1..KW consume (KW = blockDim.x / 32 - 1).
+// Dynamic shared memory: the streaming kernels' carve-up (stream_smem_init)
+// followed by kFrontExtraBytes for the routing tables; the cross-slab partial
+// buffers must hold kFrontScratchBytes.
+template <class RC, class AC, class BC>
+__global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
+    stream_front_kernel(const StreamArgs ar, const StreamArgs a0, const StreamArgs a1,
+                        const FrontArgs f) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = (int)(blockDim.x >> 5) - 1;
+  trace_begin(a0.trace, a0.trace_id);
+  float* red = reinterpret_cast<float*>(smem + (size_t)a0.NS * a0.stage_bytes + (size_t)a0.NS * 16);
+  FrontRoute* rt = front_route(red, a0.red_pp);
+  if (threadIdx.x == 0) mbar_init(&rt->bar, 1);   // fenced and synced by stream_smem_init
+  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
+  pdl_launch_dependents();
+  // the routed step reads its tables from this CTA's shared memory
+  StreamArgs b = a1;
+  b.n_active = &rt->n_active;
+  b.active_expert = rt->expert;
+  b.active_off = rt->off;
+  b.pair_list = rt->pair;
+  SegPrior pr;
+  cfg_add_prior<RC>(ar, pr);
+  cfg_add_prior<AC>(a0, pr);
+  uint32_t stage = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      // router and shared weights are static: no wait before streaming them
+      cfg_produce<RC>(ar, SegPrior(), m.stages, m.full, m.empty, stage);
+      cfg_produce<AC>(a0, SegPrior(), m.stages, m.full, m.empty, stage);
+      mbar_wait(&rt->bar, 0, a0.status);
+      cfg_produce<BC>(b, pr, m.stages, m.full, m.empty, stage);
+      stream_drain(a0, m.empty, stage);
+    }
+    __syncwarp();
+  } else {
+    const int kw = warp - 1, ct = (int)threadIdx.x - 32, cthreads = 32 * KW;
+    float bias[kFrontMaxChunks];
+#pragma unroll
+    for (int i = 0; i < kFrontMaxChunks; ++i) {
+      const int t = (kw + i * KW) * 32 + lane;
+      bias[i] = t < f.E ? __ldg(f.bias + t) : 0.f;
+    }
+    pdl_wait_prerequisites();   // x may be the previous kernel's output
+    int pp = 0, rp = 0;
+    cfg_consume<RC>(ar, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
+    // this CTA's logits are visible GPU-wide before it counts in
+    __threadfence();
+    consumer_sync(cthreads);
+    if (ct == 0) {
+      atomicAdd(f.count, 1u);
+      wait_count(f.count, gridDim.x, a0.status);
+    }
+    consumer_sync(cthreads);
+    front_topk(f, ar.out, m.red, rt, bias, kw, KW, lane, cthreads);
+    consumer_sync(cthreads);
+    if (ct == 0) mbar_arrive(&rt->bar);
+    cfg_consume<AC>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
+    cfg_consume<BC>(b, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
+  }
+  trace_end(a0.trace, a0.trace_id);
+}
+
+}  // namespace moe

@@ -1,11 +1,18 @@
 // C ABI of the MoE decode layer (see include/moe_decode.h for the contract).
 //
-// One forward = five kernels on the caller's stream, chained with programmatic
-// dependent launch:
-//   router GEMV (streamed bf16) -> top-k + routing tables
-//   -> FC1: shared gate/up (bf16) then routed gate/up (MXFP4), SwiGLU
-//   -> FC2: shared down (bf16) then routed down (MXFP4)
+// One forward is a chain of kernels on the caller's stream, linked with
+// programmatic dependent launch.  For one row on the mma.sync expert path,
+// three launches:
+//   front: router GEMV, top-k in every CTA, shared gate/up (bf16), routed
+//          gate/up (MXFP4), SwiGLU (front.cuh)
+//   -> FC2: shared down (bf16) then routed down (MXFP4); its producer reads
+//      the routing under the front's flag and streams before the front ends
 //   -> tail (combine + residual + RMSNorm)
+// Otherwise five:
+//   router GEMV -> top-k + routing tables
+//   -> FC1: shared gate/up then routed gate/up
+//   -> FC2: shared down then routed down
+//   -> tail
 // The shared expert streams first inside FC1/FC2: its weights do not depend on
 // the routing, so FC1 starts them while top-k is still finishing.
 // Optional second stream (chained layers only): L2 prefetch of the next
@@ -21,6 +28,7 @@
 
 #include "moe_decode.h"
 #include "common.cuh"
+#include "front.cuh"
 #include "mxfp4.cuh"
 #include "stream.cuh"
 #include "tail.cuh"
@@ -29,14 +37,23 @@
 
 using namespace moe;
 
-namespace {
+namespace moe_internal {
 
 std::atomic<int> g_last_cuda_error{0};
 
-inline int cuda_fail(cudaError_t e) {
+// Records a failed CUDA call for moe_last_cuda_error (shared by every entry
+// point of the library).
+int cuda_fail(cudaError_t e) {
   g_last_cuda_error.store((int)e);
   return MOE_ERR_CUDA;
 }
+
+}  // namespace moe_internal
+
+namespace {
+
+using moe_internal::cuda_fail;
+using moe_internal::g_last_cuda_error;
 
 #define MOE_CUDA(call)                             \
   do {                                             \
@@ -83,6 +100,10 @@ struct Workspace {
   // while the router's last CTAs finish)
   float* rpartial;
   unsigned* rflags;
+  // the one-row front kernel: CTAs past the router step, and the flag under
+  // which its CTA 0 publishes the routing tables (both zeroed by the tail)
+  unsigned* front_count;
+  unsigned* route_flag;
 };
 
 // Launch shape of one streaming-GEMV step.
@@ -94,7 +115,7 @@ struct StreamPlan {
   int dense_ctas = 0;   // CTAs of the dense pass (0: the whole grid)
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kStepFront, kNumSteps };
 
 // Expert paths: mma.sync on the tiled layouts (the GEMV regime: weights
 // converted to f16 in registers), or tcgen05 on the UMMA layouts (block-scaled
@@ -184,6 +205,8 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.dflags = carve<unsigned>(p, kTcMaxCtas);
   w.rpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
   w.rflags = carve<unsigned>(p, kTcMaxCtas);
+  w.front_count = carve<unsigned>(p, 1);
+  w.route_flag = carve<unsigned>(p, 1);
   if (ws) *ws = w;
   return (size_t)(p - base);
 }
@@ -229,6 +252,12 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 // FC2 the shared down first (its weights requested before FC1 is waited for).
 #define MOE_TC1_KERNEL tc_kernel<true>
 #define MOE_TC2_KERNEL tc_kernel<false>
+// One row on the mma.sync path: router (one activation row, 512-element warp
+// slabs), shared gate/up and routed gate/up in one launch.
+// The routed step takes one activation row per expert (RMAX = 1).
+using FrontRouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 1, false, 1, 1, 8, 2>;
+using FrontFc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16>;
+#define MOE_FRONT_KERNEL stream_front_kernel<FrontRouterCfg, Sh1Cfg<1>, FrontFc1Cfg>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -320,6 +349,41 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
         MOE_FC2_KERNEL(RS, 4), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
   return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<12, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>>(
       MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
+}
+
+// Launch shape of the one-row front kernel (front.cuh): three steps through
+// one ring, the selection's scratch in the cross-slab partial buffers and
+// the routing tables after them.  Every CTA must be resident at once (the
+// CTAs wait for each other's logits): one per SM, grid = SM count.
+int plan_front(const moe_dims_t& d, int n_sm, StreamPlan* p) {
+  using RC = FrontRouterCfg;
+  using AC = Sh1Cfg<1>;
+  using BC = FrontFc1Cfg;
+  const int KW = std::max({seg_warps<RC>(d.d), seg_warps<AC>(d.d), seg_warps<BC>(d.d)});
+  if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;
+  if (!seg_fits<BC>(d.d, d.f, KW)) return MOE_ERR_UNSUPPORTED;
+  if (d.n_experts > 32 * kFrontMaxChunks * KW || d.top_k > 32) return MOE_ERR_UNSUPPORTED;
+  StreamPlan r;
+  r.threads = 32 * (KW + 1);
+  r.kc = seg_kc<BC>(d.d, KW);
+  const size_t sb = std::max({seg_stage_bytes<RC>(d.d, 1), seg_stage_bytes<AC>(d.d, 1),
+                              seg_stage_bytes<BC>(d.d, r.kc)});
+  r.stage_bytes = (int)((sb + 127) / 128 * 128);
+  r.red_pp = std::max({stream_red_pp(KW, false, 1, RC::RMAX), stream_red_pp(KW, false, 1, AC::RMAX),
+                       stream_red_pp(KW, true, BC::TM, BC::RMAX), (kFrontScratchBytes + 7) / 8});
+  r.red_pp = (r.red_pp + 3) / 4 * 4;
+  const int fixed = 2 * r.red_pp * 4 + 64 + kFrontExtraBytes;
+  r.NS = std::min(16, (kBudget1 - fixed) / (r.stage_bytes + 16));
+  if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
+  r.smem = r.NS * r.stage_bytes + r.NS * 16 + fixed;
+  MOE_CUDA(cudaFuncSetAttribute(MOE_FRONT_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                r.smem));
+  int occ = 0;
+  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, MOE_FRONT_KERNEL, r.threads, r.smem));
+  if (occ < 1) return MOE_ERR_UNSUPPORTED;
+  r.grid = n_sm;
+  *p = r;
+  return MOE_OK;
 }
 
 // Launch shape of a tensor-core kernel: six warps, a stage ring sized for the
@@ -416,6 +480,7 @@ int plan_all(moe_layer* L) {
   MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg>(MOE_FC1_KERNEL(4), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][2])));
   MOE_PLAN((plan_fc2<1>(L, d, n, &L->plan[kStepFc2][0])));
+  MOE_PLAN((plan_front(d, n, &L->plan[kStepFront][0])));
   MOE_PLAN((plan_fc2<2>(L, d, n, &L->plan[kStepFc2][1])));
   MOE_PLAN((plan_fc2<4>(L, d, n, &L->plan[kStepFc2][2])));
 #undef MOE_PLAN
@@ -479,6 +544,9 @@ int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_i
 
 // The tensor-core path for a forward of B rows?
 bool use_tc(const moe_layer* L, int B) { return L->wt.ok && (!L->wm.ok || B >= L->tc_min_batch); }
+
+// The one-row front kernel (router + top-k + FC1 in one launch)?
+bool use_front(const moe_layer* L, int B) { return B == 1 && !use_tc(L, B); }
 
 int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B);
 
@@ -568,6 +636,62 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
     case 1: return launch_dual(MOE_FC1_KERNEL(2), p, sa, ra, st, grid);
     default: return launch_dual(MOE_FC1_KERNEL(4), p, sa, ra, st, grid);
   }
+}
+
+// The one-row front (front.cuh): router rows, top-k in every CTA, shared
+// gate/up, routed gate/up.  Launched as a programmatic dependent: its
+// producer streams the router weights while the previous kernel finishes,
+// its consumers wait for that kernel before reading x.
+int launch_front(moe_layer* L, cudaStream_t st, const void* x) {
+  const moe_dims_t& d = L->dims;
+  const StreamPlan& p = L->plan[kStepFront][0];
+  StreamArgs r = base_args(L);
+  r.q = static_cast<const uint8_t*>(L->w.router_w);
+  r.K = d.d;
+  r.N = d.n_experts;
+  r.B = 1;
+  r.x = static_cast<const uint16_t*>(x);
+  r.out = L->ws.logits;
+  StreamArgs sa = base_args(L);
+  sa.q = static_cast<const uint8_t*>(L->w.shared_gu);
+  sa.K = d.d;
+  sa.N = d.f_shared;
+  sa.B = 1;
+  sa.x = static_cast<const uint16_t*>(x);
+  sa.out = L->ws.hs;
+  StreamArgs ra = base_args(L);
+  ra.q = L->wm.gu_q;
+  ra.s = L->wm.gu_s;
+  ra.q_stride = L->q_gu_stride;
+  ra.s_stride = L->s_gu_stride;
+  ra.K = d.d;
+  ra.N = d.f;
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.out = L->ws.h;
+  ra.out_amax = L->ws.h_amax;
+  for (StreamArgs* a : {&r, &sa, &ra}) {
+    a->NS = p.NS;
+    a->stage_bytes = p.stage_bytes;
+    a->red_pp = p.red_pp;
+    a->kc = p.kc;
+    a->trace_id = 2;
+  }
+  FrontArgs f{};
+  f.bias = L->w.router_bias;
+  f.E = d.n_experts;
+  f.k = d.top_k;
+  f.routed_scale = d.routed_scale;
+  f.count = L->ws.front_count;
+  f.route_flag = L->ws.route_flag;
+  f.topk_idx = L->ws.topk_idx;
+  f.topk_w = L->ws.topk_w;
+  f.n_active = L->ws.n_active;
+  f.active_expert = L->ws.active_expert;
+  f.active_off = L->ws.active_off;
+  f.pair_list = L->ws.pair_list;
+  MOE_CUDA(launch_ex(MOE_FRONT_KERNEL, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, r,
+                     sa, ra, f));
+  return MOE_OK;
 }
 
 // Tensor-core path: the routed step's arguments common to FC1 and FC2.
@@ -728,8 +852,10 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   return launch_tc(MOE_TC2_KERNEL, p, b, dn, unused, st, p.grid);
 }
 
-// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).
-int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
+// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).  After the
+// one-row front (`front`), its producer takes the routing from the front's
+// flag instead of waiting for the front to finish.
+int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool front) {
   const moe_dims_t& d = L->dims;
   StreamArgs sa = base_args(L);
   sa.q = static_cast<const uint8_t*>(L->w.shared_d);
@@ -748,6 +874,7 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   ra.h = L->ws.h;
   ra.h_amax = L->ws.h_amax;
   ra.out = L->ws.y_pair;
+  ra.route_flag = front ? L->ws.route_flag : nullptr;
   sa.trace_id = ra.trace_id = 3;
   const StreamPlan& p = L->plan[kStepFc2][batch_class(B)];
   if (fc2_small(d)) {
@@ -781,6 +908,9 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.k = L->dims.top_k;
   a.eps = L->dims.rms_eps;
   a.trace = L->tracing ? L->ws.trace : nullptr;
+  a.front_count = L->ws.front_count;
+  a.route_flag = L->ws.route_flag;
+  a.h_amax = L->ws.h_amax;
   MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
   return MOE_OK;
 }
@@ -824,13 +954,21 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   }
   MOE_CUDA(cudaEventRecord(L->ev_fork, st));
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
-  if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
-  if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-  if ((rc = launch_prefetch(L))) return rc;
   const bool tc = use_tc(L, B);
-  if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
+  const bool front = use_front(L, B);
+  if (front) {
+    // router and top-k run inside the front kernel: their phase is empty
+    if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
+    if ((rc = launch_prefetch(L))) return rc;
+    if ((rc = launch_front(L, st, x))) return rc;
+  } else {
+    if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
+    if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
+    if ((rc = launch_prefetch(L))) return rc;
+    if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
+  }
   if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
+  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B, front))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
@@ -1163,7 +1301,9 @@ int moe_get_trace(moe_layer_t L, unsigned long long* ns, int n) {
 
 int moe_launches_per_forward(moe_layer_t L, int B) {
   if (!L || B < 1 || B > L->dims.max_batch) return -1;
-  return 5;   // router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
+  // one row on the mma.sync path: front (router + top-k + FC1), FC2, tail;
+  // otherwise router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
+  return use_front(L, B) ? 3 : 5;
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {

@@ -70,6 +70,10 @@ struct StreamArgs {
   int trace_id;
   uint8_t* xq;               // router only: activation planes of x [B][4K] (planes.cuh), or null
   uint8_t* xq_code;          // and their plane-0 codes, one per row [B]
+  const unsigned* route_flag;  // routed step of a two-step kernel: non-null when the routing
+                               // tables are published under this flag (the producer then
+                               // streams the routed weights without waiting for the previous
+                               // kernel to finish)
 };
 
 // Lane layout of the bf16 steps: a lane owns NQ chunks of CW consecutive K
@@ -236,7 +240,7 @@ struct StreamItem {
 template <bool ROUTED, int RW>
 __device__ __forceinline__ int stream_n_items(const StreamArgs& a, int& tiles) {
   tiles = (a.N + RW - 1) / RW;
-  return ROUTED ? __ldcg(a.n_active) * tiles : tiles;
+  return ROUTED ? ld_tab(a.n_active) * tiles : tiles;
 }
 
 template <bool ROUTED, int RW>
@@ -244,9 +248,9 @@ __device__ __forceinline__ StreamItem stream_item(const StreamArgs& a, int it, i
   StreamItem m;
   if (ROUTED) {
     const int slot = it / tiles;
-    m.e = __ldcg(a.active_expert + slot);
-    m.p0 = __ldcg(a.active_off + slot);
-    m.pr = __ldcg(a.active_off + slot + 1) - m.p0;
+    m.e = ld_tab(a.active_expert + slot);
+    m.p0 = ld_tab(a.active_off + slot);
+    m.pr = ld_tab(a.active_off + slot + 1) - m.p0;
     m.row0 = (it % tiles) * RW;
   } else {
     m.e = 0;
@@ -272,6 +276,49 @@ __device__ __forceinline__ int stream_pass_rows(int left) {
 __device__ __forceinline__ void stream_range(int n_items, int& lo, int& hi) {
   lo = (int)(((long long)blockIdx.x * n_items) / gridDim.x);
   hi = (int)(((long long)(blockIdx.x + 1) * n_items) / gridDim.x);
+}
+
+// Steps that run earlier in the same launch, split the standard way (at most
+// two; n = 0: none), as item counts and weight bytes per item.
+struct SegPrior {
+  int n0 = 0;
+  long long s0 = 0;
+  int n1 = 0;
+  long long s1 = 0;
+};
+
+__device__ __forceinline__ long long prior_bytes(const SegPrior& p, int c, int G) {
+  return (long long)(((long long)c * p.n0) / G) * p.s0 + (long long)(((long long)c * p.n1) / G) * p.s1;
+}
+
+// First item of CTA c (of G) in a step of n items of ib bytes that follows
+// `p`: chosen so that every CTA streams about the same bytes over all the
+// steps of the launch, i.e. round((c T / G - P(c)) / ib) clamped to [0, n],
+// T being the launch's total bytes and P(c) what CTAs 0..c-1 stream in the
+// earlier steps.  (The earlier steps' per-CTA shares differ by up to one of
+// their items; this step evens that out to half of one of its own.)
+__device__ __forceinline__ int balanced_start(const SegPrior& p, int c, int G, int n, long long ib) {
+  if (c >= G) return n;
+  const long long total = (long long)p.n0 * p.s0 + (long long)p.n1 * p.s1 + (long long)n * ib;
+  const long long num = (long long)c * total - (long long)G * prior_bytes(p, c, G);
+  if (num <= 0 || ib <= 0) return 0;
+  const long long den = (long long)G * ib;
+  return (int)min((long long)n, (num + den / 2) / den);
+}
+
+// [lo, hi) for this CTA: the standard split without a prior, else balanced.
+// Balanced starts need not increase with c when an earlier step's items are
+// much larger than this step's share per CTA; an empty range (hi = lo) then
+// leaves the items in between to the neighbours, which compute them both
+// (identical values), so every item is still covered.
+__device__ __forceinline__ void seg_range(const SegPrior& p, int n, long long ib, int& lo, int& hi) {
+  if (p.n0 == 0 && p.n1 == 0) {
+    stream_range(n, lo, hi);
+    return;
+  }
+  const int c = blockIdx.x, G = gridDim.x;
+  lo = balanced_start(p, c, G, n, ib);
+  hi = max(lo, balanced_start(p, c + 1, G, n, ib));
 }
 
 // End of the run that starts at item `it` (same expert for routed steps; a
@@ -414,7 +461,7 @@ __device__ __forceinline__ void stream_consume_run(const StreamArgs& a, const St
   uint32_t act[R][Sh::AW];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    pid[r] = ROUTED ? __ldcg(a.pair_list + m.p0 + done + r) : done + r;
+    pid[r] = ROUTED ? ld_tab(a.pair_list + m.p0 + done + r) : done + r;
     if constexpr (!ACTH)
       act_load_bf_x<CW, NQ>(a.x + (size_t)stream_x_row<ROUTED>(a, pid[r]) * a.K, slab, lane, a.K,
                             act[r]);
@@ -589,8 +636,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
   // outputs go first to the consumer warps that own no K blocks
   const int et = stream_epi_index(ct, min(KW, (nblk + NB - 1) / NB), KW);
   const int ei = et % R;
-  const int cpid = __ldcg(a.pair_list + m.p0 + done + ci);
-  const int epid = __ldcg(a.pair_list + m.p0 + done + ei);
+  const int cpid = ld_tab(a.pair_list + m.p0 + done + ci);
+  const int epid = ld_tab(a.pair_list + m.p0 + done + ei);
 
   int eshift;
   // one x row for the whole pass (R = 1): the same key in every lane and warp
@@ -751,11 +798,11 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
     for (int done = 0; done < m.pr;) {
       const int R = stream_pass_rows<RMAX, MMA>(m.pr - done);
       if constexpr (MMA) {
-        if (R == 1)
+        if (RMAX == 1 || R == 1)
           stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
               lane, X, xkey, xshift);
-        else
+        else if constexpr (RMAX > 1)
           stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, false>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
               lane, X, xkey, xshift);
@@ -798,26 +845,62 @@ struct StreamCfg {
   static_assert(MMA || WF == kWfBf16, "MXFP4 steps run on the tensor cores");
 };
 
+// Weight bytes one item of a step streams: MXFP4 tiles of 16 rows (K/2
+// nibble bytes + K/32 scale bytes per row), or RW bf16 rows (gate/up: pairs).
 template <class C>
-__device__ __forceinline__ void cfg_produce(const StreamArgs& a, uint8_t* stages, uint64_t* full,
-                                            uint64_t* empty, uint32_t& stage) {
+__device__ __forceinline__ long long cfg_item_bytes(const StreamArgs& a) {
+  if constexpr (C::MMA) return (long long)C::TM * 17 * (a.K / 2);
+  else return (long long)C::RW * (C::GLU ? 2 : 1) * a.K * 2;
+}
+
+// A dense step as the prior of a later step in the same launch.
+template <class C>
+__device__ __forceinline__ void cfg_add_prior(const StreamArgs& a, SegPrior& p) {
+  int tiles;
+  const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
+  if (p.n0 == 0) {
+    p.n0 = n;
+    p.s0 = cfg_item_bytes<C>(a);
+  } else {
+    p.n1 = n;
+    p.s1 = cfg_item_bytes<C>(a);
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void cfg_produce(const StreamArgs& a, const SegPrior& prior,
+                                            uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                            uint32_t& stage) {
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
-  stream_range(n, lo, hi);
+  seg_range(prior, n, cfg_item_bytes<C>(a), lo, hi);
   stream_produce_range<C::WF, C::GLU, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM>(
       a, lo, hi, tiles, stages, full, empty, stage);
 }
 
 template <class C>
-__device__ __forceinline__ void cfg_consume(const StreamArgs& a, uint8_t* stages, uint64_t* full,
-                                            uint64_t* empty, float* red, uint32_t& stage, int& pp,
-                                            int& rp, int kw, int KW, int lane) {
+__device__ __forceinline__ void cfg_consume(const StreamArgs& a, const SegPrior& prior,
+                                            uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                            float* red, uint32_t& stage, int& pp, int& rp, int kw,
+                                            int KW, int lane) {
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
-  stream_range(n, lo, hi);
+  seg_range(prior, n, cfg_item_bytes<C>(a), lo, hi);
   stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM,
                        C::NBMAX, C::CW, C::NQ>(a, lo, hi, tiles, stages, full, empty, red, stage,
                                                pp, rp, kw, KW, lane);
+}
+
+// Bounded wait for a flag another kernel (or CTA) raises with a release store.
+__device__ __forceinline__ void wait_flag(const unsigned* flag, int* status) {
+  if (ld_acquire_u32(flag) != 0u) return;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_u32(flag) == 0u) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return;
+    }
+  }
 }
 
 // Shared-memory carve-up common to both kernels.
@@ -864,7 +947,7 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   if (warp == 0) {
     if (lane == 0) {
       if (ROUTED) pdl_wait_prerequisites();
-      cfg_produce<C>(a, m.stages, m.full, m.empty, stage);
+      cfg_produce<C>(a, SegPrior(), m.stages, m.full, m.empty, stage);
       stream_drain(a, m.empty, stage);
     }
     __syncwarp();
@@ -905,7 +988,8 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
       }
     }
     int pp = 0, rp = 0;
-    cfg_consume<C>(a, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    cfg_consume<C>(a, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW,
+                   lane);
   }
   trace_end(a.trace, a.trace_id);
 }
@@ -928,18 +1012,26 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   if (warp == 0) {
     if (lane == 0) {
       if (A::ROUTED) pdl_wait_prerequisites();
-      cfg_produce<A>(a0, m.stages, m.full, m.empty, stage);
-      pdl_wait_prerequisites();
-      cfg_produce<B>(a1, m.stages, m.full, m.empty, stage);
+      cfg_produce<A>(a0, SegPrior(), m.stages, m.full, m.empty, stage);
+      // the routed step's weights are static: with the routing published
+      // under a flag they stream while the previous kernel still runs
+      if (a1.route_flag) wait_flag(a1.route_flag, a1.status);
+      else pdl_wait_prerequisites();
+      SegPrior pr;
+      if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
+      cfg_produce<B>(a1, pr, m.stages, m.full, m.empty, stage);
       stream_drain(a0, m.empty, stage);
     }
     __syncwarp();
   } else {
     if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
     int pp = 0, rp = 0;
-    cfg_consume<A>(a0, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    cfg_consume<A>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW,
+                   lane);
     pdl_wait_prerequisites();
-    cfg_consume<B>(a1, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    SegPrior pr;
+    if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
+    cfg_consume<B>(a1, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
   }
   trace_end(a0.trace, a0.trace_id);
 }

@@ -86,6 +86,37 @@ __device__ __forceinline__ uint64_t warp_bitonic_merge_desc(uint64_t key, int la
   return key;
 }
 
+// Descending bitonic sort of 32 keys held one per lane.
+__device__ __forceinline__ uint64_t warp_bitonic_sort_desc(uint64_t key, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool lower = (lane & stride) == 0;
+      const bool take = (lower == desc) ? (ok > key) : (ok < key);
+      if (take) key = ok;
+    }
+  }
+  return key;
+}
+
+// The router's score of one logit, sigma(l), in fp32.
+__device__ __forceinline__ float topk_score(float logit) { return 1.0f / (1.0f + expf(-logit)); }
+
+// Selection key of expert e: the order-preserving image of fp32 (score + bias)
+// above the complemented id, so a larger key is a better expert and equal
+// biased scores go to the lower id.
+__device__ __forceinline__ uint64_t topk_key(float score, float bias, int e) {
+  return ((uint64_t)float_order_bits(score + bias) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+// Expert id of a key.
+__device__ __forceinline__ int topk_key_expert(uint64_t key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)key);
+}
+
 static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   __shared__ int s_warp[33];
@@ -105,23 +136,12 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   // ---- scores and keys ----
   uint64_t key = 0ull;
   if (valid) {
-    const float l = __ldcg(a.logits + (size_t)b * a.E + t);
-    const float score = 1.0f / (1.0f + expf(-l));
+    const float score = topk_score(__ldcg(a.logits + (size_t)b * a.E + t));
     s_sc[t] = score;
-    key = ((uint64_t)float_order_bits(score + bias) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)t);
+    key = topk_key(score, bias, t);
   }
   // ---- per-warp bitonic sort, descending ----
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
-      const bool desc = (lane & size) == 0 || size == 32;
-      const bool lower = (lane & stride) == 0;
-      const bool take = (lower == desc) ? (ok > key) : (ok < key);
-      if (take) key = ok;
-    }
-  }
+  key = warp_bitonic_sort_desc(key, lane);
   // ---- tournament of the sorted warp lists ----
   int n = (a.E + 31) >> 5;   // lists holding valid keys
   if (warp < n) s_list[0][warp][lane] = key;
@@ -142,7 +162,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   }
   if (warp == 0) {
     if (lane < a.k) {
-      const int e = (int)(0xFFFFFFFFu - (uint32_t)s_list[src][0][lane]);
+      const int e = topk_key_expert(s_list[src][0][lane]);
       a.topk_idx[b * a.k + lane] = e;
       s_idx[b * a.k + lane] = e;
       s_score[lane] = s_sc[e];

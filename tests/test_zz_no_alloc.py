@@ -13,8 +13,9 @@ import pytest
 import torch
 
 import gen
+import oracle
 import moe_decode_step_gb300 as M
-from gen.configs import CONFIGS, T_ROUTER_W, T_ROUTER_BIAS
+from gen.configs import CONFIGS, T_ROUTER_W, T_ROUTER_BIAS, T_X
 from moe_decode_step_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
@@ -35,6 +36,31 @@ def _noalloc(router_w, bias, x, k, routed_scale):
     return rc, idx, w
 
 
+def _status():
+    v = ctypes.c_int(-1)
+    rc = M.lib().moe_router_topk_noalloc_status(ctypes.byref(v))
+    assert rc == M.MOE_OK, M.status_string(rc)
+    return v.value
+
+
+def _check_against_oracle(idx, w, ref_idx, ref_w, gap):
+    """Expert sets equal to the oracle's for every row whose k-th vs (k+1)-th
+    biased-score gap is at least 1e-5, and each weight within 1e-6 of the
+    oracle's weight for the same expert."""
+    idx = idx.cpu().numpy()
+    w = w.cpu().numpy().astype(np.float64)
+    checked = 0
+    for b in range(idx.shape[0]):
+        if gap[b] < 1e-5:
+            continue
+        assert sorted(idx[b].tolist()) == sorted(ref_idx[b].tolist()), b
+        order = {int(e): j for j, e in enumerate(ref_idx[b])}
+        for j in range(idx.shape[1]):
+            assert abs(w[b, j] - ref_w[b, order[int(idx[b, j])]]) <= 1e-6
+        checked += 1
+    return checked
+
+
 def _check_same_routing(layer_idx, layer_w, idx, w):
     assert torch.equal(idx.cpu(), layer_idx.cpu())
     np.testing.assert_allclose(w.cpu().numpy(), layer_w.cpu().numpy(), rtol=0, atol=1e-6)
@@ -53,7 +79,49 @@ def test_noalloc_router_matches_layer_router_tiny(B):
         torch.cuda.synchronize()
         assert rc == M.MOE_OK, M.status_string(rc)
         _check_same_routing(ref_idx, ref_w, idx, w)
+    assert _status() == 0
     layer.close()
+
+
+def test_noalloc_router_full_size_matches_oracle():
+    """Full-size router (896 experts, d = 7168, top-16) at B = 8 straight
+    against the oracle's fp64 routing, on the oracle's tie-free draw."""
+    cfg = CONFIGS["full_b8"]
+    inp = oracle.clean_inputs(cfg)
+    ref_logits, ref_idx, ref_w, gap = oracle.route(inp)
+    dev = torch.device("cuda")
+    rw = torch.from_numpy(inp.wr.astype(np.float32)).to(dev).to(torch.bfloat16)
+    bias = torch.from_numpy(np.asarray(inp.bias, np.float32)).to(dev)
+    x, _ = synthetic.make_activations(cfg, attempt=inp.attempt)
+    assert np.array_equal(x.float().cpu().numpy().astype(np.float64), inp.x)
+    for _ in range(2):
+        rc, idx, w = _noalloc(rw, bias, x, cfg.top_k, cfg.routed_scale)
+        torch.cuda.synchronize()
+        assert rc == M.MOE_OK, M.status_string(rc)
+        assert _check_against_oracle(idx, w, ref_idx, ref_w, gap) == cfg.B
+    assert _status() == 0
+
+
+def test_noalloc_router_largest_hidden_size_matches_oracle():
+    """d = 7680, the largest hidden size the entry point accepts, 64 experts,
+    top-4, B = 5, against the oracle's fp64 routing."""
+    d, E, k, B = 7680, 64, 4, 5
+    dev = torch.device("cuda")
+    rw = torch.empty((E, d), dtype=torch.float32, device=dev)
+    gen.normal_device(21, T_ROUTER_W, 0, rw, 0.0, float(np.float32(1 / np.sqrt(d))))
+    rw = rw.to(torch.bfloat16)
+    bias = torch.empty(E, dtype=torch.float32, device=dev)
+    gen.normal_device(21, T_ROUTER_BIAS, 0, bias, 0.0, 0.01)
+    x = torch.empty((B, d), dtype=torch.float32, device=dev)
+    gen.normal_device(21, T_X, 0, x, 0.0, 1.0)
+    x = x.to(torch.bfloat16)
+    _, ref_idx, ref_w, gap = oracle.router(x.float().cpu().numpy(), rw.float().cpu().numpy(),
+                                           bias.cpu().numpy(), k, 2.5)
+    rc, idx, w = _noalloc(rw, bias, x, k, 2.5)
+    torch.cuda.synchronize()
+    assert rc == M.MOE_OK, M.status_string(rc)
+    assert _check_against_oracle(idx, w, ref_idx, ref_w, gap) >= B - 1
+    assert _status() == 0
 
 
 def test_noalloc_router_full_size_router_weights():
@@ -96,4 +164,8 @@ def test_noalloc_router_rejects_sizes_beyond_its_scratch():
     rc, _, _ = _noalloc(weights["router_w"], weights["router_bias"], x, cfg.top_k, 2.5)
     assert rc == M.MOE_ERR_UNSUPPORTED
     rc, _, _ = _noalloc(weights["router_w"], weights["router_bias"], x[:2], 33, 2.5)
+    assert rc == M.MOE_ERR_UNSUPPORTED
+    # hidden size past the largest accepted (7680)
+    big = torch.zeros((64, 7936), dtype=torch.bfloat16, device="cuda")
+    rc, _, _ = _noalloc(big, weights["router_bias"], big[:1], cfg.top_k, 2.5)
     assert rc == M.MOE_ERR_UNSUPPORTED
