@@ -165,6 +165,17 @@ int moe_set_prefetch_next(moe_layer_t layer, moe_layer_t next);
  * (0 = ok, else a moe_status such as MOE_ERR_TIMEOUT); clears it. */
 int moe_layer_status(moe_layer_t layer, int* device_status);
 
+/* Failure-detection test hook (the pages have no counterpart; it exists so a
+ * test can watch a device-side wait expire without faulting anything).
+ * fault = 1: in later forwards of one row on the mma.sync path, one CTA of
+ * the front kernel does not count itself in after the router step, and the
+ * other CTAs' wait for that count is limited to wait_ns nanoseconds (0: the
+ * default 2 s).  The wait expires, the forward still completes (the logits
+ * it waited for were written), and moe_layer_status then reports
+ * MOE_ERR_TIMEOUT.  fault = 0 restores normal operation.  Nothing on the GPU
+ * traps, faults or hangs.  Errors: INVALID_ARG. */
+int moe_debug_set_fault(moe_layer_t layer, int fault, unsigned long long wait_ns);
+
 /* Per-phase timing of forward calls (CUDA events on the launching stream;
  * under stream capture they become event-record nodes of the graph).
  * enable != 0 records events around each phase from the next forward on.

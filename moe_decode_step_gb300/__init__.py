@@ -161,6 +161,12 @@ class MoELayer:
         check(lib().moe_layer_status(self._h, ctypes.byref(v)), "moe_layer_status")
         return v.value
 
+    def debug_set_fault(self, fault, wait_ns=0):
+        """Failure-detection test hook (see moe_debug_set_fault): fault 1 makes
+        the one-row front kernel's arrival wait expire after wait_ns."""
+        check(lib().moe_debug_set_fault(self._h, int(fault), int(wait_ns)),
+              "moe_debug_set_fault")
+
     def set_timing(self, enable):
         check(lib().moe_set_timing(self._h, int(bool(enable))), "moe_set_timing")
 

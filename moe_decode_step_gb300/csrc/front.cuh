@@ -41,6 +41,10 @@ struct FrontArgs {
   int* active_expert;
   int* active_off;
   int* pair_list;
+  // failure-detection test hook: CTA skip_arrive_cta (-1: none) does not
+  // count itself in, so every CTA's wait for the count expires after wait_ns
+  unsigned long long wait_ns;
+  int skip_arrive_cta;
 };
 
 // Routing tables of one row in shared memory, and the barrier the producer
@@ -64,12 +68,13 @@ __device__ __forceinline__ FrontRoute* front_route(float* red, int red_pp) {
   return reinterpret_cast<FrontRoute*>(reinterpret_cast<uint8_t*>(red + 2 * (size_t)red_pp) + 64);
 }
 
-// Bounded wait until *c >= target (acquire).
-__device__ __forceinline__ void wait_count(const unsigned* c, unsigned target, int* status) {
+// Wait until *c >= target (acquire), at most limit_ns.
+__device__ __forceinline__ void wait_count(const unsigned* c, unsigned target, int* status,
+                                           unsigned long long limit_ns) {
   if (ld_acquire_u32(c) >= target) return;
   const unsigned long long t0 = global_ns();
   while (ld_acquire_u32(c) < target) {
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       if (status) atomicExch(status, kStatusTimeout);
       return;
     }
@@ -221,8 +226,8 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     __threadfence();
     consumer_sync(cthreads);
     if (ct == 0) {
-      atomicAdd(f.count, 1u);
-      wait_count(f.count, gridDim.x, a0.status);
+      if ((int)blockIdx.x != f.skip_arrive_cta) atomicAdd(f.count, 1u);
+      wait_count(f.count, gridDim.x, a0.status, f.wait_ns);
     }
     consumer_sync(cthreads);
     front_topk(f, ar.out, m.red, rt, bias, kw, KW, lane, cthreads);

@@ -161,6 +161,9 @@ struct moe_layer {
   uint8_t* router_umma = nullptr;   // router weights in 128-row tiles (last one zero-padded)
   void* sh_owned = nullptr;
   void* encode_tiled = nullptr;   // the driver's tensor-map encoder
+  // failure-detection test hook (moe_debug_set_fault)
+  int debug_fault = 0;
+  unsigned long long debug_wait_ns = 0;
 };
 
 namespace {
@@ -689,6 +692,8 @@ int launch_front(moe_layer* L, cudaStream_t st, const void* x) {
   f.active_expert = L->ws.active_expert;
   f.active_off = L->ws.active_off;
   f.pair_list = L->ws.pair_list;
+  f.skip_arrive_cta = L->debug_fault == 1 ? p.grid - 1 : -1;
+  f.wait_ns = L->debug_wait_ns ? L->debug_wait_ns : kWaitLimitNs;
   MOE_CUDA(launch_ex(MOE_FRONT_KERNEL, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, r,
                      sa, ra, f));
   return MOE_OK;
@@ -1259,6 +1264,13 @@ int moe_layer_status(moe_layer_t L, int* device_status) {
   MOE_CUDA(cudaMemcpy(&v, L->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
   MOE_CUDA(cudaMemset(L->ws.status, 0, sizeof(int)));
   *device_status = v;
+  return MOE_OK;
+}
+
+int moe_debug_set_fault(moe_layer_t L, int fault, unsigned long long wait_ns) {
+  if (!L || fault < 0 || fault > 1) return MOE_ERR_INVALID_ARG;
+  L->debug_fault = fault;
+  L->debug_wait_ns = fault ? wait_ns : 0;
   return MOE_OK;
 }
 

@@ -1,0 +1,167 @@
+"""GPU parity on the layer's edge cases against the oracle, element by element,
+on both expert paths (mma.sync: one row runs the fused front kernel; tcgen05):
+
+  * an exact top-k tie: zeroed router rows with equal biases give equal biased
+    scores; ties go to the lower expert id, and the selected ids must match
+    the oracle's in order (the near-tie redraw rule is broken on purpose),
+  * a row whose max |x| is at least 2^15 (a drawn row scaled by 2^16): the
+    f16 rescaling of the mma.sync path, the per-row plane code of tcgen05,
+  * an all-zero row: FC1 and FC2 give exact zeros and z is the residual,
+  * 64 identical rows at full size: every selected expert takes 64 pairs, the
+    longest runs the work split sees.
+
+Rows are checked one at a time, so a large row cannot hide the error of a
+normal one behind its RMS."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gen.configs import CONFIGS
+from moe_decode_step_gb300 import synthetic
+
+from _parity import assert_close
+from test_gpu_layer import check_against_oracle
+
+pytestmark = pytest.mark.gpu
+
+TINY = CONFIGS["tiny_b1"]
+PATHS = [1, 2]
+PATH_IDS = ["mma_sync", "tcgen05"]
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _cfg(base, B):
+    return dataclasses.replace(base, name=f"{base.name}_B{B}", B=B)
+
+
+def _run(cfg, weights, x, res, path, max_batch):
+    """router_topk + forward_debug of one layer built on `weights`; returns
+    idx, w (numpy), the debug exports and the updated residual."""
+    layer = synthetic.make_layer(cfg, max_batch=max_batch, weights=weights, expert_path=path)
+    idx, w = layer.router_topk(x)
+    r = res.clone()
+    d = layer.forward_debug(x, r)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert layer.launches_per_forward(x.shape[0]) == (3 if x.shape[0] == 1 and path == 1 else 5)
+    layer.close()
+    dbg = {k: _np(v) for k, v in d.items()}
+    return idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg, _np(r)
+
+
+def _check_rows(ref, idx, w, dbg, res_out, rows, zero_rows=()):
+    """Parity row by row; a zero row must give exact zeros through the experts."""
+    for b in rows:
+        if b in zero_rows:
+            assert sorted(idx[b].tolist()) == sorted(ref["idx"][b].tolist())
+            assert np.all(dbg["h"][b] == 0.0) and np.all(dbg["y_routed"][b] == 0.0)
+            assert np.all(dbg["y_shared"][b] == 0.0)
+            assert np.array_equal(dbg["z"][b], ref["z"][b])   # the residual, exactly
+            assert_close(dbg["out_f32"][b], ref["out"][b], 2e-3, 5e-4, what="out of a zero row")
+        else:
+            check_against_oracle(ref, idx, w, dbg, res_out, [b])
+
+
+# ---------------------------------------------------------------------------
+TIE = [7, 11, 20, 41, 50, 63]   # six experts with equal biased scores; top-4
+
+
+@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_exact_topk_tie_goes_to_lower_ids(path, B):
+    cfg = _cfg(TINY, B)
+    w = synthetic.make_weights(TINY, layout=1 if path == 1 else 3)
+    w["router_w"][TIE] = 0
+    w["router_bias"][TIE] = 1.0
+    x, res = synthetic.make_activations(cfg)
+    inp = oracle.LayerInputs(cfg, x=_np(x), residual=_np(res))
+    inp.wr[TIE] = 0.0
+    inp.bias = np.array(inp.bias, dtype=np.float32)
+    inp.bias[TIE] = 1.0
+    ref = oracle.forward(inp)
+    # sigma(0) + 1 beats every other expert; of the six tied, the four lowest ids
+    assert all(ref["idx"][b].tolist() == TIE[:4] for b in range(B))
+    idx, wt, dbg, r = _run(cfg, w, x, res, path, max_batch=B)
+    assert np.array_equal(idx, ref["idx"])   # the order too
+    _check_rows(ref, idx, wt, dbg, r, range(B))
+
+
+# ---------------------------------------------------------------------------
+def _edge_inputs(cfg, kinds):
+    """x with row b replaced per kinds[b] ("normal", "large": the drawn row
+    times 2^16, exact in bf16, "zero"); the first draw (seed + 1000 attempt)
+    whose rows all clear the 1e-5 near-tie gap."""
+    for attempt in range(20):
+        x, res = synthetic.make_activations(cfg, attempt=attempt)
+        for b, kind in enumerate(kinds):
+            if kind == "large":
+                x[b] *= 65536.0
+            elif kind == "zero":
+                x[b] = 0
+        inp = oracle.LayerInputs(cfg, x=_np(x), residual=_np(res))
+        if np.all(oracle.route(inp)[3] >= 1e-5):
+            return x, res, inp
+    raise RuntimeError("no draw without a near-tie")
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_large_and_zero_rows_in_one_batch(path):
+    kinds = ["normal", "large", "zero"]
+    cfg = _cfg(TINY, len(kinds))
+    x, res, inp = _edge_inputs(cfg, kinds)
+    assert float(x[1].float().abs().max()) >= 2.0 ** 15
+    ref = oracle.forward(inp)
+    w = synthetic.make_weights(TINY, layout=1 if path == 1 else 3)
+    idx, wt, dbg, r = _run(cfg, w, x, res, path, max_batch=len(kinds))
+    _check_rows(ref, idx, wt, dbg, r, range(len(kinds)), zero_rows=(2,))
+
+
+@pytest.mark.parametrize("kind", ["large", "zero"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_one_edge_row(path, kind):
+    """One row alone: the fused front kernel on the mma.sync path."""
+    cfg = _cfg(TINY, 1)
+    x, res, inp = _edge_inputs(cfg, [kind])
+    ref = oracle.forward(inp)
+    w = synthetic.make_weights(TINY, layout=1 if path == 1 else 3)
+    idx, wt, dbg, r = _run(cfg, w, x, res, path, max_batch=1)
+    _check_rows(ref, idx, wt, dbg, r, [0], zero_rows=(0,) if kind == "zero" else ())
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_sixty_four_identical_rows_full_size(path):
+    """full_b64's weights with all 64 rows equal to one drawn row: 16 experts,
+    64 pairs each.  Sampled rows against the oracle element by element, and
+    every row's routed and shared outputs against the oracle's row."""
+    cfg = CONFIGS["full_b64"]
+    x, res = synthetic.make_activations(cfg)
+    gap = oracle.route(oracle.LayerInputs(cfg, x=_np(x), residual=_np(res)))[3]
+    r0 = int(np.argmax(gap >= 1e-5))
+    assert gap[r0] >= 1e-5
+    xi = x[r0:r0 + 1].repeat(cfg.B, 1).contiguous()
+    inp = oracle.LayerInputs(cfg, x=_np(xi), residual=_np(res))
+    rows = [0, 37, 63]
+    ref = oracle.forward(inp, rows=rows)
+    layer = synthetic.make_layer(cfg, expert_path=path)
+    idx, w = layer.router_topk(xi)
+    r = res.clone()
+    d = layer.forward_debug(xi, r)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    layer.close()
+    dbg = {k: _np(v) for k, v in d.items()}
+    idx = idx.cpu().numpy()
+    assert len(set(idx.ravel().tolist())) == cfg.top_k
+    for b in range(cfg.B):
+        assert idx[b].tolist() == idx[0].tolist()
+    check_against_oracle(ref, idx, w.cpu().numpy().astype(np.float64), dbg, _np(r), rows)
+    for b in range(cfg.B):
+        assert_close(dbg["y_routed"][b], ref["y_r"][0], 2e-3, 5e-4, what=f"y_routed row {b}")
+        assert_close(dbg["y_shared"][b], ref["y_s"][0], 1e-4, 1e-5, what=f"y_shared row {b}")

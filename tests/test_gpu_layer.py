@@ -184,3 +184,26 @@ def test_zero_down_weights_leave_rmsnorm_of_residual_plus_shared():
     want = z / np.sqrt((z ** 2).mean(axis=1, keepdims=True) + TINY.rms_eps) * inp.gamma
     assert_close(dbg["out_f32"], want, 2e-3, 5e-4, what="out with zero experts")
     layer.close()
+
+
+def test_bounded_wait_expiry_reports_timeout_and_layer_recovers():
+    """One CTA of the one-row front kernel skips its arrival: every other CTA's
+    wait for it expires after 1 ms, the forward completes, the status word
+    reads MOE_ERR_TIMEOUT; with the hook off the next forward passes parity."""
+    layer = synthetic.make_layer(TINY, max_batch=1, expert_path=1)
+    cfg = tiny_cfg(1)
+    inp = oracle.clean_inputs(cfg)
+    ref = oracle.forward(inp)
+    x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
+    assert layer.launches_per_forward(1) == 3
+    layer.debug_set_fault(1, 1_000_000)
+    layer.forward(x, res.clone())
+    torch.cuda.synchronize()
+    assert layer.status() == M.MOE_ERR_TIMEOUT
+    layer.debug_set_fault(0)
+    idx, w = layer.router_topk(x)
+    dbg = run_debug(layer, x, res)
+    assert layer.status() == 0
+    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg,
+                         _np(res), [0])
+    layer.close()
