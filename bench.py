@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                    help="run --warmup untimed forwards of a profiling workload (L2 flushed "
                         "between them) and exit; for ncu captures, prints no JSON line")
+    p.add_argument("--expert-path", type=int, choices=[0, 1, 2], default=0,
+                   help="profiling workload only: 0 both expert paths (by batch), 1 mma.sync, "
+                        "2 tcgen05")
     return p.parse_args()
 
 
@@ -624,7 +627,7 @@ def run_profile_case(args):
         cfg = dataclasses.replace(cfg, name=args.profile_case, n_experts=n_experts)
     dev = torch.device("cuda", 0)
     flush = L2Flush(dev)
-    layer = synthetic.make_layer(cfg)
+    layer = synthetic.make_layer(cfg, expert_path=args.expert_path)
     x, res0 = synthetic.make_activations(cfg)
     res = res0.clone()
     out = torch.empty_like(x)

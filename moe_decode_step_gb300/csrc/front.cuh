@@ -9,18 +9,19 @@
 //   R  router rows (bf16) -> logits [E] in global memory
 //   A  shared gate/up (bf16) -> h_s, SwiGLU
 //   B  routed gate/up (MXFP4, mma.sync) -> h, SwiGLU
-// Between R and A every CTA's consumers
-//   - make their logits visible and count the CTA in (one atomic per CTA),
+// After R every CTA's consumers make their logits visible and count the CTA in
+// (one atomic per CTA), stage the routed step's x operand, consume the first
+// of their A items (the other CTAs finish their router rows meanwhile), then
 //   - wait, bounded, until all CTAs have counted in,
 //   - select the row's experts themselves from all E logits, with the same
 //     keys, order and weights as topk_kernel, into routing tables in shared
 //     memory (k experts, one pair each, ordered by expert id),
-// and CTA 0 also writes those tables to global memory for FC2 and the tail
-// and raises the route flag.  The producer streams R and A without waiting
-// for anything and learns the routing from a shared-memory barrier before B,
-// so the selection runs while HBM streams the shared expert, and the routed
-// step reads no table from global memory.  The counter and the flag are
-// zeroed again by the tail kernel of the same forward.
+// and consume the rest of A; CTA 0 also writes the tables to global memory
+// for FC2 and the tail and raises the route flag.  The producer streams R and
+// A without waiting for anything and learns the routing from a shared-memory
+// barrier before B, so the selection runs while A's stages stream in, and
+// the routed step reads no table from global memory.  The counter and the
+// flag are zeroed again by the tail kernel of the same forward.
 #pragma once
 
 #include "common.cuh"
@@ -55,8 +56,12 @@ struct FrontRoute {
   int expert[32];
   int off[33];
   int pair[32];
+  int xshift;   // the routed step's x operand is x * 2^-xshift in f16
 };
-constexpr int kFrontExtraBytes = (int)((sizeof(FrontRoute) + 127) / 128 * 128);
+constexpr int kFrontRouteBytes = (int)((sizeof(FrontRoute) + 127) / 128 * 128);
+// After the routing tables: the routed step's x operand, f16, 16 bytes per
+// 8 elements (2 K bytes for a row of K).
+__host__ __device__ inline int front_extra_bytes(int K) { return kFrontRouteBytes + 2 * K; }
 
 // 32-expert chunks per consumer warp in the selection (E <= 32 * 4 * KW).
 constexpr int kFrontMaxChunks = 4;
@@ -174,10 +179,47 @@ __device__ __forceinline__ void front_topk(const FrontArgs& f, const float* logi
   }
 }
 
+// The routed step's x operand in shared memory (XS steps of stream.cuh): the
+// row's max |x| picks the power-of-two scale that keeps f16 in range, then
+// entry i holds elements 8i..8i+7 as f16 pairs (entry 4 b + t: block b, lane
+// quad t).  scratch: KW words.
+__device__ __forceinline__ void front_x_operand(const uint16_t* x, int K, uint4* xs, int* xshift,
+                                                unsigned* scratch, int kw, int KW, int lane,
+                                                int ct, int cthreads) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x);
+  uint32_t mx = 0;
+  for (int i = ct; i < K / 8; i += cthreads) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) scratch[kw] = mx;
+  consumer_sync(cthreads);
+  uint32_t amax = 0;
+  for (int w = 0; w < KW; ++w) amax = max(amax, scratch[w]);
+  const int shift = f16_shift_for_amax(bf16_bits_to_f32(amax));
+  const float sc = pow2f(-shift);
+  if (ct == 0) *xshift = shift;
+  for (int i = ct; i < K / 8; i += cthreads) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 o;
+    o.x = pack_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
+    o.y = pack_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
+    o.z = pack_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
+    o.w = pack_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
+    xs[i] = o;
+  }
+}
+
 // Warp 0 lane 0 produces; warps 1..KW consume (KW = blockDim.x / 32 - 1).
 // Dynamic shared memory: the streaming kernels' carve-up (stream_smem_init)
-// followed by kFrontExtraBytes for the routing tables; the cross-slab partial
-// buffers must hold kFrontScratchBytes.
+// followed by front_extra_bytes(K) for the routing tables and the routed
+// step's x operand; the cross-slab partial buffers must hold
+// kFrontScratchBytes.
 template <class RC, class AC, class BC>
 __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     stream_front_kernel(const StreamArgs ar, const StreamArgs a0, const StreamArgs a1,
@@ -192,11 +234,14 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
   pdl_launch_dependents();
   // the routed step reads its tables from this CTA's shared memory
+  uint4* xs = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(rt) + kFrontRouteBytes);
   StreamArgs b = a1;
   b.n_active = &rt->n_active;
   b.active_expert = rt->expert;
   b.active_off = rt->off;
   b.pair_list = rt->pair;
+  b.xs = xs;
+  b.xs_shift = &rt->xshift;
   SegPrior pr;
   cfg_add_prior<RC>(ar, pr);
   cfg_add_prior<AC>(a0, pr);
@@ -222,18 +267,27 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     pdl_wait_prerequisites();   // x may be the previous kernel's output
     int pp = 0, rp = 0;
     cfg_consume<RC>(ar, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
-    // this CTA's logits are visible GPU-wide before it counts in
-    __threadfence();
+    // count this CTA in once its logits are visible GPU-wide (the barrier
+    // orders every consumer's stores before the arriving thread's fence)
     consumer_sync(cthreads);
-    if (ct == 0) {
-      if ((int)blockIdx.x != f.skip_arrive_cta) atomicAdd(f.count, 1u);
-      wait_count(f.count, gridDim.x, a0.status, f.wait_ns);
+    if (ct == 0 && (int)blockIdx.x != f.skip_arrive_cta) {
+      __threadfence();
+      atomicAdd(f.count, 1u);
     }
+    // while the other CTAs finish their router rows: the routed step's x
+    // operand and the first of this CTA's shared gate/up items
+    front_x_operand(b.x, b.K, xs, &rt->xshift, reinterpret_cast<unsigned*>(m.red), kw, KW, lane,
+                    ct, cthreads);
+    consumer_sync(cthreads);
+    cfg_consume<AC>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane,
+                    0, 1);
+    if (ct == 0) wait_count(f.count, gridDim.x, a0.status, f.wait_ns);
     consumer_sync(cthreads);
     front_topk(f, ar.out, m.red, rt, bias, kw, KW, lane, cthreads);
     consumer_sync(cthreads);
     if (ct == 0) mbar_arrive(&rt->bar);
-    cfg_consume<AC>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
+    cfg_consume<AC>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane,
+                    1, 1);
     cfg_consume<BC>(b, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
   }
   trace_end(a0.trace, a0.trace_id);

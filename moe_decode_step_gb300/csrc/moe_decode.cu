@@ -246,8 +246,11 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
 // FC2 at batch class 0 (B = 1: one activation row per routed expert) takes
-// items of four tiles with one-column partials.
-#define MOE_FC2_TM(RS) ((RS) == 1 ? 4 : 2)
+// items of MOE_FC2_TM_B1 tiles with one-column partials.
+#ifndef MOE_FC2_TM_B1
+#define MOE_FC2_TM_B1 4
+#endif
+#define MOE_FC2_TM(RS) ((RS) == 1 ? MOE_FC2_TM_B1 : 2)
 #define MOE_FC2_RM(RS) ((RS) == 1 ? 1 : 8)
 #define MOE_FC2_KERNEL(RS, NBM) \
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
@@ -259,7 +262,7 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 // slabs), shared gate/up and routed gate/up in one launch.
 // The routed step takes one activation row per expert (RMAX = 1).
 using FrontRouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 1, false, 1, 1, 8, 2>;
-using FrontFc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16>;
+using FrontFc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8, 4, true>;
 #define MOE_FRONT_KERNEL stream_front_kernel<FrontRouterCfg, Sh1Cfg<1>, FrontFc1Cfg>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
@@ -285,10 +288,10 @@ template <class C>
 int seg_kc(int K, int KW) {
   if constexpr (C::MMA) {
     const int nblk = K / 32, NB = mx_warp_blocks(K, KW);
-    for (int kc = 1; kc <= 8; kc *= 2) {
-      if (nblk % kc != 0) break;
+    for (int kc = 1; kc <= 16; ++kc) {
+      if (nblk % kc != 0) continue;
       const int CB = nblk / kc;
-      if (kc > 1 && CB % NB != 0) break;
+      if (kc > 1 && CB % NB != 0) continue;
       if (mx_stage_bytes(K, C::TM, kc) <= 32 * 1024) return kc;
     }
     return 1;
@@ -375,7 +378,7 @@ int plan_front(const moe_dims_t& d, int n_sm, StreamPlan* p) {
   r.red_pp = std::max({stream_red_pp(KW, false, 1, RC::RMAX), stream_red_pp(KW, false, 1, AC::RMAX),
                        stream_red_pp(KW, true, BC::TM, BC::RMAX), (kFrontScratchBytes + 7) / 8});
   r.red_pp = (r.red_pp + 3) / 4 * 4;
-  const int fixed = 2 * r.red_pp * 4 + 64 + kFrontExtraBytes;
+  const int fixed = 2 * r.red_pp * 4 + 64 + front_extra_bytes(d.d);
   r.NS = std::min(16, (kBudget1 - fixed) / (r.stage_bytes + 16));
   if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + fixed;

@@ -70,6 +70,11 @@ struct StreamArgs {
   int trace_id;
   uint8_t* xq;               // router only: activation planes of x [B][4K] (planes.cuh), or null
   uint8_t* xq_code;          // and their plane-0 codes, one per row [B]
+  // routed gate/up steps of one activation row whose operand sits in shared
+  // memory (StreamCfg XS): per K block b and lane quad t, the f16 pairs of
+  // elements 8t..8t+7 at xs[4 b + t], scaled by 2^-(*xs_shift)
+  const uint4* xs;
+  const int* xs_shift;
   const unsigned* route_flag;  // routed step of a two-step kernel: non-null when the routing
                                // tables are published under this flag (the producer then
                                // streams the routed weights without waiting for the previous
@@ -601,6 +606,35 @@ __device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* 
   }
 }
 
+// The same with the activation operand read from shared memory, one 16-byte
+// load per block (xs points at this lane's entry of the warp's first block;
+// blocks are 4 entries apart).
+template <bool ONE, int NQ, bool GUARD>
+__device__ __forceinline__ void mx_group_run_xs(const uint8_t* nib, const uint8_t* scl,
+                                                const uint4* xs, int nb, float& c0, float& c1,
+                                                float& c2, float& c3) {
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (GUARD && 4 * q >= nb) break;
+    const uint2 sv = *reinterpret_cast<const uint2*>(scl + q * 64);
+    const uint4 w0 = *reinterpret_cast<const uint4*>(nib + (2 * q) * 512);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(nib + (2 * q + 1) * 512);
+    uint32_t x[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = xs[(4 * q + j) * 4];
+      x[j][0] = v.x;
+      x[j][1] = v.y;
+      x[j][2] = v.z;
+      x[j][3] = v.w;
+    }
+    mx_block_mma<ONE>(w0.x, w0.y, e8m0_byte0(sv.x), e8m0_byte1(sv.x), x[0], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w0.z, w0.w, e8m0_byte2(sv.x), e8m0_byte3(sv.x), x[1], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w1.x, w1.y, e8m0_byte0(sv.y), e8m0_byte1(sv.y), x[2], c0, c1, c2, c3);
+    mx_block_mma<ONE>(w1.z, w1.w, e8m0_byte2(sv.y), e8m0_byte3(sv.y), x[3], c0, c1, c2, c3);
+  }
+}
+
 // Consumers of an MXFP4 step (tensor cores): one pass of R <= RMAX activation
 // rows, the mma columns, over the run [it0, run_end) of items of one expert.
 //
@@ -614,11 +648,11 @@ __device__ __forceinline__ void mx_group_run(const uint8_t* nib, const uint8_t* 
 // X holds the pass's activation operand; xkey/xshift remember which single x
 // row it holds (-1: none), so a run of another expert on the same row (every
 // run at B = 1) keeps it instead of reloading and re-reducing it.
-template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE>
+template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE, bool XS>
 __device__ __forceinline__ void stream_consume_run_mma(
     const StreamArgs& a, const StreamItem& m, int done, int R, int it0, int run_end, int tiles,
     uint8_t* stages, uint64_t* full, uint64_t* empty, float* red, uint32_t& stage, int& pp,
-    int& rp, int kw, int KW, int lane, uint32_t (&X)[NBMAX][4], int& xkey, int& xshift) {
+    int& rp, int kw, int KW, int lane, uint32_t (&X)[XS ? 1 : NBMAX][4], int& xkey, int& xshift) {
   constexpr int TR = GLU ? TM * 8 : TM * 16;   // output rows (pairs) per item
   const int g = lane >> 2, t = lane & 3;
   const int nblk = a.K >> 5;
@@ -642,7 +676,9 @@ __device__ __forceinline__ void stream_consume_run_mma(
   int eshift;
   // one x row for the whole pass (R = 1): the same key in every lane and warp
   const int key = (!ACTH && R == 1) ? cpid / a.k : -1;
-  if (!ACTH && key >= 0 && key == xkey) {
+  if constexpr (XS) {
+    eshift = *a.xs_shift;   // the operand is in shared memory already
+  } else if (!ACTH && key >= 0 && key == xkey) {
     eshift = xshift;
   } else if constexpr (!ACTH) {
     // x rows (bf16): the f16 scaling shift needs max |x| over the whole row,
@@ -718,10 +754,15 @@ __device__ __forceinline__ void stream_consume_run_mma(
       const uint8_t* nib = sp + mb * nib_tile + (size_t)(lb0 >> 1) * 512 + lane * 16;
       const uint8_t* scl = sp + scl_base + (size_t)mb * CB * 16 + (size_t)(lb0 >> 2) * 64 + g * 8;
       float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-      if (nb == NBMAX)   // the common case: one straight run the compiler can schedule
+      if constexpr (XS) {
+        const uint4* xs = a.xs + (size_t)b0 * 4 + t;
+        if (nb == NBMAX) mx_group_run_xs<ONE, NBMAX / 4, false>(nib, scl, xs, nb, c0, c1, c2, c3);
+        else mx_group_run_xs<ONE, NBMAX / 4, true>(nib, scl, xs, nb, c0, c1, c2, c3);
+      } else if (nb == NBMAX) {   // the common case: one straight run the compiler can schedule
         mx_group_run<ONE, NBMAX / 4, false>(nib, scl, X, nb, c0, c1, c2, c3);
-      else
+      } else {
         mx_group_run<ONE, NBMAX / 4, true>(nib, scl, X, nb, c0, c1, c2, c3);
+      }
       acc[mb][0] = c0;
       acc[mb][1] = c1;
       acc[mb][2] = c2;
@@ -785,12 +826,12 @@ __device__ __forceinline__ void stream_consume_run_mma(
 
 // Consumers: items [lo, hi) of one step, run by run, pass by pass.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX, bool MMA, int TM,
-          int NBMAX, int CW, int NQ>
+          int NBMAX, int CW, int NQ, bool XS = false>
 __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
                                                      int& pp, int& rp, int kw, int KW, int lane) {
-  uint32_t X[MMA ? NBMAX : 1][4];
+  uint32_t X[MMA && !XS ? NBMAX : 1][4];
   int xkey = -1, xshift = 0;
   for (int it0 = lo; it0 < hi;) {
     const int run_end = stream_run_end<ROUTED>(it0, hi, tiles);
@@ -799,11 +840,11 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
       const int R = stream_pass_rows<RMAX, MMA>(m.pr - done);
       if constexpr (MMA) {
         if (RMAX == 1 || R == 1)
-          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true>(
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true, XS>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
               lane, X, xkey, xshift);
         else if constexpr (RMAX > 1)
-          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, false>(
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, false, XS>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
               lane, X, xkey, xshift);
       } else {
@@ -833,16 +874,19 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
 // use tiles of TM x 16 mma rows (RW = 16 TM rows, or 8 TM pairs for gate/up)
 // and at most NBMAX K blocks per consumer warp.
 template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_,
-          bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1, int CW_ = 8, int NQ_ = 4>
+          bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1, int CW_ = 8, int NQ_ = 4,
+          bool XS_ = false>
 struct StreamCfg {
   static constexpr int WF = WF_;
   static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_, MMA = MMA_;
+  static constexpr bool XS = XS_;   // MMA steps of one x row: the operand in shared memory
   static constexpr int SP = SP_, RW = RW_, RMAX = RMAX_, TM = TM_, NBMAX = NBMAX_;
   static constexpr int CW = CW_, NQ = NQ_;   // bf16 steps: lane chunking (see StreamShape)
   static_assert(RW % SP == 0, "an item is a whole number of stages");
   static_assert(!MMA || (WF == kWfMx && ROUTED && RW == (GLU ? 8 : 16) * TM && RMAX <= 8),
                 "tensor-core steps: routed MXFP4, one tile per item, at most 8 columns");
   static_assert(MMA || WF == kWfBf16, "MXFP4 steps run on the tensor cores");
+  static_assert(!XS || (MMA && !ACTH && RMAX == 1), "a shared-memory operand holds one x row");
 };
 
 // Weight bytes one item of a step streams: MXFP4 tiles of 16 rows (K/2
@@ -878,16 +922,21 @@ __device__ __forceinline__ void cfg_produce(const StreamArgs& a, const SegPrior&
       a, lo, hi, tiles, stages, full, empty, stage);
 }
 
+// Consumers of this CTA's items of step C; `part` (0 or 1) with `first`
+// items in part 0 consumes only part 0 ([lo, lo + first)) or part 1 (the
+// rest), so other work can run between the two (part < 0: all of them).
 template <class C>
 __device__ __forceinline__ void cfg_consume(const StreamArgs& a, const SegPrior& prior,
                                             uint8_t* stages, uint64_t* full, uint64_t* empty,
                                             float* red, uint32_t& stage, int& pp, int& rp, int kw,
-                                            int KW, int lane) {
+                                            int KW, int lane, int part = -1, int first = 0) {
   int tiles, lo, hi;
   const int n = stream_n_items<C::ROUTED, C::RW>(a, tiles);
   seg_range(prior, n, cfg_item_bytes<C>(a), lo, hi);
+  if (part == 0) hi = min(hi, lo + first);
+  else if (part == 1) lo = min(hi, lo + first);
   stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM,
-                       C::NBMAX, C::CW, C::NQ>(a, lo, hi, tiles, stages, full, empty, red, stage,
+                       C::NBMAX, C::CW, C::NQ, C::XS>(a, lo, hi, tiles, stages, full, empty, red, stage,
                                                pp, rp, kw, KW, lane);
 }
 
