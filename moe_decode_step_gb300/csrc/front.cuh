@@ -20,8 +20,12 @@
 // for FC2 and the tail and raises the route flag.  The producer streams R and
 // A without waiting for anything and learns the routing from a shared-memory
 // barrier before B, so the selection runs while A's stages stream in, and
-// the routed step reads no table from global memory.  The counter and the
-// flag are zeroed again by the tail kernel of the same forward.
+// the routed step reads no table from global memory.  Until B the producer
+// keeps only a few stages in flight (the host sets R's and A's lag): every
+// step of the chain above is a dependent round trip to L2, and a memory
+// queue of whole stage rings from every SM would make each one wait
+// microseconds behind the stream.  The counter and the flag are zeroed again
+// by the tail kernel of the same forward.
 #pragma once
 
 #include "common.cuh"
@@ -86,13 +90,36 @@ __device__ __forceinline__ void wait_count(const unsigned* c, unsigned target, i
   }
 }
 
+#ifndef MOE_FRONT_COMPACT
+#define MOE_FRONT_COMPACT 0
+#endif
+
+// The bitonic sort of 32 keys as two loops (a few hundred bytes of code
+// instead of the unrolled network's several KB).
+__device__ __forceinline__ uint64_t warp_sort_desc_loop(uint64_t key, int lane) {
+#pragma unroll 1
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool lower = (lane & stride) == 0;
+      const bool take = (lower == desc) ? (ok > key) : (ok < key);
+      if (take) key = ok;
+    }
+  }
+  return key;
+}
+
 // Selection of one row by the KW consumer warps.  Warp w sorts the 32-expert
 // chunks w, w + KW, ... and merges them into one sorted list of its 32 best
 // keys; the KW lists then meet in a tournament through shared memory, a round
 // per consumer barrier.  Warp 0 turns the winning k keys into the tables.
+// publish = false: tables in shared memory only (CTA 0 writes no global
+// tables and raises no flag).
 __device__ __forceinline__ void front_topk(const FrontArgs& f, const float* logits, float* scratch,
                                            FrontRoute* rt, const float (&bias)[kFrontMaxChunks],
-                                           int kw, int KW, int lane, int cthreads) {
+                                           int kw, int KW, int lane, int cthreads, bool publish) {
   uint64_t* lists = reinterpret_cast<uint64_t*>(scratch);   // [2][16][32]
   float* s_sc = scratch + 2 * 16 * 32 * 2;                   // [E]
   const int nch = (f.E + 31) >> 5;
@@ -103,18 +130,28 @@ __device__ __forceinline__ void front_topk(const FrontArgs& f, const float* logi
     l[i] = t < f.E ? __ldcg(logits + t) : 0.f;
   }
   uint64_t best = 0ull;
+#if MOE_FRONT_COMPACT
+#pragma unroll 1
+#else
 #pragma unroll
+#endif
   for (int i = 0; i < kFrontMaxChunks; ++i) {
     const int ch = kw + i * KW;
     if (ch < nch) {   // warp-uniform
       const int t = ch * 32 + lane;
       uint64_t key = 0ull;
       if (t < f.E) {
-        const float s = topk_score(l[i]);
+        const float li = i == 0 ? l[0] : i == 1 ? l[1] : i == 2 ? l[2] : l[3];
+        const float bi = i == 0 ? bias[0] : i == 1 ? bias[1] : i == 2 ? bias[2] : bias[3];
+        const float s = topk_score(li);
         s_sc[t] = s;
-        key = topk_key(s, bias[i], t);
+        key = topk_key(s, bi, t);
       }
+#if MOE_FRONT_COMPACT
+      key = warp_sort_desc_loop(key, lane);
+#else
       key = warp_bitonic_sort_desc(key, lane);
+#endif
       if (i == 0) {
         best = key;
       } else {
@@ -161,7 +198,7 @@ __device__ __forceinline__ void front_topk(const FrontArgs& f, const float* logi
     rt->n_active = k;
     rt->off[k] = k;
   }
-  if (blockIdx.x == 0) {
+  if (publish && blockIdx.x == 0) {
     if (lane < k) {
       f.topk_idx[lane] = e;
       f.topk_w[lane] = w;
@@ -283,7 +320,7 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
                     0, 1);
     if (ct == 0) wait_count(f.count, gridDim.x, a0.status, f.wait_ns);
     consumer_sync(cthreads);
-    front_topk(f, ar.out, m.red, rt, bias, kw, KW, lane, cthreads);
+    front_topk(f, ar.out, m.red, rt, bias, kw, KW, lane, cthreads, true);
     consumer_sync(cthreads);
     if (ct == 0) mbar_arrive(&rt->bar);
     cfg_consume<AC>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane,

@@ -259,7 +259,12 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_TC1_KERNEL tc_kernel<true>
 #define MOE_TC2_KERNEL tc_kernel<false>
 // One row on the mma.sync path: router (one activation row, 512-element warp
-// slabs), shared gate/up and routed gate/up in one launch.
+// slabs), shared gate/up and routed gate/up in one launch.  Until the
+// routed step the producer keeps at most kFrontLag stages in flight.
+#ifndef MOE_FRONT_LAG
+#define MOE_FRONT_LAG 3
+#endif
+constexpr int kFrontLag = MOE_FRONT_LAG;
 // The routed step takes one activation row per expert (RMAX = 1).
 using FrontRouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 1, false, 1, 1, 8, 2>;
 using FrontFc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8, 4, true>;
@@ -282,8 +287,13 @@ int seg_warps(int K) {
   }
 }
 
+// Largest stage of an MXFP4 segment (bytes).
+#ifndef MOE_MX_STAGE_MAX
+#define MOE_MX_STAGE_MAX (56 * 1024)
+#endif
+
 // K chunks per item of a tensor-core segment: the fewest that keep a stage
-// within 32 KB while every warp's blocks stay inside one chunk.
+// within MOE_MX_STAGE_MAX while every warp's blocks stay inside one chunk.
 template <class C>
 int seg_kc(int K, int KW) {
   if constexpr (C::MMA) {
@@ -292,7 +302,7 @@ int seg_kc(int K, int KW) {
       if (nblk % kc != 0) continue;
       const int CB = nblk / kc;
       if (kc > 1 && CB % NB != 0) continue;
-      if (mx_stage_bytes(K, C::TM, kc) <= 32 * 1024) return kc;
+      if (mx_stage_bytes(K, C::TM, kc) <= MOE_MX_STAGE_MAX) return kc;
     }
     return 1;
   } else {
@@ -682,6 +692,8 @@ int launch_front(moe_layer* L, cudaStream_t st, const void* x) {
     a->kc = p.kc;
     a->trace_id = 2;
   }
+  // router and shared rows: a short memory queue while the routing is made
+  r.lag = sa.lag = kFrontLag;
   FrontArgs f{};
   f.bias = L->w.router_bias;
   f.E = d.n_experts;

@@ -75,6 +75,9 @@ struct StreamArgs {
   // elements 8t..8t+7 at xs[4 b + t], scaled by 2^-(*xs_shift)
   const uint4* xs;
   const int* xs_shift;
+  // at most `lag` stages of this step in flight (issued, not landed; 0: the
+  // whole ring): a shorter memory queue for dependent loads issued meanwhile
+  int lag;
   const unsigned* route_flag;  // routed step of a two-step kernel: non-null when the routing
                                // tables are published under this flag (the producer then
                                // streams the routed weights without waiting for the previous
@@ -360,6 +363,12 @@ __device__ __forceinline__ void stream_produce_range(const StreamArgs& a, int lo
           const int buf = (int)(stage % (uint32_t)a.NS);
           const uint32_t use = stage / (uint32_t)a.NS;
           if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, a.status);
+          if (a.lag > 0 && stage >= (uint32_t)a.lag) {
+            // stage - lag has landed (the producer waits on every stage's
+            // "full" in order, so its parity is never ambiguous)
+            const uint32_t s0 = stage - (uint32_t)a.lag;
+            mbar_wait(&full[s0 % (uint32_t)a.NS], (s0 / (uint32_t)a.NS) & 1u, a.status);
+          }
           uint8_t* dst = stages + (size_t)buf * a.stage_bytes;
           if constexpr (MMA) {
             // tiles T0.. of the item, K chunk st: per tile its nibbles and scales
