@@ -130,20 +130,13 @@ def fc1_bytes(cfg, n_distinct, B):
             + 4 * B * cfg.top_k * cfg.f)
 
 
-def front_bytes(cfg, n_distinct, B):
-    """Algorithmic bytes of the one-row front launch (router + top-k + FC1):
-    FC1's bytes plus the router weights and bias."""
-    return fc1_bytes(cfg, n_distinct, B) + cfg.n_experts * cfg.d * 2 + 4 * cfg.n_experts
-
-
-KERNEL_SOURCES = ("common.cuh", "stream.cuh", "topk.cuh", "front.cuh", "moe_decode.cu")
+KERNEL_SOURCES = ("common.cuh", "stream.cuh", "moe_decode.cu")
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 
 
 def kernel_source_sha256():
     """sha256 over the dominant B = 1 kernel's sources (helpers, the streaming
-    kernel, the selection, the front kernel and its launch plan), concatenated
-    in that order."""
+    kernel and its launch plan), concatenated in that order."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "moe_decode_step_gb300", "csrc", f), "rb") as fh:
@@ -481,9 +474,8 @@ def run_ours(args, rank, world, local):
 
     us = reduce_max(statistics.median(times), world, dev)
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
-    fused_front = layer.launches_per_forward(cfg.B) == 3
     fc1_us = statistics.median(p[1] for p in phases)
-    fc1_b = (front_bytes if fused_front else fc1_bytes)(cfg, n_distinct, cfg.B)
+    fc1_b = fc1_bytes(cfg, n_distinct, cfg.B)
     rec = traffic_from_profile()
     traffic = None
     if rec is not None:
@@ -583,9 +575,7 @@ def run_ours(args, rank, world, local):
                 "frac_of_nominal_8tbs": btouch / us / 1e6 / 8.0, "aggregate_tbs": agg_tbs,
                 "peak_gbs": peak, "peak_kind": peak_kind},
         "expert_path": "mma.sync with register dequantisation (B = 1)",
-        "roofline": {"kernel": ("stream_front_kernel (router + top-k + shared gate/up + routed "
-                                "gate/up)") if fused_front else
-                               "stream_dual_kernel (FC1: shared + routed gate/up)",
+        "roofline": {"kernel": "stream_dual_kernel (FC1: shared + routed gate/up)",
                      "bound": "hbm",
                      "achieved": fc1_b / fc1_us / 1e3, "peak": peak, "unit": "GB/s",
                      "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,

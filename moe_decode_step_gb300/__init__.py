@@ -163,7 +163,7 @@ class MoELayer:
 
     def debug_set_fault(self, fault, wait_ns=0):
         """Failure-detection test hook (see moe_debug_set_fault): fault 1 makes
-        the one-row front kernel's arrival wait expire after wait_ns."""
+        FC2's wait for the one-row route flag expire after wait_ns."""
         check(lib().moe_debug_set_fault(self._h, int(fault), int(wait_ns)),
               "moe_debug_set_fault")
 
@@ -181,8 +181,7 @@ class MoELayer:
 
     def get_trace(self):
         """{kernel: (start_us, end_us)} of the last traced forward, relative to
-        the earliest kernel start; kernels that did not run are left out (the
-        one-row front kernel reports as "fc1", with no router or top-k)."""
+        the earliest kernel start; kernels that did not run are left out."""
         arr = (ctypes.c_ulonglong * 10)()
         check(lib().moe_get_trace(self._h, arr, 10), "moe_get_trace")
         names = ["router", "topk", "fc1", "fc2", "tail"]

@@ -1,20 +1,16 @@
 // C ABI of the MoE decode layer (see include/moe_decode.h for the contract).
 //
-// One forward is a chain of kernels on the caller's stream, linked with
-// programmatic dependent launch.  For one row on the mma.sync expert path,
-// three launches:
-//   front: router GEMV, top-k in every CTA, shared gate/up (bf16), routed
-//          gate/up (MXFP4), SwiGLU (front.cuh)
-//   -> FC2: shared down (bf16) then routed down (MXFP4); its producer reads
-//      the routing under the front's flag and streams before the front ends
+// One forward = five kernels on the caller's stream, chained with programmatic
+// dependent launch:
+//   router GEMV (streamed bf16) -> top-k + routing tables
+//   -> FC1: shared gate/up (bf16) then routed gate/up (MXFP4), SwiGLU
+//   -> FC2: shared down (bf16) then routed down (MXFP4)
 //   -> tail (combine + residual + RMSNorm)
-// Otherwise five:
-//   router GEMV -> top-k + routing tables
-//   -> FC1: shared gate/up then routed gate/up
-//   -> FC2: shared down then routed down
-//   -> tail
 // The shared expert streams first inside FC1/FC2: its weights do not depend on
-// the routing, so FC1 starts them while top-k is still finishing.
+// the routing, so FC1 starts them while top-k is still finishing (on the one
+// SM FC1 leaves it at one row).  At one row on the mma.sync path top-k also
+// raises a route flag, and FC2's producer streams its routed weights as soon
+// as the flag is up instead of waiting for FC1 to finish.
 // Optional second stream (chained layers only): L2 prefetch of the next
 // layer's router and shared-expert weights.
 // No allocation, no host synchronisation: capturable into a CUDA graph.
@@ -28,7 +24,6 @@
 
 #include "moe_decode.h"
 #include "common.cuh"
-#include "front.cuh"
 #include "mxfp4.cuh"
 #include "stream.cuh"
 #include "tail.cuh"
@@ -100,9 +95,8 @@ struct Workspace {
   // while the router's last CTAs finish)
   float* rpartial;
   unsigned* rflags;
-  // the one-row front kernel: CTAs past the router step, and the flag under
-  // which its CTA 0 publishes the routing tables (both zeroed by the tail)
-  unsigned* front_count;
+  // one row on the mma.sync path: raised by top-k once the routing tables
+  // are written (zeroed by the tail)
   unsigned* route_flag;
 };
 
@@ -115,7 +109,7 @@ struct StreamPlan {
   int dense_ctas = 0;   // CTAs of the dense pass (0: the whole grid)
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kStepFront, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kNumSteps };
 
 // Expert paths: mma.sync on the tiled layouts (the GEMV regime: weights
 // converted to f16 in registers), or tcgen05 on the UMMA layouts (block-scaled
@@ -155,6 +149,7 @@ struct moe_layer {
   ExpertWeights wm;   // mma.sync path (tiled layouts), when kept
   ExpertWeights wt;   // tcgen05 path (UMMA layouts), when kept
   int tc_min_batch = kTcMinBatch;
+  // failure-detection test hook (moe_debug_set_fault)
   // tcgen05 path: the shared expert's bf16 weights in the dense pass's tiles
   uint8_t* sh_gu_umma = nullptr;
   uint8_t* sh_d_umma = nullptr;
@@ -208,7 +203,6 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.dflags = carve<unsigned>(p, kTcMaxCtas);
   w.rpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
   w.rflags = carve<unsigned>(p, kTcMaxCtas);
-  w.front_count = carve<unsigned>(p, 1);
   w.route_flag = carve<unsigned>(p, 1);
   if (ws) *ws = w;
   return (size_t)(p - base);
@@ -244,7 +238,11 @@ using Sh2Cfg = StreamCfg<kWfBf16, false, true, false, 8, 16, R, false, 1, 1, 4, 
 template <int NBM, int TM, int RM>
 using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, TM, NBM>;
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
+// One activation row (batch class 0): the routed step takes one row per
+// expert with its x operand in shared memory.
+using Fc1OneRowCfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8, 4, true>;
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
+#define MOE_FC1_KERNEL_ONE_ROW stream_dual_kernel<Sh1Cfg<1>, Fc1OneRowCfg, false>
 // FC2 at batch class 0 (B = 1: one activation row per routed expert) takes
 // items of MOE_FC2_TM_B1 tiles with one-column partials.
 #ifndef MOE_FC2_TM_B1
@@ -258,17 +256,6 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 // FC2 the shared down first (its weights requested before FC1 is waited for).
 #define MOE_TC1_KERNEL tc_kernel<true>
 #define MOE_TC2_KERNEL tc_kernel<false>
-// One row on the mma.sync path: router (one activation row, 512-element warp
-// slabs), shared gate/up and routed gate/up in one launch.  Until the
-// routed step the producer keeps at most kFrontLag stages in flight.
-#ifndef MOE_FRONT_LAG
-#define MOE_FRONT_LAG 3
-#endif
-constexpr int kFrontLag = MOE_FRONT_LAG;
-// The routed step takes one activation row per expert (RMAX = 1).
-using FrontRouterCfg = StreamCfg<kWfBf16, false, false, false, 1, 1, 1, false, 1, 1, 8, 2>;
-using FrontFc1Cfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8, 4, true>;
-#define MOE_FRONT_KERNEL stream_front_kernel<FrontRouterCfg, Sh1Cfg<1>, FrontFc1Cfg>
 
 int batch_class(int B) { return B == 1 ? 0 : (B <= 8 ? 1 : 2); }
 
@@ -342,7 +329,9 @@ int plan_kernel(Kern kern, int KA, int NA, int KB, int NB, int n_sm, int budget,
   r.stage_bytes = (int)((std::max(sa, sb) + 127) / 128 * 128);
   r.red_pp = std::max(stream_red_pp(KW, A::MMA, A::TM, A::RMAX),
                       stream_red_pp(KW, B::MMA, B::TM, B::RMAX));
-  const int red_bytes = 2 * r.red_pp * 4 + 64;
+  // an XS routed segment keeps its x operand after the partial buffers
+  const int red_bytes = 2 * r.red_pp * 4 + 64 + (B::XS ? xs_extra_bytes(KB) : 0) +
+                        (B::ROUTED && B::RMAX == 1 ? kOneRowTablesBytes : 0);
   r.NS = std::min(16, (budget - red_bytes) / (r.stage_bytes + 16));
   if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
   r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
@@ -365,41 +354,6 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
         MOE_FC2_KERNEL(RS, 4), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
   return plan_kernel<Sh2Cfg<RS>, Fc2Cfg<12, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>>(
       MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
-}
-
-// Launch shape of the one-row front kernel (front.cuh): three steps through
-// one ring, the selection's scratch in the cross-slab partial buffers and
-// the routing tables after them.  Every CTA must be resident at once (the
-// CTAs wait for each other's logits): one per SM, grid = SM count.
-int plan_front(const moe_dims_t& d, int n_sm, StreamPlan* p) {
-  using RC = FrontRouterCfg;
-  using AC = Sh1Cfg<1>;
-  using BC = FrontFc1Cfg;
-  const int KW = std::max({seg_warps<RC>(d.d), seg_warps<AC>(d.d), seg_warps<BC>(d.d)});
-  if (KW > kMmaWarps) return MOE_ERR_UNSUPPORTED;
-  if (!seg_fits<BC>(d.d, d.f, KW)) return MOE_ERR_UNSUPPORTED;
-  if (d.n_experts > 32 * kFrontMaxChunks * KW || d.top_k > 32) return MOE_ERR_UNSUPPORTED;
-  StreamPlan r;
-  r.threads = 32 * (KW + 1);
-  r.kc = seg_kc<BC>(d.d, KW);
-  const size_t sb = std::max({seg_stage_bytes<RC>(d.d, 1), seg_stage_bytes<AC>(d.d, 1),
-                              seg_stage_bytes<BC>(d.d, r.kc)});
-  r.stage_bytes = (int)((sb + 127) / 128 * 128);
-  r.red_pp = std::max({stream_red_pp(KW, false, 1, RC::RMAX), stream_red_pp(KW, false, 1, AC::RMAX),
-                       stream_red_pp(KW, true, BC::TM, BC::RMAX), (kFrontScratchBytes + 7) / 8});
-  r.red_pp = (r.red_pp + 3) / 4 * 4;
-  const int fixed = 2 * r.red_pp * 4 + 64 + front_extra_bytes(d.d);
-  r.NS = std::min(16, (kBudget1 - fixed) / (r.stage_bytes + 16));
-  if (r.NS < 2 || r.NS < 2 * r.kc) return MOE_ERR_UNSUPPORTED;
-  r.smem = r.NS * r.stage_bytes + r.NS * 16 + fixed;
-  MOE_CUDA(cudaFuncSetAttribute(MOE_FRONT_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                r.smem));
-  int occ = 0;
-  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, MOE_FRONT_KERNEL, r.threads, r.smem));
-  if (occ < 1) return MOE_ERR_UNSUPPORTED;
-  r.grid = n_sm;
-  *p = r;
-  return MOE_OK;
 }
 
 // Launch shape of a tensor-core kernel: six warps, a stage ring sized for the
@@ -489,14 +443,13 @@ int plan_all(moe_layer* L) {
     }
   }
   if (!L->wm.ok) return MOE_OK;
-  MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1Cfg>(MOE_FC1_KERNEL(1), d.d, d.f_shared, d.d, d.f, n,
-                                           kBudget1, &L->plan[kStepFc1][0])));
+  MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1OneRowCfg>(MOE_FC1_KERNEL_ONE_ROW, d.d, d.f_shared, d.d,
+                                                 d.f, n, kBudget1, &L->plan[kStepFc1][0])));
   MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg>(MOE_FC1_KERNEL(2), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][1])));
   MOE_PLAN((plan_kernel<Sh1Cfg<4>, Fc1Cfg>(MOE_FC1_KERNEL(4), d.d, d.f_shared, d.d, d.f, n,
                                            kBudget1, &L->plan[kStepFc1][2])));
   MOE_PLAN((plan_fc2<1>(L, d, n, &L->plan[kStepFc2][0])));
-  MOE_PLAN((plan_front(d, n, &L->plan[kStepFront][0])));
   MOE_PLAN((plan_fc2<2>(L, d, n, &L->plan[kStepFc2][1])));
   MOE_PLAN((plan_fc2<4>(L, d, n, &L->plan[kStepFc2][2])));
 #undef MOE_PLAN
@@ -561,8 +514,6 @@ int launch_step(moe_layer* L, K kern, const StreamPlan& p, StreamArgs a, int n_i
 // The tensor-core path for a forward of B rows?
 bool use_tc(const moe_layer* L, int B) { return L->wt.ok && (!L->wm.ok || B >= L->tc_min_batch); }
 
-// The one-row front kernel (router + top-k + FC1 in one launch)?
-bool use_front(const moe_layer* L, int B) { return B == 1 && !use_tc(L, B); }
 
 int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B);
 
@@ -607,6 +558,9 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   t.pair_list = L->ws.pair_list;
   t.h_amax = L->ws.h_amax;
   t.trace = L->tracing ? L->ws.trace : nullptr;
+  // one row on the mma.sync path: FC2 streams its routed weights under this flag
+  t.route_flag = (B == 1 && !use_tc(L, B) && idx == L->ws.topk_idx) ? L->ws.route_flag : nullptr;
+  t.skip_flag = L->debug_fault == 1;
   MOE_CUDA(launch_ex(topk_kernel, dim3(B), dim3(kTopkThreads), 0, st, true, t));
   return MOE_OK;
 }
@@ -648,70 +602,10 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   const StreamPlan& p = L->plan[kStepFc1][batch_class(B)];
   const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
   switch (batch_class(B)) {
-    case 0: return launch_dual(MOE_FC1_KERNEL(1), p, sa, ra, st, grid);
+    case 0: return launch_dual(MOE_FC1_KERNEL_ONE_ROW, p, sa, ra, st, grid);
     case 1: return launch_dual(MOE_FC1_KERNEL(2), p, sa, ra, st, grid);
     default: return launch_dual(MOE_FC1_KERNEL(4), p, sa, ra, st, grid);
   }
-}
-
-// The one-row front (front.cuh): router rows, top-k in every CTA, shared
-// gate/up, routed gate/up.  Launched as a programmatic dependent: its
-// producer streams the router weights while the previous kernel finishes,
-// its consumers wait for that kernel before reading x.
-int launch_front(moe_layer* L, cudaStream_t st, const void* x) {
-  const moe_dims_t& d = L->dims;
-  const StreamPlan& p = L->plan[kStepFront][0];
-  StreamArgs r = base_args(L);
-  r.q = static_cast<const uint8_t*>(L->w.router_w);
-  r.K = d.d;
-  r.N = d.n_experts;
-  r.B = 1;
-  r.x = static_cast<const uint16_t*>(x);
-  r.out = L->ws.logits;
-  StreamArgs sa = base_args(L);
-  sa.q = static_cast<const uint8_t*>(L->w.shared_gu);
-  sa.K = d.d;
-  sa.N = d.f_shared;
-  sa.B = 1;
-  sa.x = static_cast<const uint16_t*>(x);
-  sa.out = L->ws.hs;
-  StreamArgs ra = base_args(L);
-  ra.q = L->wm.gu_q;
-  ra.s = L->wm.gu_s;
-  ra.q_stride = L->q_gu_stride;
-  ra.s_stride = L->s_gu_stride;
-  ra.K = d.d;
-  ra.N = d.f;
-  ra.x = static_cast<const uint16_t*>(x);
-  ra.out = L->ws.h;
-  ra.out_amax = L->ws.h_amax;
-  for (StreamArgs* a : {&r, &sa, &ra}) {
-    a->NS = p.NS;
-    a->stage_bytes = p.stage_bytes;
-    a->red_pp = p.red_pp;
-    a->kc = p.kc;
-    a->trace_id = 2;
-  }
-  // router and shared rows: a short memory queue while the routing is made
-  r.lag = sa.lag = kFrontLag;
-  FrontArgs f{};
-  f.bias = L->w.router_bias;
-  f.E = d.n_experts;
-  f.k = d.top_k;
-  f.routed_scale = d.routed_scale;
-  f.count = L->ws.front_count;
-  f.route_flag = L->ws.route_flag;
-  f.topk_idx = L->ws.topk_idx;
-  f.topk_w = L->ws.topk_w;
-  f.n_active = L->ws.n_active;
-  f.active_expert = L->ws.active_expert;
-  f.active_off = L->ws.active_off;
-  f.pair_list = L->ws.pair_list;
-  f.skip_arrive_cta = L->debug_fault == 1 ? p.grid - 1 : -1;
-  f.wait_ns = L->debug_wait_ns ? L->debug_wait_ns : kWaitLimitNs;
-  MOE_CUDA(launch_ex(MOE_FRONT_KERNEL, dim3(p.grid), dim3(p.threads), (size_t)p.smem, st, true, r,
-                     sa, ra, f));
-  return MOE_OK;
 }
 
 // Tensor-core path: the routed step's arguments common to FC1 and FC2.
@@ -872,10 +766,10 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   return launch_tc(MOE_TC2_KERNEL, p, b, dn, unused, st, p.grid);
 }
 
-// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).  After the
-// one-row front (`front`), its producer takes the routing from the front's
-// flag instead of waiting for the front to finish.
-int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool front) {
+// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).  With `flag`
+// (one row, where top-k raises the route flag) its producer takes the routing
+// tables under the flag instead of waiting for FC1 to finish.
+int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool flag) {
   const moe_dims_t& d = L->dims;
   StreamArgs sa = base_args(L);
   sa.q = static_cast<const uint8_t*>(L->w.shared_d);
@@ -894,7 +788,8 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool front) {
   ra.h = L->ws.h;
   ra.h_amax = L->ws.h_amax;
   ra.out = L->ws.y_pair;
-  ra.route_flag = front ? L->ws.route_flag : nullptr;
+  ra.route_flag = flag ? L->ws.route_flag : nullptr;
+  ra.wait_ns = L->debug_fault == 1 ? L->debug_wait_ns : 0;
   sa.trace_id = ra.trace_id = 3;
   const StreamPlan& p = L->plan[kStepFc2][batch_class(B)];
   if (fc2_small(d)) {
@@ -928,7 +823,6 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.k = L->dims.top_k;
   a.eps = L->dims.rms_eps;
   a.trace = L->tracing ? L->ws.trace : nullptr;
-  a.front_count = L->ws.front_count;
   a.route_flag = L->ws.route_flag;
   a.h_amax = L->ws.h_amax;
   MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
@@ -975,20 +869,13 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   MOE_CUDA(cudaEventRecord(L->ev_fork, st));
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   const bool tc = use_tc(L, B);
-  const bool front = use_front(L, B);
-  if (front) {
-    // router and top-k run inside the front kernel: their phase is empty
-    if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-    if ((rc = launch_prefetch(L))) return rc;
-    if ((rc = launch_front(L, st, x))) return rc;
-  } else {
-    if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
-    if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-    if ((rc = launch_prefetch(L))) return rc;
-    if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
-  }
+  if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
+  if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
+  if ((rc = launch_prefetch(L))) return rc;
+  if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B, front))) return rc;
+  // one row on the mma.sync path: FC2 takes the routing from the route flag
+  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B, B == 1))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
@@ -1328,9 +1215,7 @@ int moe_get_trace(moe_layer_t L, unsigned long long* ns, int n) {
 
 int moe_launches_per_forward(moe_layer_t L, int B) {
   if (!L || B < 1 || B > L->dims.max_batch) return -1;
-  // one row on the mma.sync path: front (router + top-k + FC1), FC2, tail;
-  // otherwise router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
-  return use_front(L, B) ? 3 : 5;
+  return 5;   // router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {

@@ -75,9 +75,9 @@ struct StreamArgs {
   // elements 8t..8t+7 at xs[4 b + t], scaled by 2^-(*xs_shift)
   const uint4* xs;
   const int* xs_shift;
-  // at most `lag` stages of this step in flight (issued, not landed; 0: the
-  // whole ring): a shorter memory queue for dependent loads issued meanwhile
-  int lag;
+  // the producer's bounded wait for route_flag ends after wait_ns (0: the
+  // default limit)
+  unsigned long long wait_ns;
   const unsigned* route_flag;  // routed step of a two-step kernel: non-null when the routing
                                // tables are published under this flag (the producer then
                                // streams the routed weights without waiting for the previous
@@ -363,12 +363,6 @@ __device__ __forceinline__ void stream_produce_range(const StreamArgs& a, int lo
           const int buf = (int)(stage % (uint32_t)a.NS);
           const uint32_t use = stage / (uint32_t)a.NS;
           if (use > 0) mbar_wait(&empty[buf], (use - 1) & 1u, a.status);
-          if (a.lag > 0 && stage >= (uint32_t)a.lag) {
-            // stage - lag has landed (the producer waits on every stage's
-            // "full" in order, so its parity is never ambiguous)
-            const uint32_t s0 = stage - (uint32_t)a.lag;
-            mbar_wait(&full[s0 % (uint32_t)a.NS], (s0 / (uint32_t)a.NS) & 1u, a.status);
-          }
           uint8_t* dst = stages + (size_t)buf * a.stage_bytes;
           if constexpr (MMA) {
             // tiles T0.. of the item, K chunk st: per tile its nibbles and scales
@@ -727,8 +721,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
     xshift = eshift;
   } else {
     // h rows (fp32): the shift comes from FC1's per-pair max |h|
-    const int cshift = f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + cpid)));
-    eshift = f16_shift_for_amax(__uint_as_float(__ldcg(a.h_amax + epid)));
+    const int cshift = f16_shift_for_amax(__int_as_float(ld_tab(reinterpret_cast<const int*>(a.h_amax) + cpid)));
+    eshift = f16_shift_for_amax(__int_as_float(ld_tab(reinterpret_cast<const int*>(a.h_amax) + epid)));
     const float sc = pow2f(-cshift);
     const float* hr = a.h + (size_t)cpid * a.K + 8 * t;
 #pragma unroll
@@ -950,11 +944,12 @@ __device__ __forceinline__ void cfg_consume(const StreamArgs& a, const SegPrior&
 }
 
 // Bounded wait for a flag another kernel (or CTA) raises with a release store.
-__device__ __forceinline__ void wait_flag(const unsigned* flag, int* status) {
+__device__ __forceinline__ void wait_flag(const unsigned* flag, int* status,
+                                          unsigned long long limit_ns) {
   if (ld_acquire_u32(flag) != 0u) return;
   const unsigned long long t0 = global_ns();
   while (ld_acquire_u32(flag) == 0u) {
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       if (status) atomicExch(status, kStatusTimeout);
       return;
     }
@@ -1052,6 +1047,73 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   trace_end(a.trace, a.trace_id);
 }
 
+// The x operand of an XS step (one activation row) in shared memory, by the
+// KW consumer warps: the row's max |x| picks the power-of-two scale that keeps
+// f16 in range, then entry i holds elements 8i..8i+7 as f16 pairs (entry
+// 4 b + t: block b, lane quad t).  scratch: KW words.
+__device__ __forceinline__ void stage_x_operand(const uint16_t* x, int K, uint4* xs, int* xshift,
+                                                unsigned* scratch, int kw, int KW, int lane,
+                                                int ct, int cthreads) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x);
+  uint32_t mx = 0;
+  for (int i = ct; i < K / 8; i += cthreads) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) scratch[kw] = mx;
+  consumer_sync(cthreads);
+  uint32_t amax = 0;
+  for (int w = 0; w < KW; ++w) amax = max(amax, scratch[w]);
+  const int shift = f16_shift_for_amax(bf16_bits_to_f32(amax));
+  const float sc = pow2f(-shift);
+  if (ct == 0) *xshift = shift;
+  for (int i = ct; i < K / 8; i += cthreads) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 o;
+    o.x = pack_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
+    o.y = pack_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
+    o.z = pack_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
+    o.w = pack_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
+    xs[i] = o;
+  }
+  consumer_sync(cthreads);   // the scratch words are free again, the operand complete
+}
+
+// Shared memory an XS step adds after the streaming carve-up: the shift word
+// (16 bytes) and the operand (2 K bytes for a row of K).
+__host__ __device__ inline int xs_extra_bytes(int K) { return 16 + 2 * K; }
+
+// Routing tables of one activation row (top-k <= 32 experts, one pair each)
+// in shared memory, for the consumers of a routed step with RMAX = 1: one
+// round of independent loads replaces the chain of dependent global reads
+// (count, then expert and offsets, then pair ids, then max |h|) at each run.
+struct OneRowTables {
+  int n_active;
+  int expert[32];
+  int off[33];
+  int pair[32];
+  unsigned amax[32];   // max |h| bits of each pair (h-activation steps)
+};
+constexpr int kOneRowTablesBytes = (int)((sizeof(OneRowTables) + 127) / 128 * 128);
+
+// Copy a's tables (global) into t; every entry a one-row layer can use is
+// read, valid or not, so the loads do not depend on n_active.  The caller
+// syncs the consumers before use.
+__device__ __forceinline__ void load_one_row_tables(const StreamArgs& a, OneRowTables* t, int ct) {
+  if (ct == 0) t->n_active = ld_tab(a.n_active);
+  if (ct < 32) {
+    t->expert[ct] = ld_tab(a.active_expert + ct);
+    t->pair[ct] = ld_tab(a.pair_list + ct);
+    if (a.h_amax) t->amax[ct] = (unsigned)ld_tab(reinterpret_cast<const int*>(a.h_amax) + ct);
+  }
+  if (ct < 33) t->off[ct] = ld_tab(a.active_off + ct);
+}
+
 // Two steps in one launch sharing the stage ring: segment A (a dense step on
 // static weights, e.g. the shared expert) then segment B (a routed step).  The
 // producer streams A's weights before waiting for the predecessor kernel;
@@ -1059,13 +1121,26 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
 // predecessor).  The stage buffers are sized for the larger segment.
 template <class A, class B, bool A_WAITS>
 __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
-    stream_dual_kernel(const StreamArgs a0, const StreamArgs a1) {
+    stream_dual_kernel(const StreamArgs a0, const StreamArgs a1_) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
   trace_begin(a0.trace, a0.trace_id);
   const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
   pdl_launch_dependents();
+  // an XS routed step: its x operand after the carve-up (the shift word, then
+  // the operand)
+  StreamArgs a1 = a1_;
+  uint8_t* xe = reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp) + 64;
+  if constexpr (B::XS) {
+    a1.xs_shift = reinterpret_cast<int*>(xe);
+    a1.xs = reinterpret_cast<uint4*>(xe + 16);
+    xe += xs_extra_bytes(a1.K);
+  }
+  // one-row routed steps: the consumers' routing tables in shared memory
+  // (the producer keeps reading them from global memory, where it may read
+  // them early)
+  OneRowTables* ort = reinterpret_cast<OneRowTables*>(xe);
   uint32_t stage = 0;
   if (warp == 0) {
     if (lane == 0) {
@@ -1073,7 +1148,7 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
       cfg_produce<A>(a0, SegPrior(), m.stages, m.full, m.empty, stage);
       // the routed step's weights are static: with the routing published
       // under a flag they stream while the previous kernel still runs
-      if (a1.route_flag) wait_flag(a1.route_flag, a1.status);
+      if (a1.route_flag) wait_flag(a1.route_flag, a1.status, a1.wait_ns ? a1.wait_ns : kWaitLimitNs);
       else pdl_wait_prerequisites();
       SegPrior pr;
       if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
@@ -1083,13 +1158,31 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     __syncwarp();
   } else {
     if (A_WAITS || A::ROUTED) pdl_wait_prerequisites();
+    if constexpr (B::XS) {
+      // x is the layer's input (read by A as well): staged before A
+      stage_x_operand(a1.x, a1.K, const_cast<uint4*>(a1.xs), const_cast<int*>(a1.xs_shift),
+                      reinterpret_cast<unsigned*>(m.red), warp - 1, KW, lane,
+                      (int)threadIdx.x - 32, 32 * KW);
+    }
     int pp = 0, rp = 0;
     cfg_consume<A>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW,
                    lane);
     pdl_wait_prerequisites();
     SegPrior pr;
     if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
-    cfg_consume<B>(a1, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    if constexpr (B::ROUTED && B::RMAX == 1) {
+      load_one_row_tables(a1, ort, (int)threadIdx.x - 32);
+      consumer_sync(32 * KW);
+      StreamArgs bt = a1;
+      bt.n_active = &ort->n_active;
+      bt.active_expert = ort->expert;
+      bt.active_off = ort->off;
+      bt.pair_list = ort->pair;
+      if (a1.h_amax) bt.h_amax = ort->amax;
+      cfg_consume<B>(bt, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    } else {
+      cfg_consume<B>(a1, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    }
   }
   trace_end(a0.trace, a0.trace_id);
 }

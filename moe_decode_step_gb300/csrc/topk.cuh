@@ -35,6 +35,9 @@ struct TopkArgs {
   int* pair_list;
   unsigned* h_amax;       // [B*k] reset to 0
   unsigned long long* trace;  // optional kernel trace, or null
+  unsigned* route_flag;   // if non-null: raised (release) once the tables are written, for a
+                          // kernel that streams routed weights before this one finishes
+  int skip_flag;          // failure-detection test hook: leave the flag down
 };
 
 constexpr int kTopkThreads = 1024;
@@ -172,6 +175,32 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     for (int i = 0; i < a.k; ++i) ssum += s_score[i];   // picks summed in rank order
     if (lane < a.k) a.topk_w[b * a.k + lane] = a.routed_scale * s_score[lane] / ssum;
     if (lane < a.k) a.h_amax[b * a.k + lane] = 0u;
+    if (gridDim.x == 1 && a.B == 1) {
+      // one row: the k experts are distinct, each with one pair; the tables
+      // list them by expert id (slot = rank of the id among the k), pair =
+      // rank by score.  Nothing else to build.
+      const int e = lane < a.k ? s_idx[lane] : 0x7FFFFFFF;
+      int slot = 0;
+      for (int i = 0; i < a.k; ++i) slot += s_idx[i] < e ? 1 : 0;
+      if (lane < a.k) {
+        a.active_expert[slot] = e;
+        a.active_off[lane] = lane;
+        a.pair_list[slot] = lane;
+      }
+      if (lane == 0) {
+        *a.n_active = a.k;
+        a.active_off[a.k] = a.k;
+      }
+      if (a.route_flag && !a.skip_flag) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u32(a.route_flag, 1u);
+      }
+    }
+  }
+  if (gridDim.x == 1 && a.B == 1) {
+    trace_end(a.trace, 1);
+    return;
   }
   // ---- the last CTA groups pairs by expert ----
   if (gridDim.x > 1) {
@@ -217,6 +246,15 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     *a.n_active = n_act;
     a.active_off[n_act] = total_pairs;
     if (gridDim.x > 1) *a.done = 0u;
+  }
+  if (a.route_flag && !a.skip_flag) {
+    // every thread's table stores are ordered before the flag by the barrier
+    // and the releasing thread's fence
+    __syncthreads();
+    if (t == 0) {
+      __threadfence();
+      st_release_u32(a.route_flag, 1u);
+    }
   }
   trace_end(a.trace, 1);
 }

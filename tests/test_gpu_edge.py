@@ -1,5 +1,5 @@
 """GPU parity on the layer's edge cases against the oracle, element by element,
-on both expert paths (mma.sync: one row runs the fused front kernel; tcgen05):
+on both expert paths (mma.sync, tcgen05):
 
   * an exact top-k tie: zeroed router rows with equal biases give equal biased
     scores; ties go to the lower expert id, and the selected ids must match
@@ -49,7 +49,6 @@ def _run(cfg, weights, x, res, path, max_batch):
     d = layer.forward_debug(x, r)
     torch.cuda.synchronize()
     assert layer.status() == 0
-    assert layer.launches_per_forward(x.shape[0]) == (3 if x.shape[0] == 1 and path == 1 else 5)
     layer.close()
     dbg = {k: _np(v) for k, v in d.items()}
     return idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg, _np(r)
@@ -125,7 +124,8 @@ def test_large_and_zero_rows_in_one_batch(path):
 @pytest.mark.parametrize("kind", ["large", "zero"])
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_one_edge_row(path, kind):
-    """One row alone: the fused front kernel on the mma.sync path."""
+    """One row alone: on the mma.sync path its own FC1 / FC2 configurations
+    (x operand and routing tables in shared memory, the route flag)."""
     cfg = _cfg(TINY, 1)
     x, res, inp = _edge_inputs(cfg, [kind])
     ref = oracle.forward(inp)
