@@ -3,8 +3,10 @@
 
 Headline: microseconds per layer for the full-size layer at B = 1 (d=7168,
 f=1536, 896 MXFP4 experts, top-16, bf16 shared expert, residual + RMSNorm
-tail), event-timed on the device with L2 flushed between steps, plus the
-achieved HBM bandwidth against the bytes the layer must touch.  B = 8 and
+tail), event-timed on the device (by default with L2 not flushed between
+steps: each step streams 360 MB of weights, 2.8x L2; --l2 flush flushes it,
+and the line reports the other mode too), plus the achieved HBM bandwidth
+against the bytes the layer must touch.  B = 8 and
 B = 64 are reported in the same line under "batches".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -46,8 +48,14 @@ def parse_args():
                    help="skip the B=8 / B=64 and four-layer chain extras")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
-                   help="run --warmup untimed forwards of a profiling workload (L2 flushed "
-                        "between them) and exit; for ncu captures, prints no JSON line")
+                   help="run --warmup untimed forwards of a profiling workload (--l2 between "
+                        "them) and exit; for ncu captures, prints no JSON line")
+    p.add_argument("--l2", choices=["none", "flush"], default="none",
+                   help="between timed steps: none (every step streams its 360 MB of weights, "
+                        "2.8x L2, so no weight byte is an L2 hit; code and the small "
+                        "activations stay warm as in a decode loop over layers) or flush "
+                        "(write 2x L2 first: code and activations cold too); the line "
+                        "reports the B = 1 value in both modes")
     p.add_argument("--expert-path", type=int, choices=[0, 1, 2], default=0,
                    help="profiling workload only: 0 both expert paths (by batch), 1 mma.sync, "
                         "2 tcgen05")
@@ -128,6 +136,16 @@ def fc1_bytes(cfg, n_distinct, B):
     shared = 2 * cfg.f_shared * cfg.d * 2
     return (shared + n_distinct * per_expert + 2 * B * cfg.d + 4 * B * cfg.f_shared
             + 4 * B * cfg.top_k * cfg.f)
+
+
+def fc2_bytes(cfg, n_distinct, B):
+    """Algorithmic bytes of FC2: the shared expert's bf16 down rows, the down
+    nibbles and scales of the touched experts, h_s and h read, y_s and the
+    per-pair outputs written."""
+    per_expert = cfg.d * cfg.f // 2 + cfg.d * cfg.f // 32
+    shared = cfg.d * cfg.f_shared * 2
+    return (shared + n_distinct * per_expert + 4 * B * cfg.f_shared + 4 * B * cfg.top_k * cfg.f
+            + 4 * B * cfg.d + 4 * B * cfg.top_k * cfg.d)
 
 
 KERNEL_SOURCES = ("common.cuh", "stream.cuh", "moe_decode.cu")
@@ -239,12 +257,17 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.sink)
 
 
+L2_MODES = {"none": "not flushed: inputs larger than L2 (each step streams 360 MB of weights "
+                    "at B = 1, 2.8x the 129 MB L2, so no weight byte survives in L2 to the next "
+                    "step; per-step DRAM bytes from ncu in profiles/)",
+            "flush": "flushed between timed steps (write of 2x L2 size)"}
+
 SLEEP_CYCLES = 1_000_000   # ~0.5 ms head start so the host enqueues a whole forward
 
 
 def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
     """Device time of one forward per step (CUDA events on the launching stream),
-    L2 flushed before every step.  graph=True replays a captured CUDA graph of
+    flush() before every step.  graph=True replays a captured CUDA graph of
     the forward (the production mode: no host launch gaps); graph=False runs the
     eager forward behind a sleep kernel so that the host has enqueued all of it
     before the GPU reaches it.  Returns (us per step, per-phase us per step)."""
@@ -295,9 +318,8 @@ def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
 
 def time_chain(layers, x0, res0, steps, warmup, flush):
     """Device time of a chain of layers (each layer's out is the next one's x,
-    the residual threads through), captured as one CUDA graph; L2 is flushed
-    once before each chain so the side-stream prefetch of the next layer's
-    router and shared weights shows.  Returns per-chain microseconds."""
+    the residual threads through), captured as one CUDA graph; flush() once
+    before each chain.  Returns per-chain microseconds."""
     import torch
     x = x0.clone()
     res = res0.clone()
@@ -341,8 +363,8 @@ def time_chain(layers, x0, res0, steps, warmup, flush):
 
 def trace_layer(layer, x, res0, flush, reps=7):
     """Device timeline of eager forwards: per kernel, the earliest CTA start and
-    the latest CTA end (globaltimer, us from the first kernel's start), L2
-    flushed before each forward; the median of each over `reps` forwards."""
+    the latest CTA end (globaltimer, us from the first kernel's start),
+    flush() before each forward; the median of each over `reps` forwards."""
     import torch
     res = res0.clone()
     out = torch.empty_like(x)
@@ -448,7 +470,8 @@ def run_ours(args, rank, world, local):
     init_dist(world, "nccl")
     cfg = CONFIGS[args.config]
     peak, peak_kind = measured_peaks()
-    flush = L2Flush(dev)
+    l2flush = L2Flush(dev)
+    flush = l2flush if args.l2 == "flush" else (lambda: None)
 
     layer = synthetic.make_layer(cfg)
     x, res0 = synthetic.make_activations(cfg)
@@ -465,6 +488,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
+    # the same forward in the other L2 mode, outside the timed region
+    alt_times, _ = time_layer(layer, x, res0, args.steps, args.warmup,
+                              (lambda: None) if args.l2 == "flush" else l2flush, graph=True,
+                              timing=False)
     # per-phase events (graph nodes) on a separate set of replays: the event
     # nodes sit between the chained kernels, so they are kept out of the value
     _, phases = time_layer(layer, x, res0, max(5, args.steps // 2), max(3, args.warmup), flush,
@@ -473,9 +500,15 @@ def run_ours(args, rank, world, local):
                                            max(3, args.warmup), flush, graph=False)
 
     us = reduce_max(statistics.median(times), world, dev)
+    us_alt = reduce_max(statistics.median(alt_times), world, dev)
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
+    # one row on the mma.sync path runs FC1 and FC2 as one launch (four per
+    # forward): that launch is the dominant kernel, with both steps' bytes
+    fused = layer.launches_per_forward(cfg.B) == 4
     fc1_us = statistics.median(p[1] for p in phases)
     fc1_b = fc1_bytes(cfg, n_distinct, cfg.B)
+    if fused:
+        fc1_b += fc2_bytes(cfg, n_distinct, cfg.B)
     rec = traffic_from_profile()
     traffic = None
     if rec is not None:
@@ -543,7 +576,8 @@ def run_ours(args, rank, world, local):
         tc_off = time_chain(chain_layers, xc, rc, stc, max(3, args.warmup), flush)
         vc_off = reduce_max(statistics.median(tc_off), world, dev)
         chain = {"layers": cc.n_layers, "B": cc.B, "us": vc, "us_per_layer": vc / cc.n_layers,
-                 "steps": stc, "l2": "flushed once before each chain",
+                 "steps": stc, "l2": ("flushed once before each chain" if args.l2 == "flush"
+                                      else "not flushed (63 GB of weights per chain)"),
                  "prefetch": "next layer's router and shared-expert weights, side stream",
                  "us_prefetch_off": vc_off, "us_per_layer_prefetch_off": vc_off / cc.n_layers,
                  "prefetch_gain_us_per_layer": (vc_off - vc) / cc.n_layers}
@@ -568,14 +602,18 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"{args.config}: one MoE decode layer, B={cfg.B}, d={cfg.d}, "
                                f"f={cfg.f}, E={cfg.n_experts}, top-{cfg.top_k}, MXFP4 experts, "
                                f"bf16 shared expert f={cfg.f_shared}, residual+RMSNorm tail",
-                   "B": cfg.B, "l2": "flushed between timed steps (write of 2x L2 size)",
+                   "B": cfg.B, "l2": L2_MODES[args.l2],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm": {"bytes_touched": btouch, "n_distinct_experts": n_distinct,
                 "tbs": btouch / us / 1e6, "frac_of_peak": btouch / us / 1e3 / peak,
                 "frac_of_nominal_8tbs": btouch / us / 1e6 / 8.0, "aggregate_tbs": agg_tbs,
                 "peak_gbs": peak, "peak_kind": peak_kind},
         "expert_path": "mma.sync with register dequantisation (B = 1)",
-        "roofline": {"kernel": "stream_dual_kernel (FC1: shared + routed gate/up)",
+        "value_other_l2_mode": {"us": us_alt, "l2": L2_MODES["flush" if args.l2 == "none"
+                                                              else "none"]},
+        "roofline": {"kernel": ("stream_expert_kernel (FC1 + FC2 in one launch: shared and "
+                                "routed gate/up, shared and routed down)") if fused else
+                               "stream_dual_kernel (FC1: shared + routed gate/up)",
                      "bound": "hbm",
                      "achieved": fc1_b / fc1_us / 1e3, "peak": peak, "unit": "GB/s",
                      "frac": fc1_b / fc1_us / 1e3 / peak, "traffic": traffic,
@@ -616,7 +654,7 @@ def run_profile_case(args):
     if n_experts is not None:
         cfg = dataclasses.replace(cfg, name=args.profile_case, n_experts=n_experts)
     dev = torch.device("cuda", 0)
-    flush = L2Flush(dev)
+    flush = L2Flush(dev) if args.l2 == "flush" else (lambda: None)
     layer = synthetic.make_layer(cfg, expert_path=args.expert_path)
     x, res0 = synthetic.make_activations(cfg)
     res = res0.clone()

@@ -167,12 +167,13 @@ int moe_layer_status(moe_layer_t layer, int* device_status);
 
 /* Failure-detection test hook (the pages have no counterpart; it exists so a
  * test can watch a device-side wait expire without faulting anything).
- * fault = 1: in later forwards of one row on the mma.sync path, top-k does
- * not raise the route flag that FC2's producer waits on before it streams
- * the routed weights, and that wait is limited to wait_ns nanoseconds (0:
- * the default 2 s).  The wait expires, the producer goes on with the routing
- * tables top-k has written, the forward completes, and moe_layer_status
- * then reports MOE_ERR_TIMEOUT.  fault = 0 restores normal operation.
+ * fault = 1: in later forwards of one row on the mma.sync path (FC1 and FC2
+ * in one launch, whose CTAs meet at a grid-wide barrier between the two
+ * steps), CTA 0 does not count itself at that barrier, and every CTA's wait
+ * there is limited to wait_ns nanoseconds (0: the default 2 s).  The waits
+ * expire, FC2 runs on the FC1 results that are already written, the forward
+ * completes, and moe_layer_status then reports MOE_ERR_TIMEOUT.  fault = 0
+ * restores normal operation.
  * Nothing on the GPU traps, faults or hangs.  Errors: INVALID_ARG. */
 int moe_debug_set_fault(moe_layer_t layer, int fault, unsigned long long wait_ns);
 

@@ -163,7 +163,8 @@ class MoELayer:
 
     def debug_set_fault(self, fault, wait_ns=0):
         """Failure-detection test hook (see moe_debug_set_fault): fault 1 makes
-        FC2's wait for the one-row route flag expire after wait_ns."""
+        the one-row expert kernel's grid-wide barrier wait expire after
+        wait_ns (one CTA does not arrive)."""
         check(lib().moe_debug_set_fault(self._h, int(fault), int(wait_ns)),
               "moe_debug_set_fault")
 

@@ -286,6 +286,20 @@ __device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// One thread waits (acquire) until the counter *c reaches target; bounded
+// by limit_ns, after which it raises the timeout status and returns.
+__device__ __forceinline__ void wait_count_at_least(const unsigned* c, unsigned target,
+                                                    int* status, unsigned long long limit_ns) {
+  if (ld_acquire_u32(c) >= target) return;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_u32(c) < target) {
+    if (global_ns() - t0 > limit_ns) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
 // Bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -8,9 +8,10 @@
 //   -> tail (combine + residual + RMSNorm)
 // The shared expert streams first inside FC1/FC2: its weights do not depend on
 // the routing, so FC1 starts them while top-k is still finishing (on the one
-// SM FC1 leaves it at one row).  At one row on the mma.sync path top-k also
-// raises a route flag, and FC2's producer streams its routed weights as soon
-// as the flag is up instead of waiting for FC1 to finish.
+// SM FC1 leaves it at one row).  At one row on the mma.sync path FC1 and FC2
+// are one persistent launch (stream_expert_kernel, four launches in all):
+// FC2's weights stream into the stage ring while FC1's last items are
+// consumed, and grid-wide counters replace the kernel boundary.
 // Optional second stream (chained layers only): L2 prefetch of the next
 // layer's router and shared-expert weights.
 // No allocation, no host synchronisation: capturable into a CUDA graph.
@@ -95,9 +96,9 @@ struct Workspace {
   // while the router's last CTAs finish)
   float* rpartial;
   unsigned* rflags;
-  // one row on the mma.sync path: raised by top-k once the routing tables
-  // are written (zeroed by the tail)
-  unsigned* route_flag;
+  // the one-row expert kernel's grid-wide counters: CTAs whose shared-expert
+  // rows h_s [0] and routed rows h [1] are written (zeroed by top-k)
+  unsigned* done_counts;
 };
 
 // Launch shape of one streaming-GEMV step.
@@ -107,9 +108,11 @@ struct StreamPlan {
   int tc_kc = 0;   // K elements per stage of the tensor-core routed pass
   int dense_kc = 0;   // K elements per stage of the tensor-core dense pass
   int dense_ctas = 0;   // CTAs of the dense pass (0: the whole grid)
+  int kc2 = 1;     // the fused one-row expert kernel: K chunks per item of routed FC2
 };
 
-enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kNumSteps };
+enum { kStepRouter, kStepFc1, kStepFc2, kStepTc1, kStepTc2, kStepTcRouter, kStepExpert,
+       kNumSteps };
 
 // Expert paths: mma.sync on the tiled layouts (the GEMV regime: weights
 // converted to f16 in registers), or tcgen05 on the UMMA layouts (block-scaled
@@ -203,7 +206,7 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
   w.dflags = carve<unsigned>(p, kTcMaxCtas);
   w.rpartial = carve<float>(p, (size_t)kTcMaxCtas * kTcDenseMaxN * 128);
   w.rflags = carve<unsigned>(p, kTcMaxCtas);
-  w.route_flag = carve<unsigned>(p, 1);
+  w.done_counts = carve<unsigned>(p, 2);
   if (ws) *ws = w;
   return (size_t)(p - base);
 }
@@ -240,7 +243,11 @@ using Fc2Cfg = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, RM, true, T
 #define MOE_ROUTER_KERNEL stream_gemv_kernel<kWfBf16, false, false, false, 1, 1, 4>
 // One activation row (batch class 0): the routed step takes one row per
 // expert with its x operand in shared memory.
-using Fc1OneRowCfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8, 4, true>;
+#ifndef MOE_FC1_TM_B1
+#define MOE_FC1_TM_B1 1
+#endif
+using Fc1OneRowCfg = StreamCfg<kWfMx, true, false, true, 8 * MOE_FC1_TM_B1, 8 * MOE_FC1_TM_B1, 1,
+                               true, MOE_FC1_TM_B1, 16, 8, 4, true>;
 #define MOE_FC1_KERNEL(RS) stream_dual_kernel<Sh1Cfg<RS>, Fc1Cfg, false>
 #define MOE_FC1_KERNEL_ONE_ROW stream_dual_kernel<Sh1Cfg<1>, Fc1OneRowCfg, false>
 // FC2 at batch class 0 (B = 1: one activation row per routed expert) takes
@@ -252,6 +259,9 @@ using Fc1OneRowCfg = StreamCfg<kWfMx, true, false, true, 8, 8, 1, true, 1, 16, 8
 #define MOE_FC2_RM(RS) ((RS) == 1 ? 1 : 8)
 #define MOE_FC2_KERNEL(RS, NBM) \
   stream_dual_kernel<Sh2Cfg<RS>, Fc2Cfg<NBM, MOE_FC2_TM(RS), MOE_FC2_RM(RS)>, true>
+// One row, both expert steps in one launch (FC1's and FC2's configurations).
+#define MOE_EXPERT_KERNEL(NBM) \
+  stream_expert_kernel<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<NBM, MOE_FC2_TM(1), 1>>
 // Tensor-core path: FC1 streams the shared gate/up first (while top-k runs),
 // FC2 the shared down first (its weights requested before FC1 is waited for).
 #define MOE_TC1_KERNEL tc_kernel<true>
@@ -356,6 +366,47 @@ int plan_fc2(moe_layer* L, const moe_dims_t& d, int n, StreamPlan* p) {
       MOE_FC2_KERNEL(RS, 12), d.f_shared, d.d, d.f, d.d, n, kBudget1, p);
 }
 
+// Launch shape of the fused one-row expert kernel: the four segments (shared
+// gate/up, routed gate/up, shared down, routed down) share one stage ring of
+// the largest segment stage; the routed segments keep their own K chunking.
+// One CTA per SM, one SM left for top-k: the grid-wide barrier between the
+// steps needs every CTA resident.
+template <class A1, class B1, class A2, class B2, typename Kern>
+int plan_expert(Kern kern, const moe_dims_t& d, int n_sm, int budget, StreamPlan* p) {
+  const int KW = std::max(std::max(seg_warps<A1>(d.d), seg_warps<B1>(d.d)),
+                          std::max(seg_warps<A2>(d.f_shared), seg_warps<B2>(d.f)));
+  if (KW > kMmaWarps || n_sm < 2) return MOE_ERR_UNSUPPORTED;
+  if (!seg_fits<A1>(d.d, d.f_shared, KW) || !seg_fits<B1>(d.d, d.f, KW) ||
+      !seg_fits<A2>(d.f_shared, d.d, KW) || !seg_fits<B2>(d.f, d.d, KW))
+    return MOE_ERR_UNSUPPORTED;
+  StreamPlan r;
+  r.threads = 32 * (KW + 1);
+  r.kc = seg_kc<B1>(d.d, KW);
+  r.kc2 = seg_kc<B2>(d.f, KW);
+  cudaFuncAttributes fa;
+  MOE_CUDA(cudaFuncGetAttributes(&fa, kern));
+  budget -= (int)fa.sharedSizeBytes;   // static shared memory of the kernel, if any
+  const size_t st = std::max(std::max(seg_stage_bytes<A1>(d.d, 1), seg_stage_bytes<B1>(d.d, r.kc)),
+                             std::max(seg_stage_bytes<A2>(d.f_shared, 1),
+                                      seg_stage_bytes<B2>(d.f, r.kc2)));
+  r.stage_bytes = (int)((st + 127) / 128 * 128);
+  r.red_pp = std::max(std::max(stream_red_pp(KW, A1::MMA, A1::TM, A1::RMAX),
+                               stream_red_pp(KW, B1::MMA, B1::TM, B1::RMAX)),
+                      std::max(stream_red_pp(KW, A2::MMA, A2::TM, A2::RMAX),
+                               stream_red_pp(KW, B2::MMA, B2::TM, B2::RMAX)));
+  const int red_bytes = 2 * r.red_pp * 4 + 64 + xs_extra_bytes(d.d) + kOneRowTablesBytes;
+  r.NS = std::min(16, (budget - red_bytes) / (r.stage_bytes + 16));
+  if (r.NS < 2 || r.NS < 2 * r.kc || r.NS < 2 * r.kc2) return MOE_ERR_UNSUPPORTED;
+  r.smem = r.NS * r.stage_bytes + r.NS * 16 + red_bytes;
+  MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, r.smem));
+  int occ = 0;
+  MOE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, r.threads, r.smem));
+  if (occ != 1) return MOE_ERR_UNSUPPORTED;
+  r.grid = n_sm - 1;
+  *p = r;
+  return MOE_OK;
+}
+
 // Launch shape of a tensor-core kernel: six warps, a stage ring sized for the
 // larger pass (routed: rmax pairs; dense: np_max columns), and tensor memory
 // for two accumulators, a scale slot per stage and the activation scales.
@@ -452,6 +503,13 @@ int plan_all(moe_layer* L) {
   MOE_PLAN((plan_fc2<1>(L, d, n, &L->plan[kStepFc2][0])));
   MOE_PLAN((plan_fc2<2>(L, d, n, &L->plan[kStepFc2][1])));
   MOE_PLAN((plan_fc2<4>(L, d, n, &L->plan[kStepFc2][2])));
+  if (fc2_small(d)) {
+    MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<4, MOE_FC2_TM(1), 1>>(
+        MOE_EXPERT_KERNEL(4), d, n, std::max(kBudget1, L->smem_optin), &L->plan[kStepExpert][0])));
+  } else {
+    MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<12, MOE_FC2_TM(1), 1>>(
+        MOE_EXPERT_KERNEL(12), d, n, std::max(kBudget1, L->smem_optin), &L->plan[kStepExpert][0])));
+  }
 #undef MOE_PLAN
   return MOE_OK;
 }
@@ -559,8 +617,7 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   t.h_amax = L->ws.h_amax;
   t.trace = L->tracing ? L->ws.trace : nullptr;
   // one row on the mma.sync path: FC2 streams its routed weights under this flag
-  t.route_flag = (B == 1 && !use_tc(L, B) && idx == L->ws.topk_idx) ? L->ws.route_flag : nullptr;
-  t.skip_flag = L->debug_fault == 1;
+  t.reset_counts = (!use_tc(L, B) && idx == L->ws.topk_idx) ? L->ws.done_counts : nullptr;
   MOE_CUDA(launch_ex(topk_kernel, dim3(B), dim3(kTopkThreads), 0, st, true, t));
   return MOE_OK;
 }
@@ -574,6 +631,14 @@ int launch_dual(K kern, const StreamPlan& p, StreamArgs a0, StreamArgs a1, cudaS
   a0.kc = a1.kc = p.kc;
   MOE_CUDA(launch_ex(kern, dim3(grid), dim3(p.threads), (size_t)p.smem, st, true, a0, a1));
   return MOE_OK;
+}
+
+// CTAs of FC1 on the mma.sync path.  At B = 1 one SM holds the top-k CTA
+// when FC1 launches; a CTA waiting for it would start (and finish) last, so
+// FC1 leaves that SM out.
+int fc1_grid(const moe_layer* L, int B) {
+  const int g = L->plan[kStepFc1][batch_class(B)].grid;
+  return B == 1 ? std::max(1, g - 1) : g;
 }
 
 // FC1: shared gate/up (bf16) then routed gate/up (MXFP4), SwiGLU epilogues.
@@ -597,10 +662,8 @@ int launch_fc1(moe_layer* L, cudaStream_t st, const void* x, int B) {
   ra.out = L->ws.h;
   ra.out_amax = L->ws.h_amax;
   sa.trace_id = ra.trace_id = 2;
-  // At B = 1 one SM holds the top-k CTA when FC1 launches; a CTA waiting for
-  // it would start (and finish) last, so FC1 leaves that SM out.
+  const int grid = fc1_grid(L, B);
   const StreamPlan& p = L->plan[kStepFc1][batch_class(B)];
-  const int grid = B == 1 ? std::max(1, p.grid - 1) : p.grid;
   switch (batch_class(B)) {
     case 0: return launch_dual(MOE_FC1_KERNEL_ONE_ROW, p, sa, ra, st, grid);
     case 1: return launch_dual(MOE_FC1_KERNEL(2), p, sa, ra, st, grid);
@@ -766,10 +829,8 @@ int launch_fc2_tc(moe_layer* L, cudaStream_t st, int B) {
   return launch_tc(MOE_TC2_KERNEL, p, b, dn, unused, st, p.grid);
 }
 
-// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).  With `flag`
-// (one row, where top-k raises the route flag) its producer takes the routing
-// tables under the flag instead of waiting for FC1 to finish.
-int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool flag) {
+// FC2: shared down (bf16, h_s) then routed down (MXFP4, h).
+int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
   const moe_dims_t& d = L->dims;
   StreamArgs sa = base_args(L);
   sa.q = static_cast<const uint8_t*>(L->w.shared_d);
@@ -788,8 +849,6 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool flag) {
   ra.h = L->ws.h;
   ra.h_amax = L->ws.h_amax;
   ra.out = L->ws.y_pair;
-  ra.route_flag = flag ? L->ws.route_flag : nullptr;
-  ra.wait_ns = L->debug_fault == 1 ? L->debug_wait_ns : 0;
   sa.trace_id = ra.trace_id = 3;
   const StreamPlan& p = L->plan[kStepFc2][batch_class(B)];
   if (fc2_small(d)) {
@@ -804,6 +863,73 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B, bool flag) {
     case 1: return launch_dual(MOE_FC2_KERNEL(2, 12), p, sa, ra, st, p.grid);
     default: return launch_dual(MOE_FC2_KERNEL(4, 12), p, sa, ra, st, p.grid);
   }
+}
+
+// One row on the mma.sync path: FC1 and FC2 in one launch (see
+// stream_expert_kernel), the segments' arguments as launch_fc1 and launch_fc2
+// build them.
+int launch_expert(moe_layer* L, cudaStream_t st, const void* x) {
+  const moe_dims_t& d = L->dims;
+  const StreamPlan& p = L->plan[kStepExpert][0];
+  StreamArgs4 g;
+  std::memset(&g, 0, sizeof(g));
+  StreamArgs& s1 = g.a[0];
+  s1 = base_args(L);
+  s1.q = static_cast<const uint8_t*>(L->w.shared_gu);
+  s1.K = d.d;
+  s1.N = d.f_shared;
+  s1.B = 1;
+  s1.x = static_cast<const uint16_t*>(x);
+  s1.out = L->ws.hs;
+  StreamArgs& r1 = g.a[1];
+  r1 = base_args(L);
+  r1.q = L->wm.gu_q;
+  r1.s = L->wm.gu_s;
+  r1.q_stride = L->q_gu_stride;
+  r1.s_stride = L->s_gu_stride;
+  r1.K = d.d;
+  r1.N = d.f;
+  r1.x = static_cast<const uint16_t*>(x);
+  r1.out = L->ws.h;
+  r1.out_amax = L->ws.h_amax;
+  r1.done_count = L->ws.done_counts;
+  r1.wait_ns = L->debug_fault == 1 ? L->debug_wait_ns : 0;
+  StreamArgs& s2 = g.a[2];
+  s2 = base_args(L);
+  s2.q = static_cast<const uint8_t*>(L->w.shared_d);
+  s2.K = d.f_shared;
+  s2.N = d.d;
+  s2.B = 1;
+  s2.h = L->ws.hs;
+  s2.out = L->ws.y_s;
+  StreamArgs& r2 = g.a[3];
+  r2 = base_args(L);
+  r2.q = L->wm.d_q;
+  r2.s = L->wm.d_s;
+  r2.q_stride = L->q_d_stride;
+  r2.s_stride = L->s_d_stride;
+  r2.K = d.f;
+  r2.N = d.d;
+  r2.h = L->ws.h;
+  r2.h_amax = L->ws.h_amax;
+  r2.out = L->ws.y_pair;
+  for (int i = 0; i < 4; ++i) {
+    g.a[i].NS = p.NS;
+    g.a[i].stage_bytes = p.stage_bytes;
+    g.a[i].red_pp = p.red_pp;
+    g.a[i].kc = 1;
+    g.a[i].trace_id = i < 2 ? 2 : 3;
+  }
+  r1.kc = p.kc;
+  r2.kc = p.kc2;
+  g.skip_count = L->debug_fault == 1;
+  if (fc2_small(d))
+    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(4), dim3(p.grid), dim3(p.threads), (size_t)p.smem, st,
+                       true, g));
+  else
+    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(12), dim3(p.grid), dim3(p.threads), (size_t)p.smem, st,
+                       true, g));
+  return MOE_OK;
 }
 
 int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out, float* y_r_dbg,
@@ -823,7 +949,6 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.k = L->dims.top_k;
   a.eps = L->dims.rms_eps;
   a.trace = L->tracing ? L->ws.trace : nullptr;
-  a.route_flag = L->ws.route_flag;
   a.h_amax = L->ws.h_amax;
   MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
   return MOE_OK;
@@ -872,11 +997,16 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
   if ((rc = launch_prefetch(L))) return rc;
-  if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
-  if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
-  // one row on the mma.sync path: FC2 takes the routing from the route flag
-  if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B, B == 1))) return rc;
-  if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
+  if (!tc && B == 1) {   // one launch for both expert steps
+    if ((rc = launch_expert(L, st, x))) return rc;
+    if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
+    if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
+  } else {
+    if ((rc = tc ? launch_fc1_tc(L, st, x, B) : launch_fc1(L, st, x, B))) return rc;
+    if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
+    if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
+    if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
+  }
   if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
   if (tm) {
@@ -1215,7 +1345,9 @@ int moe_get_trace(moe_layer_t L, unsigned long long* ns, int n) {
 
 int moe_launches_per_forward(moe_layer_t L, int B) {
   if (!L || B < 1 || B > L->dims.max_batch) return -1;
-  return 5;   // router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail
+  // router, top-k, FC1 (shared + routed), FC2 (shared + routed), tail; one
+  // row on the mma.sync path takes FC1 and FC2 in one launch
+  return (B == 1 && !use_tc(L, B)) ? 4 : 5;
 }
 
 size_t mxfp4_packed_bytes(int64_t rows, int64_t k, int layout, size_t* scale_bytes) {

@@ -75,13 +75,11 @@ struct StreamArgs {
   // elements 8t..8t+7 at xs[4 b + t], scaled by 2^-(*xs_shift)
   const uint4* xs;
   const int* xs_shift;
-  // the producer's bounded wait for route_flag ends after wait_ns (0: the
+  // the one-row expert kernel (stream_expert_kernel): its two grid-wide
+  // counters, and the limit of its wait before FC2's routed segment (0: the
   // default limit)
+  unsigned* done_count;
   unsigned long long wait_ns;
-  const unsigned* route_flag;  // routed step of a two-step kernel: non-null when the routing
-                               // tables are published under this flag (the producer then
-                               // streams the routed weights without waiting for the previous
-                               // kernel to finish)
 };
 
 // Lane layout of the bf16 steps: a lane owns NQ chunks of CW consecutive K
@@ -943,19 +941,6 @@ __device__ __forceinline__ void cfg_consume(const StreamArgs& a, const SegPrior&
                                                pp, rp, kw, KW, lane);
 }
 
-// Bounded wait for a flag another kernel (or CTA) raises with a release store.
-__device__ __forceinline__ void wait_flag(const unsigned* flag, int* status,
-                                          unsigned long long limit_ns) {
-  if (ld_acquire_u32(flag) != 0u) return;
-  const unsigned long long t0 = global_ns();
-  while (ld_acquire_u32(flag) == 0u) {
-    if (global_ns() - t0 > limit_ns) {
-      if (status) atomicExch(status, kStatusTimeout);
-      return;
-    }
-  }
-}
-
 // Shared-memory carve-up common to both kernels.
 struct StreamSmem {
   uint8_t* stages;
@@ -1089,29 +1074,44 @@ __device__ __forceinline__ void stage_x_operand(const uint16_t* x, int K, uint4*
 __host__ __device__ inline int xs_extra_bytes(int K) { return 16 + 2 * K; }
 
 // Routing tables of one activation row (top-k <= 32 experts, one pair each)
-// in shared memory, for the consumers of a routed step with RMAX = 1: one
-// round of independent loads replaces the chain of dependent global reads
-// (count, then expert and offsets, then pair ids, then max |h|) at each run.
+// in shared memory, for a routed step with RMAX = 1.  The producer brings
+// them in with one round of bulk copies as soon as it knows the routing is
+// final (every entry a one-row layer can use, valid or not, so the copies do
+// not depend on n_active); producer and consumers then read no table from
+// global memory, instead of a chain of dependent reads at each run.
 struct OneRowTables {
-  int n_active;
+  uint64_t bar;      // completes when the copies have landed
+  uint64_t pad;
+  int n_active[4];
   int expert[32];
-  int off[33];
+  int off[36];
   int pair[32];
-  unsigned amax[32];   // max |h| bits of each pair (h-activation steps)
 };
 constexpr int kOneRowTablesBytes = (int)((sizeof(OneRowTables) + 127) / 128 * 128);
+constexpr uint32_t kOneRowCopyBytes = 16 + 128 + 144 + 128;
 
-// Copy a's tables (global) into t; every entry a one-row layer can use is
-// read, valid or not, so the loads do not depend on n_active.  The caller
-// syncs the consumers before use.
-__device__ __forceinline__ void load_one_row_tables(const StreamArgs& a, OneRowTables* t, int ct) {
-  if (ct == 0) t->n_active = ld_tab(a.n_active);
-  if (ct < 32) {
-    t->expert[ct] = ld_tab(a.active_expert + ct);
-    t->pair[ct] = ld_tab(a.pair_list + ct);
-    if (a.h_amax) t->amax[ct] = (unsigned)ld_tab(reinterpret_cast<const int*>(a.h_amax) + ct);
-  }
-  if (ct < 33) t->off[ct] = ld_tab(a.active_off + ct);
+// Producer: the copies of a's tables into t (addresses and sizes are 16-byte
+// multiples; each source array's allocation extends to 256-byte multiples).
+__device__ __forceinline__ void copy_one_row_tables(const StreamArgs& a, OneRowTables* t,
+                                                    uint64_t policy) {
+  // the tables were written through the generic proxy: order them before the
+  // bulk copies' reads
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  mbar_arrive_expect_tx(&t->bar, kOneRowCopyBytes);
+  bulk_g2s(t->n_active, a.n_active, 16, &t->bar, policy);
+  bulk_g2s(t->expert, a.active_expert, 128, &t->bar, policy);
+  bulk_g2s(t->off, a.active_off, 144, &t->bar, policy);
+  bulk_g2s(t->pair, a.pair_list, 128, &t->bar, policy);
+}
+
+// a with its table pointers on t.
+__device__ __forceinline__ StreamArgs with_one_row_tables(const StreamArgs& a, OneRowTables* t) {
+  StreamArgs r = a;
+  r.n_active = t->n_active;
+  r.active_expert = t->expert;
+  r.active_off = t->off;
+  r.pair_list = t->pair;
+  return r;
 }
 
 // Two steps in one launch sharing the stage ring: segment A (a dense step on
@@ -1137,22 +1137,31 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     a1.xs = reinterpret_cast<uint4*>(xe + 16);
     xe += xs_extra_bytes(a1.K);
   }
-  // one-row routed steps: the consumers' routing tables in shared memory
-  // (the producer keeps reading them from global memory, where it may read
-  // them early)
+  // one-row routed steps: the routing tables in shared memory
+  constexpr bool kOneRow = B::ROUTED && B::RMAX == 1;
   OneRowTables* ort = reinterpret_cast<OneRowTables*>(xe);
+  if constexpr (kOneRow) {
+    if (threadIdx.x == 0) {
+      mbar_init(&ort->bar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+  }
   uint32_t stage = 0;
   if (warp == 0) {
     if (lane == 0) {
       if (A::ROUTED) pdl_wait_prerequisites();
       cfg_produce<A>(a0, SegPrior(), m.stages, m.full, m.empty, stage);
-      // the routed step's weights are static: with the routing published
-      // under a flag they stream while the previous kernel still runs
-      if (a1.route_flag) wait_flag(a1.route_flag, a1.status, a1.wait_ns ? a1.wait_ns : kWaitLimitNs);
-      else pdl_wait_prerequisites();
+      pdl_wait_prerequisites();
       SegPrior pr;
       if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
-      cfg_produce<B>(a1, pr, m.stages, m.full, m.empty, stage);
+      if constexpr (kOneRow) {
+        copy_one_row_tables(a1, ort, policy_evict_last());
+        mbar_wait(&ort->bar, 0, a1.status);
+        cfg_produce<B>(with_one_row_tables(a1, ort), pr, m.stages, m.full, m.empty, stage);
+      } else {
+        cfg_produce<B>(a1, pr, m.stages, m.full, m.empty, stage);
+      }
       stream_drain(a0, m.empty, stage);
     }
     __syncwarp();
@@ -1167,24 +1176,135 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
     int pp = 0, rp = 0;
     cfg_consume<A>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW,
                    lane);
-    pdl_wait_prerequisites();
+    if (!(A_WAITS || A::ROUTED)) pdl_wait_prerequisites();
     SegPrior pr;
     if (!A::ROUTED) cfg_add_prior<A>(a0, pr);
-    if constexpr (B::ROUTED && B::RMAX == 1) {
-      load_one_row_tables(a1, ort, (int)threadIdx.x - 32);
-      consumer_sync(32 * KW);
-      StreamArgs bt = a1;
-      bt.n_active = &ort->n_active;
-      bt.active_expert = ort->expert;
-      bt.active_off = ort->off;
-      bt.pair_list = ort->pair;
-      if (a1.h_amax) bt.h_amax = ort->amax;
-      cfg_consume<B>(bt, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
+    if constexpr (kOneRow) {
+      mbar_wait(&ort->bar, 0, a1.status);
+      cfg_consume<B>(with_one_row_tables(a1, ort), pr, m.stages, m.full, m.empty, m.red, stage, pp,
+                     rp, warp - 1, KW, lane);
     } else {
       cfg_consume<B>(a1, pr, m.stages, m.full, m.empty, m.red, stage, pp, rp, warp - 1, KW, lane);
     }
   }
   trace_end(a0.trace, a0.trace_id);
+}
+
+
+// One row (B = 1): both expert steps of the layer in one persistent launch,
+// segments A1 (shared gate/up, bf16), B1 (routed gate/up, MXFP4), A2 (shared
+// down) and B2 (routed down).  The producer streams the four segments' weights
+// back to back through one stage ring: the down weights do not depend on FC1's
+// results, so they fill the ring while the last FC1 items are consumed and
+// HBM stays busy across the FC1 -> FC2 boundary.  Each consumed segment of
+// FC2 reads every CTA's FC1 outputs, so the consumers meet at two grid-wide
+// barriers: each CTA adds 1 to counter 0 once its h_s rows (A1) are written
+// and to counter 1 once its h rows and max |h| (B1) are; A2 waits (bounded)
+// for counter 0 to reach the grid size, which it long has when a CTA gets
+// there, so A2 runs while other CTAs still finish B1; B2 waits for counter 1.
+// Every CTA of the grid must be resident at once: one CTA per SM and at most
+// as many CTAs as SMs are free (the bounded waits turn anything else into a
+// timeout status instead of a hang).
+// a[0..3]: the segments' arguments (a[1], a[3] share the routing tables, which
+// arrive in shared memory once top-k, the programmatic predecessor, is done);
+// a[1].done_count: the two counters (zeroed by top-k); a[1].wait_ns: the
+// limit of B2's wait (0: the default); skip_count: a failure-detection test
+// hook (CTA 0 does not count its B1 outputs, so every CTA's wait expires).
+struct StreamArgs4 {
+  StreamArgs a[4];
+  int skip_count;
+};
+
+template <class A1, class B1, class A2, class B2>
+__global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
+    stream_expert_kernel(const StreamArgs4 args) {
+  static_assert(B1::ROUTED && B1::RMAX == 1 && B2::ROUTED && B2::RMAX == 1 && B1::XS,
+                "one activation row: routed steps with one column, FC1's x in shared memory");
+  static_assert(!A1::ROUTED && !A2::ROUTED, "the shared expert is dense");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = (int)(blockDim.x >> 5) - 1;
+  const StreamArgs& a0 = args.a[0];
+  trace_begin(a0.trace, 2);
+  const StreamSmem m = stream_smem_init(smem, a0.NS, a0.stage_bytes, a0.red_pp, KW);
+  pdl_launch_dependents();
+  // after the carve-up: FC1's x operand (the shift word, then the operand),
+  // then the routing tables
+  StreamArgs b1 = args.a[1];
+  uint8_t* xe = reinterpret_cast<uint8_t*>(m.red + 2 * (size_t)a0.red_pp) + 64;
+  b1.xs_shift = reinterpret_cast<int*>(xe);
+  b1.xs = reinterpret_cast<uint4*>(xe + 16);
+  xe += xs_extra_bytes(b1.K);
+  OneRowTables* ort = reinterpret_cast<OneRowTables*>(xe);
+  if (threadIdx.x == 0) {
+    mbar_init(&ort->bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t stage = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      cfg_produce<A1>(a0, SegPrior(), m.stages, m.full, m.empty, stage);
+      pdl_wait_prerequisites();   // top-k's routing tables
+      copy_one_row_tables(b1, ort, policy_evict_last());
+      mbar_wait(&ort->bar, 0, b1.status);
+      SegPrior p1;
+      cfg_add_prior<A1>(a0, p1);
+      cfg_produce<B1>(with_one_row_tables(b1, ort), p1, m.stages, m.full, m.empty, stage);
+      cfg_produce<A2>(args.a[2], SegPrior(), m.stages, m.full, m.empty, stage);
+      SegPrior p2;
+      cfg_add_prior<A2>(args.a[2], p2);
+      cfg_produce<B2>(with_one_row_tables(args.a[3], ort), p2, m.stages, m.full, m.empty, stage);
+      stream_drain(a0, m.empty, stage);
+    }
+    __syncwarp();
+  } else {
+    const int ct = (int)threadIdx.x - 32, cthreads = 32 * KW, kw = warp - 1;
+    // x is the layer's input (read by A1 as well): staged before A1
+    stage_x_operand(b1.x, b1.K, const_cast<uint4*>(b1.xs), const_cast<int*>(b1.xs_shift),
+                    reinterpret_cast<unsigned*>(m.red), kw, KW, lane, ct, cthreads);
+    int pp = 0, rp = 0;
+    unsigned* const count = b1.done_count;
+    cfg_consume<A1>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);
+    // this CTA's h_s rows are written (the barrier orders every consumer's
+    // stores before the counting thread's fence)
+    consumer_sync(cthreads);
+    if (ct == 0) {
+      __threadfence();
+      atomicAdd(count, 1u);
+    }
+    pdl_wait_prerequisites();
+    SegPrior p1;
+    cfg_add_prior<A1>(a0, p1);
+    mbar_wait(&ort->bar, 0, b1.status);
+    cfg_consume<B1>(with_one_row_tables(b1, ort), p1, m.stages, m.full, m.empty, m.red, stage, pp,
+                    rp, kw, KW, lane);
+    // every CTA's h_s (for A2); this CTA's h rows and max |h| are written
+    if (ct == 0) {
+      wait_count_at_least(count, gridDim.x, b1.status, kWaitLimitNs);
+      __threadfence();
+    }
+    consumer_sync(cthreads);
+    if (ct == 0) {
+      if (b1.trace) atomicMax(b1.trace + 8 + 2, global_ns());
+      if (b1.trace) atomicMin(b1.trace + 3, global_ns());
+      __threadfence();
+      if (!(args.skip_count && blockIdx.x == 0)) atomicAdd(count + 1, 1u);
+    }
+    cfg_consume<A2>(args.a[2], SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW,
+                    lane);
+    // every CTA's h rows and max |h| (for B2)
+    if (ct == 0) {
+      wait_count_at_least(count + 1, gridDim.x, b1.status, b1.wait_ns ? b1.wait_ns : kWaitLimitNs);
+      __threadfence();
+    }
+    consumer_sync(cthreads);
+    SegPrior p2;
+    cfg_add_prior<A2>(args.a[2], p2);
+    cfg_consume<B2>(with_one_row_tables(args.a[3], ort), p2, m.stages, m.full, m.empty, m.red,
+                    stage, pp, rp, kw, KW, lane);
+  }
+  trace_end(a0.trace, 3);
 }
 
 }  // namespace moe

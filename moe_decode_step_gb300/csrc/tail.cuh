@@ -32,9 +32,7 @@ struct TailArgs {
   float eps;
   unsigned long long* trace;  // optional kernel trace, or null
   // zeroed for the next forward once every earlier kernel of this one has
-  // finished: the route flag of one-row forwards, and the per-pair max |h|
-  // that FC1's epilogues raise
-  unsigned* route_flag;
+  // finished: the per-pair max |h| that FC1's epilogues raise
   unsigned* h_amax;           // [B*k]
 };
 
@@ -62,7 +60,6 @@ tail_kernel(const TailArgs a) {
   pdl_wait_prerequisites();
   if (blockIdx.x == 0 && blockIdx.y == 0) {
     for (int i = threadIdx.x; i < a.B * a.k; i += blockDim.x) a.h_amax[i] = 0u;
-    if (threadIdx.x == 0) *a.route_flag = 0u;
   }
   float z[4] = {0.f, 0.f, 0.f, 0.f};
   float yr[4] = {0.f, 0.f, 0.f, 0.f};

@@ -35,9 +35,9 @@ struct TopkArgs {
   int* pair_list;
   unsigned* h_amax;       // [B*k] reset to 0
   unsigned long long* trace;  // optional kernel trace, or null
-  unsigned* route_flag;   // if non-null: raised (release) once the tables are written, for a
-                          // kernel that streams routed weights before this one finishes
-  int skip_flag;          // failure-detection test hook: leave the flag down
+  unsigned* reset_counts; // if non-null: two done counters of the expert kernels, zeroed
+                          // (the router before this kernel ran alone: nothing of the
+                          // previous forward still reads them)
 };
 
 constexpr int kTopkThreads = 1024;
@@ -135,6 +135,7 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   const float bias = valid ? __ldg(a.bias + t) : 0.f;
   pdl_launch_dependents();
   pdl_wait_prerequisites();
+  if (a.reset_counts && b == 0 && t < 2) a.reset_counts[t] = 0u;
 
   // ---- scores and keys ----
   uint64_t key = 0ull;
@@ -191,11 +192,6 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
         *a.n_active = a.k;
         a.active_off[a.k] = a.k;
       }
-      if (a.route_flag && !a.skip_flag) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_u32(a.route_flag, 1u);
-      }
     }
   }
   if (gridDim.x == 1 && a.B == 1) {
@@ -246,15 +242,6 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
     *a.n_active = n_act;
     a.active_off[n_act] = total_pairs;
     if (gridDim.x > 1) *a.done = 0u;
-  }
-  if (a.route_flag && !a.skip_flag) {
-    // every thread's table stores are ordered before the flag by the barrier
-    // and the releasing thread's fence
-    __syncthreads();
-    if (t == 0) {
-      __threadfence();
-      st_release_u32(a.route_flag, 1u);
-    }
   }
   trace_end(a.trace, 1);
 }

@@ -125,7 +125,8 @@ def test_large_and_zero_rows_in_one_batch(path):
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_one_edge_row(path, kind):
     """One row alone: on the mma.sync path its own FC1 / FC2 configurations
-    (x operand and routing tables in shared memory, the route flag)."""
+    (x operand and routing tables in shared memory, FC1 and FC2 in one
+    launch)."""
     cfg = _cfg(TINY, 1)
     x, res, inp = _edge_inputs(cfg, [kind])
     ref = oracle.forward(inp)

@@ -187,9 +187,10 @@ def test_zero_down_weights_leave_rmsnorm_of_residual_plus_shared():
 
 
 def test_bounded_wait_expiry_reports_timeout_and_layer_recovers():
-    """Top-k leaves the one-row route flag down: FC2's producers wait 1 ms for
-    it, the wait expires, the forward completes, the status word reads
-    MOE_ERR_TIMEOUT; with the hook off the next forward passes parity."""
+    """One CTA of the one-row expert kernel does not arrive at the grid-wide
+    barrier between FC1 and FC2: every CTA's wait there expires after 1 ms,
+    the forward completes, the status word reads MOE_ERR_TIMEOUT; with the
+    hook off the next forward passes parity."""
     layer = synthetic.make_layer(TINY, max_batch=1, expert_path=1)
     cfg = tiny_cfg(1)
     inp = oracle.clean_inputs(cfg)
