@@ -156,9 +156,12 @@ int moe_decode_forward_debug(moe_layer_t layer, void* stream, const void* x, int
  * products it scales are below 6 * 2^-127 * |activation|.) */
 int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, float* out);
 
-/* Chain layers: while this layer's routed experts run, an L2-prefetch kernel on
- * a third stream touches `next`'s router and shared-expert weights.  next may be
- * NULL to switch it off.  Both handles must live on the same device. */
+/* Chain layers: once this layer's expert kernels have finished, an L2-prefetch
+ * kernel on a third stream pulls `next`'s router weights into L2 while this
+ * layer's tail runs (HBM is otherwise idle then), and the caller's stream
+ * waits for it after the tail, so the next layer's router reads them from L2.
+ * next may be NULL to switch it off.  Both handles must live on the same
+ * device. */
 int moe_set_prefetch_next(moe_layer_t layer, moe_layer_t next);
 
 /* Synchronise the layer's streams and report the device status word

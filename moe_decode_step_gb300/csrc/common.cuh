@@ -35,13 +35,17 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const uint8_t* p) {
   return v;
 }
 
-// Routing-table entries live either in global memory (written by an earlier
-// kernel, or published under a flag) or in the CTA's own shared memory (a
-// kernel that ran the top-k itself).  A generic relaxed load at GPU scope
-// reads either coherently (for global memory it bypasses L1, like ld.cg).
-__device__ __forceinline__ int ld_tab(const int* p) {
+// Routing-table entries live either in global memory (written by top-k, an
+// earlier kernel the reader has waited for) or in the CTA's shared memory (a
+// copy whose arrival the reader has waited for): either way final before the
+// read, so a plain generic load.
+__device__ __forceinline__ int ld_tab(const int* p) { return *p; }
+
+// A word other CTAs of the same launch wrote before a release the reader has
+// acquired: a relaxed load at GPU scope (bypasses a possibly stale L1 line).
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   int v;
-  asm volatile("ld.relaxed.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 

@@ -954,17 +954,20 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   return MOE_OK;
 }
 
-int launch_prefetch(moe_layer* L) {
+// The next layer's router weights into L2 on the third stream, from the end of
+// this layer's expert kernels: the tail reads a few hundred KB, so HBM is
+// otherwise idle then, while the next router (the first kernel of the next
+// forward, which waits for this prefetch) would stream its weights cold.
+// Prefetching more (the next shared expert) or earlier (while this layer's
+// experts stream) only competes with them for HBM.
+int launch_prefetch(moe_layer* L, cudaStream_t st) {
   moe_layer* n = L->next;
   if (!n) return MOE_OK;
   PrefetchArgs a{};
-  a.n = 3;
+  a.n = 1;
   a.ptr[0] = static_cast<const char*>(n->w.router_w);
   a.bytes[0] = (size_t)n->dims.n_experts * n->dims.d * 2;
-  a.ptr[1] = static_cast<const char*>(n->w.shared_gu);
-  a.bytes[1] = (size_t)2 * n->dims.f_shared * n->dims.d * 2;
-  a.ptr[2] = static_cast<const char*>(n->w.shared_d);
-  a.bytes[2] = (size_t)n->dims.d * n->dims.f_shared * 2;
+  MOE_CUDA(cudaEventRecord(L->ev_fork, st));
   MOE_CUDA(cudaStreamWaitEvent(L->pref, L->ev_fork, 0));
   l2_prefetch_kernel<<<L->n_sm, 256, 0, L->pref>>>(a);
   MOE_CUDA(cudaGetLastError());
@@ -991,12 +994,10 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
     MOE_CUDA(cudaMemsetAsync(L->ws.trace, 0xFF, 8 * sizeof(unsigned long long), st));
     MOE_CUDA(cudaMemsetAsync(L->ws.trace + 8, 0, 8 * sizeof(unsigned long long), st));
   }
-  MOE_CUDA(cudaEventRecord(L->ev_fork, st));
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
   const bool tc = use_tc(L, B);
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
-  if ((rc = launch_prefetch(L))) return rc;
   if (!tc && B == 1) {   // one launch for both expert steps
     if ((rc = launch_expert(L, st, x))) return rc;
     if (tm) MOE_CUDA(record_time(L, kTimeFc1End, st));
@@ -1007,8 +1008,10 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
     if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
     if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   }
-  if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));   // joins the third stream
+  if ((rc = launch_prefetch(L, st))) return rc;
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
+  // the next forward on this stream starts after the prefetch (joins the third stream)
+  if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));
   if (tm) {
     MOE_CUDA(record_time(L, kTimeTailEnd, st));
     L->timed_once = true;

@@ -719,8 +719,10 @@ __device__ __forceinline__ void stream_consume_run_mma(
     xshift = eshift;
   } else {
     // h rows (fp32): the shift comes from FC1's per-pair max |h|
-    const int cshift = f16_shift_for_amax(__int_as_float(ld_tab(reinterpret_cast<const int*>(a.h_amax) + cpid)));
-    eshift = f16_shift_for_amax(__int_as_float(ld_tab(reinterpret_cast<const int*>(a.h_amax) + epid)));
+    const int cshift = f16_shift_for_amax(
+        __int_as_float(ld_relaxed_gpu(reinterpret_cast<const int*>(a.h_amax) + cpid)));
+    eshift = f16_shift_for_amax(
+        __int_as_float(ld_relaxed_gpu(reinterpret_cast<const int*>(a.h_amax) + epid)));
     const float sc = pow2f(-cshift);
     const float* hr = a.h + (size_t)cpid * a.K + 8 * t;
 #pragma unroll
