@@ -391,24 +391,26 @@ def percentile(v, q):
 
 def time_e2e(layer, cfg, x, res0, steps, warmup, flush):
     """The same layer through the host-buffer entry point: H2D of x and the
-    residual, forward, D2H of residual and out, stream sync, per step."""
+    residual, forward, D2H of residual and out, stream sync, per step, on a
+    stream of the caller's with pinned buffers (the entry point's graph path)."""
     import torch
     xh = x.cpu().pin_memory()
     r0 = res0.cpu()
     rh = torch.empty_like(r0).pin_memory()
     oh = torch.empty_like(r0).pin_memory()
+    st = torch.cuda.Stream()
     for _ in range(warmup):
         rh.copy_(r0)
         flush()
         torch.cuda.synchronize()
-        layer.forward_host(xh, rh, oh)
+        layer.forward_host(xh, rh, oh, stream=st)
     times = []
     for i in range(steps):
         rh.copy_(r0)
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        layer.forward_host(xh, rh, oh)
+        layer.forward_host(xh, rh, oh, stream=st)
         times.append((time.perf_counter() - t0) * 1e6)
     nbytes = x.numel() * 2
     return times, 2 * nbytes, 2 * nbytes

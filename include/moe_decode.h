@@ -74,7 +74,9 @@ typedef struct moe_layer* moe_layer_t;
  * copies of those weights in 128-row tiles that the handle owns (2 * (3 * d *
  * f_shared + 128 * ceil(E / 128) * d) bytes of extra device memory).  0
  * (default): the layer keeps both and takes path 1 for B = 1 and path 2 for
- * B >= 2.  All give results within the same tolerance of the exact layer.
+ * B >= 2, or only path 1 when max_batch is 1 (one copy of the expert bytes
+ * instead of two).  All give results within the same tolerance of the exact
+ * layer.
  *
  * mxfp4_layout says how the caller's expert weights are laid out: 0
  * (canonical), 1 (tiled: FC1 layout 2, FC2 layout 1) or 3 (UMMA: FC1 layout 4,
@@ -136,7 +138,12 @@ int moe_decode_forward(moe_layer_t layer, void* stream, const void* x, int B, vo
  * `stream`, runs moe_decode_forward on the handle's own device staging
  * buffers, copies residual and out back, and synchronises `stream` before
  * returning.  x_host, residual_host, out_host: host bf16 [B][d] (pinned memory
- * gives asynchronous copies; pageable memory works but copies synchronously). */
+ * gives asynchronous copies; pageable memory works but copies synchronously).
+ * With pinned buffers and a stream other than the legacy default stream, the
+ * first call captures the copies and the kernels as one CUDA graph, which
+ * later calls with the same buffers, B and stream replay (one launch per call;
+ * changing any of them captures again).  Overlapping calls on one layer race,
+ * as for moe_decode_forward. */
 int moe_decode_forward_host(moe_layer_t layer, void* stream, const void* x_host, int B,
                             void* residual_host, void* out_host);
 

@@ -161,6 +161,18 @@ struct moe_layer {
   void* encode_tiled = nullptr;   // the driver's tensor-map encoder
   // failure-detection test hook (moe_debug_set_fault)
   int debug_fault = 0;
+  // moe_decode_forward_host: the host-buffer forward captured as one CUDA graph
+  // (copies and kernels), reused while these arguments stay the same
+  struct HostGraph {
+    cudaGraphExec_t exec = nullptr;
+    cudaStream_t stream = nullptr;
+    const void* x = nullptr;
+    void *res = nullptr, *out = nullptr;
+    int B = 0, fault = 0;
+    unsigned long long fault_ns = 0;
+    bool timing = false, tracing = false;
+    moe_layer* next = nullptr;
+  } hg;
   unsigned long long debug_wait_ns = 0;
 };
 
@@ -575,6 +587,14 @@ bool use_tc(const moe_layer* L, int B) { return L->wt.ok && (!L->wm.ok || B >= L
 
 int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B);
 
+// Rows from which the tensor-core path computes the router logits on the
+// tensor cores too (one dense pass whatever the batch) rather than with the
+// CUDA-core GEMV (passes of 4 rows): measured at B = 16, 17 against 27 us for
+// the router; at B = 64 the dense pass is faster.
+#ifndef MOE_TC_ROUTER_MIN_B
+#define MOE_TC_ROUTER_MIN_B 25
+#endif
+
 int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* idx, float* w) {
   const moe_dims_t& d = L->dims;
   StreamArgs a = base_args(L);
@@ -586,10 +606,10 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
   a.out = L->ws.logits;
   a.trace_id = 0;
   int rc;
-  if (use_tc(L, B) && batch_class(B) == 2) {
-    // above 8 rows the CUDA-core router is compute-bound (passes of 4 rows):
-    // logits on the tensor cores, plus the activation planes the tensor-core
-    // FC1 streams
+  if (use_tc(L, B) && batch_class(B) == 2 && B >= MOE_TC_ROUTER_MIN_B) {
+    // from MOE_TC_ROUTER_MIN_B rows the CUDA-core router is compute-bound
+    // (passes of 4 rows): logits on the tensor cores, plus the activation
+    // planes the tensor-core FC1 streams
     if ((rc = launch_router_tc(L, st, x, B))) return rc;
   } else {
     if (use_tc(L, B)) {   // the activation planes the tensor-core FC1 streams
@@ -1190,8 +1210,9 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
   // the expert paths kept (both by default, see kTcMinBatch) fix the layouts
-  // the kernels read
-  const int path = dims->expert_path;
+  // the kernels read; a layer that only ever sees one row keeps one
+  const int path = (dims->expert_path == kPathAuto && dims->max_batch == 1) ? kPathMmaSync
+                                                                            : dims->expert_path;
   if (path != kPathTc && (rc = setup_weights(L, w, 1, L->wm))) {
     moe_layer_destroy(L);
     return rc;
@@ -1216,6 +1237,7 @@ int moe_layer_destroy(moe_layer_t L) {
   cudaGetDevice(&prev);
   cudaSetDevice(L->device);
   cudaDeviceSynchronize();
+  if (L->hg.exec) cudaGraphExecDestroy(L->hg.exec);
   if (L->pref) cudaStreamDestroy(L->pref);
   if (L->ev_fork) cudaEventDestroy(L->ev_fork);
   if (L->ev_pref) cudaEventDestroy(L->ev_pref);
@@ -1250,18 +1272,85 @@ int moe_decode_forward_debug(moe_layer_t L, void* stream, const void* x, int B, 
                       y_shared, h, z, out_f32);
 }
 
+namespace {
+
+// The host-buffer forward's work on `st`: the two input copies into the
+// workspace staging buffers, the forward, the two output copies.
+int enqueue_forward_host(moe_layer* L, cudaStream_t st, const void* x_host, int B,
+                         void* residual_host, void* out_host) {
+  const size_t bytes = (size_t)B * L->dims.d * 2;
+  MOE_CUDA(cudaMemcpyAsync(L->ws.x_stage, x_host, bytes, cudaMemcpyHostToDevice, st));
+  MOE_CUDA(cudaMemcpyAsync(L->ws.res_stage, residual_host, bytes, cudaMemcpyHostToDevice, st));
+  int rc = forward_impl(L, st, L->ws.x_stage, B, L->ws.res_stage, L->ws.out_stage, nullptr,
+                        nullptr, nullptr, nullptr, nullptr);
+  if (rc) return rc;
+  MOE_CUDA(cudaMemcpyAsync(residual_host, L->ws.res_stage, bytes, cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaMemcpyAsync(out_host, L->ws.out_stage, bytes, cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+bool pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
 int moe_decode_forward_host(moe_layer_t L, void* stream, const void* x_host, int B,
                             void* residual_host, void* out_host) {
   if (!L || !x_host || !residual_host || !out_host) return MOE_ERR_INVALID_ARG;
   if (B < 1 || B > L->dims.max_batch) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = (size_t)B * L->dims.d * 2;
-  MOE_CUDA(cudaMemcpyAsync(L->ws.x_stage, x_host, bytes, cudaMemcpyHostToDevice, st));
-  MOE_CUDA(cudaMemcpyAsync(L->ws.res_stage, residual_host, bytes, cudaMemcpyHostToDevice, st));
-  int rc = moe_decode_forward(L, stream, L->ws.x_stage, B, L->ws.res_stage, L->ws.out_stage);
-  if (rc) return rc;
-  MOE_CUDA(cudaMemcpyAsync(residual_host, L->ws.res_stage, bytes, cudaMemcpyDeviceToHost, st));
-  MOE_CUDA(cudaMemcpyAsync(out_host, L->ws.out_stage, bytes, cudaMemcpyDeviceToHost, st));
+  // Pinned buffers on a stream of the caller's: one CUDA graph of the copies
+  // and the kernels, captured on first use and replayed while the arguments
+  // (and the layer's timing, trace, prefetch and test-hook settings) stay the
+  // same, so a call costs one graph launch and the sync instead of nine
+  // enqueues.  Otherwise (the legacy default stream, pageable memory) the
+  // same work is enqueued call by call.
+  if (st == nullptr || !pinned(x_host) || !pinned(residual_host) || !pinned(out_host)) {
+    int rc = enqueue_forward_host(L, st, x_host, B, residual_host, out_host);
+    if (rc) return rc;
+    MOE_CUDA(cudaStreamSynchronize(st));
+    return MOE_OK;
+  }
+  moe_layer::HostGraph& g = L->hg;
+  const bool same = g.exec && g.stream == st && g.x == x_host && g.res == residual_host &&
+                    g.out == out_host && g.B == B && g.timing == L->timing &&
+                    g.tracing == L->tracing && g.next == L->next && g.fault == L->debug_fault &&
+                    g.fault_ns == L->debug_wait_ns;
+  if (!same) {
+    if (g.exec) {
+      MOE_CUDA(cudaGraphExecDestroy(g.exec));
+      g.exec = nullptr;
+    }
+    MOE_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    const int rc = enqueue_forward_host(L, st, x_host, B, residual_host, out_host);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    MOE_CUDA(ec);
+    const cudaError_t ei = cudaGraphInstantiate(&g.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    MOE_CUDA(ei);
+    g.stream = st;
+    g.x = x_host;
+    g.res = residual_host;
+    g.out = out_host;
+    g.B = B;
+    g.timing = L->timing;
+    g.tracing = L->tracing;
+    g.next = L->next;
+    g.fault = L->debug_fault;
+    g.fault_ns = L->debug_wait_ns;
+  }
+  MOE_CUDA(cudaGraphLaunch(g.exec, st));
   MOE_CUDA(cudaStreamSynchronize(st));
   return MOE_OK;
 }

@@ -614,7 +614,9 @@ template <bool ONE, int NQ, bool GUARD>
 __device__ __forceinline__ void mx_group_run_xs(const uint8_t* nib, const uint8_t* scl,
                                                 const uint4* xs, int nb, float& c0, float& c1,
                                                 float& c2, float& c3) {
-#pragma unroll
+  // not unrolled: four blocks (eight MMAs) per iteration already overlap, and
+  // the shorter loop body leaves the kernel's code and registers smaller
+#pragma unroll 1
   for (int q = 0; q < NQ; ++q) {
     if (GUARD && 4 * q >= nb) break;
     const uint2 sv = *reinterpret_cast<const uint2*>(scl + q * 64);

@@ -225,18 +225,20 @@ static __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const Topk
   int total_pairs, n_act;
   const int off = block_exclusive_scan(cnt, s_warp, &total_pairs);
   const int slot = block_exclusive_scan(cnt > 0 ? 1 : 0, s_warp, &n_act);
+  // each expert's first pair position (the scores are no longer needed)
+  int* s_off = reinterpret_cast<int*>(s_sc);
+  if (valid) s_off[t] = off;
   if (cnt > 0) {
     a.active_expert[slot] = t;
     a.active_off[slot] = off;
-    unsigned long long mm = mask;
-    int pos = off;
-    while (mm) {
-      const int row = __ffsll((long long)mm) - 1;
-      mm &= mm - 1;
-      int j = 0;
-      while (j < a.k && s_idx[row * a.k + j] != t) ++j;
-      a.pair_list[pos++] = row * a.k + j;
-    }
+  }
+  __syncthreads();
+  // pair p = row * k + j goes to its expert's list at the rank of its row
+  // among the expert's rows (ascending)
+  for (int p = t; p < P; p += blockDim.x) {
+    const int e = s_idx[p], row = p / a.k;
+    const unsigned long long below = (1ull << row) - 1ull;
+    a.pair_list[s_off[e] + __popcll(s_mask[e] & below)] = p;
   }
   if (t == 0) {
     *a.n_active = n_act;

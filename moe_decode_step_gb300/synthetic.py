@@ -76,9 +76,12 @@ def make_activations(cfg, layer=0, attempt=0, device="cuda", B=None):
 
 
 def make_layer(cfg, layer=0, device="cuda", max_batch=None, weights=None, expert_path=0):
+    mb = max_batch if max_batch is not None else max(cfg.B, 1)
+    # the layouts the layer reads in place: the tiled ones when it only runs
+    # the mma.sync path (expert_path 1, or the default with max_batch 1)
+    tiled = expert_path == 1 or (expert_path == 0 and mb == 1)
     w = weights if weights is not None else make_weights(
-        cfg, layer, device, layout=1 if expert_path == 1 else 3)
-    return MoELayer(cfg.d, cfg.f, cfg.n_experts, cfg.top_k, cfg.f_shared,
-                    max_batch if max_batch is not None else max(cfg.B, 1), w,
+        cfg, layer, device, layout=1 if tiled else 3)
+    return MoELayer(cfg.d, cfg.f, cfg.n_experts, cfg.top_k, cfg.f_shared, mb, w,
                     routed_scale=cfg.routed_scale, rms_eps=cfg.rms_eps,
                     expert_path=expert_path)

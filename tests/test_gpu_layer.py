@@ -153,6 +153,28 @@ def test_host_buffer_entry_matches_device_entry(tiny_layer):
     assert torch.equal(rh.view(torch.int16), r_d.cpu().view(torch.int16))
 
 
+def test_host_entry_graph_replay_and_recapture(tiny_layer):
+    """On a stream of the caller's with pinned buffers the host entry captures
+    one CUDA graph and replays it; new buffers or a new B capture again."""
+    st = torch.cuda.Stream()
+    for B in (5, 5, 3):
+        cfg = tiny_cfg(B)
+        x, res = synthetic.make_activations(cfg)
+        r_d = res.clone()
+        o_d = tiny_layer.forward(x, r_d)
+        torch.cuda.synchronize()
+        xh = x.cpu().pin_memory()
+        rh = torch.empty_like(res, device="cpu").pin_memory()
+        oh = torch.empty_like(rh).pin_memory()
+        for rep in range(2):   # the second call replays the graph the first captured
+            rh.copy_(res.cpu())
+            oh.zero_()
+            tiny_layer.forward_host(xh, rh, oh, stream=st)
+            assert torch.equal(oh.view(torch.int16), o_d.cpu().view(torch.int16))
+            assert torch.equal(rh.view(torch.int16), r_d.cpu().view(torch.int16))
+    assert tiny_layer.status() == 0
+
+
 def test_batch_outside_range_is_unsupported(tiny_layer):
     x = torch.zeros((65, 1024), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(M.MoEError) as e:
