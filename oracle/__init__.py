@@ -42,6 +42,14 @@ def lib():
         L.oracle_block_exponent.restype = ctypes.c_int
         L.oracle_mxfp4_pack.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, _P, _P]
         L.oracle_mxfp4_dequant.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int64, _P]
+        L.oracle_e4m3_value.argtypes = [ctypes.c_int]
+        L.oracle_e4m3_value.restype = ctypes.c_double
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        L.oracle_e4m3_encode.restype = ctypes.c_int
+        L.oracle_block_exponent_e4m3.argtypes = [_P]
+        L.oracle_block_exponent_e4m3.restype = ctypes.c_int
+        L.oracle_mxfp8_quant_row.argtypes = [_P, ctypes.c_int64, _P, _P]
+        L.oracle_mxfp8_dequant_row.argtypes = [_P, _P, ctypes.c_int64, _P]
         L.oracle_sigmoid.argtypes = [ctypes.c_double]
         L.oracle_sigmoid.restype = ctypes.c_double
         L.oracle_swiglu.argtypes = [ctypes.c_double, ctypes.c_double]
@@ -114,6 +122,51 @@ def mxfp4_dequant(q, s):
     out = np.empty((rows, half * 2), np.float64)
     lib().oracle_mxfp4_dequant(_p(q), _p(s), rows, half * 2, _p(out))
     return out
+
+
+# --------------------------------------------------------------------------
+# MXFP8 activations (OCP MX v1.0: E4M3 elements, E8M0 scale per 32 elements)
+# --------------------------------------------------------------------------
+def e4m3_value(code):
+    return lib().oracle_e4m3_value(int(code))
+
+
+def e4m3_encode(t):
+    return lib().oracle_e4m3_encode(float(t))
+
+
+def block_exponent_e4m3(block32):
+    b = _c(block32, np.float64)
+    assert b.size == 32
+    return lib().oracle_block_exponent_e4m3(_p(b))
+
+
+def mxfp8_quant(a):
+    """a [rows, k] (k a multiple of 32) -> (q uint8 [rows, k] E4M3 codes,
+    s uint8 [rows, k/32] E8M0 scale bytes)."""
+    a = _c(np.atleast_2d(a), np.float64)
+    rows, k = a.shape
+    assert k % 32 == 0
+    q = np.empty((rows, k), np.uint8)
+    s = np.empty((rows, k // 32), np.uint8)
+    for r in range(rows):
+        lib().oracle_mxfp8_quant_row(_p(a[r]), k, _p(q[r]), _p(s[r]))
+    return q, s
+
+
+def mxfp8_dequant(q, s):
+    q = _c(np.atleast_2d(q), np.uint8)
+    s = _c(np.atleast_2d(s), np.uint8)
+    rows, k = q.shape
+    out = np.empty((rows, k), np.float64)
+    for r in range(rows):
+        lib().oracle_mxfp8_dequant_row(_p(q[r]), _p(s[r]), k, _p(out[r]))
+    return out
+
+
+def mxfp8_round(a):
+    """The values an MXFP8 activation operand carries for a (rows, k)."""
+    return mxfp8_dequant(*mxfp8_quant(a))
 
 
 def round_bf16(a):
@@ -263,13 +316,20 @@ def route(inp):
     return router(inp.x, inp.wr, inp.bias, c.top_k, c.routed_scale)
 
 
-def forward(inp, rows=None, timings=None):
+def forward(inp, rows=None, timings=None, act="exact"):
     """Run the layer for the given rows (default all) of `inp`.
+
+    act="exact": the routed experts multiply the MXFP4 weights by x and h as
+    they are (bf16 x, fp64 h).  act="mxfp8": by their MXFP8 roundings (OCP MX
+    v1.0 E4M3 elements with one E8M0 scale per 32 along K, mxfp8_round), the
+    FP4 x MXFP8 products of the pages' routed-expert kernel; the shared
+    expert, router and tail are the same in both.
 
     Returns a dict with idx, w, gap, logits, h [B,k,f], y_pair [B,k,d], y_r,
     h_s, y_s, z, out (all fp64, pre-rounding) and residual_bf16 / out_bf16.
     Rows outside `rows` are left as NaN in the per-row outputs.
     """
+    assert act in ("exact", "mxfp8")
     c = inp.cfg
     B = c.B
     rows = list(range(B)) if rows is None else sorted(rows)
@@ -290,8 +350,10 @@ def forward(inp, rows=None, timings=None):
         t_pack += time.perf_counter() - tp
         pairs = by_expert[e]
         xr = inp.x[[b for b, _ in pairs]]
+        if act == "mxfp8":
+            xr = mxfp8_round(xr)
         he = mxfp4_fc1(q_gu, s_gu, xr)
-        ye = mxfp4_fc2(q_d, s_d, he)
+        ye = mxfp4_fc2(q_d, s_d, mxfp8_round(he) if act == "mxfp8" else he)
         for t, (b, j) in enumerate(pairs):
             h[b, j] = he[t]
             y_pair[b, j] = ye[t]

@@ -163,6 +163,72 @@ void oracle_mxfp4_dequant(const uint8_t* q, const uint8_t* s, int64_t rows, int6
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8 activations (OCP Microscaling Formats (MX) v1.0, E4M3 elements, one   */
+/* E8M0 scale per 32 contiguous elements): the pages' routed experts multiply  */
+/* FP4 weights by MXFP8 activations ("Kimi K3 on GB300", "Why batch 1 on a     */
+/* rack is not only a bandwidth problem").                                     */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3 (the OFP8 "E4M3FN" encoding the MX spec uses): bit 7 sign, bits 6..3
+ * exponent (bias 7), bits 2..0 mantissa; no infinities; S.1111.111 is NaN.
+ * Exponent field 0 is subnormal: value = 2^-6 * m/8.  Otherwise
+ * value = 2^(e-7) * (1 + m/8).  Largest finite magnitude 448 (S.1111.110). */
+double oracle_e4m3_value(int code) {
+  const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* Nearest finite E4M3 value to t; at a tie the even code (mantissa bit 0
+ * clear) wins; magnitudes past 448 land on 448 (saturation).  The sign bit is
+ * the sign bit of t (a negative value that rounds to zero encodes as -0). */
+int oracle_e4m3_encode(double t) {
+  const int sign = signbit(t) ? 0x80 : 0;
+  const double a = fabs(t);
+  int best = 0;
+  double bestd = INFINITY;
+  for (int c = 0; c < 0x7F; ++c) {   /* 0x7F is NaN */
+    const double dist = fabs(a - oracle_e4m3_value(c));
+    if (dist < bestd || (dist == bestd && (c % 2) == 0)) { best = c; bestd = dist; }
+  }
+  return sign | best;
+}
+
+/* Scale exponent of one 32-element activation block: floor(log2 amax) - 8
+ * (8 = exponent of the largest power of two E4M3 holds, 256), clamped to
+ * [-127, 127]; an all-zero block takes -127 (scale byte 0). */
+int oracle_block_exponent_e4m3(const double* v) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) {
+    const double a = fabs(v[i]);
+    if (a > amax) amax = a;
+  }
+  if (amax == 0.0) return -127;
+  int ex;
+  frexp(amax, &ex);               /* amax = m * 2^ex, m in [0.5, 1) */
+  int e = (ex - 1) - 8;           /* floor(log2 amax) - 8 */
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+/* One row of k values (k a multiple of 32) to E4M3 codes q[k] and E8M0 scale
+ * bytes s[k/32]: element = nearest E4M3 of v / 2^e (saturating). */
+void oracle_mxfp8_quant_row(const double* v, int64_t k, uint8_t* q, uint8_t* s) {
+  for (int64_t b = 0; b < k / 32; ++b) {
+    const int e = oracle_block_exponent_e4m3(v + b * 32);
+    s[b] = (uint8_t)(e + 127);
+    for (int i = 0; i < 32; ++i) q[b * 32 + i] = (uint8_t)oracle_e4m3_encode(ldexp(v[b * 32 + i], -e));
+  }
+}
+
+/* v_hat[j] = E4M3(q[j]) * E8M0(s[j/32]). */
+void oracle_mxfp8_dequant_row(const uint8_t* q, const uint8_t* s, int64_t k, double* out) {
+  for (int64_t j = 0; j < k; ++j) out[j] = oracle_e4m3_value(q[j]) * oracle_e8m0_value(s[j / 32]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Scalar pieces.                                                              */
 /* ------------------------------------------------------------------------ */
 double oracle_sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
