@@ -523,6 +523,19 @@ def run_ours(args, rank, world, local):
 
     e2e_times, h2d, d2h = time_e2e(layer, cfg, x, res0, max(5, args.steps // 2),
                                    max(3, args.warmup), flush)
+    # f1: the routed experts on MXFP8 activations (the pages' FP4 x MXFP8
+    # products), same layer and timing; one row on the mma.sync path only
+    f1 = None
+    if cfg.B == 1 and fused:
+        layer.set_act_format(1)
+        f1_times, _ = time_layer(layer, x, res0, args.steps, args.warmup, flush, graph=True,
+                                 timing=False)
+        layer.set_act_format(0)
+        f1_us = reduce_max(statistics.median(f1_times), world, dev)
+        f1 = {"us": f1_us, "p10_us": percentile(f1_times, 10), "steps": args.steps,
+              "frac_of_peak": btouch / f1_us / 1e3 / peak,
+              "activations": "x and h rounded to MXFP8 (E4M3, one E8M0 scale per 32) before "
+                             "the MXFP4 products; parity against the oracle's mxfp8 mode"}
     e2e_us = reduce_max(statistics.median(e2e_times), world, dev)
     launches = layer.launches_per_forward(cfg.B) * args.steps
     layer.close()
@@ -633,6 +646,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "f1_mxfp8": f1,
         "batches": batches,
         "chain": chain,
         "wall_s": wall,

@@ -163,6 +163,19 @@ int moe_decode_forward_debug(moe_layer_t layer, void* stream, const void* x, int
  * products it scales are below 6 * 2^-127 * |activation|.) */
 int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, float* out);
 
+/* Activation format of the routed experts' products (the pages' routed-expert
+ * kernel multiplies FP4 weights by MXFP8 activations: "Kimi K3 on GB300: 13
+ * kernels a layer", "Why batch 1 on a rack is not only a bandwidth problem").
+ * fmt 0 (default): x (bf16) and h (fp32) as they are, the exact layer within
+ * the stated tolerance.  fmt 1: x and h rounded to MXFP8 (OCP MX v1.0: E4M3
+ * elements, nearest with ties to even and saturation at 448, one E8M0 scale
+ * 2^(floor(log2 max|v|) - 8) per 32 contiguous elements) before they meet the
+ * MXFP4 weights, E4M3 x E4M3 tensor-core products; the router, shared expert
+ * and tail are unchanged.  fmt 1 runs one row on the mma.sync path only: a
+ * forward with B > 1 (or a layer without the mma.sync path's layouts) returns
+ * MOE_ERR_UNSUPPORTED.  Errors: INVALID_ARG, UNSUPPORTED. */
+int moe_set_act_format(moe_layer_t layer, int fmt);
+
 /* Chain layers: once this layer's expert kernels have finished, an L2-prefetch
  * kernel on a third stream pulls `next`'s router weights into L2 while this
  * layer's tail runs (HBM is otherwise idle then), and the caller's stream

@@ -161,6 +161,11 @@ class MoELayer:
         check(lib().moe_layer_status(self._h, ctypes.byref(v)), "moe_layer_status")
         return v.value
 
+    def set_act_format(self, fmt):
+        """Routed experts' activations: 0 exact (default), 1 MXFP8 (one row on
+        the mma.sync path; see moe_set_act_format)."""
+        check(lib().moe_set_act_format(self._h, int(fmt)), "moe_set_act_format")
+
     def debug_set_fault(self, fault, wait_ns=0):
         """Failure-detection test hook (see moe_debug_set_fault): fault 1 makes
         the one-row expert kernel's grid-wide barrier wait expire after

@@ -59,6 +59,7 @@ _PROTOS = {
     "moe_layer_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),
     "moe_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_debug_set_fault": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_ulonglong]),
+    "moe_set_act_format": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_get_timing": (ctypes.c_int, [_P, _P, ctypes.c_int]),
     "moe_launches_per_forward": (ctypes.c_int, [_P, ctypes.c_int]),
     "moe_set_trace": (ctypes.c_int, [_P, ctypes.c_int]),

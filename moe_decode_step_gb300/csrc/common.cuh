@@ -172,6 +172,57 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
 // 2^e for integer e in [-126, 127].
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
+// ---- MXFP8 activations (OCP MX v1.0: E4M3 elements, one E8M0 scale per 32)
+
+// Scale exponent of a block of activations with maximum magnitude amax:
+// floor(log2 amax) - 8 (8: the exponent of 256, E4M3's largest power of two),
+// -127 for amax 0 or subnormal (where the clamp to [-127, 127] lands anyway).
+__device__ __forceinline__ int e4m3_block_exp(float amax) {
+  const int be = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  return be == 0 ? -127 : max(-127, be - 127 - 8);
+}
+
+// 2^e for e in [-127, 127], exactly (2^-127 is a subnormal float).
+__device__ __forceinline__ float pow2_e8m0(int e) {
+  return e == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// Two floats (already divided by their block scale) to their nearest E4M3
+// values: cvt.rn.satfinite.e4m3x2.f32 (nearest, ties to even, magnitudes past
+// 448 saturating: the OCP MX conversion with clamping), then back through
+// cvt.rn.f16x2.e4m3x2 (exact).
+__device__ __forceinline__ void e4m3x2_round(float& a, float& b) {
+  float ra, rb;
+  asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c, %3, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
+      "mov.b32 {lo, hi}, h;\n\t"
+      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a), "f"(b));
+  a = ra;
+  b = rb;
+}
+
+// MXFP8 rounding of one 32-element block held by a lane quad (lanes 4g..4g+3,
+// 8 elements each; every lane of the warp takes part): scale 2^e with
+// e = floor(log2 max |v|) - 8 over the block (e4m3_block_exp), each element
+// replaced by its nearest E4M3 value times 2^e.  Exact in fp32.
+__device__ __forceinline__ void mxfp8_round8(float4& v0, float4& v1) {
+  float mx = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                   fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const int e = e4m3_block_exp(mx);
+  const float inv = pow2_e8m0(-e), sc = pow2_e8m0(e);
+  float f[8] = {v0.x * inv, v0.y * inv, v0.z * inv, v0.w * inv,
+                v1.x * inv, v1.y * inv, v1.z * inv, v1.w * inv};
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) e4m3x2_round(f[j], f[j + 1]);
+  v0 = make_float4(f[0] * sc, f[1] * sc, f[2] * sc, f[3] * sc);
+  v1 = make_float4(f[4] * sc, f[5] * sc, f[6] * sc, f[7] * sc);
+}
+
 // Exponent shift that keeps |v| <= amax below 2^15 after scaling by 2^-shift,
 // so f16 (max 65504) never overflows: 0 for amax < 2^15.
 __device__ __forceinline__ int f16_shift_for_amax(float amax) {

@@ -161,6 +161,7 @@ struct moe_layer {
   void* encode_tiled = nullptr;   // the driver's tensor-map encoder
   // failure-detection test hook (moe_debug_set_fault)
   int debug_fault = 0;
+  int act_fmt = 0;   // routed experts' activations: 0 exact, 1 MXFP8 (moe_set_act_format)
   // moe_decode_forward_host: the host-buffer forward captured as one CUDA graph
   // (copies and kernels), reused while these arguments stay the same
   struct HostGraph {
@@ -274,6 +275,15 @@ using Fc1OneRowCfg = StreamCfg<kWfMx, true, false, true, 8 * MOE_FC1_TM_B1, 8 * 
 // One row, both expert steps in one launch (FC1's and FC2's configurations).
 #define MOE_EXPERT_KERNEL(NBM) \
   stream_expert_kernel<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<NBM, MOE_FC2_TM(1), 1>>
+// The same with MXFP8 activations (moe_set_act_format): x and h rounded to
+// E4M3 with one E8M0 scale per 32 elements, then the same f16 MMAs.
+using Fc1OneRowCfgF8 = StreamCfg<kWfMx, true, false, true, 8 * MOE_FC1_TM_B1, 8 * MOE_FC1_TM_B1, 1,
+                                 true, MOE_FC1_TM_B1, 16, 8, 4, true, true>;
+template <int NBM, int TM>
+using Fc2CfgF8 = StreamCfg<kWfMx, false, true, true, 16 * TM, 16 * TM, 1, true, TM, NBM, 8, 4,
+                           false, true>;
+#define MOE_EXPERT_KERNEL_F8(NBM) \
+  stream_expert_kernel<Sh1Cfg<1>, Fc1OneRowCfgF8, Sh2Cfg<1>, Fc2CfgF8<NBM, MOE_FC2_TM(1)>>
 // Tensor-core path: FC1 streams the shared gate/up first (while top-k runs),
 // FC2 the shared down first (its weights requested before FC1 is waited for).
 #define MOE_TC1_KERNEL tc_kernel<true>
@@ -515,12 +525,18 @@ int plan_all(moe_layer* L) {
   MOE_PLAN((plan_fc2<1>(L, d, n, &L->plan[kStepFc2][0])));
   MOE_PLAN((plan_fc2<2>(L, d, n, &L->plan[kStepFc2][1])));
   MOE_PLAN((plan_fc2<4>(L, d, n, &L->plan[kStepFc2][2])));
+  // the fused one-row kernel: [0] exact activations, [1] MXFP8 activations
+  const int bud1 = std::max(kBudget1, L->smem_optin);
   if (fc2_small(d)) {
     MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<4, MOE_FC2_TM(1), 1>>(
-        MOE_EXPERT_KERNEL(4), d, n, std::max(kBudget1, L->smem_optin), &L->plan[kStepExpert][0])));
+        MOE_EXPERT_KERNEL(4), d, n, bud1, &L->plan[kStepExpert][0])));
+    MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfgF8, Sh2Cfg<1>, Fc2CfgF8<4, MOE_FC2_TM(1)>>(
+        MOE_EXPERT_KERNEL_F8(4), d, n, bud1, &L->plan[kStepExpert][1])));
   } else {
     MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfg, Sh2Cfg<1>, Fc2Cfg<12, MOE_FC2_TM(1), 1>>(
-        MOE_EXPERT_KERNEL(12), d, n, std::max(kBudget1, L->smem_optin), &L->plan[kStepExpert][0])));
+        MOE_EXPERT_KERNEL(12), d, n, bud1, &L->plan[kStepExpert][0])));
+    MOE_PLAN((plan_expert<Sh1Cfg<1>, Fc1OneRowCfgF8, Sh2Cfg<1>, Fc2CfgF8<12, MOE_FC2_TM(1)>>(
+        MOE_EXPERT_KERNEL_F8(12), d, n, bud1, &L->plan[kStepExpert][1])));
   }
 #undef MOE_PLAN
   return MOE_OK;
@@ -890,7 +906,8 @@ int launch_fc2(moe_layer* L, cudaStream_t st, int B) {
 // build them.
 int launch_expert(moe_layer* L, cudaStream_t st, const void* x) {
   const moe_dims_t& d = L->dims;
-  const StreamPlan& p = L->plan[kStepExpert][0];
+  const bool f8 = L->act_fmt == 1;
+  const StreamPlan& p = L->plan[kStepExpert][f8 ? 1 : 0];
   StreamArgs4 g;
   std::memset(&g, 0, sizeof(g));
   StreamArgs& s1 = g.a[0];
@@ -943,12 +960,17 @@ int launch_expert(moe_layer* L, cudaStream_t st, const void* x) {
   r1.kc = p.kc;
   r2.kc = p.kc2;
   g.skip_count = L->debug_fault == 1;
-  if (fc2_small(d))
-    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(4), dim3(p.grid), dim3(p.threads), (size_t)p.smem, st,
-                       true, g));
-  else
-    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(12), dim3(p.grid), dim3(p.threads), (size_t)p.smem, st,
-                       true, g));
+  const dim3 grid(p.grid), block(p.threads);
+  if (f8) {
+    if (fc2_small(d))
+      MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL_F8(4), grid, block, (size_t)p.smem, st, true, g));
+    else
+      MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL_F8(12), grid, block, (size_t)p.smem, st, true, g));
+  } else if (fc2_small(d)) {
+    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(4), grid, block, (size_t)p.smem, st, true, g));
+  } else {
+    MOE_CUDA(launch_ex(MOE_EXPERT_KERNEL(12), grid, block, (size_t)p.smem, st, true, g));
+  }
   return MOE_OK;
 }
 
@@ -1010,12 +1032,13 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (!residual || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(residual) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   const bool tm = L->timing;
+  const bool tc = use_tc(L, B);
+  if (L->act_fmt == 1 && (B != 1 || tc)) return MOE_ERR_UNSUPPORTED;   // one row, mma.sync
   if (L->tracing) {
     MOE_CUDA(cudaMemsetAsync(L->ws.trace, 0xFF, 8 * sizeof(unsigned long long), st));
     MOE_CUDA(cudaMemsetAsync(L->ws.trace + 8, 0, 8 * sizeof(unsigned long long), st));
   }
   if (tm) MOE_CUDA(record_time(L, kTimeRouterStart, st));
-  const bool tc = use_tc(L, B);
   if ((rc = launch_router(L, st, x, B, L->ws.topk_idx, L->ws.topk_w))) return rc;
   if (tm) MOE_CUDA(record_time(L, kTimeRouterEnd, st));
   if (!tc && B == 1) {   // one launch for both expert steps
@@ -1370,6 +1393,13 @@ int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float*
   mxfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       q, s, rows, k, layout, out);
   MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+int moe_set_act_format(moe_layer_t L, int fmt) {
+  if (!L || fmt < 0 || fmt > 1) return MOE_ERR_INVALID_ARG;
+  if (fmt == 1 && !L->wm.ok) return MOE_ERR_UNSUPPORTED;   // needs the mma.sync layouts
+  L->act_fmt = fmt;
   return MOE_OK;
 }
 

@@ -651,7 +651,7 @@ __device__ __forceinline__ void mx_group_run_xs(const uint8_t* nib, const uint8_
 // X holds the pass's activation operand; xkey/xshift remember which single x
 // row it holds (-1: none), so a run of another expert on the same row (every
 // run at B = 1) keeps it instead of reloading and re-reducing it.
-template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE, bool XS>
+template <bool GLU, bool ACTH, int TM, int NBMAX, int RMAX, bool ONE, bool XS, bool F8 = false>
 __device__ __forceinline__ void stream_consume_run_mma(
     const StreamArgs& a, const StreamItem& m, int done, int R, int it0, int run_end, int tiles,
     uint8_t* stages, uint64_t* full, uint64_t* empty, float* red, uint32_t& stage, int& pp,
@@ -734,6 +734,8 @@ __device__ __forceinline__ void stream_consume_run_mma(
         v0 = __ldcg(reinterpret_cast<const float4*>(hr + (size_t)(b0 + b) * 32));
         v1 = __ldcg(reinterpret_cast<const float4*>(hr + (size_t)(b0 + b) * 32 + 4));
       }
+      // MXFP8: the block's 32 values sit in this lane quad (all lanes take part)
+      if constexpr (F8) mxfp8_round8(v0, v1);
       X[b][0] = pack_f16x2(v0.x * sc, v0.y * sc);
       X[b][1] = pack_f16x2(v0.z * sc, v0.w * sc);
       X[b][2] = pack_f16x2(v1.x * sc, v1.y * sc);
@@ -831,7 +833,7 @@ __device__ __forceinline__ void stream_consume_run_mma(
 
 // Consumers: items [lo, hi) of one step, run by run, pass by pass.
 template <int WF, bool GLU, bool ACTH, bool ROUTED, int SP, int RW, int RMAX, bool MMA, int TM,
-          int NBMAX, int CW, int NQ, bool XS = false>
+          int NBMAX, int CW, int NQ, bool XS = false, bool F8 = false>
 __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo, int hi, int tiles,
                                                      uint8_t* stages, uint64_t* full,
                                                      uint64_t* empty, float* red, uint32_t& stage,
@@ -845,7 +847,7 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
       const int R = stream_pass_rows<RMAX, MMA>(m.pr - done);
       if constexpr (MMA) {
         if (RMAX == 1 || R == 1)
-          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true, XS>(
+          stream_consume_run_mma<GLU, ACTH, TM, NBMAX, RMAX, true, XS, F8>(
               a, m, done, R, it0, run_end, tiles, stages, full, empty, red, stage, pp, rp, kw, KW,
               lane, X, xkey, xshift);
         else if constexpr (RMAX > 1)
@@ -880,7 +882,7 @@ __device__ __forceinline__ void stream_consume_range(const StreamArgs& a, int lo
 // and at most NBMAX K blocks per consumer warp.
 template <int WF_, bool GLU_, bool ACTH_, bool ROUTED_, int SP_, int RW_, int RMAX_,
           bool MMA_ = false, int TM_ = 1, int NBMAX_ = 1, int CW_ = 8, int NQ_ = 4,
-          bool XS_ = false>
+          bool XS_ = false, bool F8_ = false>
 struct StreamCfg {
   static constexpr int WF = WF_;
   static constexpr bool GLU = GLU_, ACTH = ACTH_, ROUTED = ROUTED_, MMA = MMA_;
@@ -892,6 +894,11 @@ struct StreamCfg {
                 "tensor-core steps: routed MXFP4, one tile per item, at most 8 columns");
   static_assert(MMA || WF == kWfBf16, "MXFP4 steps run on the tensor cores");
   static_assert(!XS || (MMA && !ACTH && RMAX == 1), "a shared-memory operand holds one x row");
+  // MXFP4 steps of one activation row with MXFP8 activations: x or h rounded
+  // to E4M3 with one E8M0 scale per 32 elements (mxfp8_round8), then carried
+  // into the same f16 MMAs exactly
+  static constexpr bool F8 = F8_;
+  static_assert(!F8 || (MMA && RMAX == 1), "MXFP8 activations: one-row MXFP4 steps");
 };
 
 // Weight bytes one item of a step streams: MXFP4 tiles of 16 rows (K/2
@@ -941,8 +948,8 @@ __device__ __forceinline__ void cfg_consume(const StreamArgs& a, const SegPrior&
   if (part == 0) hi = min(hi, lo + first);
   else if (part == 1) lo = min(hi, lo + first);
   stream_consume_range<C::WF, C::GLU, C::ACTH, C::ROUTED, C::SP, C::RW, C::RMAX, C::MMA, C::TM,
-                       C::NBMAX, C::CW, C::NQ, C::XS>(a, lo, hi, tiles, stages, full, empty, red, stage,
-                                               pp, rp, kw, KW, lane);
+                       C::NBMAX, C::CW, C::NQ, C::XS, C::F8>(a, lo, hi, tiles, stages, full, empty,
+                                                       red, stage, pp, rp, kw, KW, lane);
 }
 
 // Shared-memory carve-up common to both kernels.
@@ -1040,6 +1047,7 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
 // KW consumer warps: the row's max |x| picks the power-of-two scale that keeps
 // f16 in range, then entry i holds elements 8i..8i+7 as f16 pairs (entry
 // 4 b + t: block b, lane quad t).  scratch: KW words.
+template <bool F8 = false>
 __device__ __forceinline__ void stage_x_operand(const uint16_t* x, int K, uint4* xs, int* xshift,
                                                 unsigned* scratch, int kw, int KW, int lane,
                                                 int ct, int cthreads) {
@@ -1060,14 +1068,21 @@ __device__ __forceinline__ void stage_x_operand(const uint16_t* x, int K, uint4*
   const int shift = f16_shift_for_amax(bf16_bits_to_f32(amax));
   const float sc = pow2f(-shift);
   if (ct == 0) *xshift = shift;
+  // (K / 8 is a multiple of 32, so every warp runs whole iterations, and the
+  // four chunks of a 32-element block sit in one lane quad)
   for (int i = ct; i < K / 8; i += cthreads) {
     const uint4 v = xr[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float4 f0 = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                            __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+    float4 f1 = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                            __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+    if constexpr (F8) mxfp8_round8(f0, f1);   // MXFP8 activations: the rounded values
     uint4 o;
-    o.x = pack_f16x2(__uint_as_float(w[0] << 16) * sc, __uint_as_float(w[0] & 0xFFFF0000u) * sc);
-    o.y = pack_f16x2(__uint_as_float(w[1] << 16) * sc, __uint_as_float(w[1] & 0xFFFF0000u) * sc);
-    o.z = pack_f16x2(__uint_as_float(w[2] << 16) * sc, __uint_as_float(w[2] & 0xFFFF0000u) * sc);
-    o.w = pack_f16x2(__uint_as_float(w[3] << 16) * sc, __uint_as_float(w[3] & 0xFFFF0000u) * sc);
+    o.x = pack_f16x2(f0.x * sc, f0.y * sc);
+    o.y = pack_f16x2(f0.z * sc, f0.w * sc);
+    o.z = pack_f16x2(f1.x * sc, f1.y * sc);
+    o.w = pack_f16x2(f1.z * sc, f1.w * sc);
     xs[i] = o;
   }
   consumer_sync(cthreads);   // the scratch words are free again, the operand complete
@@ -1225,6 +1240,7 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   static_assert(B1::ROUTED && B1::RMAX == 1 && B2::ROUTED && B2::RMAX == 1 && B1::XS,
                 "one activation row: routed steps with one column, FC1's x in shared memory");
   static_assert(!A1::ROUTED && !A2::ROUTED, "the shared expert is dense");
+  static_assert(B1::F8 == B2::F8, "one activation format for both routed steps");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KW = (int)(blockDim.x >> 5) - 1;
@@ -1265,8 +1281,8 @@ __global__ void __launch_bounds__(32 * (kMmaWarps + 1), 1)
   } else {
     const int ct = (int)threadIdx.x - 32, cthreads = 32 * KW, kw = warp - 1;
     // x is the layer's input (read by A1 as well): staged before A1
-    stage_x_operand(b1.x, b1.K, const_cast<uint4*>(b1.xs), const_cast<int*>(b1.xs_shift),
-                    reinterpret_cast<unsigned*>(m.red), kw, KW, lane, ct, cthreads);
+    stage_x_operand<B1::F8>(b1.x, b1.K, const_cast<uint4*>(b1.xs), const_cast<int*>(b1.xs_shift),
+                            reinterpret_cast<unsigned*>(m.red), kw, KW, lane, ct, cthreads);
     int pp = 0, rp = 0;
     unsigned* const count = b1.done_count;
     cfg_consume<A1>(a0, SegPrior(), m.stages, m.full, m.empty, m.red, stage, pp, rp, kw, KW, lane);

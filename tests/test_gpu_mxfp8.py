@@ -1,0 +1,84 @@
+"""GPU parity of the MXFP8-activation expert path (moe_set_act_format 1: x and
+h rounded to E4M3 with one E8M0 scale per 32 elements before they meet the
+MXFP4 weights) against the oracle's mxfp8 mode, element by element, at the
+layer's stated tolerance: both sides round the same values the same way
+(nearest E4M3, ties to even, saturation at 448), so they differ only by
+summation order and by h's fp32 (GPU) against fp64 (oracle) values."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_decode_step_gb300 as M
+from gen.configs import CONFIGS
+from moe_decode_step_gb300 import synthetic
+
+from _parity import assert_close
+from test_gpu_layer import check_against_oracle, run_debug
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _parity(cfg, rows=None):
+    inp = oracle.clean_inputs(cfg)
+    ref = oracle.forward(inp, act="mxfp8")
+    ex = oracle.forward(inp)
+    x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
+    layer = synthetic.make_layer(cfg)
+    layer.set_act_format(1)
+    idx, w = layer.router_topk(x)
+    dbg = run_debug(layer, x, res)
+    assert layer.status() == 0
+    layer.close()
+    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg,
+                         _np(res), range(cfg.B) if rows is None else rows)
+    # and it is the MXFP8 layer, not the exact one: y_routed sits a few per
+    # cent of its RMS from the exact oracle's
+    dev = np.abs(dbg["y_routed"][0] - ex["y_r"][0])
+    assert np.sqrt(np.mean(dev ** 2)) > 5e-3 * np.sqrt(np.mean(ex["y_r"][0] ** 2))
+
+
+def test_tiny_one_row_matches_oracle_mxfp8_mode():
+    _parity(CONFIGS["tiny_b1"])
+
+
+def test_full_size_one_row_matches_oracle_mxfp8_mode():
+    _parity(CONFIGS["full_b1"])
+
+
+def test_format_is_one_row_only_and_switches_back():
+    cfg = CONFIGS["tiny_b1"]
+    layer = synthetic.make_layer(cfg, max_batch=4)
+    layer.set_act_format(1)
+    x3, r3 = synthetic.make_activations(dataclasses.replace(cfg, name="tiny_b3", B=3))
+    with pytest.raises(M.MoEError) as e:
+        layer.forward(x3, r3.clone())
+    assert e.value.code == M.MOE_ERR_UNSUPPORTED
+    with pytest.raises(M.MoEError) as e:
+        layer.set_act_format(2)
+    assert e.value.code == M.MOE_ERR_INVALID_ARG
+    # back to exact activations: the exact oracle's parity
+    layer.set_act_format(0)
+    inp = oracle.clean_inputs(cfg)
+    ref = oracle.forward(inp)
+    x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
+    idx, w = layer.router_topk(x)
+    dbg = run_debug(layer, x, res)
+    assert layer.status() == 0
+    check_against_oracle(ref, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), dbg,
+                         _np(res), [0])
+    layer.close()
+
+
+def test_tensor_core_only_layer_rejects_the_format():
+    layer = synthetic.make_layer(CONFIGS["tiny_b1"], expert_path=2)
+    with pytest.raises(M.MoEError) as e:
+        layer.set_act_format(1)
+    assert e.value.code == M.MOE_ERR_UNSUPPORTED
+    layer.close()
