@@ -632,7 +632,9 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
       a.xq = L->ws.x_act;
       a.xq_code = L->ws.x_code;
     }
-    rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts, st, false);
+    // programmatic launch: behind the previous layer's tail the router
+    // streams its weights while that tail runs (it waits before reading x)
+    rc = launch_step(L, MOE_ROUTER_KERNEL, L->plan[kStepRouter][0], a, d.n_experts, st, true);
     if (rc) return rc;
   }
   TopkArgs t{};

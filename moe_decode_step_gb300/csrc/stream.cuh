@@ -991,17 +991,26 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
   const int KW = (int)(blockDim.x >> 5) - 1;
   trace_begin(a.trace, a.trace_id);
   const StreamSmem m = stream_smem_init(smem, a.NS, a.stage_bytes, a.red_pp, KW);
-  pdl_launch_dependents();
+  // The weights stream at once (they depend on nothing), but no thread lets
+  // the next kernel launch before it has waited for this one's predecessor:
+  // a kernel launched behind this one may read what that predecessor wrote
+  // (the layer's input x) without waiting itself.
   uint32_t stage = 0;
   if (warp == 0) {
     if (lane == 0) {
       if (ROUTED) pdl_wait_prerequisites();
       cfg_produce<C>(a, SegPrior(), m.stages, m.full, m.empty, stage);
+      pdl_wait_prerequisites();
+      pdl_launch_dependents();
       stream_drain(a, m.empty, stage);
+    } else {
+      pdl_wait_prerequisites();
+      pdl_launch_dependents();
     }
     __syncwarp();
   } else {
     pdl_wait_prerequisites();
+    pdl_launch_dependents();
     if (a.xq) {
       // the activation planes of x for the tensor-core experts, one plane-0
       // code per row: a share of the B * K/32 blocks per CTA, one block per
