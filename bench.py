@@ -263,14 +263,17 @@ L2_MODES = {"none": "not flushed: inputs larger than L2 (each step streams 360 M
             "flush": "flushed between timed steps (write of 2x L2 size)"}
 
 SLEEP_CYCLES = 1_000_000   # ~0.5 ms head start so the host enqueues a whole forward
+                           # (or graph launch) before the GPU reaches the start event
 
 
 def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
     """Device time of one forward per step (CUDA events on the launching stream),
     flush() before every step.  graph=True replays a captured CUDA graph of
     the forward (the production mode: no host launch gaps); graph=False runs the
-    eager forward behind a sleep kernel so that the host has enqueued all of it
-    before the GPU reaches it.  Returns (us per step, per-phase us per step)."""
+    eager forward.  Either way a sleep kernel runs before the start event, so
+    that the host has submitted the whole step before the GPU reaches the event
+    and the host's submission latency stays outside the device time.  Returns
+    (us per step, per-phase us per step)."""
     import torch
     res = res0.clone()
     out = torch.empty_like(x)
@@ -299,8 +302,7 @@ def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
     for _ in range(steps):
         res.copy_(res0)
         flush()
-        if not graph:
-            torch.cuda._sleep(SLEEP_CYCLES)
+        torch.cuda._sleep(SLEEP_CYCLES)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(cur)
@@ -316,10 +318,68 @@ def time_layer(layer, x, res0, steps, warmup, flush, graph=True, timing=True):
     return times, phases
 
 
+def time_steps(layer, x, res0, steps, warmup):
+    """Device time per step of `steps` forwards captured back to back in one
+    CUDA graph, as the layer runs inside a decode step's graph (one graph
+    launch for all of them, each forward chained to the next by programmatic
+    dependent launch), timed once with CUDA events around the replay behind a
+    sleep kernel; `warmup` single-forward replays run before it.  x stays, the
+    residual carries from step to step.  Nothing can be flushed between the
+    steps, so this is the L2 mode "none" only (inputs larger than L2)."""
+    import torch
+    res = res0.clone()
+    out = torch.empty_like(x)
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        layer.forward(x, res, out)
+    cur.wait_stream(side)
+    torch.cuda.synchronize()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        layer.forward(x, res, out)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk):
+        for _ in range(steps):
+            layer.forward(x, res, out)
+    for _ in range(warmup):
+        g1.replay()
+    res.copy_(res0)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(SLEEP_CYCLES)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    gk.replay()
+    b.record(cur)
+    b.synchronize()
+    us = a.elapsed_time(b) * 1000.0 / steps
+    del gk, g1
+    return us
+
+
+def measure(layer, x, res0, steps, warmup, l2, l2flush):
+    """The reported time of one forward in L2 mode `l2`, and the per-step
+    times of single-forward graph replays (for the spread).  "none": `steps`
+    forwards in one graph (time_steps), the single-forward replays run after
+    it, outside the timed steps; "flush": the median of single-forward
+    replays, L2 flushed before each."""
+    import statistics
+    if l2 == "none":
+        us = time_steps(layer, x, res0, steps, warmup)
+        single, _ = time_layer(layer, x, res0, steps, warmup, lambda: None, graph=True,
+                               timing=False)
+        return us, single
+    single, _ = time_layer(layer, x, res0, steps, warmup, l2flush, graph=True, timing=False)
+    return statistics.median(single), single
+
+
 def time_chain(layers, x0, res0, steps, warmup, flush):
     """Device time of a chain of layers (each layer's out is the next one's x,
     the residual threads through), captured as one CUDA graph; flush() once
-    before each chain.  Returns per-chain microseconds."""
+    before each chain, then a sleep kernel ahead of the start event (the host
+    submits the graph launch meanwhile).  Returns per-chain microseconds."""
     import torch
     x = x0.clone()
     res = res0.clone()
@@ -350,6 +410,7 @@ def time_chain(layers, x0, res0, steps, warmup, flush):
     for _ in range(steps):
         res.copy_(res0)
         flush()
+        torch.cuda._sleep(SLEEP_CYCLES)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(cur)
@@ -485,15 +546,13 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with ClockSampler(local) as clk:
-        times, _ = time_layer(layer, x, res0, args.steps, args.warmup, flush, graph=True,
-                              timing=False)
+        us_mode, times = measure(layer, x, res0, args.steps, args.warmup, args.l2, l2flush)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     # the same forward in the other L2 mode, outside the timed region
-    alt_times, _ = time_layer(layer, x, res0, args.steps, args.warmup,
-                              (lambda: None) if args.l2 == "flush" else l2flush, graph=True,
-                              timing=False)
+    us_alt, _ = measure(layer, x, res0, args.steps, args.warmup,
+                        "flush" if args.l2 == "none" else "none", l2flush)
     # per-phase events (graph nodes) on a separate set of replays: the event
     # nodes sit between the chained kernels, so they are kept out of the value
     _, phases = time_layer(layer, x, res0, max(5, args.steps // 2), max(3, args.warmup), flush,
@@ -501,8 +560,9 @@ def run_ours(args, rank, world, local):
     eager_times, eager_phases = time_layer(layer, x, res0, max(5, args.steps // 2),
                                            max(3, args.warmup), flush, graph=False)
 
-    us = reduce_max(statistics.median(times), world, dev)
-    us_alt = reduce_max(statistics.median(alt_times), world, dev)
+    us = reduce_max(us_mode, world, dev)
+    us_alt = reduce_max(us_alt, world, dev)
+    us_single = reduce_max(statistics.median(times), world, dev)
     btouch = bytes_touched(cfg, n_distinct, cfg.B)
     # one row on the mma.sync path runs FC1 and FC2 as one launch (four per
     # forward): that launch is the dominant kernel, with both steps' bytes
@@ -528,11 +588,11 @@ def run_ours(args, rank, world, local):
     f1 = None
     if cfg.B == 1 and fused:
         layer.set_act_format(1)
-        f1_times, _ = time_layer(layer, x, res0, args.steps, args.warmup, flush, graph=True,
-                                 timing=False)
+        f1_mode, f1_times = measure(layer, x, res0, args.steps, args.warmup, args.l2, l2flush)
         layer.set_act_format(0)
-        f1_us = reduce_max(statistics.median(f1_times), world, dev)
-        f1 = {"us": f1_us, "p10_us": percentile(f1_times, 10), "steps": args.steps,
+        f1_us = reduce_max(f1_mode, world, dev)
+        f1 = {"us": f1_us, "single_forward_us": statistics.median(f1_times),
+              "p10_us": percentile(f1_times, 10), "steps": args.steps,
               "frac_of_peak": btouch / f1_us / 1e3 / peak,
               "activations": "x and h rounded to MXFP8 (E4M3, one E8M0 scale per 32) before "
                              "the MXFP4 products; parity against the oracle's mxfp8 mode"}
@@ -551,10 +611,9 @@ def run_ours(args, rank, world, local):
             i2, _ = L2.router_topk(x2)
             nd2 = int(torch.unique(i2).numel())
             st2 = max(5, args.steps)
-            t2, _ = time_layer(L2, x2, r2, st2, max(3, args.warmup), flush, graph=True,
-                               timing=False)
+            v2m, t2 = measure(L2, x2, r2, st2, max(3, args.warmup), args.l2, l2flush)
             _, p2 = time_layer(L2, x2, r2, 5, 3, flush, graph=True, timing=True)
-            v2 = reduce_max(statistics.median(t2), world, dev)
+            v2 = reduce_max(v2m, world, dev)
             b2 = bytes_touched(c2, nd2, c2.B)
             f2_us = statistics.median(p[1] for p in p2)
             f2_b = fc1_bytes(c2, nd2, c2.B)
@@ -562,7 +621,8 @@ def run_ours(args, rank, world, local):
             key = str(c2.B) if c2.drafts == 0 else (f"{c2.B} (rows in correlated groups of "
                                                        f"{1 + c2.drafts}, rho {c2.corr})")
             batches[key] = {
-                "us": v2, "steps": st2, "n_distinct_experts": nd2, "bytes_touched": b2,
+                "us": v2, "single_forward_us": statistics.median(t2), "steps": st2,
+                "n_distinct_experts": nd2, "bytes_touched": b2,
                 "hbm_tbs": b2 / v2 / 1e6, "frac_of_peak": b2 / v2 / 1e3 / peak,
                 "expert_path": "tcgen05 block-scaled MXF4 MMA",
                 "fc1_roofline": {"kernel": "tc_kernel (FC1: shared gate/up as a bf16 kind::f16 pass, "
@@ -612,6 +672,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
         "p10_us": percentile(times, 10), "p90_us": percentile(times, 90),
+        "single_forward_us": us_single,
         "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": DATA,
         "config": {"workload": f"{args.config}: one MoE decode layer, B={cfg.B}, d={cfg.d}, "
@@ -636,8 +697,14 @@ def run_ours(args, rank, world, local):
                      "algorithmic_bytes": fc1_b, "launch_us": fc1_us, "peak_kind": peak_kind},
         "phases_us": phase_med,
         "trace_us": trace,
-        "timing_mode": "CUDA graph replay of the forward (value); per-phase events as graph "
-                       "nodes on separate replays (phases_us)",
+        "timing_mode": (f"value: {args.steps} forwards captured back to back in one CUDA graph "
+                        "(as inside a decode step's graph), one replay timed with CUDA events, "
+                        "divided by the steps; single_forward_us, p10_us, p90_us: one forward "
+                        "per graph replay, each timed alone (a one-kernel graph measures "
+                        "~5 us between its events on this GPU)" if args.l2 == "none" else
+                        "value: median of single-forward CUDA graph replays, L2 flushed before "
+                        "each") + "; per-phase events as graph nodes on separate replays "
+                                  "(phases_us)",
         "eager_us": statistics.median(eager_times),
         "eager_phases_us": {n: statistics.median(p[i] for p in eager_phases)
                             for i, n in enumerate(phase_names)},
