@@ -584,7 +584,7 @@ def run_ours(args, rank, world, local):
     e2e_times, h2d, d2h = time_e2e(layer, cfg, x, res0, max(5, args.steps // 2),
                                    max(3, args.warmup), flush)
     # f1: the routed experts on MXFP8 activations (the pages' FP4 x MXFP8
-    # products), same layer and timing; one row on the mma.sync path only
+    # products), same layer and timing (the batches below report theirs)
     f1 = None
     if cfg.B == 1 and fused:
         layer.set_act_format(1)
@@ -618,6 +618,14 @@ def run_ours(args, rank, world, local):
             f2_us = statistics.median(p[1] for p in p2)
             f2_b = fc1_bytes(c2, nd2, c2.B)
             tr2 = trace_layer(L2, x2, r2, flush)
+            # f1 on the same layer: the activation planes hold the MXFP8
+            # roundings of x and h
+            L2.set_act_format(1)
+            f1m, f1t = measure(L2, x2, r2, st2, max(3, args.warmup), args.l2, l2flush)
+            _, f1p = time_layer(L2, x2, r2, 5, 3, flush, graph=True, timing=True)
+            L2.set_act_format(0)
+            f1v = reduce_max(f1m, world, dev)
+            f1_fc1 = statistics.median(p[1] for p in f1p)
             key = str(c2.B) if c2.drafts == 0 else (f"{c2.B} (rows in correlated groups of "
                                                        f"{1 + c2.drafts}, rho {c2.corr})")
             batches[key] = {
@@ -632,7 +640,13 @@ def run_ours(args, rank, world, local):
                                  "launch_us": f2_us, "peak_kind": peak_kind},
                 "phases_us": {n: statistics.median(p[i] for p in p2)
                               for i, n in enumerate(phase_names)},
-                "trace_us": tr2}
+                "trace_us": tr2,
+                "f1_mxfp8": {"us": f1v, "single_forward_us": statistics.median(f1t),
+                             "frac_of_peak": b2 / f1v / 1e3 / peak,
+                             "fc1_frac": f2_b / f1_fc1 / 1e3 / peak, "fc1_launch_us": f1_fc1,
+                             "activations": "planes of the MXFP8 roundings of x and h (E4M3, "
+                                            "one E8M0 scale per 32); parity against the "
+                                            "oracle's mxfp8 mode"}}
             L2.close()
             del L2
             torch.cuda.empty_cache()

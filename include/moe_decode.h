@@ -170,10 +170,12 @@ int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, fl
  * the stated tolerance.  fmt 1: x and h rounded to MXFP8 (OCP MX v1.0: E4M3
  * elements, nearest with ties to even and saturation at 448, one E8M0 scale
  * 2^(floor(log2 max|v|) - 8) per 32 contiguous elements) before they meet the
- * MXFP4 weights, E4M3 x E4M3 tensor-core products; the router, shared expert
- * and tail are unchanged.  fmt 1 runs one row on the mma.sync path only: a
- * forward with B > 1 (or a layer without the mma.sync path's layouts) returns
- * MOE_ERR_UNSUPPORTED.  Errors: INVALID_ARG, UNSUPPORTED. */
+ * MXFP4 weights; the router, shared expert and tail are unchanged.  The
+ * one-row mma.sync kernel carries the rounded values exactly in its f16
+ * operands; the tensor-core path builds its activation planes (E2M1 digits,
+ * block-scaled MMAs) from them.  fmt 1 runs on the tensor-core path at any B
+ * and on the mma.sync path at B = 1; a forward of B > 1 rows on the mma.sync
+ * path returns MOE_ERR_UNSUPPORTED.  Errors: INVALID_ARG. */
 int moe_set_act_format(moe_layer_t layer, int fmt);
 
 /* Chain layers: once this layer's expert kernels have finished, an L2-prefetch

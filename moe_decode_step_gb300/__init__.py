@@ -162,8 +162,9 @@ class MoELayer:
         return v.value
 
     def set_act_format(self, fmt):
-        """Routed experts' activations: 0 exact (default), 1 MXFP8 (one row on
-        the mma.sync path; see moe_set_act_format)."""
+        """Routed experts' activations: 0 exact (default), 1 MXFP8 (the
+        tensor-core path at any B, the mma.sync path at B = 1; see
+        moe_set_act_format)."""
         check(lib().moe_set_act_format(self._h, int(fmt)), "moe_set_act_format")
 
     def debug_set_fault(self, fault, wait_ns=0):

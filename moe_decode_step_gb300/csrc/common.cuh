@@ -242,6 +242,15 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// MXFP8 rounding of one 32-element block held one element per lane (the whole
+// warp takes part): the scale and the rounding of mxfp8_round8.
+__device__ __forceinline__ float mxfp8_round1(float v) {
+  const int e = e4m3_block_exp(warp_max(fabsf(v)));
+  float q = v * pow2_e8m0(-e), unused = 0.0f;
+  e4m3x2_round(q, unused);
+  return q * pow2_e8m0(e);
+}
+
 // Butterfly reduce-scatter of V = 2^m per-lane partials over the warp.  On
 // return, lane l holds the full warp sum of value index
 //   vidx(l) = l >> (5 - m)            (the top m bits of the lane id)

@@ -631,6 +631,7 @@ int launch_router(moe_layer* L, cudaStream_t st, const void* x, int B, int32_t* 
     if (use_tc(L, B)) {   // the activation planes the tensor-core FC1 streams
       a.xq = L->ws.x_act;
       a.xq_code = L->ws.x_code;
+      a.xq_f8 = L->act_fmt == 1;
     }
     // programmatic launch: behind the previous layer's tail the router
     // streams its weights while that tail runs (it waits before reading x)
@@ -786,6 +787,7 @@ int launch_router_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   xp.K = d.d;
   xp.xq = L->ws.x_act;
   xp.xq_code = L->ws.x_code;
+  xp.f8 = L->act_fmt == 1;
   CUtensorMap xmap;
   int rc = encode_x_map(L, x, B, dn.NP, &xmap);
   if (rc) return rc;
@@ -816,6 +818,7 @@ int launch_fc1_tc(moe_layer* L, cudaStream_t st, const void* x, int B) {
   b.out_amax = L->ws.h_amax;
   b.out_act = L->ws.h_act;
   b.out_sfb = L->ws.h_sfb;
+  b.out_f8 = L->act_fmt == 1;
   b.trace_id = 2;
   TcDense dn = dense_base_args(L, p, B);
   dn.w = L->sh_gu_umma;
@@ -1035,7 +1038,9 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
   if (!aligned16(residual) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   const bool tm = L->timing;
   const bool tc = use_tc(L, B);
-  if (L->act_fmt == 1 && (B != 1 || tc)) return MOE_ERR_UNSUPPORTED;   // one row, mma.sync
+  // MXFP8 activations: the tensor-core path (its activation planes hold the
+  // rounded values) or the one-row mma.sync kernel, not the mma.sync batches
+  if (L->act_fmt == 1 && !tc && B != 1) return MOE_ERR_UNSUPPORTED;
   if (L->tracing) {
     MOE_CUDA(cudaMemsetAsync(L->ws.trace, 0xFF, 8 * sizeof(unsigned long long), st));
     MOE_CUDA(cudaMemsetAsync(L->ws.trace + 8, 0, 8 * sizeof(unsigned long long), st));
@@ -1400,7 +1405,6 @@ int moe_debug_dequant(moe_layer_t L, void* stream, int expert, int which, float*
 
 int moe_set_act_format(moe_layer_t L, int fmt) {
   if (!L || fmt < 0 || fmt > 1) return MOE_ERR_INVALID_ARG;
-  if (fmt == 1 && !L->wm.ok) return MOE_ERR_UNSUPPORTED;   // needs the mma.sync layouts
   L->act_fmt = fmt;
   return MOE_OK;
 }

@@ -81,6 +81,38 @@ __device__ __forceinline__ int planes_block(float v, int lane, uint8_t* blk) {
   return c0;
 }
 
+// Bits of max |v| over a bf16 row of K elements (K / 8 a multiple of 32),
+// this warp's share: lane entry i0, i0 + stride, ... of the row's K / 8 chunks
+// of 8 elements, reduced over the warp (stride a multiple of 32, so every lane
+// runs the same iterations).  f8: of the row's MXFP8 rounding instead (a lane
+// quad holds one 32-element block).  The bits of a non-negative float.
+__device__ __forceinline__ uint32_t row_amax_bits(const uint16_t* row, int K, int i0, int stride,
+                                                  int f8) {
+  const uint4* xr = reinterpret_cast<const uint4*>(row);
+  uint32_t mx = 0;
+  for (int i = i0; i < K / 8; i += stride) {
+    const uint4 v = xr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (f8) {
+      float4 f0 = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                              __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+      float4 f1 = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                              __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+      mxfp8_round8(f0, f1);
+      const float m = fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f0.z), fabsf(f0.w))),
+                            fmaxf(fmaxf(fabsf(f1.x), fabsf(f1.y)), fmaxf(fabsf(f1.z), fabsf(f1.w))));
+      mx = max(mx, __float_as_uint(m));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    }
+  }
+  if (!f8) mx <<= 16;   // bf16 magnitude bits -> float bits
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  return mx;
+}
+
 // Scale code of plane p given the block's plane-0 code.
 __device__ __forceinline__ uint32_t planes_code(uint32_t c0, int p) {
   const int c = (int)c0 - 2 * p;

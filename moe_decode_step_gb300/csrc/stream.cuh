@@ -70,6 +70,7 @@ struct StreamArgs {
   int trace_id;
   uint8_t* xq;               // router only: activation planes of x [B][4K] (planes.cuh), or null
   uint8_t* xq_code;          // and their plane-0 codes, one per row [B]
+  int xq_f8;                 // 1: the planes hold x's MXFP8 rounding (mxfp8_round8)
   // routed gate/up steps of one activation row whose operand sits in shared
   // memory (StreamCfg XS): per K block b and lane quad t, the f16 pairs of
   // elements 8t..8t+7 at xs[4 b + t], scaled by 2^-(*xs_shift)
@@ -1015,32 +1016,26 @@ __global__ void __launch_bounds__(288, 1) stream_gemv_kernel(const StreamArgs a)
       // the activation planes of x for the tensor-core experts, one plane-0
       // code per row: a share of the B * K/32 blocks per CTA, one block per
       // warp, while the first stages land; each row this CTA touches first
-      // gets its max |x| from all consumer warps
+      // gets its max |x| from all consumer warps (with xq_f8, of x's MXFP8
+      // rounding, which the planes then hold)
       const int nb = a.K / 32, total = a.B * nb;
       const int lo = (int)((long long)total * blockIdx.x / gridDim.x);
       const int hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
       unsigned* slots = reinterpret_cast<unsigned*>(m.red);
       for (int row = lo / nb; lo < hi && row <= (hi - 1) / nb; ++row) {
-        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)row * a.K);
-        uint32_t mx = 0;
-        for (int i = (warp - 1) * 32 + lane; i < a.K / 8; i += KW * 32) {
-          const uint4 v = xr[i];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const uint16_t* xrow = a.x + (size_t)row * a.K;
+        const uint32_t mx = row_amax_bits(xrow, a.K, (warp - 1) * 32 + lane, KW * 32, a.xq_f8);
         if (lane == 0) slots[warp - 1] = mx;
         consumer_sync(KW * 32);
         uint32_t amax = 0;
         for (int w = 0; w < KW; ++w) amax = max(amax, slots[w]);
         consumer_sync(KW * 32);
-        const int c0 = planes_code0(bf16_bits_to_f32(amax));
+        const int c0 = planes_code0(__uint_as_float(amax));
         if (warp == 1 && lane == 0) a.xq_code[row] = (uint8_t)c0;
         const int b0 = max(lo, row * nb) - row * nb, b1 = min(hi, (row + 1) * nb) - row * nb;
         for (int blk = b0 + warp - 1; blk < b1; blk += KW) {
-          const float v = bf16_bits_to_f32(a.x[(size_t)row * a.K + blk * 32 + lane]);
+          float v = bf16_bits_to_f32(xrow[blk * 32 + lane]);
+          if (a.xq_f8) v = mxfp8_round1(v);
           planes_block_c(v, lane, a.xq + (size_t)row * planes_row_bytes(a.K) + blk * 128, c0);
         }
       }

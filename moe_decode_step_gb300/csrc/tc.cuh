@@ -171,6 +171,7 @@ struct TcArgs {
   unsigned* out_amax;        // gate/up: max |h| bits per pair, or null
   uint8_t* out_act;          // gate/up: h planes [pairs][4N], or null
   uint8_t* out_sfb;          // gate/up: h plane scales per run (N/128 atoms), with out_act
+  int out_f8;                // gate/up: 1 = the h planes hold h's MXFP8 rounding
   float* partial;            // [kTcMaxCtas][kTcRmax][128]
   unsigned* flags;           // [kTcMaxCtas], zero between forwards
   int* status;
@@ -592,7 +593,9 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& b, const TcSmem& t, ui
             if (lane == 0 && b.out_amax) atomicMax(b.out_amax + pid[r], __float_as_uint(hm));
             if (b.out_act) {
               // the down projection's B operand: h planes and their block scales
-              const int c0 = planes_block(hv, lane, b.out_act + (size_t)pid[r] * planes_row_bytes(b.N) + blk * 128);
+              // (out_f8: of h's MXFP8 rounding; out and out_amax keep h itself)
+              const int c0 = planes_block(b.out_f8 ? mxfp8_round1(hv) : hv, lane,
+                                          b.out_act + (size_t)pid[r] * planes_row_bytes(b.N) + blk * 128);
               if (lane < kPlanes) {
                 const int n = 8 * r + lane;
                 b.out_sfb[(size_t)rho * 4 * b.N + tc_sfb_offset(blk / 4, n, blk % 4)] =
@@ -1065,6 +1068,7 @@ struct TcXPlanes {
   int B, K;
   uint8_t* xq;         // planes [B][4 K], or null
   uint8_t* xq_code;    // plane-0 code per row
+  int f8;              // 1: the planes hold x's MXFP8 rounding
 };
 
 // Warps 2..6 only (named barrier 3).
@@ -1077,27 +1081,20 @@ __device__ __forceinline__ void tc_xplanes(const TcXPlanes& p, int cta, int ncta
   const int lo = (int)((long long)total * cta / ncta);
   const int hi = (int)((long long)total * (cta + 1) / ncta);
   for (int row = lo / nb; lo < hi && row <= (hi - 1) / nb; ++row) {
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.K);
-    uint32_t mx = 0;
-    for (int i = wi * 32 + lane; i < p.K / 8; i += NW * 32) {
-      const uint4 v = xr[i];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const uint16_t* xrow = p.x + (size_t)row * p.K;
+    const uint32_t mx = row_amax_bits(xrow, p.K, wi * 32 + lane, NW * 32, p.f8);
     if (lane == 0) slots[wi] = mx;
     tc_plane_sync();
     uint32_t amax = 0;
 #pragma unroll
     for (int w = 0; w < NW; ++w) amax = max(amax, slots[w]);
     tc_plane_sync();
-    const int c0 = planes_code0(bf16_bits_to_f32(amax));
+    const int c0 = planes_code0(__uint_as_float(amax));
     if (wi == 0 && lane == 0) p.xq_code[row] = (uint8_t)c0;
     const int b0 = max(lo, row * nb) - row * nb, b1 = min(hi, (row + 1) * nb) - row * nb;
     for (int blk = b0 + wi; blk < b1; blk += NW) {
-      const float v = bf16_bits_to_f32(p.x[(size_t)row * p.K + blk * 32 + lane]);
+      float v = bf16_bits_to_f32(xrow[blk * 32 + lane]);
+      if (p.f8) v = mxfp8_round1(v);
       planes_block_c(v, lane, p.xq + (size_t)row * planes_row_bytes(p.K) + blk * 128, c0);
     }
   }

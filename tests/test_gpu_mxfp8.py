@@ -3,7 +3,9 @@ h rounded to E4M3 with one E8M0 scale per 32 elements before they meet the
 MXFP4 weights) against the oracle's mxfp8 mode, element by element, at the
 layer's stated tolerance: both sides round the same values the same way
 (nearest E4M3, ties to even, saturation at 448), so they differ only by
-summation order and by h's fp32 (GPU) against fp64 (oracle) values."""
+summation order and by h's fp32 (GPU) against fp64 (oracle) values.  The
+one-row mma.sync kernel and the tensor-core path (any B) take the format; the
+mma.sync batch kernels refuse it."""
 import dataclasses
 
 import numpy as np
@@ -25,12 +27,12 @@ def _np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def _parity(cfg, rows=None):
+def _parity(cfg, rows=None, expert_path=0, max_batch=None):
     inp = oracle.clean_inputs(cfg)
-    ref = oracle.forward(inp, act="mxfp8")
-    ex = oracle.forward(inp)
+    ref = oracle.forward(inp, rows=rows, act="mxfp8")
+    ex = oracle.forward(inp, rows=rows)
     x, res = synthetic.make_activations(cfg, attempt=inp.attempt)
-    layer = synthetic.make_layer(cfg)
+    layer = synthetic.make_layer(cfg, expert_path=expert_path, max_batch=max_batch)
     layer.set_act_format(1)
     idx, w = layer.router_topk(x)
     dbg = run_debug(layer, x, res)
@@ -52,9 +54,25 @@ def test_full_size_one_row_matches_oracle_mxfp8_mode():
     _parity(CONFIGS["full_b1"])
 
 
-def test_format_is_one_row_only_and_switches_back():
+@pytest.mark.parametrize("B", [1, 3, 8, 17, 64])
+def test_tiny_tensor_core_path_matches_oracle_mxfp8_mode(B):
+    """The tensor-core path's activation planes hold the MXFP8 roundings of x
+    (built by the CUDA-core router below 25 rows, by the tensor-core router
+    from 25) and of h (FC1's epilogue)."""
+    _parity(dataclasses.replace(CONFIGS["tiny_b1"], name=f"tiny_b{B}", B=B), expert_path=2,
+            max_batch=64)
+
+
+@pytest.mark.parametrize("name,rows", [("full_b8", [0, 7]), ("verify_b16", [0, 5, 15]),
+                                       ("full_b64", [0, 33, 63])])
+def test_full_size_batches_match_oracle_mxfp8_mode(name, rows):
+    """The batches the benchmark times, on their tensor-core path."""
+    _parity(CONFIGS[name], rows=rows)
+
+
+def test_mma_sync_batches_reject_the_format_and_it_switches_back():
     cfg = CONFIGS["tiny_b1"]
-    layer = synthetic.make_layer(cfg, max_batch=4)
+    layer = synthetic.make_layer(cfg, max_batch=4, expert_path=1)
     layer.set_act_format(1)
     x3, r3 = synthetic.make_activations(dataclasses.replace(cfg, name="tiny_b3", B=3))
     with pytest.raises(M.MoEError) as e:
@@ -76,9 +94,3 @@ def test_format_is_one_row_only_and_switches_back():
     layer.close()
 
 
-def test_tensor_core_only_layer_rejects_the_format():
-    layer = synthetic.make_layer(CONFIGS["tiny_b1"], expert_path=2)
-    with pytest.raises(M.MoEError) as e:
-        layer.set_act_format(1)
-    assert e.value.code == M.MOE_ERR_UNSUPPORTED
-    layer.close()
