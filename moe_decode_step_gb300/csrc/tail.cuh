@@ -49,6 +49,7 @@ tail_kernel(const TailArgs a) {
   const bool ok = (int)threadIdx.x * 4 < per_cta;
   __shared__ float s_warp[8];
   __shared__ float s_part[kTailCluster];
+  __shared__ float s_w[32];   // the row's combine weights (k <= 32)
   trace_begin(a.trace, 4);
   // first cluster phase: every CTA of the cluster has started (required before
   // any remote shared-memory store); arrive now, wait just before the stores
@@ -63,28 +64,41 @@ tail_kernel(const TailArgs a) {
   }
   float z[4] = {0.f, 0.f, 0.f, 0.f};
   float yr[4] = {0.f, 0.f, 0.f, 0.f};
-  if (ok) {
-    const size_t o = (size_t)b * a.d + n;
-    // every load of this thread is issued before the first use
-    const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.y_s + o));
-    const uint2 rb = __ldcg(reinterpret_cast<const uint2*>(a.residual + o));
-    const float* yp = a.y_pair + (size_t)b * a.k * a.d + n;
-    for (int j0 = 0; j0 < a.k; j0 += kTailBatch) {
-      float4 v[kTailBatch];
-      float w[kTailBatch];
+  // the row's k combine weights, read once per CTA (not once per thread)
+  for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_w[i] = __ldcg(a.topk_w + b * a.k + i);
+  const size_t o = (size_t)b * a.d + n;
+  const float* yp = a.y_pair + (size_t)b * a.k * a.d + n;
+  // every load of this thread is issued before the first use: the first
+  // batch of pair rows goes out before the barrier that publishes s_w
+  float4 ys = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint2 rb = make_uint2(0u, 0u);
+  float4 v[kTailBatch];
 #pragma unroll
-      for (int j = 0; j < kTailBatch; ++j) {
-        const bool in = j0 + j < a.k;
-        v[j] = in ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)(j0 + j) * a.d))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-        w[j] = in ? __ldcg(a.topk_w + b * a.k + j0 + j) : 0.f;
+  for (int j = 0; j < kTailBatch; ++j) {
+    v[j] = ok && j < a.k ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)j * a.d))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (ok) {
+    ys = __ldcg(reinterpret_cast<const float4*>(a.y_s + o));
+    rb = __ldcg(reinterpret_cast<const uint2*>(a.residual + o));
+  }
+  __syncthreads();
+  if (ok) {
+    for (int j0 = 0; j0 < a.k; j0 += kTailBatch) {
+      if (j0 > 0) {
+#pragma unroll
+        for (int j = 0; j < kTailBatch; ++j)
+          v[j] = j0 + j < a.k
+                     ? __ldcg(reinterpret_cast<const float4*>(yp + (size_t)(j0 + j) * a.d))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kTailBatch; ++j) {
-        yr[0] = fmaf(w[j], v[j].x, yr[0]);
-        yr[1] = fmaf(w[j], v[j].y, yr[1]);
-        yr[2] = fmaf(w[j], v[j].z, yr[2]);
-        yr[3] = fmaf(w[j], v[j].w, yr[3]);
+        const float w = j0 + j < a.k ? s_w[j0 + j] : 0.f;
+        yr[0] = fmaf(w, v[j].x, yr[0]);
+        yr[1] = fmaf(w, v[j].y, yr[1]);
+        yr[2] = fmaf(w, v[j].z, yr[2]);
+        yr[3] = fmaf(w, v[j].w, yr[3]);
       }
     }
     z[0] = bf16_bits_to_f32(rb.x & 0xFFFFu) + yr[0] + ys.x;

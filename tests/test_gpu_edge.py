@@ -40,10 +40,12 @@ def _cfg(base, B):
     return dataclasses.replace(base, name=f"{base.name}_B{B}", B=B)
 
 
-def _run(cfg, weights, x, res, path, max_batch):
-    """router_topk + forward_debug of one layer built on `weights`; returns
-    idx, w (numpy), the debug exports and the updated residual."""
+def _run(cfg, weights, x, res, path, max_batch, act_format=0):
+    """router_topk + forward_debug of one layer built on `weights` (routed
+    activations in format act_format); returns idx, w (numpy), the debug
+    exports and the updated residual."""
     layer = synthetic.make_layer(cfg, max_batch=max_batch, weights=weights, expert_path=path)
+    layer.set_act_format(act_format)
     idx, w = layer.router_topk(x)
     r = res.clone()
     d = layer.forward_debug(x, r)

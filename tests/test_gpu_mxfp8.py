@@ -94,3 +94,34 @@ def test_mma_sync_batches_reject_the_format_and_it_switches_back():
     layer.close()
 
 
+
+
+# ---------------------------------------------------------------------------
+# Edge rows in the MXFP8 format: a row with max |x| >= 2^15 (its blocks' E8M0
+# scales far above 1; on the one-row mma.sync kernel the f16 shift applies to
+# the rounded values) and an all-zero row (every block's scale code is the
+# smallest, every element rounds to 0, so h and the routed output are exact
+# zeros).
+from test_gpu_edge import _cfg, _check_rows, _edge_inputs, _run  # noqa: E402
+
+
+def test_large_and_zero_rows_tensor_core_path_mxfp8():
+    kinds = ["normal", "large", "zero"]
+    cfg = _cfg(CONFIGS["tiny_b1"], len(kinds))
+    x, res, inp = _edge_inputs(cfg, kinds)
+    assert float(x[1].float().abs().max()) >= 2.0 ** 15
+    ref = oracle.forward(inp, act="mxfp8")
+    w = synthetic.make_weights(CONFIGS["tiny_b1"], layout=3)
+    idx, wt, dbg, r = _run(cfg, w, x, res, 2, max_batch=len(kinds), act_format=1)
+    _check_rows(ref, idx, wt, dbg, r, range(len(kinds)), zero_rows=(2,))
+
+
+@pytest.mark.parametrize("kind", ["large", "zero"])
+@pytest.mark.parametrize("path", [1, 2], ids=["mma_sync", "tcgen05"])
+def test_one_edge_row_mxfp8(path, kind):
+    cfg = _cfg(CONFIGS["tiny_b1"], 1)
+    x, res, inp = _edge_inputs(cfg, [kind])
+    ref = oracle.forward(inp, act="mxfp8")
+    w = synthetic.make_weights(CONFIGS["tiny_b1"], layout=1 if path == 1 else 3)
+    idx, wt, dbg, r = _run(cfg, w, x, res, path, max_batch=1, act_format=1)
+    _check_rows(ref, idx, wt, dbg, r, [0], zero_rows=(0,) if kind == "zero" else ())
