@@ -667,7 +667,7 @@ def run_ours(args, rank, world, local):
         chain = {"layers": cc.n_layers, "B": cc.B, "us": vc, "us_per_layer": vc / cc.n_layers,
                  "steps": stc, "l2": ("flushed once before each chain" if args.l2 == "flush"
                                       else "not flushed (63 GB of weights per chain)"),
-                 "prefetch": "next layer's router weights into L2 during the tail, side stream",
+                 "prefetch": "next layer's router weights into L2, issued by this layer's tail",
                  "us_prefetch_off": vc_off, "us_per_layer_prefetch_off": vc_off / cc.n_layers,
                  "prefetch_gain_us_per_layer": (vc_off - vc) / cc.n_layers}
         for L in chain_layers:

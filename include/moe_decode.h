@@ -21,7 +21,8 @@
  * section "What the fused path changes" (router/MoE front, shared expert on a
  * side stream, one persistent routed-expert kernel for FC1 and FC2, a tail that
  * folds the down-projection reduction and the next norm together, L2 prefetch
- * of upcoming weights on a third stream).  The pages give the structure only;
+ * of upcoming weights on a third stream; here the prefetch is issued by the
+ * tail kernel).  The pages give the structure only;
  * the formulas above are the plainest reading of that structure.  Element and
  * scale encodings: OCP Microscaling Formats (MX) Specification v1.0.
  *
@@ -113,8 +114,8 @@ typedef struct {
 } moe_weights_t;
 
 /* Validate dims, device (must be sm_103) and pointer alignment (16 bytes),
- * allocate the workspace (routing tables, intermediates, two events and one
- * side stream) on the current device and return a handle in *out.
+ * allocate the workspace (routing tables, intermediates, timing events) on
+ * the current device and return a handle in *out.
  * Errors: INVALID_ARG (null or bad dims), UNSUPPORTED (device/alignment),
  * ALLOC (workspace), CUDA. */
 int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_layer_t* out);
@@ -178,12 +179,12 @@ int moe_debug_dequant(moe_layer_t layer, void* stream, int expert, int which, fl
  * path returns MOE_ERR_UNSUPPORTED.  Errors: INVALID_ARG. */
 int moe_set_act_format(moe_layer_t layer, int fmt);
 
-/* Chain layers: once this layer's expert kernels have finished, an L2-prefetch
- * kernel on a third stream pulls `next`'s router weights into L2 while this
- * layer's tail runs (HBM is otherwise idle then), and the caller's stream
- * waits for it after the tail, so the next layer's router reads them from L2.
- * next may be NULL to switch it off.  Both handles must live on the same
- * device. */
+/* Chain layers: this layer's tail kernel, whose CTAs start while the expert
+ * kernels finish, issues L2 prefetches (prefetch.global.L2::evict_last) of
+ * `next`'s router weights before it waits for them, so the next layer's
+ * router, the first kernel of the next forward, finds them in L2.  No extra
+ * launch or stream.  next may be NULL to switch it off.  Both handles must
+ * live on the same device. */
 int moe_set_prefetch_next(moe_layer_t layer, moe_layer_t next);
 
 /* Synchronise the layer's streams and report the device status word
@@ -220,8 +221,7 @@ int moe_get_timing(moe_layer_t layer, float* us, int n);
 int moe_set_trace(moe_layer_t layer, int enable);
 int moe_get_trace(moe_layer_t layer, unsigned long long* ns, int n);
 
-/* Number of kernel launches one forward makes for batch B (excluding the
- * optional prefetch kernel, which adds one when enabled). */
+/* Number of kernel launches one forward makes for batch B. */
 int moe_launches_per_forward(moe_layer_t layer, int B);
 
 /* ---- MXFP4 packing (OCP MX v1.0: E2M1 elements, E8M0 scale per 32 K) ---- */

@@ -142,8 +142,6 @@ struct moe_layer {
   int smem_optin = 0;   // largest dynamic shared memory a block may opt into
   void* ws_base = nullptr;
   Workspace ws{};
-  cudaStream_t pref = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_pref = nullptr;
   cudaEvent_t ev_time[kNumTimeEvents] = {};
   bool timing = false, timed_once = false, tracing = false;
   moe_layer* next = nullptr;
@@ -997,28 +995,16 @@ int launch_tail(moe_layer* L, cudaStream_t st, int B, void* residual, void* out,
   a.eps = L->dims.rms_eps;
   a.trace = L->tracing ? L->ws.trace : nullptr;
   a.h_amax = L->ws.h_amax;
+  if (L->next) {
+    // the next layer's router weights into L2 from the tail's CTAs, which
+    // start while this layer's expert kernels finish: HBM is then idle but
+    // for the last expert items, and the next router streams those weights
+    // first.  Prefetching more (the next shared expert) or earlier (while
+    // this layer's experts stream) only competes with them for HBM.
+    a.pref = static_cast<const char*>(L->next->w.router_w);
+    a.pref_bytes = (size_t)L->next->dims.n_experts * L->next->dims.d * 2;
+  }
   MOE_CUDA(launch_ex(tail_kernel, dim3(kTailCluster, B), dim3(L->dims.d / 32), 0, st, pdl, a));
-  return MOE_OK;
-}
-
-// The next layer's router weights into L2 on the third stream, from the end of
-// this layer's expert kernels: the tail reads a few hundred KB, so HBM is
-// otherwise idle then, while the next router (the first kernel of the next
-// forward, which waits for this prefetch) would stream its weights cold.
-// Prefetching more (the next shared expert) or earlier (while this layer's
-// experts stream) only competes with them for HBM.
-int launch_prefetch(moe_layer* L, cudaStream_t st) {
-  moe_layer* n = L->next;
-  if (!n) return MOE_OK;
-  PrefetchArgs a{};
-  a.n = 1;
-  a.ptr[0] = static_cast<const char*>(n->w.router_w);
-  a.bytes[0] = (size_t)n->dims.n_experts * n->dims.d * 2;
-  MOE_CUDA(cudaEventRecord(L->ev_fork, st));
-  MOE_CUDA(cudaStreamWaitEvent(L->pref, L->ev_fork, 0));
-  l2_prefetch_kernel<<<L->n_sm, 256, 0, L->pref>>>(a);
-  MOE_CUDA(cudaGetLastError());
-  MOE_CUDA(cudaEventRecord(L->ev_pref, L->pref));
   return MOE_OK;
 }
 
@@ -1058,10 +1044,7 @@ int forward_impl(moe_layer* L, cudaStream_t st, const void* x, int B, void* resi
     if ((rc = tc ? launch_fc2_tc(L, st, B) : launch_fc2(L, st, B))) return rc;
     if (tm) MOE_CUDA(record_time(L, kTimeFc2End, st));
   }
-  if ((rc = launch_prefetch(L, st))) return rc;
   if ((rc = launch_tail(L, st, B, residual, out, y_r_dbg, z_dbg, out_dbg, true))) return rc;
-  // the next forward on this stream starts after the prefetch (joins the third stream)
-  if (L->next) MOE_CUDA(cudaStreamWaitEvent(st, L->ev_pref, 0));
   if (tm) {
     MOE_CUDA(record_time(L, kTimeTailEnd, st));
     L->timed_once = true;
@@ -1234,9 +1217,6 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
   };
   cudaError_t e;
   if ((e = cudaMemset(L->ws_base, 0, bytes)) != cudaSuccess) return fail(e);
-  if ((e = cudaStreamCreateWithFlags(&L->pref, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
-  if ((e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
-  if ((e = cudaEventCreateWithFlags(&L->ev_pref, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
   // the expert paths kept (both by default, see kTcMinBatch) fix the layouts
@@ -1268,9 +1248,6 @@ int moe_layer_destroy(moe_layer_t L) {
   cudaSetDevice(L->device);
   cudaDeviceSynchronize();
   if (L->hg.exec) cudaGraphExecDestroy(L->hg.exec);
-  if (L->pref) cudaStreamDestroy(L->pref);
-  if (L->ev_fork) cudaEventDestroy(L->ev_fork);
-  if (L->ev_pref) cudaEventDestroy(L->ev_pref);
   for (int i = 0; i < kNumTimeEvents; ++i)
     if (L->ev_time[i]) cudaEventDestroy(L->ev_time[i]);
   if (L->ws_base) cudaFree(L->ws_base);
@@ -1418,7 +1395,6 @@ int moe_set_prefetch_next(moe_layer_t L, moe_layer_t next) {
 
 int moe_layer_status(moe_layer_t L, int* device_status) {
   if (!L || !device_status) return MOE_ERR_INVALID_ARG;
-  MOE_CUDA(cudaStreamSynchronize(L->pref));
   MOE_CUDA(cudaDeviceSynchronize());
   int v = 0;
   MOE_CUDA(cudaMemcpy(&v, L->ws.status, sizeof(int), cudaMemcpyDeviceToHost));

@@ -34,6 +34,10 @@ struct TailArgs {
   // zeroed for the next forward once every earlier kernel of this one has
   // finished: the per-pair max |h| that FC1's epilogues raise
   unsigned* h_amax;           // [B*k]
+  // optional L2 prefetch of static weights of the next layer (no dependency:
+  // issued before the wait for the predecessor), or null / 0
+  const char* pref;
+  size_t pref_bytes;
 };
 
 constexpr int kTailCluster = 8;
@@ -57,6 +61,17 @@ tail_kernel(const TailArgs a) {
   // gamma is a static weight: it may be read before the predecessor finishes
   uint2 g = make_uint2(0, 0);
   if (ok) g = *reinterpret_cast<const uint2*>(a.gamma + n);
+  if (a.pref_bytes) {
+    // one prefetch.global.L2::evict_last per 256-byte segment, spread over
+    // every thread of the grid
+    const size_t segs = (a.pref_bytes + 255) / 256;
+    const size_t nt = (size_t)gridDim.x * gridDim.y * blockDim.x;
+    const size_t t0 = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    for (size_t i = t0; i < segs; i += nt) {
+      const size_t off = i * 256 < a.pref_bytes ? i * 256 : a.pref_bytes - 1;   // stay inside
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a.pref + off));
+    }
+  }
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   if (blockIdx.x == 0 && blockIdx.y == 0) {
@@ -140,29 +155,6 @@ tail_kernel(const TailArgs a) {
     if (a.out_dbg) *reinterpret_cast<float4*>(a.out_dbg + o) = make_float4(v[0], v[1], v[2], v[3]);
   }
   trace_end(a.trace, 4);
-}
-
-// L2 prefetch of upcoming weights ("What the fused path changes": a small
-// kernel walks a table of upcoming weight ranges and pulls them into L2 on a
-// third stream).  One prefetch.global.L2::evict_last per 256-byte segment.
-struct PrefetchArgs {
-  const char* ptr[4];
-  size_t bytes[4];
-  int n;
-};
-
-__global__ void __launch_bounds__(256)
-l2_prefetch_kernel(const PrefetchArgs a) {
-  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (int r = 0; r < a.n; ++r) {
-    if (a.bytes[r] == 0) continue;
-    const size_t segs = (a.bytes[r] + 255) / 256;
-    for (size_t i = tid; i < segs; i += stride) {
-      const size_t off = i * 256 < a.bytes[r] ? i * 256 : a.bytes[r] - 1;   // stay inside
-      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a.ptr[r] + off));
-    }
-  }
 }
 
 }  // namespace moe
