@@ -178,7 +178,8 @@ class MoELayer:
         check(lib().moe_set_timing(self._h, int(bool(enable))), "moe_set_timing")
 
     def get_timing(self):
-        """[router, routed FC1, routed FC2, shared (side stream), tail, layer] in us."""
+        """[router + top-k, FC1, FC2, 0 (no phase of its own), tail, layer] in us
+        (see moe_get_timing)."""
         arr = (ctypes.c_float * 6)()
         check(lib().moe_get_timing(self._h, arr, 6), "moe_get_timing")
         return list(arr)
