@@ -557,8 +557,12 @@ def run_ours(args, rank, world, local):
     # nodes sit between the chained kernels, so they are kept out of the value
     _, phases = time_layer(layer, x, res0, max(5, args.steps // 2), max(3, args.warmup), flush,
                            graph=True, timing=True)
-    eager_times, eager_phases = time_layer(layer, x, res0, max(5, args.steps // 2),
-                                           max(3, args.warmup), flush, graph=False)
+    # without a graph: the plain forward (no events between its kernels), and
+    # separately the per-phase events, which break the programmatic chain
+    eager_times, _ = time_layer(layer, x, res0, max(5, args.steps // 2), max(3, args.warmup),
+                                flush, graph=False, timing=False)
+    _, eager_phases = time_layer(layer, x, res0, max(5, args.steps // 2), max(3, args.warmup),
+                                 flush, graph=False)
 
     us = reduce_max(us_mode, world, dev)
     us_alt = reduce_max(us_alt, world, dev)

@@ -71,7 +71,7 @@ typedef struct moe_layer* moe_layer_t;
  * layout 1), the shared expert and the router on the CUDA cores.  2: tcgen05
  * tensor cores, block-scaled MXFP4 MMAs with tensor-memory accumulators (the
  * UMMA layouts, FC1 in layout 4 and FC2 in layout 3); the shared expert (and,
- * for B > 8, the router) as bf16 MMAs on the same tensor cores, from bf16
+ * from 25 rows, the router) as bf16 MMAs on the same tensor cores, from bf16
  * copies of those weights in 128-row tiles that the handle owns (2 * (3 * d *
  * f_shared + 128 * ceil(E / 128) * d) bytes of extra device memory).  0
  * (default): the layer keeps both and takes path 1 for B = 1 and path 2 for

@@ -15,7 +15,7 @@
 //    dense pass (h_s = hi + lo to 2^-16 relative, far inside fp32 sums of
 //    bf16 products).  FC2 runs its dense pass first too: its weight copies go
 //    out before FC1 is waited for, and the (hi, lo) columns after.
-//    Above 8 rows the router is a dense pass of its own (tc_router_kernel).
+//    From 25 rows the router is a dense pass of its own (tc_router_kernel).
 // fp32 accumulators live in tensor memory until the epilogue reads them back;
 // nothing is converted on the CUDA cores on the way in.
 //
