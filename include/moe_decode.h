@@ -61,9 +61,9 @@ typedef enum {
 
 typedef struct moe_layer* moe_layer_t;
 
-/* Layer dimensions.  d % 256 == 0 and d <= 7680; f % 256 == 0 and f <= 4096;
+/* Layer dimensions.  d % 256 == 0 and d <= 7680; f % 256 == 0 and f <= 3072;
  * f_shared % 256 == 0 and f_shared <= 4096; 1 <= top_k <= 32; top_k <= n_experts
- * <= 1024; 1 <= max_batch <= 64.
+ * <= 1024; 1 <= max_batch <= 64 (INVALID_ARG otherwise).
  *
  * expert_path picks how the routed experts run.  1: mma.sync tensor cores
  * with the weights converted to f16 in registers (the GEMV regime; the
@@ -76,8 +76,11 @@ typedef struct moe_layer* moe_layer_t;
  * f_shared + 128 * ceil(E / 128) * d) bytes of extra device memory).  0
  * (default): the layer keeps both and takes path 1 for B = 1 and path 2 for
  * B >= 2, or only path 1 when max_batch is 1 (one copy of the expert bytes
- * instead of two).  All give results within the same tolerance of the exact
- * layer.
+ * instead of two).  Path 1's kernels hold a ring of shared-memory stages
+ * sized for the dims; where it does not fit (large d with large f, or
+ * f_shared above 3072, for example), path 1 returns UNSUPPORTED and path 0
+ * keeps path 2 alone.  All give results within the same tolerance of the
+ * exact layer.
  *
  * mxfp4_layout says how the caller's expert weights are laid out: 0
  * (canonical), 1 (tiled: FC1 layout 2, FC2 layout 1) or 3 (UMMA: FC1 layout 4,

@@ -224,7 +224,7 @@ size_t workspace_bytes(const moe_dims_t& d, Workspace* ws, char* base) {
 
 int validate_dims(const moe_dims_t& d) {
   if (d.d <= 0 || d.d % 256 != 0 || d.d > 7680) return MOE_ERR_INVALID_ARG;
-  if (d.f <= 0 || d.f % 256 != 0 || d.f > 4096) return MOE_ERR_INVALID_ARG;
+  if (d.f <= 0 || d.f % 256 != 0 || d.f > 3072) return MOE_ERR_INVALID_ARG;
   if (d.f_shared <= 0 || d.f_shared % 256 != 0 || d.f_shared > 4096) return MOE_ERR_INVALID_ARG;
   if (d.top_k < 1 || d.top_k > 32) return MOE_ERR_INVALID_ARG;
   if (d.n_experts < d.top_k || d.n_experts > 1024) return MOE_ERR_INVALID_ARG;
@@ -490,6 +490,8 @@ int plan_tc_router(int K, int np_max, int E, int n_sm, int budget, StreamPlan* p
   return MOE_OK;
 }
 
+int plan_mma(moe_layer* L);
+
 int plan_all(moe_layer* L) {
   const moe_dims_t& d = L->dims;
   const int n = L->n_sm;
@@ -513,7 +515,19 @@ int plan_all(moe_layer* L) {
                                &L->plan[kStepTcRouter][c])));
     }
   }
-  if (!L->wm.ok) return MOE_OK;
+  if (L->wm.ok && (rc = plan_mma(L))) return rc;
+#undef MOE_PLAN
+  return MOE_OK;
+}
+
+// Launch shapes of the mma.sync path's kernels (they depend on the dims and
+// the device alone).
+int plan_mma(moe_layer* L) {
+  const moe_dims_t& d = L->dims;
+  const int n = L->n_sm;
+  int rc;
+#define MOE_PLAN(expr) \
+  if ((rc = (expr))) return rc;
   MOE_PLAN((plan_kernel<Sh1Cfg<1>, Fc1OneRowCfg>(MOE_FC1_KERNEL_ONE_ROW, d.d, d.f_shared, d.d,
                                                  d.f, n, kBudget1, &L->plan[kStepFc1][0])));
   MOE_PLAN((plan_kernel<Sh1Cfg<2>, Fc1Cfg>(MOE_FC1_KERNEL(2), d.d, d.f_shared, d.d, d.f, n,
@@ -1221,8 +1235,19 @@ int moe_layer_create(const moe_dims_t* dims, const moe_weights_t* weights, moe_l
     if ((e = cudaEventCreate(&L->ev_time[i])) != cudaSuccess) return fail(e);
   // the expert paths kept (both by default, see kTcMinBatch) fix the layouts
   // the kernels read; a layer that only ever sees one row keeps one
-  const int path = (dims->expert_path == kPathAuto && dims->max_batch == 1) ? kPathMmaSync
-                                                                            : dims->expert_path;
+  int path = (dims->expert_path == kPathAuto && dims->max_batch == 1) ? kPathMmaSync
+                                                                      : dims->expert_path;
+  if (path != kPathTc) {
+    // a shape whose stage rings the mma.sync kernels cannot fit leaves an
+    // automatic layer to the tensor-core path alone
+    rc = plan_mma(L);
+    if (rc == MOE_ERR_UNSUPPORTED && dims->expert_path == kPathAuto) {
+      path = kPathTc;
+    } else if (rc) {
+      moe_layer_destroy(L);
+      return rc;
+    }
+  }
   if (path != kPathTc && (rc = setup_weights(L, w, 1, L->wm))) {
     moe_layer_destroy(L);
     return rc;

@@ -89,7 +89,8 @@ def test_create_rejects_bad_dims_and_null_weights_before_touching_the_gpu():
                 routed_scale=2.5, rms_eps=1e-6, mxfp4_layout=0)
     for bad in (dict(d=1000), dict(f=100), dict(f=384), dict(top_k=0), dict(top_k=65), dict(n_experts=2),
                 dict(max_batch=65), dict(max_batch=0), dict(f_shared=0), dict(d=16384),
-                dict(d=7936), dict(expert_path=3), dict(expert_path=-1)):
+                dict(d=7936), dict(f=3328), dict(f=4096), dict(f_shared=4352),
+                dict(expert_path=3), dict(expert_path=-1)):
         dims = M.MoEDims(**{**good, **bad})
         assert L.moe_layer_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(h)) == \
             M.MOE_ERR_INVALID_ARG, bad
